@@ -1,0 +1,87 @@
+"""Pins for the oracle's decode attention (dequantize, then softmax(q k^T * scale) v in float64).
+
+Source: MTPLX pull request #267, "feat(kv-cache): add q6 paged KV quantization", description
+(plain KV quant dequantizes and runs SDPA).  Pinned to textbook special cases (one token; equal
+keys -> uniform weights; two tokens in closed form) and to PyTorch's
+scaled_dot_product_attention in float64 as an independent library routine.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import kvgen
+from oracle import attention as A
+from oracle import symmetric as S
+
+
+def _fp16(shape, seed, tag=60):
+    return kvgen.normal_fp16_np(seed, tag, np.arange(int(np.prod(shape)))).reshape(shape)
+
+
+def test_single_token_returns_its_value():
+    q = _fp16((6, 32), 1)
+    k = _fp16((1, 1, 32), 2)
+    v = _fp16((1, 1, 32), 3)
+    out = A.attend(q, k, v, 0.25)
+    assert np.array_equal(out, np.repeat(v[0].astype(np.float64), 6, axis=0))
+
+
+def test_equal_keys_give_the_mean_of_values():
+    q = _fp16((4, 16), 4)
+    k = np.repeat(_fp16((1, 2, 16), 5), 50, axis=0)
+    v = _fp16((50, 2, 16), 6)
+    out = A.attend(q, k, v, 1.0)
+    for j in range(4):
+        assert np.allclose(out[j], v[:, j // 2].astype(np.float64).mean(0), rtol=0, atol=1e-12)
+
+
+def test_two_tokens_closed_form():
+    # scores 0 and 1: weights 1/(1+e) and e/(1+e)
+    q = np.zeros((1, 4), np.float16)
+    q[0, 0] = 1
+    k = np.zeros((2, 1, 4), np.float16)
+    k[1, 0, 0] = 1
+    v = np.array([[[1, 0, 0, 2]], [[0, 1, 0, -2]]], np.float16)
+    out = A.attend(q, k, v, 1.0)[0]
+    e = math.e
+    expect = np.array([1 / (1 + e), e / (1 + e), 0, 2 / (1 + e) - 2 * e / (1 + e)])
+    assert np.allclose(out, expect, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("T,H,G,D", [(1, 1, 1, 8), (37, 2, 3, 64), (300, 4, 6, 256)])
+def test_matches_torch_sdpa_float64(T, H, G, D):
+    q = _fp16((H * G, D), 7)
+    k = _fp16((T, H, D), 8)
+    v = _fp16((T, H, D), 9)
+    out = A.attend(q, k, v, 1.0 / math.sqrt(D))
+    qt = torch.from_numpy(q.astype(np.float64)).view(1, H * G, 1, D)
+    kt = torch.from_numpy(k.astype(np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)[None]
+    vt = torch.from_numpy(v.astype(np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)[None]
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=1.0 / math.sqrt(D))
+    assert np.allclose(out, ref.view(H * G, D).numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_empty_sequence_is_zero():
+    out = A.attend(_fp16((6, 8), 1), np.zeros((0, 1, 8), np.float16),
+                   np.zeros((0, 1, 8), np.float16), 1.0)
+    assert np.all(out == 0)
+
+
+@pytest.mark.parametrize("bits", [8, 6, 4])
+def test_paged_equals_contiguous(bits):
+    H, G, D, ps = 2, 3, 32, 4
+    lens = np.array([0, 1, 9, 16], np.int32)
+    pt = kvgen.random_page_table(3, len(lens), 4)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    k = _fp16((int(cu[-1]), H, D), 10)
+    v = _fp16((int(cu[-1]), H, D), 11)
+    kp, vp = S.PagedPool(bits, H, D, ps, pt.size), S.PagedPool(bits, H, D, ps, pt.size)
+    S.quant_pack_paged(kp, k, pt, cu, np.zeros(4, np.int32))
+    S.quant_pack_paged(vp, v, pt, cu, np.zeros(4, np.int32))
+    q = _fp16((len(lens), H * G, D), 12)
+    out = A.decode_attention_paged(q, kp, vp, pt, lens, 0.125)
+    for s in range(len(lens)):
+        ref = A.decode_attention_fp16(q[s], k[cu[s]:cu[s + 1]], v[cu[s]:cu[s + 1]], bits, 0.125)
+        assert np.array_equal(out[s], ref)
