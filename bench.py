@@ -1,0 +1,525 @@
+"""Benchmark: one step of the quantized paged KV-cache hot path on the paged-prefill workload.
+
+Workload (per GPU): 16 layers x {K, V} x 8 sequences x 32,768 tokens x 4 KV heads x D = 256 fp16,
+page size 16, a seeded random page table; the KIVI cache 16 layers x {K, V} [16, 8, 4096, 64].
+One step runs, in order:
+  1. kvq_quant_pack_paged over all 32 K/V tensors (q6 by default)   -- symmetric quantize + pack
+  2. kvq_dequant_paged over all 32 tensors                           -- gather + unpack + dequant
+  3. kvq_decode_attn: one decode query per sequence (24 query heads, GQA 6:1) over the packed
+     cache just written, all 16 layers in one call                  -- packed decode attention
+  4. kivi_quant_dequant of the 128 aged tokens [3840, 3968) of all 32 KIVI tensors
+The metric is algorithmic bytes moved per second (GB/s, 1e9) over the whole step; per-kernel
+figures, the packed-decode tokens/s, the q8/q4 variants and the 262,144-token decode are reported
+alongside.  Inputs are far larger than L2 (129 MB), so no explicit flush between steps.
+
+`--impl reference` times the CPU oracle (the plain restatement of the pages) on a bounded sample
+of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+# the CPU baseline is reported for the threads it uses: keep BLAS single-threaded
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import kvgen  # noqa: E402
+
+METRIC = "KV quant+pack / dequant GB/s and % of HBM roofline; packed decode attn tok/s"
+WL = kvgen.WORKLOADS["paged_prefill_16L_8x32768_4x256"]
+KV = kvgen.WORKLOADS["kivi_flush_16L_16x8x4096x64"]
+HQ = 24
+SOFTMAX_SCALE = 1.0 / 16.0
+KIVI_LO, KIVI_HI = 3840, 3968
+FALLBACK_HBM_GBS = 6800.0
+
+
+def packed_dim(D, bits):
+    return {8: D, 6: D * 3 // 4, 4: D // 2}[bits]
+
+
+def bytes_quant(rows, D, bits):        # read fp16 row, write packed row + fp16 scale
+    return rows * (2 * D + packed_dim(D, bits) + 2)
+
+
+def bytes_decode(layers, tokens_total, H, D, bits, nseq, hq):
+    kv = layers * tokens_total * H * 2 * (packed_dim(D, bits) + 2)
+    return kv + layers * nseq * hq * D * (2 + 4)
+
+
+def bytes_kivi(n_tensors, B, H, span, D):
+    return n_tensors * B * H * span * D * 4
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [s for s in sm if s >= 0.5 * max(sm)]
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- GPU arm
+class Workload:
+    """Device-resident inputs and outputs of one replica."""
+
+    def __init__(self, kvq, dev, bits):
+        self.kvq, self.dev = kvq, dev
+        L, nseq, ntok, H, D, ps = (WL["n_layers"], WL["n_seq"], WL["n_tok"], WL["H"], WL["D"],
+                                   WL["page_size"])
+        self.L, self.nseq, self.ntok, self.H, self.D, self.ps = L, nseq, ntok, H, D, ps
+        self.specs = [kvgen.KVSpec(seed=WL["seed"], layer=l, is_key=k, n_seq=nseq, n_tok=ntok,
+                                   num_heads=H, head_dim=D)
+                      for l in range(L) for k in (True, False)]
+        self.x = [s.full_torch(dev) for s in self.specs]
+        self.pt_np = kvgen.random_page_table(1, nseq, ntok // ps)
+        self.pt = torch.from_numpy(self.pt_np).to(dev)
+        self.pt1 = self.pt.reshape(1, -1).contiguous()      # one 262,144-token sequence
+        self.cu = torch.tensor(np.arange(nseq + 1) * ntok, dtype=torch.int32, device=dev)
+        self.start = torch.zeros(nseq, dtype=torch.int32, device=dev)
+        self.lens = torch.full((nseq,), ntok, dtype=torch.int32, device=dev)
+        self.lens1 = torch.tensor([nseq * ntok], dtype=torch.int32, device=dev)
+        self.pools = {}
+        self.bits = bits
+        self.pools[bits] = self.make_pools(bits)
+        self.deq = [torch.empty_like(t) for t in self.x]
+        self.q = kvgen.queries_torch(WL["seed"], L, nseq, HQ, D, dev)
+        self.q1 = kvgen.queries_torch(WL["seed"] + 1, L, 1, HQ, D, dev)
+        self.out = torch.empty((L, nseq, HQ, D), dtype=torch.float32, device=dev)
+        self.out1 = torch.empty((L, 1, HQ, D), dtype=torch.float32, device=dev)
+        p0 = self.pools[bits][0]
+        self.ws = kvq.decode_workspace(self.pools[bits][0::2], nseq, HQ, ntok, dev)
+        self.ws1 = kvq.decode_workspace(self.pools[bits][0::2], 1, HQ, nseq * ntok, dev)
+        del p0
+        self.kivi = [kvgen.KiviSpec(seed=KV["seed"], layer=l, is_key=k, batch=KV["B"],
+                                    num_heads=KV["H"], seq=KV["S"], head_dim=KV["D"]
+                                    ).full_torch(dev)
+                     for l in range(KV["n_layers"]) for k in (True, False)]
+        self.kivi_flags = [k for _ in range(KV["n_layers"]) for k in (True, False)]
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def make_pools(self, bits):
+        return [self.kvq.Pool.empty(bits, self.H, self.D, self.ps, self.pt_np.size, self.dev)
+                for _ in self.x]
+
+    # the four stages of one step
+    def quant(self, bits):
+        self.kvq.kvq_quant_pack_paged(self.pools[bits], self.x, self.pt, self.cu, self.start,
+                                      self.err)
+
+    def dequant(self, bits):
+        self.kvq.kvq_dequant_paged(self.pools[bits], self.deq, self.pt, self.cu, self.start,
+                                   self.err)
+
+    def decode(self, bits):
+        p = self.pools[bits]
+        self.kvq.kvq_decode_attn(p[0::2], p[1::2], self.q, self.pt, self.lens, self.ntok,
+                                 SOFTMAX_SCALE, self.out, self.ws, self.err)
+
+    def decode_full_context(self, bits):
+        p = self.pools[bits]
+        self.kvq.kvq_decode_attn(p[0::2], p[1::2], self.q1, self.pt1, self.lens1,
+                                 self.nseq * self.ntok, SOFTMAX_SCALE, self.out1, self.ws1,
+                                 self.err)
+
+    def kivi_flush(self):
+        self.kvq.kivi_quant_dequant(self.kivi, self.kivi_flags, KIVI_LO, KIVI_HI,
+                                    KV["group_size"], KV["levels"], KV["eps"])
+
+    def bytes(self, bits):
+        rows = self.L * 2 * self.nseq * self.ntok * self.H
+        return {
+            "quant_pack": bytes_quant(rows, self.D, bits),
+            "dequant": bytes_quant(rows, self.D, bits),
+            "decode_attn": bytes_decode(self.L, self.nseq * self.ntok, self.H, self.D, bits,
+                                        self.nseq, HQ),
+            "kivi": bytes_kivi(len(self.kivi), KV["B"], KV["H"], KIVI_HI - KIVI_LO, KV["D"]),
+        }
+
+
+def time_step(w, bits, steps, stream):
+    """Run `steps` steps with events between the stages; returns (total_s, per-stage seconds)."""
+    names = ["quant_pack", "dequant", "decode_attn", "kivi"]
+    fns = [lambda: w.quant(bits), lambda: w.dequant(bits), lambda: w.decode(bits), w.kivi_flush]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(steps):
+        for i, fn in enumerate(fns):
+            ev[k][i].record(stream)
+            fn()
+        ev[k][4].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    per = {n: [] for n in names}
+    for k in range(steps):
+        for i, n in enumerate(names):
+            per[n].append(ev[k][i].elapsed_time(ev[k][i + 1]) / 1e3)
+    return start.elapsed_time(end) / 1e3, per
+
+
+def time_fn(fn, steps, warmup, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / steps
+
+
+def run_gpu(args):
+    world, rank, local = dist_setup(args.gpus)
+    import paged_kv_cache_fp16_gb300 as kvq
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    bits = args.bits
+    w = Workload(kvq, dev, bits)
+    B = w.bytes(bits)
+    step_bytes = sum(B.values())
+
+    for _ in range(args.warmup):
+        w.quant(bits); w.dequant(bits); w.decode(bits); w.kivi_flush()
+    torch.cuda.synchronize()
+    if int(w.err.item()) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        total, per = time_step(w, bits, args.steps, stream)
+        barrier(world)
+        torch.cuda.synchronize()
+    clocks = clk.summary()
+    total = max_over_ranks(total, world, dev)
+    ms_per_step = total / args.steps * 1e3
+    value = world * step_bytes * args.steps / total / 1e9
+    launches_per_step = 6   # quant, dequant, decode + merge, kivi keys + values
+
+    stage = {}
+    for n, ts in per.items():
+        avg = sum(ts) / len(ts)
+        stage[n] = {"ms": avg * 1e3, "GB_s": B[n] / avg / 1e9}
+    stage["decode_attn"]["tok_s"] = w.nseq / (sum(per["decode_attn"]) / len(per["decode_attn"]))
+    peak, peak_kind = measured_peaks()
+    dom = max(per, key=lambda n: sum(per[n]))
+    dom_avg = sum(per[dom]) / len(per[dom])
+    achieved = B[dom] / dom_avg / 1e9
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+                "traffic": args.traffic}
+
+    # extras outside the timed step: 262,144-token decode, q8/q4 variants
+    extras = {}
+    t = time_fn(lambda: w.decode_full_context(bits), args.steps, args.warmup, stream)
+    extras["decode_attn_262144_1seq"] = {"ms": t * 1e3, "tok_s": 1.0 / t,
+                                         "GB_s": bytes_decode(w.L, w.nseq * w.ntok, w.H, w.D,
+                                                              bits, 1, HQ) / t / 1e9}
+    if not args.no_widths:
+        for b2 in (8, 4):
+            if b2 == bits:
+                continue
+            w.pools[b2] = w.make_pools(b2)
+            tq = time_fn(lambda: w.quant(b2), args.steps, args.warmup, stream)
+            td = time_fn(lambda: w.dequant(b2), args.steps, args.warmup, stream)
+            ta = time_fn(lambda: w.decode_full_context(b2), args.steps, args.warmup, stream)
+            Bq = bytes_quant(w.L * 2 * w.nseq * w.ntok * w.H, w.D, b2)
+            extras[f"q{b2}"] = {"quant_pack_GB_s": Bq / tq / 1e9, "dequant_GB_s": Bq / td / 1e9,
+                                "decode_attn_262144_tok_s": 1.0 / ta,
+                                "decode_attn_GB_s": bytes_decode(w.L, w.nseq * w.ntok, w.H, w.D,
+                                                                 b2, 1, HQ) / ta / 1e9}
+            del w.pools[b2]
+            torch.cuda.empty_cache()
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(w, kvq, bits, args, stream, world, dev, step_bytes)
+
+    if int(w.err.item()) != 0:
+        raise RuntimeError("device error word set")
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic (seeded counter-based generator, shapes of the pages' workloads)",
+            "config": {"workload": "paged_prefill_16L_8x32768_4x256 step: quant-pack -> "
+                                   "dequant -> packed decode attn (8 seqs x 24 q heads) -> "
+                                   "KIVI flush 128 tok of 16L x [16,8,4096,64]",
+                       "bits": bits, "layers": w.L, "seqs": w.nseq, "tokens_per_seq": w.ntok,
+                       "kv_heads": w.H, "head_dim": w.D, "page_size": w.ps, "q_heads": HQ,
+                       "l2": "inputs larger than L2 (no flush)",
+                       "bytes_per_step": step_bytes, "parallelism": f"replicas x{world}"},
+            "stages": {k: {kk: round(vv, 3) for kk, vv in v.items()} for k, v in stage.items()},
+            "extras": {k: {kk: round(vv, 3) for kk, vv in v.items()} for k, v in extras.items()},
+            "roofline": roofline,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+
+
+def run_e2e(w, kvq, bits, args, stream, world, dev, step_bytes):
+    """Per step: copy the step's fp16 K/V inputs and queries from pinned host memory, run the
+    four stages through the public API, read the attention output back."""
+    host_x = [t.cpu().pin_memory() for t in w.x]
+    host_q = w.q.cpu().pin_memory()
+    host_out = torch.empty(w.out.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_x) + host_q.numel() * 2
+    d2h = host_out.numel() * 4
+
+    def step():
+        for d, h in zip(w.x, host_x):
+            d.copy_(h, non_blocking=True)
+        w.q.copy_(host_q, non_blocking=True)
+        w.quant(bits); w.dequant(bits); w.decode(bits); w.kivi_flush()
+        host_out.copy_(w.out, non_blocking=True)
+
+    n = max(1, min(args.steps, 5))
+    for _ in range(min(args.warmup, 2)):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    t = max_over_ranks(a.elapsed_time(b) / 1e3, world, dev)
+    del host_x
+    return {"value": round(world * step_bytes * n / t / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "ms_per_step": round(t / n * 1e3, 3)}
+
+
+# ----------------------------------------------------------------------------- CPU (oracle) arm
+_CPU_INPUTS = {}
+
+
+def _cpu_inputs():
+    """Seeded inputs of the CPU sample (generated once, outside the timed oracle work)."""
+    if not _CPU_INPUTS:
+        D, H, ps, n_tok = WL["D"], WL["H"], WL["page_size"], 4096
+        _CPU_INPUTS["pt"] = kvgen.random_page_table(1, 1, n_tok // ps)
+        _CPU_INPUTS["xs"] = [kvgen.KVSpec(seed=WL["seed"], layer=0, is_key=k, n_seq=1,
+                                          n_tok=n_tok, num_heads=H, head_dim=D).full_np()
+                             for k in (True, False)]
+        _CPU_INPUTS["q"] = kvgen.queries_np(WL["seed"], 1, 1, HQ, D)
+        _CPU_INPUTS["kivi"] = [kvgen.KiviSpec(seed=KV["seed"], layer=0, is_key=k, batch=1,
+                                              num_heads=KV["H"], seq=KV["S"], head_dim=KV["D"]
+                                              ).full_np() for k in (True, False)]
+    return _CPU_INPUTS
+
+
+def cpu_sample_step():
+    """One bounded sample of the step, run through the oracle: returns algorithmic bytes."""
+    from oracle import attention as oa
+    from oracle import kivi as ok
+    from oracle import symmetric as osym
+    D, H, ps, n_tok = WL["D"], WL["H"], WL["page_size"], 4096
+    inp = _cpu_inputs()
+    pt = inp["pt"]
+    pools = []
+    for x in inp["xs"]:
+        p = osym.PagedPool(6, H, D, ps, pt.size)
+        osym.quant_pack_paged(p, x, pt, np.array([0, n_tok]), np.array([0]))
+        osym.dequant_paged(p, pt, np.array([0, n_tok]), np.array([0]))
+        pools.append(p)
+    oa.decode_attention_paged(inp["q"][0], pools[0], pools[1], pt, np.array([n_tok]),
+                              SOFTMAX_SCALE)
+    kk, vv = (t.copy() for t in inp["kivi"])
+    ok.flush(kk, vv, KIVI_LO, KIVI_HI, KV["group_size"], KV["levels"], KV["eps"])
+    rows = 2 * n_tok * H
+    return (2 * bytes_quant(rows, D, 6) + bytes_decode(1, n_tok, H, D, 6, 1, HQ)
+            + bytes_kivi(2, 1, KV["H"], KIVI_HI - KIVI_LO, KV["D"]))
+
+
+def cpu_baseline(seconds):
+    _cpu_inputs()
+    t0 = time.perf_counter()
+    total, n = 0, 0
+    while True:
+        total += cpu_sample_step()
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(total / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} x (1 layer K+V of 4,096 tokens x 4 heads x 256 quant-pack + dequant "
+                      f"(q6, page 16), decode attn over it (24 q heads), KIVI flush of 128 "
+                      f"tokens of 1 layer [1, 8, 4096, 64] K+V); {dt:.1f} s"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and rank != 0:
+        return
+    _cpu_inputs()
+    for _ in range(args.warmup):
+        cpu_sample_step()
+    t0 = time.perf_counter()
+    total = 0
+    for _ in range(args.steps):
+        total += cpu_sample_step()
+    dt = time.perf_counter() - t0
+    value = total / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": "paged_prefill_16L_8x32768_4x256 step, bounded sample per step",
+                   "bits": 6},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "per step: 1 layer K+V of 4,096 tokens (quant-pack + dequant "
+                                   "q6), decode attn over it, KIVI flush of 128 tokens of 1 "
+                                   "layer [1, 8, 4096, 64]"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
+    ap.add_argument("--bits", type=int, default=6, choices=[8, 6, 4])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-widths", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per launch of the dominant kernel, if captured")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "kvq":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,261 @@
+/*
+ * kvq.h -- C ABI of libkvq: quantized paged KV cache kernels for NVIDIA GB300 (sm_103a).
+ *
+ * Operations (each defined on the page cited at its declaration):
+ *   kvq_quant_pack_paged   symmetric per-token-per-head quantize + pack into paged storage
+ *   kvq_dequant_paged      gather + unpack + dequantize back to fp16
+ *   kivi_quant_dequant     KIVI asymmetric group quantize->dequantize, in place
+ *   kvq_decode_attn        decode attention that reads the packed pages directly
+ * plus host helpers: packed_dim, the KIVI residual boundary, and a page allocator.
+ *
+ * Conventions shared by every entry point
+ *   - The caller owns all memory.  The library never allocates or frees device memory and never
+ *     synchronizes a stream.  Pointers documented "device" must be device (or managed) memory;
+ *     "host" pointers are read before the call returns.
+ *   - fp16 values are passed as their 16-bit patterns (uint16_t).
+ *   - Every GPU entry point validates its arguments on the host first and returns a status
+ *     without launching anything if they are invalid.  Otherwise it enqueues its kernels on
+ *     `stream` (NULL = the legacy default stream) and returns KVQ_OK, or KVQ_ERR_CUDA if a launch
+ *     was rejected.  Asynchronous device faults surface at the caller's next synchronization.
+ *   - Kernels that read a page table check every page id they use against the pool size.  An id
+ *     outside [0, num_pages) or a logical page beyond max_pages is skipped (nothing is read or
+ *     written for that row) and, if `dev_err` is non-NULL, bit KVQ_DEVERR_PAGE_RANGE is OR-ed
+ *     into *dev_err (device int32, caller zeroes it).  The kernels never trap.
+ *   - kvq_last_error() returns a thread-local message describing the last non-OK status.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* kvq_stream_t;
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_BITS = 1,      /* bit width not in {8, 6, 4} (the explicit width table)            */
+  KVQ_ERR_SHAPE = 2,     /* head_dim / heads / group / range shape not supported              */
+  KVQ_ERR_NULL = 3,      /* a required pointer is NULL                                        */
+  KVQ_ERR_ALIGN = 4,     /* a device pointer is not 16-byte aligned                           */
+  KVQ_ERR_RANGE = 5,     /* a count or index is out of range                                  */
+  KVQ_ERR_CUDA = 6,      /* a CUDA launch or query failed                                     */
+  KVQ_ERR_NOMEM = 7,     /* the host page allocator has too few free pages                    */
+  KVQ_ERR_WORKSPACE = 8  /* the caller's workspace is too small                               */
+} kvq_status;
+
+/* Bits OR-ed into the optional device error word. */
+#define KVQ_DEVERR_PAGE_RANGE 1
+
+/* Maximum number of tensors one quant/dequant/KIVI call may batch, and of layers per decode
+ * attention call. */
+#define KVQ_MAX_TENSORS 64
+
+/*
+ * One page pool: the packed storage of one (layer, K-or-V) tensor.
+ *   codes  : device uint8  [num_pages][num_heads][page_size][packed_dim(head_dim, bits)]
+ *   scales : device fp16   [num_pages][num_heads][page_size]  (one scale per token per head)
+ * Token `pos` of sequence `s` lives in physical page page_table[s * max_pages + pos / page_size],
+ * slot pos % page_size.  Both arrays must be 16-byte aligned.  Within one page, the rows of one
+ * head are contiguous (page_size * packed_dim bytes).
+ */
+typedef struct kvq_pool {
+  int32_t bits;       /* 8, 6 or 4 */
+  int32_t num_heads;  /* KV heads H */
+  int32_t head_dim;   /* D: a multiple of 8, at most 256 */
+  int32_t page_size;  /* tokens per page, >= 1 */
+  int64_t num_pages;
+  uint8_t* codes;
+  uint16_t* scales;
+} kvq_pool;
+
+/* ---------------------------------------------------------------------------------------------
+ * Host helpers
+ * ------------------------------------------------------------------------------------------ */
+
+/* Library version string. */
+KVQ_API const char* kvq_version(void);
+
+/* Thread-local message for the last non-OK status returned on this thread ("" if none). */
+KVQ_API const char* kvq_last_error(void);
+
+/* Name of a status code. */
+KVQ_API const char* kvq_status_string(kvq_status status);
+
+/*
+ * Bytes per packed row.  MTPLX pull request #267, "feat(kv-cache): add q6 paged KV
+ * quantization", description, packed_dim sentence: packed_dim(D, 6) = D*3/4 and q6 needs
+ * D % 4 == 0; q8 stores one code per byte, q4 two per byte (D % 2 == 0).
+ * Returns -1 for an unknown width or an unsupported D (no error state is set).
+ */
+KVQ_API int kvq_packed_dim(int head_dim, int bits);
+
+/*
+ * KIVI residual-window boundary.  VeloxQuant-MLX source page "veloxquant_mlx.cache.kivi_cache",
+ * KIVIKVCache._quantization_boundary: the tokens older than the newest `residual_length`,
+ * snapped down to a multiple of `group_size`: ((max(0, offset - residual_length)) / group_size)
+ * * group_size.  Returns -1 if group_size < 1 or residual_length < 0.
+ */
+KVQ_API int kivi_boundary(int offset, int residual_length, int group_size);
+
+/*
+ * Host page allocator over page ids [0, num_pages) (a LIFO free list; not thread-safe).
+ * The pages themselves are the caller's kvq_pool memory; this only hands out ids.
+ * MTPLX pull request #267, description: cache allocation is width-generic through packed_dim --
+ * the allocator deals in pages, never in bytes.
+ */
+typedef struct kvq_allocator kvq_allocator;
+
+/* Returns NULL on bad size or host allocation failure. */
+KVQ_API kvq_allocator* kvq_alloc_create(int64_t num_pages);
+KVQ_API void kvq_alloc_destroy(kvq_allocator* a);
+KVQ_API int64_t kvq_alloc_free_count(const kvq_allocator* a);
+
+/* Take n page ids into out_ids (host int32[n]).  All or nothing: KVQ_ERR_NOMEM if fewer than n
+ * are free (nothing taken). */
+KVQ_API kvq_status kvq_alloc_pages(kvq_allocator* a, int64_t n, int32_t* out_ids);
+
+/* Return n page ids.  KVQ_ERR_RANGE (nothing returned) if an id is out of range, not currently
+ * allocated, or repeated in `ids`. */
+KVQ_API kvq_status kvq_free_pages(kvq_allocator* a, int64_t n, const int32_t* ids);
+
+/*
+ * Map the pages that an append of new_tokens[s] tokens at position cur_len[s] needs, for every
+ * sequence s: every logical page in [cur_len[s] / page_size, ceil((cur_len[s] + new_tokens[s]) /
+ * page_size)) whose entry in the host table page_table[s * max_pages + p] is negative gets a
+ * fresh page id.  Entries already >= 0 are kept (a partially filled tail page is appended into).
+ * All or nothing: on KVQ_ERR_NOMEM or KVQ_ERR_RANGE (a page beyond max_pages) the table is left
+ * unchanged.  The caller then copies the table to the device.
+ */
+KVQ_API kvq_status kvq_table_reserve(kvq_allocator* a, int32_t* page_table, int max_pages, int page_size,
+                             const int32_t* cur_len, const int32_t* new_tokens, int nseq);
+
+/* ---------------------------------------------------------------------------------------------
+ * Quantize + pack into pages
+ * ------------------------------------------------------------------------------------------ */
+
+/*
+ * MTPLX pull request #267, "feat(kv-cache): add q6 paged KV quantization", description:
+ * symmetric per-token-per-head quantizer with one fp16 scale per row, qmax 127 / 31 / 7 for
+ * 8 / 6 / 4 bits (bit-width table paragraph); q6 codes biased by +32 and packed four per three
+ * bytes, byte0 = u0 | (u1 & 3) << 6, byte1 = (u1 >> 2) | (u2 & 15) << 4,
+ * byte2 = (u2 >> 4) | (u3 & 63) << 2 (byte-layout formula).
+ *
+ * Per row x (one token, one KV head, D fp16):
+ *   scale = fp16_rne(float32(max_d |x_d|) / qmax)           (IEEE float32 divide)
+ *   c_d   = clamp(rint_half_even(float32(x_d) / float32(scale)), -qmax, qmax), or 0 if scale == 0
+ *   q8: byte = int8 two's complement of c; q6: u = c + 32, 4 -> 3 bytes as above;
+ *   q4: u = c + 8, element 2i in the low nibble of byte i.
+ *
+ * pools      host array [n_tensors]: the destination pools (all with the same bits, num_heads,
+ *            head_dim, page_size).
+ * x          host array [n_tensors] of device pointers, each fp16 [total_new_tokens][H][D],
+ *            16-byte aligned: the new rows of every sequence, sequence s owning rows
+ *            cu_new_tokens[s] .. cu_new_tokens[s+1]-1, which are its tokens start_pos[s],
+ *            start_pos[s]+1, ...
+ * page_table device int32 [nseq][max_pages], shared by every tensor of the call.
+ * cu_new_tokens device int32 [nseq+1], non-decreasing, cu[0] = 0, cu[nseq] = total_new_tokens.
+ * start_pos  device int32 [nseq].
+ * dev_err    optional device int32 error word (see the file header).
+ * Rows are independent; a row's packed bytes and scale are written whole.  Two rows of one call
+ * mapping to the same (page, slot) race (a caller error).
+ * Errors: KVQ_ERR_BITS, KVQ_ERR_SHAPE (D % 8, D > 256, mismatched pools), KVQ_ERR_NULL,
+ * KVQ_ERR_ALIGN, KVQ_ERR_RANGE (n_tensors not in [1, KVQ_MAX_TENSORS], nseq < 0,
+ * total_new_tokens < 0, max_pages < 1), KVQ_ERR_CUDA.
+ */
+KVQ_API kvq_status kvq_quant_pack_paged(const kvq_pool* pools, const uint16_t* const* x, int n_tensors,
+                                const int32_t* page_table, int max_pages,
+                                const int32_t* cu_new_tokens, const int32_t* start_pos, int nseq,
+                                int total_new_tokens, int32_t* dev_err, kvq_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Gather + unpack + dequantize
+ * ------------------------------------------------------------------------------------------ */
+
+/*
+ * MTPLX pull request #267, description: dequantization runs over the active window; the inverse
+ * of kvq_quant_pack_paged: x_hat_d = fp16_rne(float32(c_d) * float32(scale)) (the product is
+ * exact in float32).
+ *
+ * Same addressing as kvq_quant_pack_paged: out[i] (host array of device pointers, each fp16
+ * [total_tokens][H][D], 16-byte aligned) receives rows cu_tokens[s] .. cu_tokens[s+1]-1 =
+ * tokens start_pos[s], start_pos[s]+1, ... of sequence s.  Rows whose page id is out of range
+ * are left untouched.  Errors as for kvq_quant_pack_paged.
+ */
+KVQ_API kvq_status kvq_dequant_paged(const kvq_pool* pools, uint16_t* const* out, int n_tensors,
+                             const int32_t* page_table, int max_pages, const int32_t* cu_tokens,
+                             const int32_t* start_pos, int nseq, int total_tokens,
+                             int32_t* dev_err, kvq_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * KIVI group quantize -> dequantize, in place
+ * ------------------------------------------------------------------------------------------ */
+
+/*
+ * VeloxQuant-MLX source page "veloxquant_mlx.cache.kivi_cache", KIVIKVCache._quant_dequant_along
+ * and update_and_fetch.  For every tensor i, the token slice [lo, hi) of x[i] (device fp16
+ * [B][H][S][D], 16-byte aligned, modified in place) is round-tripped in float32:
+ *   keys   (is_key[i] != 0): per channel, groups of group_size tokens starting at lo;
+ *   values (is_key[i] == 0): per token, groups of group_size channels starting at channel 0;
+ *   a ragged last group uses only its real elements (the page pads it with its last element,
+ *   which leaves min and max unchanged);
+ *   scale = max((gmax - gmin) / levels, eps); c = clamp(rint_half_even((x - gmin) / scale), 0,
+ *   levels); y = fp16_rne((c * scale) + gmin) with two roundings (no fused multiply-add).
+ * is_key     host int32 [n_tensors].
+ * levels     2^b - 1 for b-bit KIVI (the page's default b = 2 gives 3); >= 1.
+ * eps        the page's 1e-8 (as float32).
+ * Use kivi_boundary() for hi and the previous frontier for lo (update_and_fetch).
+ * Errors: KVQ_ERR_SHAPE (D % 8, D > 256, 0 <= lo <= hi <= S violated, group_size < 1,
+ * levels < 1), KVQ_ERR_NULL, KVQ_ERR_ALIGN, KVQ_ERR_RANGE (n_tensors, B, H, S), KVQ_ERR_CUDA.
+ * An empty slice (lo == hi) launches nothing and returns KVQ_OK.
+ */
+KVQ_API kvq_status kivi_quant_dequant(uint16_t* const* x, const int32_t* is_key, int n_tensors, int B,
+                              int H, int S, int D, int lo, int hi, int group_size, int levels,
+                              float eps, kvq_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Decode attention over packed pages
+ * ------------------------------------------------------------------------------------------ */
+
+/*
+ * Attention for one decode query per sequence over that sequence's whole packed cache, reading
+ * the packed pages directly (MTPLX pull request #267, description: the reference path instead
+ * dequantizes to fp16 and runs SDPA; this computes the same function without materialising fp16).
+ * For layer l, sequence s, query head j (KV head h = j / (Hq / H)):
+ *   s_t = softmax_scale * sum_d q[l][s][j][d] * k_hat_t[d],   t in [0, seq_lens[s])
+ *   out[l][s][j][:] = sum_t softmax(s)_t * v_hat_t[:]    (float32 accumulation)
+ * where k_hat, v_hat are the fp16 dequantized rows of k_pools[l], v_pools[l].
+ * k_pools, v_pools host arrays [n_layers] (same bits/H/D/page_size for all).
+ * q          device fp16 [n_layers][nseq][num_q_heads][D], 16-byte aligned.
+ * out        device float32 [n_layers][nseq][num_q_heads][D]; a sequence of length 0 gets 0.
+ * page_table device int32 [nseq][max_pages] (shared by all layers); seq_lens device int32 [nseq].
+ * max_seq_len host upper bound on seq_lens (sizes the split over tokens).
+ * workspace  device scratch of at least kvq_decode_attn_workspace(...) bytes, 16-byte aligned;
+ *            its contents need no initialisation and are garbage afterwards.
+ * Errors: KVQ_ERR_SHAPE (num_q_heads % H, num_q_heads / H > 8, D != 256 for now), KVQ_ERR_BITS,
+ * KVQ_ERR_NULL, KVQ_ERR_ALIGN, KVQ_ERR_RANGE, KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA.
+ */
+KVQ_API size_t kvq_decode_attn_workspace(int n_layers, int nseq, int num_kv_heads, int num_q_heads,
+                                 int head_dim, int page_size, int max_seq_len);
+
+KVQ_API kvq_status kvq_decode_attn(const kvq_pool* k_pools, const kvq_pool* v_pools, int n_layers,
+                           const uint16_t* q, int num_q_heads, const int32_t* page_table,
+                           int max_pages, const int32_t* seq_lens, int nseq, int max_seq_len,
+                           float softmax_scale, float* out, void* workspace,
+                           size_t workspace_bytes, int32_t* dev_err, kvq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,323 @@
+"""Python binding of libkvq (quantized paged KV cache kernels for GB300, sm_103a).
+
+Argument marshalling only: every step of the hot path runs in the CUDA library's kernels.  The
+functions carry the C ABI's names (``include/kvq.h``) and take torch tensors for device memory;
+they enqueue work on the current torch stream (or the one given) and never synchronize.
+
+There is no fallback: if ``libkvq.so`` cannot be loaded, importing this package raises.
+Build it with ``python -c "import __graft_entry__ as g; g.build()"`` or
+``python -m paged_kv_cache_fp16_gb300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvq.so")
+
+KVQ_MAX_TENSORS = 64
+KVQ_DEVERR_PAGE_RANGE = 1
+STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_BITS", 2: "KVQ_ERR_SHAPE", 3: "KVQ_ERR_NULL",
+          4: "KVQ_ERR_ALIGN", 5: "KVQ_ERR_RANGE", 6: "KVQ_ERR_CUDA", 7: "KVQ_ERR_NOMEM",
+          8: "KVQ_ERR_WORKSPACE"}
+
+
+class KVQError(RuntimeError):
+    """A libkvq entry point returned a non-OK status."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class kvq_pool(ctypes.Structure):
+    _fields_ = [("bits", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_pages", ctypes.c_int64), ("codes", ctypes.c_void_p),
+                ("scales", ctypes.c_void_p)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libkvq.so is not built ({LIB_PATH} missing); run paged_kv_cache_fp16_gb300.build")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, I64, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    pool_p = ctypes.POINTER(kvq_pool)
+    sig = {
+        "kvq_version": (ctypes.c_char_p, []),
+        "kvq_last_error": (ctypes.c_char_p, []),
+        "kvq_status_string": (ctypes.c_char_p, [I]),
+        "kvq_packed_dim": (I, [I, I]),
+        "kivi_boundary": (I, [I, I, I]),
+        "kvq_alloc_create": (P, [I64]),
+        "kvq_alloc_destroy": (None, [P]),
+        "kvq_alloc_free_count": (I64, [P]),
+        "kvq_alloc_pages": (I, [P, I64, P]),
+        "kvq_free_pages": (I, [P, I64, P]),
+        "kvq_table_reserve": (I, [P, P, I, I, P, P, I]),
+        "kvq_quant_pack_paged": (I, [pool_p, P, I, P, I, P, P, I, I, P, P]),
+        "kvq_dequant_paged": (I, [pool_p, P, I, P, I, P, P, I, I, P, P]),
+        "kivi_quant_dequant": (I, [P, P, I, I, I, I, I, I, I, I, I, F, P]),
+        "kvq_decode_attn_workspace": (S, [I, I, I, I, I, I, I]),
+        "kvq_decode_attn": (I, [pool_p, pool_p, I, P, I, P, I, P, I, I, F, P, P, S, P, P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise KVQError(status, _lib.kvq_last_error().decode())
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        if torch.cuda.is_available():
+            return torch.cuda.current_stream().cuda_stream
+        return None
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr_array(tensors: Sequence[torch.Tensor]):
+    arr = (ctypes.c_void_p * len(tensors))()
+    for i, t in enumerate(tensors):
+        arr[i] = t.data_ptr()
+    return arr
+
+
+def _cuda_tensor(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+# ------------------------------------------------------------------------------- host helpers
+def kvq_version() -> str:
+    return _lib.kvq_version().decode()
+
+
+def kvq_packed_dim(head_dim: int, bits: int) -> int:
+    return _lib.kvq_packed_dim(head_dim, bits)
+
+
+def kivi_boundary(offset: int, residual_length: int = 128, group_size: int = 32) -> int:
+    return _lib.kivi_boundary(offset, residual_length, group_size)
+
+
+_MODES = {"q8": 8, "8": 8, "int8": 8, "q6": 6, "6": 6, "6bit": 6, "int6": 6, "uint6": 6,
+          "q4": 4, "4": 4, "int4": 4}
+
+
+def parse_mode(mode) -> int:
+    """Quantization width from a mode name.  q6 aliases stay narrow (q6, 6, 6bit, int6, uint6);
+    llama.cpp-style names such as q6_k or q6_0 are a different format and are rejected
+    (MTPLX pull request #267, description, aliases paragraph)."""
+    key = str(mode).strip().lower()
+    if key not in _MODES:
+        raise ValueError(f"unknown KV quantization mode {mode!r}")
+    return _MODES[key]
+
+
+@dataclass
+class Pool:
+    """Packed storage of one (layer, K-or-V) tensor: codes [num_pages, H, page_size, pd] uint8 and
+    scales [num_pages, H, page_size] fp16."""
+    bits: int
+    num_heads: int
+    head_dim: int
+    page_size: int
+    codes: torch.Tensor
+    scales: torch.Tensor
+
+    @staticmethod
+    def empty(bits, num_heads, head_dim, page_size, num_pages, device="cuda"):
+        pd = kvq_packed_dim(head_dim, bits)
+        if pd < 0:
+            raise ValueError("unsupported bits / head_dim")
+        codes = torch.empty((num_pages, num_heads, page_size, pd), dtype=torch.uint8,
+                            device=device)
+        scales = torch.empty((num_pages, num_heads, page_size), dtype=torch.float16,
+                             device=device)
+        return Pool(bits, num_heads, head_dim, page_size, codes, scales)
+
+    @property
+    def num_pages(self) -> int:
+        return self.codes.shape[0]
+
+    def as_c(self) -> kvq_pool:
+        return kvq_pool(self.bits, self.num_heads, self.head_dim, self.page_size,
+                        self.num_pages, self.codes.data_ptr(), self.scales.data_ptr())
+
+
+def _pool_array(pools: Sequence[Pool]):
+    arr = (kvq_pool * len(pools))()
+    for i, p in enumerate(pools):
+        arr[i] = p.as_c()
+    return arr
+
+
+class Allocator:
+    """Host page allocator (kvq_alloc_*): hands out page ids of a pool."""
+
+    def __init__(self, num_pages: int):
+        self._h = _lib.kvq_alloc_create(num_pages)
+        if not self._h:
+            raise ValueError("kvq_alloc_create failed")
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            _lib.kvq_alloc_destroy(h)
+            self._h = None
+
+    @property
+    def free_count(self) -> int:
+        return _lib.kvq_alloc_free_count(self._h)
+
+    def alloc(self, n: int) -> torch.Tensor:
+        out = torch.empty(n, dtype=torch.int32)
+        _check(_lib.kvq_alloc_pages(self._h, n, out.data_ptr()))
+        return out
+
+    def free(self, ids: torch.Tensor) -> None:
+        ids = ids.to(torch.int32).contiguous().cpu()
+        _check(_lib.kvq_free_pages(self._h, ids.numel(), ids.data_ptr()))
+
+    def reserve(self, page_table: torch.Tensor, page_size: int, cur_len, new_tokens) -> None:
+        """Map pages for appends into a host int32 table [nseq, max_pages] (-1 = unmapped)."""
+        if page_table.is_cuda or page_table.dtype != torch.int32 or not page_table.is_contiguous():
+            raise TypeError("page_table must be a contiguous host int32 tensor")
+        cur = torch.as_tensor(cur_len, dtype=torch.int32).contiguous()
+        new = torch.as_tensor(new_tokens, dtype=torch.int32).contiguous()
+        nseq, max_pages = page_table.shape
+        _check(_lib.kvq_table_reserve(self._h, page_table.data_ptr(), max_pages, page_size,
+                                      cur.data_ptr(), new.data_ptr(), nseq))
+
+
+# ------------------------------------------------------------------------------- kernels
+def _check_table(page_table: torch.Tensor, nseq: int, n_cu: int) -> None:
+    if page_table.dim() != 2 or page_table.shape[0] < nseq:
+        raise ValueError("page_table must be [nseq, max_pages] with a row per sequence")
+    if n_cu != nseq + 1:
+        raise ValueError("cu tensor must have nseq + 1 entries")
+
+
+def kvq_quant_pack_paged(pools: Sequence[Pool], xs: Sequence[torch.Tensor],
+                         page_table: torch.Tensor, cu_new_tokens: torch.Tensor,
+                         start_pos: torch.Tensor, dev_err: torch.Tensor | None = None,
+                         stream=None) -> None:
+    """Quantize + pack new rows xs[i] (fp16 [total, H, D]) into pools[i] through page_table."""
+    if len(pools) != len(xs):
+        raise ValueError("one input tensor per pool")
+    for i, x in enumerate(xs):
+        _cuda_tensor(x, torch.float16, f"xs[{i}]")
+    _cuda_tensor(page_table, torch.int32, "page_table")
+    _cuda_tensor(cu_new_tokens, torch.int32, "cu_new_tokens")
+    _cuda_tensor(start_pos, torch.int32, "start_pos")
+    total = xs[0].shape[0] if xs else 0
+    _check_table(page_table, start_pos.numel(), cu_new_tokens.numel())
+    _check(_lib.kvq_quant_pack_paged(_pool_array(pools), _ptr_array(xs), len(xs),
+                                     page_table.data_ptr(), page_table.shape[1],
+                                     cu_new_tokens.data_ptr(), start_pos.data_ptr(),
+                                     start_pos.numel(), total, _ptr(dev_err), _stream(stream)))
+
+
+def kvq_dequant_paged(pools: Sequence[Pool], outs: Sequence[torch.Tensor],
+                      page_table: torch.Tensor, cu_tokens: torch.Tensor, start_pos: torch.Tensor,
+                      dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """Gather + dequantize rows of pools[i] into outs[i] (fp16 [total, H, D])."""
+    if len(pools) != len(outs):
+        raise ValueError("one output tensor per pool")
+    for i, o in enumerate(outs):
+        _cuda_tensor(o, torch.float16, f"outs[{i}]")
+    _cuda_tensor(page_table, torch.int32, "page_table")
+    _cuda_tensor(cu_tokens, torch.int32, "cu_tokens")
+    _cuda_tensor(start_pos, torch.int32, "start_pos")
+    total = outs[0].shape[0] if outs else 0
+    _check_table(page_table, start_pos.numel(), cu_tokens.numel())
+    _check(_lib.kvq_dequant_paged(_pool_array(pools), _ptr_array(outs), len(outs),
+                                  page_table.data_ptr(), page_table.shape[1],
+                                  cu_tokens.data_ptr(), start_pos.data_ptr(), start_pos.numel(),
+                                  total, _ptr(dev_err), _stream(stream)))
+
+
+def kivi_quant_dequant(xs: Sequence[torch.Tensor], is_key: Sequence[bool], lo: int, hi: int,
+                       group_size: int = 32, levels: int = 3, eps: float = 1e-8,
+                       stream=None) -> None:
+    """In-place KIVI round trip of tokens [lo, hi) of every fp16 [B, H, S, D] tensor."""
+    if len(xs) != len(is_key):
+        raise ValueError("one is_key flag per tensor")
+    for i, x in enumerate(xs):
+        _cuda_tensor(x, torch.float16, f"xs[{i}]")
+        if x.dim() != 4 or x.shape != xs[0].shape:
+            raise ValueError("all tensors must be [B, H, S, D] of one shape")
+    B, H, S, D = xs[0].shape
+    flags = (ctypes.c_int32 * len(xs))(*[1 if k else 0 for k in is_key])
+    _check(_lib.kivi_quant_dequant(_ptr_array(xs), flags, len(xs), B, H, S, D, lo, hi,
+                                   group_size, levels, eps, _stream(stream)))
+
+
+def kvq_decode_attn_workspace(n_layers: int, nseq: int, num_kv_heads: int, num_q_heads: int,
+                              head_dim: int, page_size: int, max_seq_len: int) -> int:
+    return _lib.kvq_decode_attn_workspace(n_layers, nseq, num_kv_heads, num_q_heads, head_dim,
+                                          page_size, max_seq_len)
+
+
+def kvq_decode_attn(k_pools: Sequence[Pool], v_pools: Sequence[Pool], q: torch.Tensor,
+                    page_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                    softmax_scale: float, out: torch.Tensor, workspace: torch.Tensor,
+                    dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """Decode attention over packed pages: q fp16 [n_layers, nseq, Hq, D] -> out float32."""
+    if len(k_pools) != len(v_pools):
+        raise ValueError("one V pool per K pool")
+    _cuda_tensor(q, torch.float16, "q")
+    _cuda_tensor(out, torch.float32, "out")
+    _cuda_tensor(page_table, torch.int32, "page_table")
+    _cuda_tensor(seq_lens, torch.int32, "seq_lens")
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous CUDA tensor")
+    n_layers, nseq, hq, _ = q.shape
+    if page_table.dim() != 2 or page_table.shape[0] < nseq or seq_lens.numel() < nseq:
+        raise ValueError("page_table needs a row and seq_lens an entry per sequence")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    _check(_lib.kvq_decode_attn(_pool_array(k_pools), _pool_array(v_pools), n_layers,
+                                q.data_ptr(), hq, page_table.data_ptr(), page_table.shape[1],
+                                seq_lens.data_ptr(), nseq, max_seq_len, softmax_scale,
+                                out.data_ptr(), workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(), _ptr(dev_err),
+                                _stream(stream)))
+
+
+def decode_workspace(k_pools: Sequence[Pool], nseq: int, num_q_heads: int, max_seq_len: int,
+                     device="cuda") -> torch.Tensor:
+    """A workspace tensor of the size kvq_decode_attn needs."""
+    p = k_pools[0]
+    n = kvq_decode_attn_workspace(len(k_pools), nseq, p.num_heads, num_q_heads, p.head_dim,
+                                  p.page_size, max_seq_len)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+__all__ = ["KVQError", "Pool", "Allocator", "parse_mode", "kvq_version", "kvq_packed_dim",
+           "kivi_boundary", "kvq_quant_pack_paged", "kvq_dequant_paged", "kivi_quant_dequant",
+           "kvq_decode_attn_workspace", "kvq_decode_attn", "decode_workspace", "LIB_PATH"]

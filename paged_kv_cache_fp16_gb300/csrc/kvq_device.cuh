@@ -1,0 +1,88 @@
+// Device-side helpers shared by the libkvq kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// A pool as the kernels see it (bits/H/D/page_size are uniform per call and passed separately).
+struct PoolRef {
+  uint8_t* codes;
+  uint16_t* scales;
+  int64_t num_pages;
+};
+
+__device__ __forceinline__ void report(int32_t* err, int bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// Streaming 16-byte load that does not allocate in L1 (input read exactly once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint2 ld_nc_v2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint16_t ld_nc_u16(const void* p) {
+  uint16_t r;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  return r;
+}
+
+// Largest s in [0, nseq) with cu[s] <= i.  For a well-formed cu (non-decreasing, cu[0] = 0,
+// i < cu[nseq]) this is the sequence that owns new-token row i; for any cu it stays in range.
+__device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu, int nseq, int i) {
+  int lo = 0, hi = nseq - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= i) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Physical row index ((page * H + h) * page_size + slot) of token `pos` of sequence `s`,
+// or -1 (and the error bit) if the logical or physical page is out of range.
+__device__ __forceinline__ int64_t locate_row(const int32_t* __restrict__ page_table,
+                                              int max_pages, int page_size, int num_heads,
+                                              int64_t num_pages, int s, int64_t pos, int h,
+                                              int32_t* err) {
+  if (pos < 0) { report(err, KVQ_DEVERR_PAGE_RANGE); return -1; }
+  int64_t lp = pos / page_size;
+  if (lp >= max_pages) { report(err, KVQ_DEVERR_PAGE_RANGE); return -1; }
+  int slot = static_cast<int>(pos - lp * page_size);
+  int page = __ldg(page_table + static_cast<int64_t>(s) * max_pages + lp);
+  if (page < 0 || page >= num_pages) { report(err, KVQ_DEVERR_PAGE_RANGE); return -1; }
+  return (static_cast<int64_t>(page) * num_heads + h) * page_size + slot;
+}
+
+__device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+__device__ __forceinline__ uint16_t f2h(float f) { return __half_as_ushort(__float2half_rn(f)); }
+
+}  // namespace kvq

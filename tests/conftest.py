@@ -17,3 +17,20 @@ def pytest_configure(config):
 
 def golden_path(name: str) -> str:
     return os.path.join(GOLDEN, name)
+
+
+@pytest.fixture(scope="session")
+def kvq():
+    """The built package (builds libkvq.so in-tree first if needed)."""
+    from paged_kv_cache_fp16_gb300 import build as _b
+    _b.build()
+    import paged_kv_cache_fp16_gb300 as pkg
+    return pkg
+
+
+@pytest.fixture(scope="session")
+def cuda_dev():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")

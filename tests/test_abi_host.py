@@ -1,0 +1,195 @@
+"""C-ABI library (no GPU needed): it loads, exports every symbol include/kvq.h declares, and its
+host logic (packed_dim, KIVI boundary, page allocator, argument validation) behaves as
+specified.  No call here launches a kernel: every invalid argument is rejected on the host."""
+import ctypes
+import json
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+from conftest import ROOT, golden_path
+from oracle import kivi as okivi
+from oracle import symmetric as osym
+
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"KVQ_API[^;(]*?\b((?:kvq|kivi)_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(kvq):
+    names = _declared()
+    assert len(names) >= 16
+    lib = ctypes.CDLL(kvq.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", kvq.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = set(re.findall(r" T ((?:kvq|kivi)_\w+)", out))
+    assert set(names) == exported
+
+
+def test_version_and_status_strings(kvq):
+    assert "sm_103a" in kvq.kvq_version()
+    assert kvq._lib.kvq_status_string(6) == b"KVQ_ERR_CUDA"
+
+
+def test_packed_dim_matches_oracle(kvq):
+    for bits in (8, 6, 4):
+        for d in range(1, 300):
+            try:
+                expect = osym.packed_dim(d, bits)
+            except ValueError:
+                expect = -1
+            assert kvq.kvq_packed_dim(d, bits) == expect, (d, bits)
+    for bits in (0, 2, 5, 7, 16):
+        assert kvq.kvq_packed_dim(256, bits) == -1
+    assert kvq.kvq_packed_dim(256, 6) == 192
+
+
+def test_kivi_boundary_matches_golden_and_oracle(kvq):
+    g = json.load(open(golden_path("kivi_groups.json")))["boundary"]
+    for off, b in g["cases"]:
+        assert kvq.kivi_boundary(off, g["residual_length"], g["group_size"]) == b
+    for off in range(0, 700, 7):
+        for R in (0, 1, 128):
+            for gs in (1, 5, 32):
+                assert kvq.kivi_boundary(off, R, gs) == okivi.quantization_boundary(off, R, gs)
+    assert kvq.kivi_boundary(10, 0, 0) == -1 and kvq.kivi_boundary(10, -1, 4) == -1
+
+
+def test_parse_mode_aliases(kvq):
+    for m in ("q6", "6", "6bit", "int6", "uint6", 6, "Q6"):
+        assert kvq.parse_mode(m) == 6
+    assert kvq.parse_mode("q8") == 8 and kvq.parse_mode("q4") == 4
+    for bad in ("q6_k", "q6_0", "q5", "fp16", ""):
+        with pytest.raises(ValueError):
+            kvq.parse_mode(bad)
+
+
+def test_allocator(kvq):
+    a = kvq.Allocator(10)
+    assert a.free_count == 10
+    ids = a.alloc(4)
+    assert sorted(ids.tolist()) == [0, 1, 2, 3] and a.free_count == 6
+    with pytest.raises(kvq.KVQError) as e:
+        a.alloc(7)
+    assert e.value.status == 7 and a.free_count == 6          # all or nothing
+    with pytest.raises(kvq.KVQError):
+        a.free(ids.new_tensor([1, 1]))                        # repeated id
+    with pytest.raises(kvq.KVQError):
+        a.free(ids.new_tensor([9]))                           # not allocated
+    with pytest.raises(kvq.KVQError):
+        a.free(ids.new_tensor([10]))                          # out of range
+    assert a.free_count == 6
+    a.free(ids[:2])
+    assert a.free_count == 8
+    with pytest.raises(kvq.KVQError):
+        a.free(ids[:1])                                       # double free
+    more = a.alloc(8)
+    assert len(set(more.tolist()) | set(ids[2:].tolist())) == 10 and a.free_count == 0
+
+
+def test_table_reserve_appends_into_partial_pages(kvq):
+    import torch
+    a = kvq.Allocator(100)
+    pt = torch.full((3, 8), -1, dtype=torch.int32)
+    a.reserve(pt, 16, [0, 0, 0], [16, 17, 0])
+    assert (pt[0, :1] >= 0).all() and (pt[0, 1:] == -1).all()
+    assert (pt[1, :2] >= 0).all() and (pt[1, 2:] == -1).all()
+    assert (pt[2] == -1).all()
+    before = pt.clone()
+    a.reserve(pt, 16, [16, 17, 0], [1, 14, 0])          # seq 1 fills its partial page 1
+    assert (pt[0, 1] >= 0) and torch.equal(pt[1], before[1])
+    used = pt[pt >= 0]
+    assert used.unique().numel() == used.numel() == a.free_count * 0 + (100 - a.free_count)
+    with pytest.raises(kvq.KVQError) as e:                  # beyond max_pages: unchanged
+        a.reserve(pt, 16, [0, 0, 0], [0, 0, 16 * 9])
+    assert e.value.status == 5
+    snap, free = pt.clone(), a.free_count
+    small = kvq.Allocator(1)
+    with pytest.raises(kvq.KVQError) as e:
+        small.reserve(pt, 16, [0, 0, 0], [0, 0, 40])        # needs 3, has 1
+    assert e.value.status == 7 and torch.equal(pt, snap) and small.free_count == 1
+
+
+# --------------------------------------------------------------------- host validation
+FAKE = 0x10000  # aligned, never dereferenced: validation fails first
+
+
+def _pool(kvq, bits=6, H=4, D=256, ps=16, pages=8, codes=FAKE, scales=FAKE):
+    return kvq.kvq_pool(bits, H, D, ps, pages, codes, scales)
+
+
+def _qp(kvq, pool, n=1, x=FAKE, total=16, nseq=1, max_pages=4, pt=FAKE, cu=FAKE, st=FAKE):
+    pools = (kvq.kvq_pool * max(n, 1))(*([pool] * max(n, 1)))
+    xs = (ctypes.c_void_p * max(n, 1))(*([x] * max(n, 1)))
+    return kvq._lib.kvq_quant_pack_paged(pools, xs, n, pt, max_pages, cu, st, nseq, total, None,
+                                         None)
+
+
+def test_quant_pack_rejects_bad_arguments_before_launch(kvq):
+    assert _qp(kvq, _pool(kvq, bits=5)) == 1
+    assert _qp(kvq, _pool(kvq, bits=16)) == 1
+    assert _qp(kvq, _pool(kvq, D=12)) == 2
+    assert _qp(kvq, _pool(kvq, D=264)) == 2
+    assert _qp(kvq, _pool(kvq, H=0)) == 2
+    assert _qp(kvq, _pool(kvq, ps=0)) == 2
+    assert _qp(kvq, _pool(kvq, codes=0)) == 3
+    assert _qp(kvq, _pool(kvq, scales=FAKE + 2)) == 4
+    assert _qp(kvq, _pool(kvq), x=FAKE + 8) == 4
+    assert _qp(kvq, _pool(kvq), x=0) == 3
+    assert _qp(kvq, _pool(kvq), n=0) == 5
+    assert _qp(kvq, _pool(kvq), n=65) == 5
+    assert _qp(kvq, _pool(kvq), total=-1) == 5
+    assert _qp(kvq, _pool(kvq), max_pages=0) == 5
+    assert _qp(kvq, _pool(kvq), pt=0) == 3
+    assert b"KVQ_ERR_NULL" in kvq._lib.kvq_last_error()
+    # mismatched pools in one call
+    pools = (kvq.kvq_pool * 2)(_pool(kvq), _pool(kvq, bits=8))
+    xs = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    assert kvq._lib.kvq_quant_pack_paged(pools, xs, 2, FAKE, 4, FAKE, FAKE, 1, 16, None,
+                                         None) == 2
+
+
+def test_dequant_rejects_bad_arguments_before_launch(kvq):
+    pools = (kvq.kvq_pool * 1)(_pool(kvq, bits=3))
+    xs = (ctypes.c_void_p * 1)(FAKE)
+    assert kvq._lib.kvq_dequant_paged(pools, xs, 1, FAKE, 4, FAKE, FAKE, 1, 16, None, None) == 1
+
+
+def test_kivi_rejects_bad_arguments_before_launch(kvq):
+    xs = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    flags = (ctypes.c_int32 * 2)(1, 0)
+    f = kvq._lib.kivi_quant_dequant
+    assert f(xs, flags, 2, 1, 1, 64, 12, 0, 32, 32, 3, 1e-8, None) == 2     # D % 8
+    assert f(xs, flags, 2, 1, 1, 64, 64, 40, 32, 32, 3, 1e-8, None) == 2    # lo > hi
+    assert f(xs, flags, 2, 1, 1, 64, 64, 0, 65, 32, 3, 1e-8, None) == 2     # hi > S
+    assert f(xs, flags, 2, 1, 1, 64, 64, 0, 32, 0, 3, 1e-8, None) == 2      # group 0
+    assert f(xs, flags, 2, 1, 1, 64, 64, 0, 32, 32, 0, 1e-8, None) == 2     # levels 0
+    assert f(xs, flags, 0, 1, 1, 64, 64, 0, 32, 32, 3, 1e-8, None) == 5
+    bad = (ctypes.c_void_p * 2)(FAKE, FAKE + 4)
+    assert f(bad, flags, 2, 1, 1, 64, 64, 0, 32, 32, 3, 1e-8, None) == 4
+    assert f(xs, flags, 2, 1, 1, 64, 64, 16, 16, 32, 3, 1e-8, None) == 0    # empty: no launch
+
+
+def test_decode_attn_rejects_bad_arguments_before_launch(kvq):
+    f = kvq._lib.kvq_decode_attn
+    P = lambda **kw: (kvq.kvq_pool * 1)(_pool(kvq, **kw))
+    args = lambda kp, vp, hq=24, ws=1 << 30, maxlen=64: f(kp, vp, 1, FAKE, hq, FAKE, 4, FAKE, 1,
+                                                         maxlen, 0.0625, FAKE, FAKE, ws, None,
+                                                         None)
+    assert args(P(D=128), P(D=128)) == 2            # head_dim 256 only
+    assert args(P(), P(bits=8)) == 2                # K/V mismatch
+    assert args(P(), P(), hq=18) == 2               # 18 % 4
+    assert args(P(), P(), hq=36) == 2               # 9 query heads per KV head
+    assert args(P(), P(), ws=16) == 8               # workspace too small
+    assert args(P(), P(), maxlen=65) == 5           # beyond max_pages * page_size
+    assert args(P(bits=7), P(bits=7)) == 1
+    need = kvq.kvq_decode_attn_workspace(16, 1, 4, 24, 256, 16, 262144)
+    assert need > 0 and need % 16 == 0
