@@ -6,7 +6,7 @@ they enqueue work on the current torch stream (or the one given) and never synch
 
 There is no fallback: if ``libkvq.so`` cannot be loaded, importing this package raises.
 Build it with ``python -c "import __graft_entry__ as g; g.build()"`` or
-``python -m paged_kv_cache_fp16_gb300.build``.
+``python paged_kv_cache_fp16_gb300/build.py``.
 """
 from __future__ import annotations
 
@@ -45,7 +45,7 @@ class kvq_pool(ctypes.Structure):
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
-            f"libkvq.so is not built ({LIB_PATH} missing); run paged_kv_cache_fp16_gb300.build")
+            f"libkvq.so is not built ({LIB_PATH} missing); run paged_kv_cache_fp16_gb300/build.py")
     lib = ctypes.CDLL(LIB_PATH)
     P, I, I64, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     pool_p = ctypes.POINTER(kvq_pool)

@@ -22,8 +22,8 @@ def golden_path(name: str) -> str:
 @pytest.fixture(scope="session")
 def kvq():
     """The built package (builds libkvq.so in-tree first if needed)."""
-    from paged_kv_cache_fp16_gb300 import build as _b
-    _b.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import paged_kv_cache_fp16_gb300 as pkg
     return pkg
 
