@@ -165,12 +165,12 @@ def max_over_ranks(x: float, world: int, device) -> float:
 
 # ----------------------------------------------------------------------------- GPU arm
 class Workload:
-    """Device-resident inputs and outputs of one replica."""
+    """Device-resident inputs and outputs of one replica (outputs allocated on first use)."""
 
-    def __init__(self, kvq, dev, bits):
+    def __init__(self, kvq, dev, bits, layers=None):
         self.kvq, self.dev = kvq, dev
-        L, nseq, ntok, H, D, ps = (WL["n_layers"], WL["n_seq"], WL["n_tok"], WL["H"], WL["D"],
-                                   WL["page_size"])
+        L = WL["n_layers"] if layers is None else layers
+        nseq, ntok, H, D, ps = WL["n_seq"], WL["n_tok"], WL["H"], WL["D"], WL["page_size"]
         self.L, self.nseq, self.ntok, self.H, self.D, self.ps = L, nseq, ntok, H, D, ps
         self.specs = [kvgen.KVSpec(seed=WL["seed"], layer=l, is_key=k, n_seq=nseq, n_tok=ntok,
                                    num_heads=H, head_dim=D)
@@ -183,24 +183,56 @@ class Workload:
         self.start = torch.zeros(nseq, dtype=torch.int32, device=dev)
         self.lens = torch.full((nseq,), ntok, dtype=torch.int32, device=dev)
         self.lens1 = torch.tensor([nseq * ntok], dtype=torch.int32, device=dev)
-        self.pools = {}
         self.bits = bits
-        self.pools[bits] = self.make_pools(bits)
-        self.deq = [torch.empty_like(t) for t in self.x]
-        self.q = kvgen.queries_torch(WL["seed"], L, nseq, HQ, D, dev)
-        self.q1 = kvgen.queries_torch(WL["seed"] + 1, L, 1, HQ, D, dev)
-        self.out = torch.empty((L, nseq, HQ, D), dtype=torch.float32, device=dev)
-        self.out1 = torch.empty((L, 1, HQ, D), dtype=torch.float32, device=dev)
-        p0 = self.pools[bits][0]
-        self.ws = kvq.decode_workspace(self.pools[bits][0::2], nseq, HQ, ntok, dev)
-        self.ws1 = kvq.decode_workspace(self.pools[bits][0::2], 1, HQ, nseq * ntok, dev)
-        del p0
-        self.kivi = [kvgen.KiviSpec(seed=KV["seed"], layer=l, is_key=k, batch=KV["B"],
-                                    num_heads=KV["H"], seq=KV["S"], head_dim=KV["D"]
-                                    ).full_torch(dev)
-                     for l in range(KV["n_layers"]) for k in (True, False)]
-        self.kivi_flags = [k for _ in range(KV["n_layers"]) for k in (True, False)]
+        self.pools = {bits: self.make_pools(bits)}
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self._deq = self._dec = self._dec1 = self._kivi = None
+        self.kivi_layers = KV["n_layers"] if layers is None else layers
+
+    @property
+    def deq(self):
+        if self._deq is None:
+            self._deq = [torch.empty_like(t) for t in self.x]
+        return self._deq
+
+    def dec_buffers(self, full_context=False):
+        if full_context:
+            if self._dec1 is None:
+                q = kvgen.queries_torch(WL["seed"] + 1, self.L, 1, HQ, self.D, self.dev)
+                out = torch.empty((self.L, 1, HQ, self.D), dtype=torch.float32, device=self.dev)
+                ws = self.kvq.decode_workspace(self.pools[self.bits][0::2], 1, HQ,
+                                               self.nseq * self.ntok, self.dev)
+                self._dec1 = (q, out, ws)
+            return self._dec1
+        if self._dec is None:
+            q = kvgen.queries_torch(WL["seed"], self.L, self.nseq, HQ, self.D, self.dev)
+            out = torch.empty((self.L, self.nseq, HQ, self.D), dtype=torch.float32,
+                              device=self.dev)
+            ws = self.kvq.decode_workspace(self.pools[self.bits][0::2], self.nseq, HQ,
+                                           self.ntok, self.dev)
+            self._dec = (q, out, ws)
+        return self._dec
+
+    @property
+    def q(self):
+        return self.dec_buffers()[0]
+
+    @property
+    def out(self):
+        return self.dec_buffers()[1]
+
+    @property
+    def kivi(self):
+        if self._kivi is None:
+            self._kivi = [kvgen.KiviSpec(seed=KV["seed"], layer=l, is_key=k, batch=KV["B"],
+                                         num_heads=KV["H"], seq=KV["S"], head_dim=KV["D"]
+                                         ).full_torch(self.dev)
+                          for l in range(self.kivi_layers) for k in (True, False)]
+        return self._kivi
+
+    @property
+    def kivi_flags(self):
+        return [k for _ in range(self.kivi_layers) for k in (True, False)]
 
     def make_pools(self, bits):
         return [self.kvq.Pool.empty(bits, self.H, self.D, self.ps, self.pt_np.size, self.dev)
@@ -217,14 +249,15 @@ class Workload:
 
     def decode(self, bits):
         p = self.pools[bits]
-        self.kvq.kvq_decode_attn(p[0::2], p[1::2], self.q, self.pt, self.lens, self.ntok,
-                                 SOFTMAX_SCALE, self.out, self.ws, self.err)
+        q, out, ws = self.dec_buffers()
+        self.kvq.kvq_decode_attn(p[0::2], p[1::2], q, self.pt, self.lens, self.ntok,
+                                 SOFTMAX_SCALE, out, ws, self.err)
 
     def decode_full_context(self, bits):
         p = self.pools[bits]
-        self.kvq.kvq_decode_attn(p[0::2], p[1::2], self.q1, self.pt1, self.lens1,
-                                 self.nseq * self.ntok, SOFTMAX_SCALE, self.out1, self.ws1,
-                                 self.err)
+        q, out, ws = self.dec_buffers(full_context=True)
+        self.kvq.kvq_decode_attn(p[0::2], p[1::2], q, self.pt1, self.lens1,
+                                 self.nseq * self.ntok, SOFTMAX_SCALE, out, ws, self.err)
 
     def kivi_flush(self):
         self.kvq.kivi_quant_dequant(self.kivi, self.kivi_flags, KIVI_LO, KIVI_HI,
@@ -282,7 +315,10 @@ def run_gpu(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     bits = args.bits
-    w = Workload(kvq, dev, bits)
+    w = Workload(kvq, dev, bits, layers=args.layers)
+    if args.only:
+        run_only(w, bits, args, stream)
+        return
     B = w.bytes(bits)
     step_bytes = sum(B.values())
 
@@ -373,6 +409,18 @@ def run_gpu(args):
             "cpu_baseline": cpu,
         }
         print(json.dumps(line))
+
+
+def run_only(w, bits, args, stream):
+    """Profiling aid: run one stage warmup + steps times on a (possibly reduced) workload."""
+    fn = {"quant_pack": lambda: w.quant(bits), "dequant": lambda: w.dequant(bits),
+          "decode_attn": lambda: w.decode(bits), "kivi": w.kivi_flush,
+          "decode_attn_262144": lambda: w.decode_full_context(bits)}[args.only]
+    w.quant(bits)
+    torch.cuda.synchronize()
+    t = time_fn(fn, args.steps, args.warmup, stream)
+    print(json.dumps({"profile_only": args.only, "layers": w.L, "bits": bits,
+                      "ms": round(t * 1e3, 4), "err": int(w.err.item())}))
 
 
 def run_e2e(w, kvq, bits, args, stream, world, dev, step_bytes):
@@ -510,11 +558,18 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-widths", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="profiling only: fewer layers than the workload's 16")
+    ap.add_argument("--only", default=None,
+                    choices=["quant_pack", "dequant", "decode_attn", "kivi", "decode_attn_262144"],
+                    help="profiling only: run one stage and print its time, no bench line")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the dominant kernel, if captured")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "kvq":
         ap.error("--warmup must be >= 3")
+    if args.layers is not None and not args.only:
+        ap.error("--layers is a profiling option: use it with --only")
     if args.impl == "reference":
         run_reference(args)
     else:

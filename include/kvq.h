@@ -55,7 +55,9 @@ typedef enum kvq_status {
 } kvq_status;
 
 /* Bits OR-ed into the optional device error word. */
-#define KVQ_DEVERR_PAGE_RANGE 1
+#define KVQ_DEVERR_PAGE_RANGE 1  /* a page id or logical page was out of range (row skipped)   */
+#define KVQ_DEVERR_TIMEOUT 2     /* a bounded wait for an asynchronous copy gave up (the
+                                    affected output is invalid; the kernel returned normally)  */
 
 /* Maximum number of tensors one quant/dequant/KIVI call may batch, and of layers per decode
  * attention call. */

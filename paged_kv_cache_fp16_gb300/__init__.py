@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libkvq.so")
 
 KVQ_MAX_TENSORS = 64
 KVQ_DEVERR_PAGE_RANGE = 1
+KVQ_DEVERR_TIMEOUT = 2
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_BITS", 2: "KVQ_ERR_SHAPE", 3: "KVQ_ERR_NULL",
           4: "KVQ_ERR_ALIGN", 5: "KVQ_ERR_RANGE", 6: "KVQ_ERR_CUDA", 7: "KVQ_ERR_NOMEM",
           8: "KVQ_ERR_WORKSPACE"}

@@ -16,17 +16,21 @@
 //   P^T via movmatrix (the S^T accumulator layout transposed into the B-operand layout)
 //   O^T[256 x 8] += V_hat^T[256 x 16] . P^T[16 x 8]          16 x mma.m16n8k16
 // The contraction index order is free, so the head dimension is permuted such that every thread
-// unpacks whole 24-bit q6 quads (or q4/q8 words) it loaded itself: no shared-memory staging of
-// the dequantized tile.  The 4 warps' (m, l, O) are merged in shared memory, each split writes
-// one partial, and a second kernel merges the splits (log-sum-exp).
+// unpacks whole 24-bit q6 quads (or q4/q8 words) it reads itself: no dequantized tile is ever
+// staged.  The 4 warps' (m, l, O) are merged in shared memory, each split writes one partial,
+// and a second kernel merges the splits (log-sum-exp).
 //
-// The unpack turns each 6/4/8-bit field into an fp16 with a known exponent by OR-ing it into
-// the mantissa of 1024 (0x6400), then one half2 FMA removes the 1024 and the bias exactly.
+// Loads: when page_size is a multiple of 16, a tile is 16 contiguous rows of one page, so each
+// warp streams its tiles through a ring of shared-memory stages with the bulk-copy engine
+// (cp.async.bulk: the page's K codes, V codes, K scales and V scales, completing on one mbarrier
+// per stage); waits are bounded and report KVQ_DEVERR_TIMEOUT instead of hanging.  Other page
+// sizes gather rows with plain loads.
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
+#include "kvq_math.cuh"
 
 namespace kvq {
 namespace {
@@ -36,6 +40,7 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 16;
 constexpr int kRec = kD + 4;   // workspace record per (split, head): O[256], m, l, pad, pad
+constexpr long long kWaitLimit = 1LL << 22;  // try_wait polls before giving up
 #define kNegInf (-__int_as_float(0x7f800000))
 
 struct LayerPools {
@@ -59,69 +64,17 @@ struct AttnArgs {
 };
 
 template <int BITS> struct Wd;
-template <> struct Wd<8> { static constexpr int kPd = 256, kKWords = 16, kVWords = 8; };
-template <> struct Wd<6> { static constexpr int kPd = 192, kKWords = 12, kVWords = 6; };
-template <> struct Wd<4> { static constexpr int kPd = 128, kKWords = 8, kVWords = 4; };
+template <> struct Wd<8> { static constexpr int kPd = 256, kKWords = 16, kVWords = 8, kStages = 3; };
+template <> struct Wd<6> { static constexpr int kPd = 192, kKWords = 12, kVWords = 6, kStages = 4; };
+template <> struct Wd<4> { static constexpr int kPd = 128, kKWords = 8, kVWords = 4, kStages = 4; };
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
+// shared-memory stage: [K codes 16 x pd][V codes 16 x pd][K scales 16 x 2][V scales 16 x 2]
+template <int BITS> __host__ __device__ constexpr int stage_bytes() { return 2 * kTile * Wd<BITS>::kPd + 4 * kTile; }
+template <int BITS> __host__ __device__ constexpr int warp_bytes() { return Wd<BITS>::kStages * stage_bytes<BITS>(); }
+template <int BITS> __host__ __device__ constexpr int tma_smem_bytes() {
+  return kWarps * warp_bytes<BITS>() + kWarps * Wd<BITS>::kStages * 16;  // + barriers, flags
 }
-
-__device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t r;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-// fp16x2 constants
-constexpr uint32_t kH1 = 0x3C003C00u;        // 1.0
-constexpr uint32_t kH16th = 0x2C002C00u;     // 0.0625
-constexpr uint32_t kHQuarter = 0x34003400u;  // 0.25
-constexpr uint32_t kHm1056 = 0xE420E420u;    // -1056
-constexpr uint32_t kHm96 = 0xD600D600u;      // -96
-constexpr uint32_t kHm288 = 0xDC80DC80u;     // -288
-constexpr uint32_t kHm1032 = 0xE408E408u;    // -1032
-constexpr uint32_t kHm1152 = 0xE480E480u;    // -1152
-
-// Eight consecutive elements e0..e7 (group `gi` of a thread's loaded words) -> four half2 holding
-// the exact signed codes {e_k, e_{k+4}}, k = 0..3.
-template <int BITS, int GI>
-__device__ __forceinline__ void unpack_group(const uint32_t* w, uint32_t p[4]) {
-  if constexpr (BITS == 6) {
-    // two 24-bit quads at byte 6*GI: fields u0..u3 (quad 0) and u0'..u3' (quad 1)
-    constexpr int b = 6 * GI;
-    constexpr int w0 = b / 4;
-    const uint32_t x = w[w0], y = w[w0 + 1];
-    constexpr uint32_t s1 = (b % 4 == 0) ? 0x4310u : 0x6532u;  // [B0 B1 B3 B4]
-    constexpr uint32_t s2 = (b % 4 == 0) ? 0x5421u : 0x7643u;  // [B1 B2 B4 B5]
-    const uint32_t p1 = prmt(x, y, s1);
-    const uint32_t p2 = prmt(x, y, s2);
-    p[0] = hfma2u((p1 & 0x003F003Fu) | 0x64006400u, kH1, kHm1056);            // 1024 + u0
-    p[1] = hfma2u(((p1 >> 2) & 0x03F003F0u) | 0x64006400u, kH16th, kHm96);     // 1024 + 16 u1
-    p[2] = hfma2u((p2 & 0x03F003F0u) | 0x64006400u, kH16th, kHm96);            // 1024 + 16 u2
-    p[3] = hfma2u(((p2 >> 8) & 0x00FC00FCu) | 0x64006400u, kHQuarter, kHm288); // 1024 + 4 u3
-  } else if constexpr (BITS == 4) {
-    const uint32_t x = w[GI];  // nibble n = element n
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      p[k] = hfma2u(((x >> (4 * k)) & 0x000F000Fu) | 0x64006400u, kH1, kHm1032);
-  } else {
-    const uint32_t x = w[2 * GI], y = w[2 * GI + 1];  // bytes e0..e3, e4..e7 (int8)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t sel = static_cast<uint32_t>(k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12));
-      p[k] = hfma2u((prmt(x, y, sel) & 0x00FF00FFu) ^ 0x64806480u, kH1, kHm1152);  // 1024+c+128
-    }
-  }
-}
+constexpr int kMergeBytes = kWarps * 8 * kD * 4 + 2 * kWarps * 8 * 4;
 
 __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -143,191 +96,172 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Physical row of token `t` of sequence `s`, head h; -1 if out of range (error bit set).
-__device__ __forceinline__ int64_t token_row(const AttnArgs& a, int s, int t, int h,
-                                             int64_t num_pages) {
-  return locate_row(a.pt, a.max_pages, a.ps, a.H, num_pages, s, t, h, a.err);
+// ------------------------------------------------------------------------------ mbarrier / TMA
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for a phase; false if it did not complete within kWaitLimit polls.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  for (long long i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ------------------------------------------------------------------------------ tile compute
+// One 16-token tile: K words of rows g, g+8 (thread's 64 head-dim elements), V words of tokens
+// 2c, 2c+1, 2c+8, 2c+9 (thread's 32 head-dim elements), their fp16 scales (0 for masked tokens).
 template <int BITS>
-__global__ void __launch_bounds__(kThreads, 2) decode_attn_kernel(const AttnArgs a) {
-  using W = Wd<BITS>;
-  __shared__ float sm_o[kWarps][8][kD];
-  __shared__ float sm_m[kWarps][8];
-  __shared__ float sm_l[kWarps][8];
+struct TileRegs {
+  uint32_t kw[2][Wd<BITS>::kKWords];
+  uint32_t ksc[2];   // fp16 scale duplicated in both halves
+  bool kval[2];
+  uint32_t vw[4][Wd<BITS>::kVWords];
+  uint32_t vsc[4];   // fp16 scale bits (0 if the token is masked)
+};
 
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int g = lane >> 2;   // fragment row group
-  const int c = lane & 3;    // fragment column pair
-  const int split = blockIdx.x;
-  const int h = blockIdx.y;
-  const int ls = blockIdx.z;             // layer * nseq + seq
-  const int layer = ls / a.nseq;
-  const int s = ls - layer * a.nseq;
-  const LayerPools P = a.L[layer];
-  const int len = __ldg(a.lens + s);
-  const int n_tiles = (len + kTile - 1) / kTile;
-  const int tile0 = split * a.tiles_per_cta;
-  const int tile1 = min(n_tiles, tile0 + a.tiles_per_cta);
-
-  // Q^T B-fragments for head g of this KV head's group (zero for padding heads).
-  uint32_t qf[16][2];
-  {
-    uint32_t qw[32];
-    if (g < a.G && len > 0) {
-      const uint16_t* qp = a.q + ((static_cast<int64_t>(ls) * a.Hq) + h * a.G + g) * kD + 64 * c;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint4 v = ld_nc_v4(qp + 8 * i);
-        qw[4 * i] = v.x; qw[4 * i + 1] = v.y; qw[4 * i + 2] = v.z; qw[4 * i + 3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) qw[i] = 0;
-    }
-#pragma unroll
-    for (int gi = 0; gi < 8; ++gi)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        qf[2 * gi + j][0] = prmt(qw[4 * gi + j], qw[4 * gi + j + 2], 0x5410u);
-        qf[2 * gi + j][1] = prmt(qw[4 * gi + j], qw[4 * gi + j + 2], 0x7632u);
-      }
+template <int BITS>
+__device__ __forceinline__ void tile_compute(const TileRegs<BITS>& T, const uint32_t (&qf)[16][2],
+                                             float (&acc)[16][4], float& m0, float& m1,
+                                             float& l0, float& l1, float qk_scale) {
+  // ---------------- S^T = K_hat . Q^T
+  float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#define KVQ_QK_GROUP(GI)                                                                \
+  {                                                                                     \
+    uint32_t p0[4], p1[4];                                                              \
+    unpack_group<BITS, GI>(T.kw[0], p0);                                                \
+    unpack_group<BITS, GI>(T.kw[1], p1);                                                \
+    _Pragma("unroll") for (int k = 0; k < 4; ++k) {                                     \
+      p0[k] = hmul2u(p0[k], T.ksc[0]);                                                  \
+      p1[k] = hmul2u(p1[k], T.ksc[1]);                                                  \
+    }                                                                                   \
+    mma16816(sacc, p0[0], p1[0], p0[1], p1[1], qf[2 * GI][0], qf[2 * GI][1]);           \
+    mma16816(sacc, p0[2], p1[2], p0[3], p1[3], qf[2 * GI + 1][0], qf[2 * GI + 1][1]);   \
   }
-
-  float acc[16][4];
-#pragma unroll
-  for (int mt = 0; mt < 16; ++mt)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) acc[mt][k] = 0.f;
-  float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
-
-  for (int tile = tile0 + warp; tile < tile1; tile += kWarps) {
-    const int tb = tile * kTile;
-    // ---------------- S^T = K_hat . Q^T
-    uint32_t kw[2][W::kKWords];
-    uint32_t ksc[2];
-    bool kval[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int t = tb + g + 8 * r;
-      int64_t row = -1;
-      if (t < len) row = token_row(a, s, t, h, P.k_pages);
-      kval[r] = row >= 0;
-      ksc[r] = 0;
-#pragma unroll
-      for (int i = 0; i < W::kKWords; ++i) kw[r][i] = 0;
-      if (row >= 0) {
-        const uint8_t* src = P.kc + row * W::kPd + c * (4 * W::kKWords);
-#pragma unroll
-        for (int i = 0; i < W::kKWords / 4; ++i) {
-          const uint4 v = ld_nc_v4(src + 16 * i);
-          kw[r][4 * i] = v.x; kw[r][4 * i + 1] = v.y; kw[r][4 * i + 2] = v.z; kw[r][4 * i + 3] = v.w;
-        }
-        const uint32_t sb = ld_nc_u16(P.ks + row);
-        ksc[r] = sb | (sb << 16);
-      }
-    }
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-#define KVQ_QK_GROUP(GI)                                                              \
-    {                                                                                 \
-      uint32_t p0[4], p1[4];                                                          \
-      unpack_group<BITS, GI>(kw[0], p0);                                              \
-      unpack_group<BITS, GI>(kw[1], p1);                                              \
-      _Pragma("unroll") for (int k = 0; k < 4; ++k) {                                 \
-        p0[k] = hmul2u(p0[k], ksc[0]);                                                \
-        p1[k] = hmul2u(p1[k], ksc[1]);                                                \
-      }                                                                               \
-      mma16816(sacc, p0[0], p1[0], p0[1], p1[1], qf[2 * GI][0], qf[2 * GI][1]);       \
-      mma16816(sacc, p0[2], p1[2], p0[3], p1[3], qf[2 * GI + 1][0], qf[2 * GI + 1][1]); \
-    }
-    KVQ_QK_GROUP(0) KVQ_QK_GROUP(1) KVQ_QK_GROUP(2) KVQ_QK_GROUP(3)
-    KVQ_QK_GROUP(4) KVQ_QK_GROUP(5) KVQ_QK_GROUP(6) KVQ_QK_GROUP(7)
+  KVQ_QK_GROUP(0) KVQ_QK_GROUP(1) KVQ_QK_GROUP(2) KVQ_QK_GROUP(3)
+  KVQ_QK_GROUP(4) KVQ_QK_GROUP(5) KVQ_QK_GROUP(6) KVQ_QK_GROUP(7)
 #undef KVQ_QK_GROUP
 
-    // ---------------- online softmax (log2 domain); sacc: [tok g | g+8][head 2c | 2c+1]
-    float sc[4];
-    sc[0] = kval[0] ? sacc[0] * a.qk_scale : kNegInf;
-    sc[1] = kval[0] ? sacc[1] * a.qk_scale : kNegInf;
-    sc[2] = kval[1] ? sacc[2] * a.qk_scale : kNegInf;
-    sc[3] = kval[1] ? sacc[3] * a.qk_scale : kNegInf;
-    float tm0 = fmaxf(sc[0], sc[2]), tm1 = fmaxf(sc[1], sc[3]);
+  // ---------------- online softmax (log2 domain); sacc: [tok g | g+8][head 2c | 2c+1]
+  float sc[4];
+  sc[0] = T.kval[0] ? sacc[0] * qk_scale : kNegInf;
+  sc[1] = T.kval[0] ? sacc[1] * qk_scale : kNegInf;
+  sc[2] = T.kval[1] ? sacc[2] * qk_scale : kNegInf;
+  sc[3] = T.kval[1] ? sacc[3] * qk_scale : kNegInf;
+  float tm0 = fmaxf(sc[0], sc[2]), tm1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      tm0 = fmaxf(tm0, __shfl_xor_sync(kFullMask, tm0, o));
-      tm1 = fmaxf(tm1, __shfl_xor_sync(kFullMask, tm1, o));
-    }
-    const float n0 = fmaxf(m0, tm0), n1 = fmaxf(m1, tm1);
-    const float al0 = (n0 == kNegInf) ? 1.f : exp2f(m0 - n0);
-    const float al1 = (n1 == kNegInf) ? 1.f : exp2f(m1 - n1);
-    float p[4];
-    p[0] = (n0 == kNegInf) ? 0.f : exp2f(sc[0] - n0);
-    p[2] = (n0 == kNegInf) ? 0.f : exp2f(sc[2] - n0);
-    p[1] = (n1 == kNegInf) ? 0.f : exp2f(sc[1] - n1);
-    p[3] = (n1 == kNegInf) ? 0.f : exp2f(sc[3] - n1);
-    l0 = l0 * al0 + (p[0] + p[2]);
-    l1 = l1 * al1 + (p[1] + p[3]);
-    m0 = n0;
-    m1 = n1;
-    if (__any_sync(kFullMask, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-      for (int mt = 0; mt < 16; ++mt) {
-        acc[mt][0] *= al0; acc[mt][1] *= al1; acc[mt][2] *= al0; acc[mt][3] *= al1;
-      }
-    }
-    const uint32_t pb0 = movtrans(pack_h2(p[0], p[1]));   // tokens 2c, 2c+1 ; head g
-    const uint32_t pb1 = movtrans(pack_h2(p[2], p[3]));   // tokens 8+2c, 8+2c+1 ; head g
-
-    // ---------------- O^T += V_hat^T . P^T ; thread tokens 2c, 2c+1, 2c+8, 2c+9, d in [32g, 32g+32)
-    uint32_t vw[4][W::kVWords];
-    uint32_t vsc[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int t = tb + 2 * c + (q & 1) + 8 * (q >> 1);
-      int64_t row = -1;
-      if (t < len) row = token_row(a, s, t, h, P.v_pages);
-      vsc[q] = 0;
-#pragma unroll
-      for (int i = 0; i < W::kVWords; ++i) vw[q][i] = 0;
-      if (row >= 0) {
-        const uint8_t* src = P.vc + row * W::kPd + g * (4 * W::kVWords);
-        if constexpr (W::kVWords % 4 == 0) {
-#pragma unroll
-          for (int i = 0; i < W::kVWords / 4; ++i) {
-            const uint4 v = ld_nc_v4(src + 16 * i);
-            vw[q][4 * i] = v.x; vw[q][4 * i + 1] = v.y; vw[q][4 * i + 2] = v.z; vw[q][4 * i + 3] = v.w;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < W::kVWords / 2; ++i) {
-            const uint2 v = ld_nc_v2(src + 8 * i);
-            vw[q][2 * i] = v.x; vw[q][2 * i + 1] = v.y;
-          }
-        }
-        vsc[q] = ld_nc_u16(P.vs + row);
-      }
-    }
-    const uint32_t sab = vsc[0] | (vsc[1] << 16), scd = vsc[2] | (vsc[3] << 16);
-#define KVQ_PV_GROUP(GI)                                                                \
-    {                                                                                   \
-      uint32_t pa[4], pb[4], pc[4], pd[4];                                              \
-      unpack_group<BITS, GI>(vw[0], pa);                                                \
-      unpack_group<BITS, GI>(vw[1], pb);                                                \
-      unpack_group<BITS, GI>(vw[2], pc);                                                \
-      unpack_group<BITS, GI>(vw[3], pd);                                                \
-      _Pragma("unroll") for (int k = 0; k < 4; ++k) {                                   \
-        const uint32_t lab = hmul2u(prmt(pa[k], pb[k], 0x5410u), sab);                 \
-        const uint32_t hab = hmul2u(prmt(pa[k], pb[k], 0x7632u), sab);                 \
-        const uint32_t lcd = hmul2u(prmt(pc[k], pd[k], 0x5410u), scd);                 \
-        const uint32_t hcd = hmul2u(prmt(pc[k], pd[k], 0x7632u), scd);                 \
-        mma16816(acc[4 * GI + k], lab, hab, lcd, hcd, pb0, pb1);                        \
-      }                                                                                 \
-    }
-    KVQ_PV_GROUP(0) KVQ_PV_GROUP(1) KVQ_PV_GROUP(2) KVQ_PV_GROUP(3)
-#undef KVQ_PV_GROUP
+  for (int o = 4; o < 32; o <<= 1) {
+    tm0 = fmaxf(tm0, __shfl_xor_sync(kFullMask, tm0, o));
+    tm1 = fmaxf(tm1, __shfl_xor_sync(kFullMask, tm1, o));
   }
+  const float n0 = fmaxf(m0, tm0), n1 = fmaxf(m1, tm1);
+  const float al0 = (n0 == kNegInf) ? 1.f : exp2f(m0 - n0);
+  const float al1 = (n1 == kNegInf) ? 1.f : exp2f(m1 - n1);
+  float p[4];
+  p[0] = (n0 == kNegInf) ? 0.f : exp2f(sc[0] - n0);
+  p[2] = (n0 == kNegInf) ? 0.f : exp2f(sc[2] - n0);
+  p[1] = (n1 == kNegInf) ? 0.f : exp2f(sc[1] - n1);
+  p[3] = (n1 == kNegInf) ? 0.f : exp2f(sc[3] - n1);
+  l0 = l0 * al0 + (p[0] + p[2]);
+  l1 = l1 * al1 + (p[1] + p[3]);
+  m0 = n0;
+  m1 = n1;
+  if (__any_sync(kFullMask, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+    for (int mt = 0; mt < 16; ++mt) {
+      acc[mt][0] *= al0; acc[mt][1] *= al1; acc[mt][2] *= al0; acc[mt][3] *= al1;
+    }
+  }
+  const uint32_t pb0 = movtrans(pack_h2(p[0], p[1]));   // tokens 2c, 2c+1 ; head g
+  const uint32_t pb1 = movtrans(pack_h2(p[2], p[3]));   // tokens 8+2c, 8+2c+1 ; head g
 
-  // ---------------- merge the warps in shared memory
+  // ---------------- O^T += V_hat^T . P^T
+  const uint32_t sab = T.vsc[0] | (T.vsc[1] << 16), scd = T.vsc[2] | (T.vsc[3] << 16);
+#define KVQ_PV_GROUP(GI)                                                                \
+  {                                                                                     \
+    uint32_t pa[4], pb[4], pc[4], pd[4];                                                \
+    unpack_group<BITS, GI>(T.vw[0], pa);                                                \
+    unpack_group<BITS, GI>(T.vw[1], pb);                                                \
+    unpack_group<BITS, GI>(T.vw[2], pc);                                                \
+    unpack_group<BITS, GI>(T.vw[3], pd);                                                \
+    _Pragma("unroll") for (int k = 0; k < 4; ++k) {                                     \
+      const uint32_t lab = hmul2u(prmt(pa[k], pb[k], 0x5410u), sab);                   \
+      const uint32_t hab = hmul2u(prmt(pa[k], pb[k], 0x7632u), sab);                   \
+      const uint32_t lcd = hmul2u(prmt(pc[k], pd[k], 0x5410u), scd);                   \
+      const uint32_t hcd = hmul2u(prmt(pc[k], pd[k], 0x7632u), scd);                   \
+      mma16816(acc[4 * GI + k], lab, hab, lcd, hcd, pb0, pb1);                          \
+    }                                                                                   \
+  }
+  KVQ_PV_GROUP(0) KVQ_PV_GROUP(1) KVQ_PV_GROUP(2) KVQ_PV_GROUP(3)
+#undef KVQ_PV_GROUP
+}
+
+// Q^T B-fragments for head g of this KV head's group (zero for padding heads).
+__device__ __forceinline__ void load_q_frags(const AttnArgs& a, int ls, int h, int g, int c,
+                                             bool any, uint32_t (&qf)[16][2]) {
+  uint32_t qw[32];
+  if (g < a.G && any) {
+    const uint16_t* qp = a.q + ((static_cast<int64_t>(ls) * a.Hq) + h * a.G + g) * kD + 64 * c;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 v = ld_nc_v4(qp + 8 * i);
+      qw[4 * i] = v.x; qw[4 * i + 1] = v.y; qw[4 * i + 2] = v.z; qw[4 * i + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) qw[i] = 0;
+  }
+#pragma unroll
+  for (int gi = 0; gi < 8; ++gi)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      qf[2 * gi + j][0] = prmt(qw[4 * gi + j], qw[4 * gi + j + 2], 0x5410u);
+      qf[2 * gi + j][1] = prmt(qw[4 * gi + j], qw[4 * gi + j + 2], 0x7632u);
+    }
+}
+
+// Merge the CTA's warps in shared memory and write the split's partial record.
+__device__ __forceinline__ void cta_merge_write(const AttnArgs& a, float* sm, int ls, int h,
+                                                int split, int warp, int g, int c,
+                                                const float (&acc)[16][4], float m0, float m1,
+                                                float l0, float l1) {
+  float (*sm_o)[8][kD] = reinterpret_cast<float (*)[8][kD]>(sm);
+  float (*sm_m)[8] = reinterpret_cast<float (*)[8]>(sm + kWarps * 8 * kD);
+  float (*sm_l)[8] = reinterpret_cast<float (*)[8]>(sm + kWarps * 8 * kD + kWarps * 8);
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
     l0 += __shfl_xor_sync(kFullMask, l0, o);
@@ -368,10 +302,247 @@ __global__ void __launch_bounds__(kThreads, 2) decode_attn_kernel(const AttnArgs
   }
 }
 
-// One CTA per (layer, seq, query head); thread d merges the splits of output element d.
+// ------------------------------------------------------------------------------ TMA kernel
+template <int BITS>
+__global__ void __launch_bounds__(kThreads, 2) decode_attn_tma_kernel(const AttnArgs a) {
+  using W = Wd<BITS>;
+  constexpr int S = W::kStages;
+  constexpr int kPd = W::kPd;
+  constexpr uint32_t kStageBytes = stage_bytes<BITS>();
+  extern __shared__ __align__(128) uint8_t smem[];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;
+  const int c = lane & 3;
+  const int split = blockIdx.x;
+  const int h = blockIdx.y;
+  const int ls = blockIdx.z;
+  const int layer = ls / a.nseq;
+  const int s = ls - layer * a.nseq;
+  const LayerPools P = a.L[layer];
+  const int len = __ldg(a.lens + s);
+  const int n_tiles = (len + kTile - 1) / kTile;
+  const int tile0 = split * a.tiles_per_cta;
+  const int tile1 = min(n_tiles, tile0 + a.tiles_per_cta);
+  const int n_mine = (tile1 - tile0 - warp + kWarps - 1) > 0
+                         ? (tile1 - tile0 - warp + kWarps - 1) / kWarps : 0;
+
+  uint8_t* wbase = smem + warp * warp_bytes<BITS>();
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * warp_bytes<BITS>()) + warp * S;
+  int* flags = reinterpret_cast<int*>(smem + kWarps * warp_bytes<BITS>() + kWarps * S * 8) +
+               warp * S;
+
+  if (lane == 0) {
+    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+
+  // Issue the loads of this warp's j-th tile into stage j % S (lane 0 only).
+  auto issue = [&](int j) {
+    const int st = j % S;
+    const int tb = (tile0 + warp + j * kWarps) * kTile;
+    const int lp = tb / a.ps;
+    const int slot0 = tb - lp * a.ps;
+    int page = -1;
+    if (lp < a.max_pages) page = __ldg(a.pt + static_cast<int64_t>(s) * a.max_pages + lp);
+    const bool ok = page >= 0 && page < P.k_pages && page < P.v_pages;
+    flags[st] = ok ? 1 : 0;
+    uint8_t* dst = wbase + st * kStageBytes;
+    if (ok) {
+      const int64_t row = (static_cast<int64_t>(page) * a.H + h) * a.ps + slot0;
+      mbar_expect_tx(&bars[st], kStageBytes);
+      bulk_g2s(dst, P.kc + row * kPd, kTile * kPd, &bars[st]);
+      bulk_g2s(dst + kTile * kPd, P.vc + row * kPd, kTile * kPd, &bars[st]);
+      bulk_g2s(dst + 2 * kTile * kPd, P.ks + row, 2 * kTile, &bars[st]);
+      bulk_g2s(dst + 2 * kTile * kPd + 2 * kTile, P.vs + row, 2 * kTile, &bars[st]);
+    } else {
+      report(a.err, KVQ_DEVERR_PAGE_RANGE);
+      mbar_arrive(&bars[st]);
+    }
+  };
+
+  if (lane == 0)
+    for (int j = 0; j < S && j < n_mine; ++j) issue(j);
+
+  uint32_t qf[16][2];
+  load_q_frags(a, ls, h, g, c, len > 0, qf);
+  float acc[16][4];
+#pragma unroll
+  for (int mt = 0; mt < 16; ++mt)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[mt][k] = 0.f;
+  float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
+  bool timed_out = false;
+  int issued = (S < n_mine) ? S : n_mine;
+
+  for (int j = 0; j < n_mine; ++j) {
+    const int st = j % S;
+    const uint32_t parity = static_cast<uint32_t>((j / S) & 1);
+    const bool arrived = mbar_wait_bounded(&bars[st], parity);
+    if (__any_sync(kFullMask, !arrived)) {   // warp-uniform exit
+      timed_out = true;
+      break;
+    }
+    const uint8_t* sk = wbase + st * kStageBytes;
+    const uint8_t* sv = sk + kTile * kPd;
+    const uint16_t* sks = reinterpret_cast<const uint16_t*>(sk + 2 * kTile * kPd);
+    const uint16_t* svs = sks + kTile;
+    const bool ok = flags[st] != 0;
+    const int tb = (tile0 + warp + j * kWarps) * kTile;
+    TileRegs<BITS> T;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int row = g + 8 * r;
+      T.kval[r] = ok && tb + row < len;
+      const uint32_t sb = sks[row];
+      T.ksc[r] = sb | (sb << 16);
+      const uint4* src = reinterpret_cast<const uint4*>(sk + row * kPd + c * (4 * W::kKWords));
+#pragma unroll
+      for (int i = 0; i < W::kKWords / 4; ++i) {
+        const uint4 v = src[i];
+        T.kw[r][4 * i] = v.x; T.kw[r][4 * i + 1] = v.y;
+        T.kw[r][4 * i + 2] = v.z; T.kw[r][4 * i + 3] = v.w;
+      }
+    }
+#pragma unroll
+    for (int qi = 0; qi < 4; ++qi) {
+      const int row = 2 * c + (qi & 1) + 8 * (qi >> 1);
+      const bool v_ok = ok && tb + row < len;
+      T.vsc[qi] = v_ok ? svs[row] : 0u;
+      const uint8_t* src = sv + row * kPd + g * (4 * W::kVWords);
+      if constexpr (W::kVWords % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < W::kVWords / 4; ++i) {
+          const uint4 v = reinterpret_cast<const uint4*>(src)[i];
+          T.vw[qi][4 * i] = v.x; T.vw[qi][4 * i + 1] = v.y;
+          T.vw[qi][4 * i + 2] = v.z; T.vw[qi][4 * i + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < W::kVWords / 2; ++i) {
+          const uint2 v = reinterpret_cast<const uint2*>(src)[i];
+          T.vw[qi][2 * i] = v.x; T.vw[qi][2 * i + 1] = v.y;
+        }
+      }
+    }
+    // the stage's bytes are in registers: hand it back to the copy engine
+    __syncwarp();
+    if (lane == 0 && j + S < n_mine) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(j + S);
+      ++issued;
+    }
+    tile_compute<BITS>(T, qf, acc, m0, m1, l0, l1, a.qk_scale);
+  }
+
+  if (timed_out) {
+    // drain the copies still in flight (bounded) before the shared memory is released: the
+    // phases of one stage complete in order, so its last issued phase is the one to wait for
+    if (lane == 0) {
+      report(a.err, KVQ_DEVERR_TIMEOUT);
+      for (int j = issued - S > 0 ? issued - S : 0; j < issued; ++j)
+        mbar_wait_bounded(&bars[j % S], static_cast<uint32_t>((j / S) & 1));
+    }
+    m0 = m1 = kNegInf;
+    l0 = l1 = 0.f;
+  }
+  __syncthreads();  // every warp is done with its stages: reuse them for the merge
+  cta_merge_write(a, reinterpret_cast<float*>(smem), ls, h, split, warp, g, c, acc, m0, m1, l0,
+                  l1);
+}
+
+// ------------------------------------------------------------------------------ gather kernel
+// Any page size: each thread loads the rows of its tokens with plain loads.
+template <int BITS>
+__global__ void __launch_bounds__(kThreads, 2) decode_attn_gather_kernel(const AttnArgs a) {
+  using W = Wd<BITS>;
+  __shared__ __align__(16) float sm[kMergeBytes / 4];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;
+  const int c = lane & 3;
+  const int split = blockIdx.x;
+  const int h = blockIdx.y;
+  const int ls = blockIdx.z;
+  const int layer = ls / a.nseq;
+  const int s = ls - layer * a.nseq;
+  const LayerPools P = a.L[layer];
+  const int len = __ldg(a.lens + s);
+  const int n_tiles = (len + kTile - 1) / kTile;
+  const int tile0 = split * a.tiles_per_cta;
+  const int tile1 = min(n_tiles, tile0 + a.tiles_per_cta);
+
+  uint32_t qf[16][2];
+  load_q_frags(a, ls, h, g, c, len > 0, qf);
+  float acc[16][4];
+#pragma unroll
+  for (int mt = 0; mt < 16; ++mt)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[mt][k] = 0.f;
+  float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
+
+  for (int tile = tile0 + warp; tile < tile1; tile += kWarps) {
+    const int tb = tile * kTile;
+    TileRegs<BITS> T;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int t = tb + g + 8 * r;
+      int64_t row = -1;
+      if (t < len) row = locate_row(a.pt, a.max_pages, a.ps, a.H, P.k_pages, s, t, h, a.err);
+      T.kval[r] = row >= 0;
+      T.ksc[r] = 0;
+#pragma unroll
+      for (int i = 0; i < W::kKWords; ++i) T.kw[r][i] = 0;
+      if (row >= 0) {
+        const uint8_t* src = P.kc + row * W::kPd + c * (4 * W::kKWords);
+#pragma unroll
+        for (int i = 0; i < W::kKWords / 4; ++i) {
+          const uint4 v = ld_nc_v4(src + 16 * i);
+          T.kw[r][4 * i] = v.x; T.kw[r][4 * i + 1] = v.y;
+          T.kw[r][4 * i + 2] = v.z; T.kw[r][4 * i + 3] = v.w;
+        }
+        const uint32_t sb = ld_nc_u16(P.ks + row);
+        T.ksc[r] = sb | (sb << 16);
+      }
+    }
+#pragma unroll
+    for (int qi = 0; qi < 4; ++qi) {
+      const int t = tb + 2 * c + (qi & 1) + 8 * (qi >> 1);
+      int64_t row = -1;
+      if (t < len) row = locate_row(a.pt, a.max_pages, a.ps, a.H, P.v_pages, s, t, h, a.err);
+      T.vsc[qi] = 0;
+#pragma unroll
+      for (int i = 0; i < W::kVWords; ++i) T.vw[qi][i] = 0;
+      if (row >= 0) {
+        const uint8_t* src = P.vc + row * W::kPd + g * (4 * W::kVWords);
+        if constexpr (W::kVWords % 4 == 0) {
+#pragma unroll
+          for (int i = 0; i < W::kVWords / 4; ++i) {
+            const uint4 v = ld_nc_v4(src + 16 * i);
+            T.vw[qi][4 * i] = v.x; T.vw[qi][4 * i + 1] = v.y;
+            T.vw[qi][4 * i + 2] = v.z; T.vw[qi][4 * i + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < W::kVWords / 2; ++i) {
+            const uint2 v = ld_nc_v2(src + 8 * i);
+            T.vw[qi][2 * i] = v.x; T.vw[qi][2 * i + 1] = v.y;
+          }
+        }
+        T.vsc[qi] = ld_nc_u16(P.vs + row);
+      }
+    }
+    tile_compute<BITS>(T, qf, acc, m0, m1, l0, l1, a.qk_scale);
+  }
+  cta_merge_write(a, sm, ls, h, split, warp, g, c, acc, m0, m1, l0, l1);
+}
+
+// One CTA per (query head, layer * nseq + seq); thread d merges the splits of element d.
 __global__ void __launch_bounds__(kD) decode_merge_kernel(const AttnArgs a) {
-  const int j = blockIdx.x;        // query head
-  const int ls = blockIdx.y;       // layer * nseq + seq
+  const int j = blockIdx.x;
+  const int ls = blockIdx.y;
   const int h = j / a.G, jj = j - h * a.G;
   const int d = threadIdx.x;
   const float* base = a.ws + ((static_cast<int64_t>(ls) * a.H + h) * a.n_splits) * 8 * kRec +
@@ -396,13 +567,28 @@ int tiles_per_cta_for(int n_layers, int nseq, int H, int max_seq_len) {
   const int tiles = (max_seq_len + kTile - 1) / kTile;
   const int sms = sm_count() > 0 ? sm_count() : 152;
   const int64_t units = static_cast<int64_t>(n_layers) * nseq * H;
-  // aim for >= 8 CTAs per SM over the whole grid, at most 64 tiles (1024 tokens) per CTA
+  // aim for >= 4 resident waves (2 CTAs per SM), at most 256 tiles (4096 tokens) per CTA
   const int64_t want_splits = (8LL * sms + units - 1) / units;
   int64_t t = (tiles + want_splits - 1) / want_splits;
-  if (t > 64) t = 64;
+  if (t > 256) t = 256;
   t = ((t + kWarps - 1) / kWarps) * kWarps;
   if (t < kWarps) t = kWarps;
   return static_cast<int>(t);
+}
+
+template <int BITS>
+cudaError_t launch_attn(const AttnArgs& a, dim3 grid, bool tma, cudaStream_t cs) {
+  if (tma) {
+    constexpr int smem = tma_smem_bytes<BITS>();
+    static_assert(smem >= kMergeBytes, "merge buffer must fit in the stage ring");
+    cudaError_t e = cudaFuncSetAttribute(decode_attn_tma_kernel<BITS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    decode_attn_tma_kernel<BITS><<<grid, kThreads, smem, cs>>>(a);
+  } else {
+    decode_attn_gather_kernel<BITS><<<grid, kThreads, 0, cs>>>(a);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -491,13 +677,17 @@ extern "C" kvq_status kvq_decode_attn(const kvq_pool* k_pools, const kvq_pool* v
 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const dim3 grid(a.n_splits, H, n_layers * nseq);
+  const bool tma = (k0.page_size % kTile) == 0;
+  cudaError_t e;
   switch (k0.bits) {
-    case 8: decode_attn_kernel<8><<<grid, kThreads, 0, cs>>>(a); break;
-    case 6: decode_attn_kernel<6><<<grid, kThreads, 0, cs>>>(a); break;
-    default: decode_attn_kernel<4><<<grid, kThreads, 0, cs>>>(a); break;
+    case 8: e = launch_attn<8>(a, grid, tma, cs); break;
+    case 6: e = launch_attn<6>(a, grid, tma, cs); break;
+    default: e = launch_attn<4>(a, grid, tma, cs); break;
   }
-  decode_merge_kernel<<<dim3(num_q_heads, n_layers * nseq), kD, 0, cs>>>(a);
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) {
+    decode_merge_kernel<<<dim3(num_q_heads, n_layers * nseq), kD, 0, cs>>>(a);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "decode attention launch: %s",
                                     cudaGetErrorString(e));
   return ok();

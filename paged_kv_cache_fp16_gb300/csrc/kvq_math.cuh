@@ -1,0 +1,112 @@
+// Device arithmetic shared by the quantize, dequantize and attention kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace kvq {
+
+// ---------------------------------------------------------------------------------------------
+// Quotient x / s, correctly rounded, from a per-row reciprocal.
+//
+// Markstein's correction (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with y = RN(1/s) and q0 = RN(x * y)
+// (within one ulp of x/s), the remainder r = x - s*q0 is exact in one fused multiply-add and
+// q1 = RN(q0 + r*y) is the correctly rounded quotient.  The row's scale s is shared by all its
+// elements, so y is computed once per row (__frcp_rn, IEEE round to nearest) and each element
+// costs one multiply and two FMAs.  tests/test_gpu_division_exhaustive.py checks q1 against
+// IEEE division for every finite fp16 x and every positive fp16 s.
+__device__ __forceinline__ float div_by_row_scale(float x, float s, float y) {
+  const float q0 = __fmul_rn(x, y);
+  const float r = __fmaf_rn(-q0, s, x);
+  return __fmaf_rn(r, y, q0);
+}
+
+// Round half to even and bias in one add: for |q| < 2^22, RN(q + 1.5 * 2^23 + bias) has an
+// ulp of 1, so its low mantissa bits hold rint(q) + bias (1.5 * 2^23 is even, so ties go to the
+// even integer exactly as rint does).  The field is then the low BITS bits of the sum's pattern:
+// c + bias for q6/q4, and the int8 two's-complement byte of c for q8 (bias 0).
+template <int BIAS>
+__device__ __forceinline__ uint32_t rint_biased_bits(float q) {
+  return __float_as_uint(__fadd_rn(q, 12582912.0f + static_cast<float>(BIAS)));
+}
+
+// One element of the symmetric quantizer: the stored field of clamp(rint(x / s), -QMAX, QMAX)
+// (+ BIAS, or the int8 byte for q8), given the row's se = s (1 if s == 0), y = RN(1/s) (0 if
+// s == 0) and clip = (s is subnormal in fp16).  For a normal fp16 s = fp16(amax / QMAX) every
+// |x| <= amax gives |x / s| <= QMAX * (1 + 2^-10) < QMAX + 1/2, so the clamp can only act on
+// rows with a subnormal scale and is skipped elsewhere.
+template <int QMAX, int BIAS, int MASK>
+__device__ __forceinline__ uint32_t quant_field(float x, float se, float y, bool clip) {
+  float q = div_by_row_scale(x, se, y);
+  if (clip) q = fminf(fmaxf(q, -static_cast<float>(QMAX)), static_cast<float>(QMAX));
+  return rint_biased_bits<BIAS>(q) & static_cast<uint32_t>(MASK);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Packed fields -> exact fp16 codes.  A field u placed in the low mantissa bits of 1024 (fp16
+// 0x6400) reads as 1024 + u (or 1024 + 16u / 1024 + 4u when it sits higher); one half2 FMA then
+// removes the offset and the bias exactly (every intermediate is a small integer).
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// fp16x2 constants
+constexpr uint32_t kH1 = 0x3C003C00u;        // 1.0
+constexpr uint32_t kH16th = 0x2C002C00u;     // 0.0625
+constexpr uint32_t kHQuarter = 0x34003400u;  // 0.25
+constexpr uint32_t kHm1056 = 0xE420E420u;    // -1056 = -(1024 + 32)
+constexpr uint32_t kHm96 = 0xD600D600u;      // -96   = -(64 + 32)
+constexpr uint32_t kHm288 = 0xDC80DC80u;     // -288  = -(256 + 32)
+constexpr uint32_t kHm1032 = 0xE408E408u;    // -1032 = -(1024 + 8)
+constexpr uint32_t kHm1152 = 0xE480E480u;    // -1152 = -(1024 + 128)
+
+// Eight consecutive elements e0..e7 of a packed row -> four half2 holding the exact signed codes
+// {e_k, e_{k+4}}, k = 0..3.  The bytes of the group start at byte 6*GI (q6), word GI (q4) or
+// word 2*GI (q8) of `w`.
+template <int BITS, int GI>
+__device__ __forceinline__ void unpack_group(const uint32_t* w, uint32_t p[4]) {
+  if constexpr (BITS == 6) {
+    // two 24-bit little-endian quads: fields u0..u3 then u0'..u3'
+    constexpr int b = 6 * GI;
+    constexpr int w0 = b / 4;
+    const uint32_t x = w[w0], y = w[w0 + 1];
+    constexpr uint32_t s1 = (b % 4 == 0) ? 0x4310u : 0x6532u;  // bytes [B0 B1 B3 B4]
+    constexpr uint32_t s2 = (b % 4 == 0) ? 0x5421u : 0x7643u;  // bytes [B1 B2 B4 B5]
+    const uint32_t p1 = prmt(x, y, s1);
+    const uint32_t p2 = prmt(x, y, s2);
+    p[0] = hfma2u((p1 & 0x003F003Fu) | 0x64006400u, kH1, kHm1056);            // 1024 + u0
+    p[1] = hfma2u(((p1 >> 2) & 0x03F003F0u) | 0x64006400u, kH16th, kHm96);     // 1024 + 16 u1
+    p[2] = hfma2u((p2 & 0x03F003F0u) | 0x64006400u, kH16th, kHm96);            // 1024 + 16 u2
+    p[3] = hfma2u(((p2 >> 8) & 0x00FC00FCu) | 0x64006400u, kHQuarter, kHm288); // 1024 + 4 u3
+  } else if constexpr (BITS == 4) {
+    const uint32_t x = w[GI];  // nibble n = element n
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      p[k] = hfma2u(((x >> (4 * k)) & 0x000F000Fu) | 0x64006400u, kH1, kHm1032);
+  } else {
+    const uint32_t x = w[2 * GI], y = w[2 * GI + 1];  // int8 bytes e0..e3, e4..e7
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t sel = static_cast<uint32_t>(k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12));
+      p[k] = hfma2u((prmt(x, y, sel) & 0x00FF00FFu) ^ 0x64806480u, kH1, kHm1152);
+    }
+  }
+}
+
+}  // namespace kvq

@@ -107,7 +107,7 @@ def test_table_reserve_appends_into_partial_pages(kvq):
     a.reserve(pt, 16, [16, 17, 0], [1, 14, 0])          # seq 1 fills its partial page 1
     assert (pt[0, 1] >= 0) and torch.equal(pt[1], before[1])
     used = pt[pt >= 0]
-    assert used.unique().numel() == used.numel() == a.free_count * 0 + (100 - a.free_count)
+    assert used.unique().numel() == used.numel() == 100 - a.free_count
     with pytest.raises(kvq.KVQError) as e:                  # beyond max_pages: unchanged
         a.reserve(pt, 16, [0, 0, 0], [0, 0, 16 * 9])
     assert e.value.status == 5

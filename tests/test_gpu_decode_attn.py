@@ -67,8 +67,10 @@ def test_small_caches(kvq, cuda_dev, bits, H, G):
     assert np.all(got[0, len(lens) - 1] == 0)     # empty sequence
 
 
-@pytest.mark.parametrize("ps", [1, 7, 64])
+@pytest.mark.parametrize("ps", [1, 7, 32, 64])
 def test_other_page_sizes(kvq, cuda_dev, ps):
+    """Page sizes that are multiples of 16 stream pages through the bulk-copy ring; others
+    gather rows one by one."""
     bits, H, G, D = 6, 2, 3, 256
     lens = [5, 130]
     pps = max((n + ps - 1) // ps for n in lens)
