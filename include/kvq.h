@@ -74,7 +74,7 @@ typedef enum kvq_status {
 typedef struct kvq_pool {
   int32_t bits;       /* 8, 6 or 4 */
   int32_t num_heads;  /* KV heads H */
-  int32_t head_dim;   /* D: a multiple of 8, at most 256 */
+  int32_t head_dim;   /* D: a multiple of 16, at most 256 */
   int32_t page_size;  /* tokens per page, >= 1 */
   int64_t num_pages;
   uint8_t* codes;
@@ -171,7 +171,7 @@ KVQ_API kvq_status kvq_table_reserve(kvq_allocator* a, int32_t* page_table, int 
  * dev_err    optional device int32 error word (see the file header).
  * Rows are independent; a row's packed bytes and scale are written whole.  Two rows of one call
  * mapping to the same (page, slot) race (a caller error).
- * Errors: KVQ_ERR_BITS, KVQ_ERR_SHAPE (D % 8, D > 256, mismatched pools), KVQ_ERR_NULL,
+ * Errors: KVQ_ERR_BITS, KVQ_ERR_SHAPE (D % 16, D > 256, mismatched pools), KVQ_ERR_NULL,
  * KVQ_ERR_ALIGN, KVQ_ERR_RANGE (n_tensors not in [1, KVQ_MAX_TENSORS], nseq < 0,
  * total_new_tokens < 0, max_pages < 1), KVQ_ERR_CUDA.
  */

@@ -158,8 +158,8 @@ template <int BITS>
 __device__ __forceinline__ void tile_compute(const TileRegs<BITS>& T, const uint32_t (&qf)[16][2],
                                              float (&acc)[16][4], float& m0, float& m1,
                                              float& l0, float& l1, float qk_scale) {
-  // ---------------- S^T = K_hat . Q^T
-  float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+  // ---------------- S^T = K_hat . Q^T  (four independent accumulation chains)
+  float sacc4[4][4] = {};
 #define KVQ_QK_GROUP(GI)                                                                \
   {                                                                                     \
     uint32_t p0[4], p1[4];                                                              \
@@ -169,12 +169,16 @@ __device__ __forceinline__ void tile_compute(const TileRegs<BITS>& T, const uint
       p0[k] = hmul2u(p0[k], T.ksc[0]);                                                  \
       p1[k] = hmul2u(p1[k], T.ksc[1]);                                                  \
     }                                                                                   \
-    mma16816(sacc, p0[0], p1[0], p0[1], p1[1], qf[2 * GI][0], qf[2 * GI][1]);           \
-    mma16816(sacc, p0[2], p1[2], p0[3], p1[3], qf[2 * GI + 1][0], qf[2 * GI + 1][1]);   \
+    mma16816(sacc4[(2 * GI) & 3], p0[0], p1[0], p0[1], p1[1], qf[2 * GI][0], qf[2 * GI][1]); \
+    mma16816(sacc4[(2 * GI + 1) & 3], p0[2], p1[2], p0[3], p1[3], qf[2 * GI + 1][0],        \
+             qf[2 * GI + 1][1]);                                                        \
   }
   KVQ_QK_GROUP(0) KVQ_QK_GROUP(1) KVQ_QK_GROUP(2) KVQ_QK_GROUP(3)
   KVQ_QK_GROUP(4) KVQ_QK_GROUP(5) KVQ_QK_GROUP(6) KVQ_QK_GROUP(7)
 #undef KVQ_QK_GROUP
+  float sacc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) sacc[k] = (sacc4[0][k] + sacc4[1][k]) + (sacc4[2][k] + sacc4[3][k]);
 
   // ---------------- online softmax (log2 domain); sacc: [tok g | g+8][head 2c | 2c+1]
   float sc[4];

@@ -22,6 +22,15 @@ __device__ __forceinline__ float div_by_row_scale(float x, float s, float y) {
   return __fmaf_rn(r, y, q0);
 }
 
+// fp16 row scale fp16_rne(float32(amax) / qmax) without a division instruction: the same
+// Markstein step with the constant y = RN(1/qmax) gives the correctly rounded float32 quotient
+// for every fp16 amax (checked exhaustively with the quotient above), then one rounding to fp16.
+template <int QMAX>
+__device__ __forceinline__ float row_scale_f32(float amax) {
+  constexpr float y = 1.0f / static_cast<float>(QMAX);  // RN(1/qmax), folded at compile time
+  return div_by_row_scale(amax, static_cast<float>(QMAX), y);
+}
+
 // Round half to even and bias in one add: for |q| < 2^22, RN(q + 1.5 * 2^23 + bias) has an
 // ulp of 1, so its low mantissa bits hold rint(q) + bias (1.5 * 2^23 is even, so ties go to the
 // even integer exactly as rint does).  The field is then the low BITS bits of the sum's pattern:

@@ -7,11 +7,13 @@
 // w = u0 | u1 << 6 | u2 << 12 | u3 << 18, whose three bytes are exactly the page's byte0..2.
 //
 // Thread layout: a warp takes a block of 8 new tokens (all their heads: rows contiguous in the
-// input); lanes 0..7 look up the page of one token each and broadcast it by shuffle.  Each lane
-// owns one 16-byte chunk (8 elements) of a row; a row spans next_pow2(D/8) lanes, so a warp
-// covers 32 / that rows per step, with 8 steps of loads in flight.  Row loads and stores are
-// contiguous across lanes (coalesced), the row max is an fp16 max plus a segmented shuffle, and
-// codes are packed in registers.  Per element: the quotient by the row's scale from a per-row
+// input); lanes 0..7 look up the page of one token each and broadcast it by shuffle.  A row is
+// cut into 16-element units (32 input bytes; 16 / 12 / 8 packed bytes for q8 / q6 / q4, so every
+// lane's packed access is aligned and uniform); 8 lanes share a row (fewer for short rows), so
+// one warp instruction serves 4 rows and the per-row scalar work (scale, reciprocal, address)
+// is amortized over them.  Lane j of a row takes units j and j + 8, so each load or store
+// instruction covers a contiguous span of every row (coalesced).  The row max is an fp16 max
+// plus a segmented shuffle, and codes are packed in registers.  Per element: the quotient by the row's scale from a per-row
 // reciprocal with one Markstein correction (exact), then one add that rounds half to even and
 // leaves the biased field in the low bits.  HBM-bound: per row 2D bytes in, packed_dim + 2 out.
 #include <cuda_runtime.h>
@@ -26,7 +28,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarpsPerBlock = kThreads / 32;
 constexpr int kTok = 8;     // tokens per warp work item (all heads of each)
-constexpr int kUnroll = 8;  // row steps with loads in flight per lane
+constexpr int kUnroll = 2;  // warp steps with loads in flight
 
 struct PackArgs {
   const uint16_t* x[KVQ_MAX_TENSORS];  // quant: inputs; dequant: outputs (cast back)
@@ -36,14 +38,14 @@ struct PackArgs {
   const int32_t* start;
   int32_t* err;
   int n_tensors, total_tokens, H, D, page_size, pd, max_pages, nseq;
-  int lpr_log2;             // lanes per row = 1 << lpr_log2
-  int chunks;               // D / 8
+  int units;     // 16-element units per row: ceil(D / 16)
+  int lpr_log2;  // lanes per row = 1 << lpr_log2 = min(next_pow2(units), 8)
 };
 
 template <int BITS> struct Q;
-template <> struct Q<8> { static constexpr int kQmax = 127, kBias = 0, kMask = 0xff; };
-template <> struct Q<6> { static constexpr int kQmax = 31, kBias = 32, kMask = 0x3f; };
-template <> struct Q<4> { static constexpr int kQmax = 7, kBias = 8, kMask = 0x0f; };
+template <> struct Q<8> { static constexpr int kQmax = 127, kBias = 0, kMask = 0xff, kUnitBytes = 16; };
+template <> struct Q<6> { static constexpr int kQmax = 31, kBias = 32, kMask = 0x3f, kUnitBytes = 12; };
+template <> struct Q<4> { static constexpr int kQmax = 7, kBias = 8, kMask = 0x0f, kUnitBytes = 8; };
 
 // Physical row of head 0 of new token `tok` ((page * H) * page_size + slot), or -1.
 __device__ __forceinline__ long long token_base(const PackArgs& a, int64_t num_pages, int tok) {
@@ -58,80 +60,80 @@ __device__ __forceinline__ long long shfl_ll(long long v, int src) {
   return (static_cast<long long>(hi) << 32) | static_cast<unsigned int>(lo);
 }
 
-__device__ __forceinline__ float half2_absmax(const uint4& v) {
-  const __half2 a = __habs2(*reinterpret_cast<const __half2*>(&v.x));
-  const __half2 b = __habs2(*reinterpret_cast<const __half2*>(&v.y));
-  const __half2 c = __habs2(*reinterpret_cast<const __half2*>(&v.z));
-  const __half2 d = __habs2(*reinterpret_cast<const __half2*>(&v.w));
-  const __half2 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
-  return fmaxf(__low2float(m), __high2float(m));
+__device__ __forceinline__ __half2 habs2u(uint32_t w) {
+  return __habs2(*reinterpret_cast<const __half2*>(&w));
 }
 
-// Store the 8 fields of one chunk; `m` = physical row * chunks + chunk, so the chunk's bytes
-// start at m * BITS (8 fields of BITS bits).
+__device__ __forceinline__ __half2 absmax8(const uint4& v) {
+  return __hmax2(__hmax2(habs2u(v.x), habs2u(v.y)), __hmax2(habs2u(v.z), habs2u(v.w)));
+}
+
+// 8 fields (each < 2^BITS) -> packed little-endian bits: q6 two 24-bit words, q4 one word,
+// q8 two words.
 template <int BITS>
-__device__ __forceinline__ void store_fields(uint8_t* codes, int64_t m, const uint32_t f[8]) {
-  if constexpr (BITS == 8) {
-    const uint32_t w0 = f[0] | (f[1] << 8) | (f[2] << 16) | (f[3] << 24);
-    const uint32_t w1 = f[4] | (f[5] << 8) | (f[6] << 16) | (f[7] << 24);
-    *reinterpret_cast<uint2*>(codes + m * 8) = make_uint2(w0, w1);
+__device__ __forceinline__ void pack8(const uint32_t f[8], uint32_t& a, uint32_t& b) {
+  if constexpr (BITS == 6) {
+    a = f[0] | (f[1] << 6) | (f[2] << 12) | (f[3] << 18);
+    b = f[4] | (f[5] << 6) | (f[6] << 12) | (f[7] << 18);
   } else if constexpr (BITS == 4) {
-    uint32_t w = 0;
+    a = 0;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) w |= f[k] << (4 * k);
-    *reinterpret_cast<uint32_t*>(codes + m * 4) = w;
+    for (int k = 0; k < 8; ++k) a |= f[k] << (4 * k);
+    b = 0;
   } else {
-    // two 24-bit little-endian words w = u0 | u1 << 6 | u2 << 12 | u3 << 18
-    const uint32_t w0 = f[0] | (f[1] << 6) | (f[2] << 12) | (f[3] << 18);
-    const uint32_t w1 = f[4] | (f[5] << 6) | (f[6] << 12) | (f[7] << 18);
-    const uint32_t lo = w0 | (w1 << 24);                  // bytes 0..3
-    const uint32_t hi = w1 >> 8;                          // bytes 4..5
-    uint8_t* p = codes + m * 6;
-    if ((m & 1) == 0) {  // 6m % 4 == 0
-      *reinterpret_cast<uint32_t*>(p) = lo;
-      *reinterpret_cast<uint16_t*>(p + 4) = static_cast<uint16_t>(hi);
-    } else {             // 6m % 4 == 2
-      *reinterpret_cast<uint16_t*>(p) = static_cast<uint16_t>(lo & 0xffffu);
-      *reinterpret_cast<uint32_t*>(p + 2) = (lo >> 16) | (hi << 16);
-    }
+    a = f[0] | (f[1] << 8) | (f[2] << 16) | (f[3] << 24);
+    b = f[4] | (f[5] << 8) | (f[6] << 16) | (f[7] << 24);
   }
 }
 
-// Load the packed bytes of one chunk as words for unpack_group<BITS, 0>.
+// Store one unit (16 elements) of packed codes.  With D % 16 == 0 the row stride packed_dim is
+// a multiple of 12 / 16 / 8 bytes (q6 / q8 / q4), so a unit is 4- / 16- / 8-byte aligned.
 template <int BITS>
-__device__ __forceinline__ void load_fields(const uint8_t* codes, int64_t m, uint32_t w[2]) {
-  if constexpr (BITS == 8) {
-    const uint2 v = ld_nc_v2(codes + m * 8);
-    w[0] = v.x;
-    w[1] = v.y;
+__device__ __forceinline__ void store_unit(uint8_t* p, const uint32_t a0, const uint32_t b0,
+                                           const uint32_t a1, const uint32_t b1) {
+  if constexpr (BITS == 6) {
+    // fields 0..7 -> 24-bit words a0, b0; fields 8..15 -> a1, b1; 12 bytes = 3 words
+    *reinterpret_cast<uint32_t*>(p) = a0 | (b0 << 24);
+    *reinterpret_cast<uint32_t*>(p + 4) = (b0 >> 8) | (a1 << 16);
+    *reinterpret_cast<uint32_t*>(p + 8) = (a1 >> 16) | (b1 << 8);
   } else if constexpr (BITS == 4) {
-    w[0] = ld_nc_u32(codes + m * 4);
-    w[1] = 0;
+    *reinterpret_cast<uint2*>(p) = make_uint2(a0, a1);
   } else {
-    const uint8_t* p = codes + m * 6;
-    if ((m & 1) == 0) {
-      w[0] = ld_nc_u32(p);
-      w[1] = ld_nc_u16(p + 4);
-    } else {
-      const uint32_t a = ld_nc_u16(p), b = ld_nc_u32(p + 2);
-      w[0] = a | (b << 16);
-      w[1] = b >> 16;
-    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(a0, b0, a1, b1);
   }
 }
 
+// Load one unit of packed codes (words for unpack_group<BITS, 0> and <BITS, 1>).
 template <int BITS>
+__device__ __forceinline__ void load_unit(const uint8_t* p, uint32_t w[4]) {
+  if constexpr (BITS == 6) {
+    w[0] = ld_nc_u32(p);
+    w[1] = ld_nc_u32(p + 4);
+    w[2] = ld_nc_u32(p + 8);
+    w[3] = 0;
+  } else if constexpr (BITS == 4) {
+    const uint2 v = ld_nc_v2(p);
+    w[0] = v.x; w[1] = v.y; w[2] = w[3] = 0;
+  } else {
+    const uint4 v = ld_nc_v4(p);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  }
+}
+
+template <int BITS, int UPL>
 __global__ void __launch_bounds__(kThreads) quant_pack_kernel(const PackArgs a) {
-  constexpr float kQ = static_cast<float>(Q<BITS>::kQmax);
+  constexpr int kQm = Q<BITS>::kQmax;
+  constexpr int kB = Q<BITS>::kBias;
+  constexpr int kM = Q<BITS>::kMask;
   const int t = blockIdx.y;
   const uint16_t* __restrict__ x = a.x[t];
   const PoolRef pool = a.pool[t];
   const int lane = threadIdx.x & 31;
   const int lpr = 1 << a.lpr_log2;
   const int rps = 32 >> a.lpr_log2;
-  const int chunk = lane & (lpr - 1);
-  const int sub = lane >> a.lpr_log2;
-  const int H = a.H;
+  const int lr = lane & (lpr - 1);       // lane within the row
+  const int sub = lane >> a.lpr_log2;    // row within the step
+  const int H = a.H, D = a.D;
   const int n_items = (a.total_tokens + kTok - 1) / kTok;
   const int n_warps = gridDim.x * kWarpsPerBlock;
 
@@ -142,47 +144,71 @@ __global__ void __launch_bounds__(kThreads) quant_pack_kernel(const PackArgs a) 
     long long base = -1;
     if (lane < ntok) base = token_base(a, pool.num_pages, tok0 + lane);
     const int nrows = ntok * H;
-    const uint16_t* xi = x + static_cast<int64_t>(tok0) * H * a.D + chunk * 8;
+    const uint16_t* xi = x + static_cast<int64_t>(tok0) * H * D;
     for (int r0 = 0; r0 < nrows; r0 += rps * kUnroll) {
-      uint4 v[kUnroll];
+      uint4 v[kUnroll][UPL][2];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int row = r0 + u * rps + sub;
-        v[u] = make_uint4(0, 0, 0, 0);
-        if (row < nrows && chunk < a.chunks)
-          v[u] = ld_stream_v4(xi + static_cast<int64_t>(row) * a.D);
+#pragma unroll
+        for (int j = 0; j < UPL; ++j) {
+          const int unit = lr + j * lpr;
+          const int e0 = unit * 16;
+          v[u][j][0] = v[u][j][1] = make_uint4(0, 0, 0, 0);
+          if (row < nrows && e0 < D) {
+            const uint16_t* src = xi + static_cast<int64_t>(row) * D + e0;
+            v[u][j][0] = ld_stream_v4(src);
+            v[u][j][1] = ld_stream_v4(src + 8);
+          }
+        }
       }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int row = r0 + u * rps + sub;
-        float amax = half2_absmax(v[u]);
+        __half2 m2 = absmax8(v[u][0][0]);
+        m2 = __hmax2(m2, absmax8(v[u][0][1]));
+#pragma unroll
+        for (int j = 1; j < UPL; ++j) m2 = __hmax2(m2, __hmax2(absmax8(v[u][j][0]), absmax8(v[u][j][1])));
+        float amax = fmaxf(__low2float(m2), __high2float(m2));
         for (int o = lpr >> 1; o >= 1; o >>= 1)
           amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, o));
         const int k = row / H;
         const long long b = shfl_ll(base, k < kTok ? k : 0);
-        if (row >= nrows || chunk >= a.chunks || b < 0) continue;
+        if (row >= nrows || b < 0) continue;
         const int64_t prow = b + static_cast<int64_t>(row - k * H) * a.page_size;
-        const uint16_t sbits = f2h(__fdiv_rn(amax, kQ));
+        const uint16_t sbits = f2h(row_scale_f32<kQm>(amax));
         const float s = h2f(sbits);
         // s == 0: y = 0 gives a zero quotient (codes 0); subnormal s: clip to +-qmax
         const float y = (s == 0.f) ? 0.f : __frcp_rn(s);
         const float se = (s == 0.f) ? 1.f : s;
         const bool clip = s < 6.103515625e-05f;   // 2^-14, smallest normal fp16
-        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        uint32_t f[8];
+        uint8_t* crow = pool.codes + prow * a.pd;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float xe = h2f(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
-          f[e] = quant_field<Q<BITS>::kQmax, Q<BITS>::kBias, Q<BITS>::kMask>(xe, se, y, clip);
+        for (int j = 0; j < UPL; ++j) {
+          const int unit = lr + j * lpr;
+          if (unit * 16 >= D) continue;
+          uint32_t pk[4];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint4& vv = v[u][j][hh];
+            const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+            uint32_t f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float xe = h2f(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
+              f[e] = quant_field<kQm, kB, kM>(xe, se, y, clip);
+            }
+            pack8<BITS>(f, pk[2 * hh], pk[2 * hh + 1]);
+          }
+          store_unit<BITS>(crow + unit * Q<BITS>::kUnitBytes, pk[0], pk[1], pk[2], pk[3]);
         }
-        store_fields<BITS>(pool.codes, prow * a.chunks + chunk, f);
-        if (chunk == 0) pool.scales[prow] = sbits;
+        if (lr == 0) pool.scales[prow] = sbits;
       }
     }
   }
 }
 
-template <int BITS>
+template <int BITS, int UPL>
 __global__ void __launch_bounds__(kThreads) dequant_kernel(const PackArgs a) {
   const int t = blockIdx.y;
   uint16_t* __restrict__ out = const_cast<uint16_t*>(a.x[t]);
@@ -190,9 +216,9 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const PackArgs a) {
   const int lane = threadIdx.x & 31;
   const int lpr = 1 << a.lpr_log2;
   const int rps = 32 >> a.lpr_log2;
-  const int chunk = lane & (lpr - 1);
+  const int lr = lane & (lpr - 1);
   const int sub = lane >> a.lpr_log2;
-  const int H = a.H;
+  const int H = a.H, D = a.D;
   const int n_items = (a.total_tokens + kTok - 1) / kTok;
   const int n_warps = gridDim.x * kWarpsPerBlock;
 
@@ -203,9 +229,9 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const PackArgs a) {
     long long base = -1;
     if (lane < ntok) base = token_base(a, pool.num_pages, tok0 + lane);
     const int nrows = ntok * H;
-    uint16_t* oi = out + static_cast<int64_t>(tok0) * H * a.D + chunk * 8;
+    uint16_t* oi = out + static_cast<int64_t>(tok0) * H * D;
     for (int r0 = 0; r0 < nrows; r0 += rps * kUnroll) {
-      uint32_t w[kUnroll][2];
+      uint32_t w[kUnroll][UPL][4];
       uint32_t sc[kUnroll];
       bool act[kUnroll];
 #pragma unroll
@@ -213,12 +239,18 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const PackArgs a) {
         const int row = r0 + u * rps + sub;
         const int k = row / H;
         const long long b = shfl_ll(base, k < kTok ? k : 0);
-        act[u] = row < nrows && chunk < a.chunks && b >= 0;
-        w[u][0] = w[u][1] = 0;
+        act[u] = row < nrows && b >= 0;
         sc[u] = 0;
+#pragma unroll
+        for (int j = 0; j < UPL; ++j) w[u][j][0] = w[u][j][1] = w[u][j][2] = w[u][j][3] = 0;
         if (act[u]) {
           const int64_t prow = b + static_cast<int64_t>(row - k * H) * a.page_size;
-          load_fields<BITS>(pool.codes, prow * a.chunks + chunk, w[u]);
+          const uint8_t* crow = pool.codes + prow * a.pd;
+#pragma unroll
+          for (int j = 0; j < UPL; ++j) {
+            const int unit = lr + j * lpr;
+            if (unit * 16 < D) load_unit<BITS>(crow + unit * Q<BITS>::kUnitBytes, w[u][j]);
+          }
           sc[u] = ld_nc_u16(pool.scales + prow);
         }
       }
@@ -226,16 +258,27 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const PackArgs a) {
       for (int u = 0; u < kUnroll; ++u) {
         if (!act[u]) continue;
         const int row = r0 + u * rps + sub;
-        uint32_t p[4];
-        unpack_group<BITS, 0>(w[u], p);          // {e_k, e_{k+4}}
         const uint32_t s2 = sc[u] | (sc[u] << 16);
-        // exact codes times the fp16 scale: one rounding, the same as fp16(float(c) * scale)
-        const uint32_t o0 = hmul2u(prmt(p[0], p[1], 0x5410u), s2);   // e0 e1
-        const uint32_t o1 = hmul2u(prmt(p[2], p[3], 0x5410u), s2);   // e2 e3
-        const uint32_t o2 = hmul2u(prmt(p[0], p[1], 0x7632u), s2);   // e4 e5
-        const uint32_t o3 = hmul2u(prmt(p[2], p[3], 0x7632u), s2);   // e6 e7
-        *reinterpret_cast<uint4*>(oi + static_cast<int64_t>(row) * a.D) =
-            make_uint4(o0, o1, o2, o3);
+        uint16_t* orow = oi + static_cast<int64_t>(row) * D;
+#pragma unroll
+        for (int j = 0; j < UPL; ++j) {
+          const int unit = lr + j * lpr;
+          if (unit * 16 >= D) continue;
+          uint32_t p[4], q[4];
+          unpack_group<BITS, 0>(w[u][j], p);     // elements 0..7 of the unit: {e_k, e_k+4}
+          unpack_group<BITS, 1>(w[u][j], q);     // elements 8..15
+          // exact codes times the fp16 scale: one rounding, the same as fp16(float(c) * scale)
+          const uint4 o0 = make_uint4(hmul2u(prmt(p[0], p[1], 0x5410u), s2),
+                                      hmul2u(prmt(p[2], p[3], 0x5410u), s2),
+                                      hmul2u(prmt(p[0], p[1], 0x7632u), s2),
+                                      hmul2u(prmt(p[2], p[3], 0x7632u), s2));
+          const uint4 o1 = make_uint4(hmul2u(prmt(q[0], q[1], 0x5410u), s2),
+                                      hmul2u(prmt(q[2], q[3], 0x5410u), s2),
+                                      hmul2u(prmt(q[0], q[1], 0x7632u), s2),
+                                      hmul2u(prmt(q[2], q[3], 0x7632u), s2));
+          *reinterpret_cast<uint4*>(orow + unit * 16) = o0;
+          *reinterpret_cast<uint4*>(orow + unit * 16 + 8) = o1;
+        }
       }
     }
   }
@@ -249,25 +292,46 @@ int ceil_log2(int v) {
 
 // Persistent grid: blockIdx.y = tensor; per tensor enough blocks for its token blocks, with all
 // tensors together at most what is resident on the SMs at once.
-template <int BITS, bool QUANT>
-dim3 grid_for(int n_tensors, int total_tokens) {
-  static int blocks_per_sm = 0;
-  if (blocks_per_sm == 0) {
+template <typename K>
+dim3 grid_for(K kernel, int& cache, int n_tensors, int total_tokens) {
+  if (cache == 0) {
     int b = 0;
-    cudaError_t e = QUANT ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                &b, quant_pack_kernel<BITS>, kThreads, 0)
-                          : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                &b, dequant_kernel<BITS>, kThreads, 0);
-    blocks_per_sm = (e != cudaSuccess || b < 1) ? 1 : b;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0);
+    cache = (e != cudaSuccess || b < 1) ? 1 : b;
   }
   const int64_t items = (static_cast<int64_t>(total_tokens) + kTok - 1) / kTok;
   const int64_t need = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const int sms = sm_count();
-  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * blocks_per_sm;
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * cache;
   int64_t per = (cap + n_tensors - 1) / n_tensors;
   if (per > need) per = need;
   if (per < 1) per = 1;
   return dim3(static_cast<unsigned>(per), static_cast<unsigned>(n_tensors));
+}
+
+template <int BITS, int UPL, bool QUANT>
+cudaError_t launch_one(const PackArgs& a, cudaStream_t stream) {
+  static int cache = 0;
+  if (QUANT) {
+    quant_pack_kernel<BITS, UPL>
+        <<<grid_for(quant_pack_kernel<BITS, UPL>, cache, a.n_tensors, a.total_tokens), kThreads,
+           0, stream>>>(a);
+  } else {
+    dequant_kernel<BITS, UPL>
+        <<<grid_for(dequant_kernel<BITS, UPL>, cache, a.n_tensors, a.total_tokens), kThreads, 0,
+           stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+template <bool QUANT>
+cudaError_t launch_bits(const PackArgs& a, int bits, cudaStream_t stream) {
+  const int upl = (a.units + (1 << a.lpr_log2) - 1) >> a.lpr_log2;  // 1 or 2 for D <= 256
+  switch (bits) {
+    case 8: return upl == 1 ? launch_one<8, 1, QUANT>(a, stream) : launch_one<8, 2, QUANT>(a, stream);
+    case 6: return upl == 1 ? launch_one<6, 1, QUANT>(a, stream) : launch_one<6, 2, QUANT>(a, stream);
+    default: return upl == 1 ? launch_one<4, 1, QUANT>(a, stream) : launch_one<4, 2, QUANT>(a, stream);
+  }
 }
 
 kvq_status prepare(PackArgs& a, const kvq_pool* pools, const uint16_t* const* x, int n_tensors,
@@ -292,6 +356,8 @@ kvq_status prepare(PackArgs& a, const kvq_pool* pools, const uint16_t* const* x,
     if (!aligned16(x[i])) return fail(KVQ_ERR_ALIGN, "%s: tensor %d not 16-byte aligned", what, i);
   }
   const kvq_pool& p0 = pools[0];
+  if (p0.head_dim % 16)
+    return fail(KVQ_ERR_SHAPE, "%s: head_dim %d must be a multiple of 16", what, p0.head_dim);
   a.n_tensors = n_tensors;
   a.H = p0.num_heads;
   a.D = p0.head_dim;
@@ -299,8 +365,8 @@ kvq_status prepare(PackArgs& a, const kvq_pool* pools, const uint16_t* const* x,
   a.pd = kvq_packed_dim(p0.head_dim, p0.bits);
   a.max_pages = max_pages;
   a.nseq = nseq;
-  a.chunks = p0.head_dim / 8;
-  a.lpr_log2 = ceil_log2(a.chunks);
+  a.units = (p0.head_dim + 15) / 16;
+  a.lpr_log2 = ceil_log2(a.units) < 3 ? ceil_log2(a.units) : 3;
   a.total_tokens = total_tokens;
   a.page_table = page_table;
   a.cu = cu;
@@ -319,24 +385,14 @@ kvq_status prepare(PackArgs& a, const kvq_pool* pools, const uint16_t* const* x,
 // explicit launchers (kernel templates cannot be template-template args portably)
 static kvq_status launch_quant(const PackArgs& a, int bits, cudaStream_t stream) {
   if (a.total_tokens == 0) return ok();
-  switch (bits) {
-    case 8: quant_pack_kernel<8><<<grid_for<8, true>(a.n_tensors, a.total_tokens), kThreads, 0, stream>>>(a); break;
-    case 6: quant_pack_kernel<6><<<grid_for<6, true>(a.n_tensors, a.total_tokens), kThreads, 0, stream>>>(a); break;
-    default: quant_pack_kernel<4><<<grid_for<4, true>(a.n_tensors, a.total_tokens), kThreads, 0, stream>>>(a); break;
-  }
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_bits<true>(a, bits, stream);
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "quant_pack launch: %s", cudaGetErrorString(e));
   return ok();
 }
 
 static kvq_status launch_dequant(const PackArgs& a, int bits, cudaStream_t stream) {
   if (a.total_tokens == 0) return ok();
-  switch (bits) {
-    case 8: dequant_kernel<8><<<grid_for<8, false>(a.n_tensors, a.total_tokens), kThreads, 0, stream>>>(a); break;
-    case 6: dequant_kernel<6><<<grid_for<6, false>(a.n_tensors, a.total_tokens), kThreads, 0, stream>>>(a); break;
-    default: dequant_kernel<4><<<grid_for<4, false>(a.n_tensors, a.total_tokens), kThreads, 0, stream>>>(a); break;
-  }
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_bits<false>(a, bits, stream);
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "dequant launch: %s", cudaGetErrorString(e));
   return ok();
 }

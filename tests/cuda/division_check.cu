@@ -1,11 +1,12 @@
 // Exhaustive check of the quantizer's per-element arithmetic (test only).
 //
 // For every finite fp16 x and every positive finite fp16 scale s it compares
-//   (1) the per-row-reciprocal quotient (Markstein correction) with IEEE float32 division, and
+//   (1) the per-row-reciprocal quotient (Markstein correction) with IEEE float32 division,
 //   (2) the stored field of q8/q6/q4 with clamp(rint_half_even(x / s), -qmax, qmax) + bias computed
 //       from IEEE division, on the inputs the quantizer can see: all x when s is subnormal, and
 //       |x| <= qmax * s * (1 + 2^-9) when s is normal (a superset of |x| <= amax, since
-//       s = fp16(amax / qmax)).
+//       s = fp16(amax / qmax)), and
+//   (3) the division-free row scale amax / qmax with IEEE division for every fp16 amax.
 #include <cstdint>
 #include <cstdio>
 #include <cuda_runtime.h>
@@ -48,15 +49,25 @@ __global__ void check_kernel(unsigned long long* bad) {
   if (n4) atomicAdd(bad + 3, n4);
 }
 
+__global__ void scale_kernel(unsigned long long* bad) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;   // all positive finite fp16 amax
+  if (i < 1 || i > 0x7BFF) return;
+  const float amax = __half2float(__ushort_as_half(static_cast<uint16_t>(i)));
+  if (kvq::row_scale_f32<127>(amax) != __fdiv_rn(amax, 127.f)) atomicAdd(bad + 4, 1ull);
+  if (kvq::row_scale_f32<31>(amax) != __fdiv_rn(amax, 31.f)) atomicAdd(bad + 4, 1ull);
+  if (kvq::row_scale_f32<7>(amax) != __fdiv_rn(amax, 7.f)) atomicAdd(bad + 4, 1ull);
+}
+
 }  // namespace
 
 extern "C" int run_division_check(unsigned long long* host_bad) {
   unsigned long long* d = nullptr;
-  if (cudaMalloc(&d, 4 * sizeof(unsigned long long)) != cudaSuccess) return 1;
-  cudaMemset(d, 0, 4 * sizeof(unsigned long long));
+  if (cudaMalloc(&d, 5 * sizeof(unsigned long long)) != cudaSuccess) return 1;
+  cudaMemset(d, 0, 5 * sizeof(unsigned long long));
   check_kernel<<<4096, 256>>>(d);
+  scale_kernel<<<(0x7C00 + 255) / 256, 256>>>(d);
   cudaError_t e = cudaDeviceSynchronize();
-  if (e == cudaSuccess) e = cudaMemcpy(host_bad, d, 4 * sizeof(unsigned long long),
+  if (e == cudaSuccess) e = cudaMemcpy(host_bad, d, 5 * sizeof(unsigned long long),
                                        cudaMemcpyDeviceToHost);
   cudaFree(d);
   return e == cudaSuccess ? 0 : 2;

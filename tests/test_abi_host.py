@@ -137,6 +137,7 @@ def test_quant_pack_rejects_bad_arguments_before_launch(kvq):
     assert _qp(kvq, _pool(kvq, bits=5)) == 1
     assert _qp(kvq, _pool(kvq, bits=16)) == 1
     assert _qp(kvq, _pool(kvq, D=12)) == 2
+    assert _qp(kvq, _pool(kvq, D=24)) == 2          # multiple of 8 but not of 16
     assert _qp(kvq, _pool(kvq, D=264)) == 2
     assert _qp(kvq, _pool(kvq, H=0)) == 2
     assert _qp(kvq, _pool(kvq, ps=0)) == 2

@@ -25,6 +25,6 @@ def test_fast_quotient_and_fields_match_ieee_division_exhaustively(kvq, cuda_dev
            "-I", os.path.join(ROOT, "include"), src, "-o", so]
     subprocess.run(cmd, check=True, capture_output=True)
     lib = ctypes.CDLL(so)
-    bad = (ctypes.c_ulonglong * 4)()
+    bad = (ctypes.c_ulonglong * 5)()
     assert lib.run_division_check(bad) == 0
-    assert list(bad) == [0, 0, 0, 0], f"mismatches quotient/q8/q6/q4: {list(bad)}"
+    assert list(bad) == [0] * 5, f"mismatches quotient/q8/q6/q4/row-scale: {list(bad)}"

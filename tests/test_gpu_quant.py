@@ -66,10 +66,11 @@ def test_contiguous_roundtrip_one_layer(kvq, cuda_dev, bits):
 
 
 @pytest.mark.parametrize("bits", [8, 6, 4])
-@pytest.mark.parametrize("D", [8, 24, 64, 96, 128, 192, 256])
+@pytest.mark.parametrize("D", [16, 48, 64, 80, 96, 128, 192, 256])
 def test_edge_rows_all_head_dims(kvq, cuda_dev, bits, D):
     """Magnitudes from fp16-subnormal scales to 2^11, outliers, zero rows, exact ties; ragged
-    sequence lengths (0, 1, page-1, page, page+1, many pages) over a random page table."""
+    sequence lengths (0, 1, page-1, page, page+1, many pages) over a random page table; head
+    dims whose rows take 1 to 16 units of 16 elements."""
     H, ps = 3, 16
     lens = [0, 1, 15, 16, 17, 100, 0, 333]
     pps = max((n + ps - 1) // ps for n in lens)
