@@ -64,9 +64,10 @@ struct AttnArgs {
 };
 
 template <int BITS> struct Wd;
-template <> struct Wd<8> { static constexpr int kPd = 256, kKWords = 16, kVWords = 8, kStages = 3; };
-template <> struct Wd<6> { static constexpr int kPd = 192, kKWords = 12, kVWords = 6, kStages = 4; };
-template <> struct Wd<4> { static constexpr int kPd = 128, kKWords = 8, kVWords = 4, kStages = 4; };
+// Stage counts keep three CTAs (12 warps) resident per SM within 228 KB of shared memory.
+template <> struct Wd<8> { static constexpr int kPd = 256, kKWords = 16, kVWords = 8, kStages = 2; };
+template <> struct Wd<6> { static constexpr int kPd = 192, kKWords = 12, kVWords = 6, kStages = 3; };
+template <> struct Wd<4> { static constexpr int kPd = 128, kKWords = 8, kVWords = 4, kStages = 3; };
 
 // shared-memory stage: [K codes 16 x pd][V codes 16 x pd][K scales 16 x 2][V scales 16 x 2]
 template <int BITS> __host__ __device__ constexpr int stage_bytes() { return 2 * kTile * Wd<BITS>::kPd + 4 * kTile; }
@@ -143,21 +144,28 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 }
 
 // ------------------------------------------------------------------------------ tile compute
-// One 16-token tile: K words of rows g, g+8 (thread's 64 head-dim elements), V words of tokens
-// 2c, 2c+1, 2c+8, 2c+9 (thread's 32 head-dim elements), their fp16 scales (0 for masked tokens).
+// One 16-token tile: K words of rows g, g+8 (thread's 64 head-dim elements) with their fp16
+// scales; V words of tokens 2c, 2c+1, 2c+8, 2c+9 (thread's 32 head-dim elements) with their
+// scales (0 for masked tokens).  V is read only after Q.K^T so the two share registers.
 template <int BITS>
-struct TileRegs {
+struct KRegs {
   uint32_t kw[2][Wd<BITS>::kKWords];
   uint32_t ksc[2];   // fp16 scale duplicated in both halves
   bool kval[2];
+};
+
+template <int BITS>
+struct VRegs {
   uint32_t vw[4][Wd<BITS>::kVWords];
   uint32_t vsc[4];   // fp16 scale bits (0 if the token is masked)
 };
 
+// Q.K^T of one tile and the online-softmax update; returns P^T as the two B-operand registers.
 template <int BITS>
-__device__ __forceinline__ void tile_compute(const TileRegs<BITS>& T, const uint32_t (&qf)[16][2],
-                                             float (&acc)[16][4], float& m0, float& m1,
-                                             float& l0, float& l1, float qk_scale) {
+__device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const uint32_t (&qf)[16][2],
+                                                float (&acc)[16][4], float& m0, float& m1,
+                                                float& l0, float& l1, float qk_scale,
+                                                uint32_t& pb0, uint32_t& pb1) {
   // ---------------- S^T = K_hat . Q^T  (four independent accumulation chains)
   float sacc4[4][4] = {};
 #define KVQ_QK_GROUP(GI)                                                                \
@@ -210,9 +218,15 @@ __device__ __forceinline__ void tile_compute(const TileRegs<BITS>& T, const uint
       acc[mt][0] *= al0; acc[mt][1] *= al1; acc[mt][2] *= al0; acc[mt][3] *= al1;
     }
   }
-  const uint32_t pb0 = movtrans(pack_h2(p[0], p[1]));   // tokens 2c, 2c+1 ; head g
-  const uint32_t pb1 = movtrans(pack_h2(p[2], p[3]));   // tokens 8+2c, 8+2c+1 ; head g
+  pb0 = movtrans(pack_h2(p[0], p[1]));   // tokens 2c, 2c+1 ; head g
+  pb1 = movtrans(pack_h2(p[2], p[3]));   // tokens 8+2c, 8+2c+1 ; head g
+}
 
+
+// O^T += V_hat^T . P^T for one tile.
+template <int BITS>
+__device__ __forceinline__ void tile_pv(const VRegs<BITS>& T, uint32_t pb0, uint32_t pb1,
+                                        float (&acc)[16][4]) {
   // ---------------- O^T += V_hat^T . P^T
   const uint32_t sab = T.vsc[0] | (T.vsc[1] << 16), scd = T.vsc[2] | (T.vsc[3] << 16);
 #define KVQ_PV_GROUP(GI)                                                                \
@@ -308,7 +322,7 @@ __device__ __forceinline__ void cta_merge_write(const AttnArgs& a, float* sm, in
 
 // ------------------------------------------------------------------------------ TMA kernel
 template <int BITS>
-__global__ void __launch_bounds__(kThreads, 2) decode_attn_tma_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) decode_attn_tma_kernel(const AttnArgs a) {
   using W = Wd<BITS>;
   constexpr int S = W::kStages;
   constexpr int kPd = W::kPd;
@@ -395,39 +409,42 @@ __global__ void __launch_bounds__(kThreads, 2) decode_attn_tma_kernel(const Attn
     const uint16_t* svs = sks + kTile;
     const bool ok = flags[st] != 0;
     const int tb = (tile0 + warp + j * kWarps) * kTile;
-    TileRegs<BITS> T;
+    KRegs<BITS> K;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int row = g + 8 * r;
-      T.kval[r] = ok && tb + row < len;
+      K.kval[r] = ok && tb + row < len;
       const uint32_t sb = sks[row];
-      T.ksc[r] = sb | (sb << 16);
+      K.ksc[r] = sb | (sb << 16);
       const uint4* src = reinterpret_cast<const uint4*>(sk + row * kPd + c * (4 * W::kKWords));
 #pragma unroll
       for (int i = 0; i < W::kKWords / 4; ++i) {
         const uint4 v = src[i];
-        T.kw[r][4 * i] = v.x; T.kw[r][4 * i + 1] = v.y;
-        T.kw[r][4 * i + 2] = v.z; T.kw[r][4 * i + 3] = v.w;
+        K.kw[r][4 * i] = v.x; K.kw[r][4 * i + 1] = v.y;
+        K.kw[r][4 * i + 2] = v.z; K.kw[r][4 * i + 3] = v.w;
       }
     }
+    uint32_t pb0, pb1;
+    tile_qk_softmax<BITS>(K, qf, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1);
+    VRegs<BITS> V;
 #pragma unroll
     for (int qi = 0; qi < 4; ++qi) {
       const int row = 2 * c + (qi & 1) + 8 * (qi >> 1);
       const bool v_ok = ok && tb + row < len;
-      T.vsc[qi] = v_ok ? svs[row] : 0u;
+      V.vsc[qi] = v_ok ? svs[row] : 0u;
       const uint8_t* src = sv + row * kPd + g * (4 * W::kVWords);
       if constexpr (W::kVWords % 4 == 0) {
 #pragma unroll
         for (int i = 0; i < W::kVWords / 4; ++i) {
           const uint4 v = reinterpret_cast<const uint4*>(src)[i];
-          T.vw[qi][4 * i] = v.x; T.vw[qi][4 * i + 1] = v.y;
-          T.vw[qi][4 * i + 2] = v.z; T.vw[qi][4 * i + 3] = v.w;
+          V.vw[qi][4 * i] = v.x; V.vw[qi][4 * i + 1] = v.y;
+          V.vw[qi][4 * i + 2] = v.z; V.vw[qi][4 * i + 3] = v.w;
         }
       } else {
 #pragma unroll
         for (int i = 0; i < W::kVWords / 2; ++i) {
           const uint2 v = reinterpret_cast<const uint2*>(src)[i];
-          T.vw[qi][2 * i] = v.x; T.vw[qi][2 * i + 1] = v.y;
+          V.vw[qi][2 * i] = v.x; V.vw[qi][2 * i + 1] = v.y;
         }
       }
     }
@@ -438,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_attn_tma_kernel(const Attn
       issue(j + S);
       ++issued;
     }
-    tile_compute<BITS>(T, qf, acc, m0, m1, l0, l1, a.qk_scale);
+    tile_pv<BITS>(V, pb0, pb1, acc);
   }
 
   if (timed_out) {
@@ -460,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_attn_tma_kernel(const Attn
 // ------------------------------------------------------------------------------ gather kernel
 // Any page size: each thread loads the rows of its tokens with plain loads.
 template <int BITS>
-__global__ void __launch_bounds__(kThreads, 2) decode_attn_gather_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) decode_attn_gather_kernel(const AttnArgs a) {
   using W = Wd<BITS>;
   __shared__ __align__(16) float sm[kMergeBytes / 4];
   const int warp = threadIdx.x >> 5;
@@ -489,56 +506,59 @@ __global__ void __launch_bounds__(kThreads, 2) decode_attn_gather_kernel(const A
 
   for (int tile = tile0 + warp; tile < tile1; tile += kWarps) {
     const int tb = tile * kTile;
-    TileRegs<BITS> T;
+    KRegs<BITS> K;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int t = tb + g + 8 * r;
       int64_t row = -1;
       if (t < len) row = locate_row(a.pt, a.max_pages, a.ps, a.H, P.k_pages, s, t, h, a.err);
-      T.kval[r] = row >= 0;
-      T.ksc[r] = 0;
+      K.kval[r] = row >= 0;
+      K.ksc[r] = 0;
 #pragma unroll
-      for (int i = 0; i < W::kKWords; ++i) T.kw[r][i] = 0;
+      for (int i = 0; i < W::kKWords; ++i) K.kw[r][i] = 0;
       if (row >= 0) {
         const uint8_t* src = P.kc + row * W::kPd + c * (4 * W::kKWords);
 #pragma unroll
         for (int i = 0; i < W::kKWords / 4; ++i) {
           const uint4 v = ld_nc_v4(src + 16 * i);
-          T.kw[r][4 * i] = v.x; T.kw[r][4 * i + 1] = v.y;
-          T.kw[r][4 * i + 2] = v.z; T.kw[r][4 * i + 3] = v.w;
+          K.kw[r][4 * i] = v.x; K.kw[r][4 * i + 1] = v.y;
+          K.kw[r][4 * i + 2] = v.z; K.kw[r][4 * i + 3] = v.w;
         }
         const uint32_t sb = ld_nc_u16(P.ks + row);
-        T.ksc[r] = sb | (sb << 16);
+        K.ksc[r] = sb | (sb << 16);
       }
     }
+    uint32_t pb0, pb1;
+    tile_qk_softmax<BITS>(K, qf, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1);
+    VRegs<BITS> V;
 #pragma unroll
     for (int qi = 0; qi < 4; ++qi) {
       const int t = tb + 2 * c + (qi & 1) + 8 * (qi >> 1);
       int64_t row = -1;
       if (t < len) row = locate_row(a.pt, a.max_pages, a.ps, a.H, P.v_pages, s, t, h, a.err);
-      T.vsc[qi] = 0;
+      V.vsc[qi] = 0;
 #pragma unroll
-      for (int i = 0; i < W::kVWords; ++i) T.vw[qi][i] = 0;
+      for (int i = 0; i < W::kVWords; ++i) V.vw[qi][i] = 0;
       if (row >= 0) {
         const uint8_t* src = P.vc + row * W::kPd + g * (4 * W::kVWords);
         if constexpr (W::kVWords % 4 == 0) {
 #pragma unroll
           for (int i = 0; i < W::kVWords / 4; ++i) {
             const uint4 v = ld_nc_v4(src + 16 * i);
-            T.vw[qi][4 * i] = v.x; T.vw[qi][4 * i + 1] = v.y;
-            T.vw[qi][4 * i + 2] = v.z; T.vw[qi][4 * i + 3] = v.w;
+            V.vw[qi][4 * i] = v.x; V.vw[qi][4 * i + 1] = v.y;
+            V.vw[qi][4 * i + 2] = v.z; V.vw[qi][4 * i + 3] = v.w;
           }
         } else {
 #pragma unroll
           for (int i = 0; i < W::kVWords / 2; ++i) {
             const uint2 v = ld_nc_v2(src + 8 * i);
-            T.vw[qi][2 * i] = v.x; T.vw[qi][2 * i + 1] = v.y;
+            V.vw[qi][2 * i] = v.x; V.vw[qi][2 * i + 1] = v.y;
           }
         }
-        T.vsc[qi] = ld_nc_u16(P.vs + row);
+        V.vsc[qi] = ld_nc_u16(P.vs + row);
       }
     }
-    tile_compute<BITS>(T, qf, acc, m0, m1, l0, l1, a.qk_scale);
+    tile_pv<BITS>(V, pb0, pb1, acc);
   }
   cta_merge_write(a, sm, ls, h, split, warp, g, c, acc, m0, m1, l0, l1);
 }
@@ -571,8 +591,8 @@ int tiles_per_cta_for(int n_layers, int nseq, int H, int max_seq_len) {
   const int tiles = (max_seq_len + kTile - 1) / kTile;
   const int sms = sm_count() > 0 ? sm_count() : 152;
   const int64_t units = static_cast<int64_t>(n_layers) * nseq * H;
-  // aim for >= 4 resident waves (2 CTAs per SM), at most 256 tiles (4096 tokens) per CTA
-  const int64_t want_splits = (8LL * sms + units - 1) / units;
+  // aim for >= 2 resident waves (3 CTAs per SM), at most 256 tiles (4096 tokens) per CTA
+  const int64_t want_splits = (6LL * sms + units - 1) / units;
   int64_t t = (tiles + want_splits - 1) / want_splits;
   if (t > 256) t = 256;
   t = ((t + kWarps - 1) / kWarps) * kWarps;

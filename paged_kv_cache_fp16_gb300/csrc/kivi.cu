@@ -8,12 +8,10 @@
 // rounding (explicit __f*_rn intrinsics so the compiler cannot fuse the multiply-add).  A ragged
 // last group reduces over its real elements only, which equals the page's padding by repetition.
 //
-// Keys: one warp per (tensor, b, h, token group); each lane owns a 16-byte chunk of 8 channels,
-// a group's rows are spread over the warp, per-channel min/max are reduced across the lanes that
-// share a chunk, and the tile is kept in registers between the two passes when it fits.
-// Values: each lane owns a chunk of one row; channel groups made of a power-of-two number of
-// whole chunks reduce with a segmented shuffle.  Other group sizes use a scalar kernel with one
-// thread per (row, channel group).  All of this is HBM-bound: 4 bytes per element (read + write).
+// Keys: one thread per (tensor, b, h, token group, channel pair) walks the group's tokens with the
+// pair's values in registers; adjacent threads own adjacent pairs of a row (coalesced rows).
+// Values: one thread per (row, channel group) holds the group in 16-byte vectors.  Groups that
+// are not a multiple of 8 channels use a scalar kernel.  HBM-bound: 4 bytes per element.
 // The data are modified in place, so loads use the coherent path (no ld.global.nc).
 #include <cuda_runtime.h>
 
@@ -24,7 +22,6 @@ namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kKeepChunks = 8;  // per-lane register cache for the key tile (8 x 16 B)
 
 // Passed by value (kernel parameter space): the library allocates no device memory.
 struct KiviArgs {
@@ -32,7 +29,7 @@ struct KiviArgs {
   int key_list[KVQ_MAX_TENSORS];  // indices into x of the key tensors
   int val_list[KVQ_MAX_TENSORS];  // indices into x of the value tensors
   int n_keys, n_vals;
-  int B, H, S, D, lo, hi, gs, chunks, lpr_log2;
+  int B, H, S, D, lo, hi, gs;
   float levels, eps;
 };
 
@@ -67,124 +64,118 @@ __device__ __forceinline__ uint4 roundtrip8(const float f[8], const float mn[8],
 }
 
 // ------------------------------------------------------------------------------ keys
-// Work item: (key tensor index among the call's tensors, b, h, group g).
+// One thread per (key tensor, b, h, token group, channel pair): it walks the group's tokens, keeps
+// the pair's values in registers (up to kKeepRows tokens; longer groups are read twice), reduces
+// min/max per channel without any cross-thread step, and writes the round trip back.  Adjacent
+// threads own adjacent channel pairs of the same token row, so every load and store of a row is
+// contiguous across the warp.
+constexpr int kKeepRows = 32;
+
 __global__ void __launch_bounds__(kThreads) kivi_keys_kernel(const KiviArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int lpr = 1 << a.lpr_log2;
-  const int rps = 32 >> a.lpr_log2;
-  const int chunk = lane & (lpr - 1);
-  const int sub = lane >> a.lpr_log2;
-  const bool lane_on = chunk < a.chunks;
   const int span = a.hi - a.lo;
   const int n_groups = (span + a.gs - 1) / a.gs;
-  const int64_t items = static_cast<int64_t>(a.n_keys) * a.B * a.H * n_groups;
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-
-  for (int64_t it = warp; it < items; it += n_warps) {
-    const int g = static_cast<int>(it % n_groups);
-    const int64_t bh_all = it / n_groups;
-    const int bh = static_cast<int>(bh_all % (static_cast<int64_t>(a.B) * a.H));
-    const int ti = a.key_list[bh_all / (static_cast<int64_t>(a.B) * a.H)];
+  const int pairs = a.D / 2;
+  const int64_t bh_count = static_cast<int64_t>(a.B) * a.H;
+  const int64_t items = static_cast<int64_t>(a.n_keys) * bh_count * n_groups * pairs;
+  for (int64_t it = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; it < items;
+       it += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int pr = static_cast<int>(it % pairs);
+    const int64_t r1 = it / pairs;
+    const int g = static_cast<int>(r1 % n_groups);
+    const int64_t r2 = r1 / n_groups;
+    const int64_t bh = r2 % bh_count;
+    const int ti = a.key_list[r2 / bh_count];
     const int t0 = a.lo + g * a.gs;
     const int n = min(a.gs, a.hi - t0);
-    uint16_t* base = a.x[ti] + (static_cast<int64_t>(bh) * a.S + t0) * a.D + chunk * 8;
-    const int steps = (n + rps - 1) / rps;
-
-    float mn[8], mx[8];
+    uint32_t* base = reinterpret_cast<uint32_t*>(a.x[ti] + (bh * a.S + t0) * a.D) + pr;
+    const int stride = a.D / 2;   // in half2 words
+    uint32_t keep[kKeepRows];
+    // fp16 +-inf as the identities (inputs are finite)
+    __half2 mn = __halves2half2(__ushort_as_half(0x7c00), __ushort_as_half(0x7c00));
+    __half2 mx = __halves2half2(__ushort_as_half(0xfc00), __ushort_as_half(0xfc00));
 #pragma unroll
-    for (int k = 0; k < 8; ++k) { mn[k] = __int_as_float(0x7f800000); mx[k] = -mn[k]; }
-    uint4 keep[kKeepChunks];
-#pragma unroll
-    for (int j = 0; j < kKeepChunks; ++j) keep[j] = make_uint4(0, 0, 0, 0);
-    for (int j = 0; j < steps; ++j) {
-      const int row = j * rps + sub;
-      if (lane_on && row < n) {
-        const uint4 v = *reinterpret_cast<const uint4*>(base + static_cast<int64_t>(row) * a.D);
-        float f[8];
-        to_f8(v, f);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) { mn[k] = fminf(mn[k], f[k]); mx[k] = fmaxf(mx[k], f[k]); }
-#pragma unroll
-        for (int q = 0; q < kKeepChunks; ++q) if (q == j) keep[q] = v;
+    for (int r = 0; r < kKeepRows; ++r) {
+      keep[r] = 0;
+      if (r < n) {
+        keep[r] = base[static_cast<int64_t>(r) * stride];
+        const __half2 v = *reinterpret_cast<const __half2*>(&keep[r]);
+        mn = __hmin2(mn, v);
+        mx = __hmax2(mx, v);
       }
     }
-    // lanes sharing a chunk differ in the bits above lpr_log2
-    for (int o = lpr; o < 32; o <<= 1) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        mn[k] = fminf(mn[k], __shfl_xor_sync(kFullMask, mn[k], o));
-        mx[k] = fmaxf(mx[k], __shfl_xor_sync(kFullMask, mx[k], o));
-      }
+    for (int r = kKeepRows; r < n; ++r) {
+      const uint32_t w = base[static_cast<int64_t>(r) * stride];
+      const __half2 v = *reinterpret_cast<const __half2*>(&w);
+      mn = __hmin2(mn, v);
+      mx = __hmax2(mx, v);
     }
-    float sc[8];
+    // fp16 min/max are exact; the group arithmetic is float32
+    const float mn0 = __low2float(mn), mn1 = __high2float(mn);
+    const float sc0 = group_scale(mn0, __low2float(mx), a.levels, a.eps);
+    const float sc1 = group_scale(mn1, __high2float(mx), a.levels, a.eps);
+    auto rt = [&](uint32_t w) -> uint32_t {
+      const uint32_t lo = roundtrip(h2f(static_cast<uint16_t>(w & 0xffffu)), mn0, sc0, a.levels);
+      const uint32_t hi = roundtrip(h2f(static_cast<uint16_t>(w >> 16)), mn1, sc1, a.levels);
+      return lo | (hi << 16);
+    };
 #pragma unroll
-    for (int k = 0; k < 8; ++k) sc[k] = group_scale(mn[k], mx[k], a.levels, a.eps);
-    if (!lane_on) continue;
-    for (int j = 0; j < steps; ++j) {
-      const int row = j * rps + sub;
-      if (row >= n) continue;
-      uint4 v;
-      if (j < kKeepChunks) {
-        v = keep[0];
-#pragma unroll
-        for (int q = 1; q < kKeepChunks; ++q) if (q == j) v = keep[q];
-      } else {
-        v = *reinterpret_cast<const uint4*>(base + static_cast<int64_t>(row) * a.D);
-      }
-      float f[8];
-      to_f8(v, f);
-      *reinterpret_cast<uint4*>(base + static_cast<int64_t>(row) * a.D) =
-          roundtrip8(f, mn, sc, a.levels);
-    }
+    for (int r = 0; r < kKeepRows; ++r)
+      if (r < n) base[static_cast<int64_t>(r) * stride] = rt(keep[r]);
+    for (int r = kKeepRows; r < n; ++r)
+      base[static_cast<int64_t>(r) * stride] = rt(base[static_cast<int64_t>(r) * stride]);
   }
 }
 
 // ------------------------------------------------------------------------------ values
-// One lane per 16-byte chunk of a row; channel groups of (1 << glog2) chunks starting at
-// channel 0.  Work item: one warp step of rows over all value tensors.
-__global__ void __launch_bounds__(kThreads) kivi_values_kernel(const KiviArgs a, int glog2) {
-  const int lane = threadIdx.x & 31;
-  const int lpr = 1 << a.lpr_log2;
-  const int rps = 32 >> a.lpr_log2;
-  const int chunk = lane & (lpr - 1);
-  const int sub = lane >> a.lpr_log2;
-  const int span = a.hi - a.lo;
-  const int64_t rows_per_tensor = static_cast<int64_t>(a.B) * a.H * span;
-  const int64_t total_rows = rows_per_tensor * a.n_vals;
-  const int64_t n_steps = (total_rows + rps - 1) / rps;
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-  const int gl = 1 << glog2;
+// One thread per (value tensor, row, channel group) for groups of a multiple of 8 channels
+// (16-byte vectors, at most 64 channels held in registers); the group's min/max, scale and round
+// trip stay in the thread.
+constexpr int kMaxVecs = 8;
 
-  for (int64_t st = warp; st < n_steps; st += n_warps) {
-    const int64_t row = st * rps + sub;
-    const bool on = row < total_rows && chunk < a.chunks;
-    uint16_t* p = nullptr;
-    float f[8];
+__global__ void __launch_bounds__(kThreads) kivi_values_kernel(const KiviArgs a) {
+  const int span = a.hi - a.lo;
+  const int groups = (a.D + a.gs - 1) / a.gs;
+  const int64_t rows_per_tensor = static_cast<int64_t>(a.B) * a.H * span;
+  const int64_t items = rows_per_tensor * a.n_vals * groups;
+  for (int64_t it = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; it < items;
+       it += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int g = static_cast<int>(it % groups);
+    const int64_t row = it / groups;
+    const int64_t vi = row / rows_per_tensor;
+    const int64_t r = row - vi * rows_per_tensor;
+    const int64_t bh = r / span;
+    const int t = a.lo + static_cast<int>(r - bh * span);
+    const int c0 = g * a.gs;
+    const int nv = (min(a.D, c0 + a.gs) - c0) / 8;   // 16-byte vectors in this group
+    uint4* p = reinterpret_cast<uint4*>(a.x[a.val_list[vi]] + (bh * a.S + t) * a.D + c0);
+    uint4 v[kMaxVecs];
+    __half2 mn = __halves2half2(__ushort_as_half(0x7c00), __ushort_as_half(0x7c00));
+    __half2 mx = __halves2half2(__ushort_as_half(0xfc00), __ushort_as_half(0xfc00));
 #pragma unroll
-    for (int k = 0; k < 8; ++k) f[k] = 0.f;
-    float mn = __int_as_float(0x7f800000), mx = -mn;
-    if (on) {
-      const int64_t vi = row / rows_per_tensor;
-      const int64_t r = row - vi * rows_per_tensor;
-      const int64_t bh = r / span;
-      const int t = a.lo + static_cast<int>(r - bh * span);
-      p = a.x[a.val_list[vi]] + (bh * a.S + t) * a.D + chunk * 8;
-      to_f8(*reinterpret_cast<const uint4*>(p), f);
+    for (int k = 0; k < kMaxVecs; ++k) {
+      v[k] = make_uint4(0, 0, 0, 0);
+      if (k < nv) {
+        v[k] = p[k];
+        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
-      for (int k = 0; k < 8; ++k) { mn = fminf(mn, f[k]); mx = fmaxf(mx, f[k]); }
+        for (int e = 0; e < 4; ++e) {
+          const __half2 h = *reinterpret_cast<const __half2*>(&w[e]);
+          mn = __hmin2(mn, h);
+          mx = __hmax2(mx, h);
+        }
+      }
     }
-    for (int o = 1; o < gl; o <<= 1) {
-      mn = fminf(mn, __shfl_xor_sync(kFullMask, mn, o));
-      mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, o));
-    }
-    if (!on) continue;
-    const float sc = group_scale(mn, mx, a.levels, a.eps);
-    float mn8[8], sc8[8];
+    const float mnf = fminf(__low2float(mn), __high2float(mn));
+    const float sc = group_scale(mnf, fmaxf(__low2float(mx), __high2float(mx)), a.levels, a.eps);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) { mn8[k] = mn; sc8[k] = sc; }
-    *reinterpret_cast<uint4*>(p) = roundtrip8(f, mn8, sc8, a.levels);
+    for (int k = 0; k < kMaxVecs; ++k) {
+      if (k >= nv) continue;
+      float f[8], mn8[8], sc8[8];
+      to_f8(v[k], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) { mn8[e] = mnf; sc8[e] = sc; }
+      p[k] = roundtrip8(f, mn8, sc8, a.levels);
+    }
   }
 }
 
@@ -211,19 +202,14 @@ __global__ void __launch_bounds__(kThreads) kivi_values_scalar_kernel(const Kivi
   }
 }
 
-int ceil_log2(int v) {
-  int l = 0;
-  while ((1 << l) < v) ++l;
-  return l;
-}
 
 int grid_cap() {
   const int sms = sm_count();
   return (sms > 0 ? sms : 1) * (2048 / kThreads);
 }
 
-int blocks_for_warps(int64_t warps) {
-  int64_t b = (warps + (kThreads / 32) - 1) / (kThreads / 32);
+int blocks_for_threads(int64_t threads) {
+  int64_t b = (threads + kThreads - 1) / kThreads;
   const int cap = grid_cap();
   if (b > cap) b = cap;
   return static_cast<int>(b < 1 ? 1 : b);
@@ -260,8 +246,6 @@ extern "C" kvq_status kivi_quant_dequant(uint16_t* const* x, const int32_t* is_k
 
   KiviArgs a;
   a.B = B; a.H = H; a.S = S; a.D = D; a.lo = lo; a.hi = hi; a.gs = group_size;
-  a.chunks = D / 8;
-  a.lpr_log2 = ceil_log2(a.chunks);
   a.levels = static_cast<float>(levels);
   a.eps = eps;
   a.n_keys = a.n_vals = 0;
@@ -275,26 +259,17 @@ extern "C" kvq_status kivi_quant_dequant(uint16_t* const* x, const int32_t* is_k
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int span = hi - lo;
   if (a.n_keys > 0) {
-    const int64_t items = static_cast<int64_t>(a.n_keys) * B * H * ((span + group_size - 1) / group_size);
-    kivi_keys_kernel<<<blocks_for_warps(items), kThreads, 0, st>>>(a);
+    const int64_t items = static_cast<int64_t>(a.n_keys) * B * H *
+                          ((span + group_size - 1) / group_size) * (D / 2);
+    kivi_keys_kernel<<<blocks_for_threads(items), kThreads, 0, st>>>(a);
   }
   if (a.n_vals > 0) {
-    // fast path: a group is a power-of-two number of whole 16-byte chunks (or the whole row)
-    int glog2 = -1;
-    const int lpr = 1 << a.lpr_log2;
-    if (group_size >= lpr * 8) {
-      glog2 = a.lpr_log2;
-    } else if (group_size % 8 == 0 && (group_size / 8 & (group_size / 8 - 1)) == 0) {
-      glog2 = ceil_log2(group_size / 8);
-    }
     const int64_t rows = static_cast<int64_t>(a.n_vals) * B * H * span;
-    if (glog2 >= 0) {
-      const int rps = 32 >> a.lpr_log2;
-      kivi_values_kernel<<<blocks_for_warps((rows + rps - 1) / rps), kThreads, 0, st>>>(a, glog2);
-    } else {
-      const int64_t items = rows * ((D + group_size - 1) / group_size);
-      kivi_values_scalar_kernel<<<blocks_for_warps((items + 31) / 32), kThreads, 0, st>>>(a);
-    }
+    const int64_t items = rows * ((D + group_size - 1) / group_size);
+    if (group_size % 8 == 0 && group_size <= 8 * kMaxVecs)
+      kivi_values_kernel<<<blocks_for_threads(items), kThreads, 0, st>>>(a);
+    else
+      kivi_values_scalar_kernel<<<blocks_for_threads(items), kThreads, 0, st>>>(a);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "kivi launch: %s", cudaGetErrorString(e));
