@@ -256,6 +256,31 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_pool* k_pools, const kvq_pool* v_po
                            float softmax_scale, float* out, void* workspace,
                            size_t workspace_bytes, int32_t* dev_err, kvq_stream_t stream);
 
+/*
+ * Decode attention for callers that cannot allocate device memory (no counterpart on the pages:
+ * it is an addition of this library).  Same arguments, semantics and errors as kvq_decode_attn,
+ * minus the workspace: the split partials go to a scratch array of 32 MiB that the library owns
+ * in device memory, which every GPU that loads the library holds until the process exits.
+ * Meant for code that cannot call cudaMalloc where it runs attention -- for example inside a
+ * runtime whose allocator owns all device memory, or a serving loop that must not allocate
+ * (cudaMalloc may synchronize the device) once it is running.  It calls no allocation routine.
+ *   - The first call on a device looks up the scratch array's device address (cached per
+ *     device); make that first call before any stream capture.
+ *   - All calls share the one array: calls whose kernels overlap on the GPU (other streams,
+ *     other threads) race on it and must be serialized by the caller.  Nothing in it needs to be
+ *     cleared between calls: every partial a call reads was written earlier by that same call.
+ *   - To fit the array, the number of splits over tokens is capped (each split of each
+ *     (layer, sequence, KV head) unit takes 8,320 bytes); a problem with more than 4,032
+ *     n_layers * nseq * num_kv_heads units does not fit even with one split each and returns
+ *     KVQ_ERR_RANGE with the byte counts in kvq_last_error().
+ */
+KVQ_API kvq_status kvq_decode_attn_noalloc(const kvq_pool* k_pools, const kvq_pool* v_pools,
+                                           int n_layers, const uint16_t* q, int num_q_heads,
+                                           const int32_t* page_table, int max_pages,
+                                           const int32_t* seq_lens, int nseq, int max_seq_len,
+                                           float softmax_scale, float* out, int32_t* dev_err,
+                                           kvq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -67,6 +67,7 @@ def _load() -> ctypes.CDLL:
         "kivi_quant_dequant": (I, [P, P, I, I, I, I, I, I, I, I, I, F, P]),
         "kvq_decode_attn_workspace": (S, [I, I, I, I, I, I, I]),
         "kvq_decode_attn": (I, [pool_p, pool_p, I, P, I, P, I, P, I, I, F, P, P, S, P, P]),
+        "kvq_decode_attn_noalloc": (I, [pool_p, pool_p, I, P, I, P, I, P, I, I, F, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -310,6 +311,32 @@ def kvq_decode_attn(k_pools: Sequence[Pool], v_pools: Sequence[Pool], q: torch.T
                                 _stream(stream)))
 
 
+def kvq_decode_attn_noalloc(k_pools: Sequence[Pool], v_pools: Sequence[Pool], q: torch.Tensor,
+                            page_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                            softmax_scale: float, out: torch.Tensor,
+                            dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """kvq_decode_attn without a workspace, for callers that cannot allocate device memory where
+    they run attention: the split partials use the library's own 32 MiB device array (shared by
+    all calls; calls that overlap on the GPU race).  Make the first call on a device before any
+    stream capture (it looks up that array's address)."""
+    if len(k_pools) != len(v_pools):
+        raise ValueError("one V pool per K pool")
+    _cuda_tensor(q, torch.float16, "q")
+    _cuda_tensor(out, torch.float32, "out")
+    _cuda_tensor(page_table, torch.int32, "page_table")
+    _cuda_tensor(seq_lens, torch.int32, "seq_lens")
+    n_layers, nseq, hq, _ = q.shape
+    if page_table.dim() != 2 or page_table.shape[0] < nseq or seq_lens.numel() < nseq:
+        raise ValueError("page_table needs a row and seq_lens an entry per sequence")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    _check(_lib.kvq_decode_attn_noalloc(_pool_array(k_pools), _pool_array(v_pools), n_layers,
+                                        q.data_ptr(), hq, page_table.data_ptr(),
+                                        page_table.shape[1], seq_lens.data_ptr(), nseq,
+                                        max_seq_len, softmax_scale, out.data_ptr(), _ptr(dev_err),
+                                        _stream(stream)))
+
+
 def decode_workspace(k_pools: Sequence[Pool], nseq: int, num_q_heads: int, max_seq_len: int,
                      device="cuda") -> torch.Tensor:
     """A workspace tensor of the size kvq_decode_attn needs."""
@@ -321,4 +348,5 @@ def decode_workspace(k_pools: Sequence[Pool], nseq: int, num_q_heads: int, max_s
 
 __all__ = ["KVQError", "Pool", "Allocator", "parse_mode", "kvq_version", "kvq_packed_dim",
            "kivi_boundary", "kvq_quant_pack_paged", "kvq_dequant_paged", "kivi_quant_dequant",
-           "kvq_decode_attn_workspace", "kvq_decode_attn", "decode_workspace", "LIB_PATH"]
+           "kvq_decode_attn_workspace", "kvq_decode_attn", "kvq_decode_attn_noalloc",
+           "decode_workspace", "LIB_PATH"]

@@ -25,6 +25,9 @@
 // (cp.async.bulk: the page's K codes, V codes, K scales and V scales, completing on one mbarrier
 // per stage); waits are bounded and report KVQ_DEVERR_TIMEOUT instead of hanging.  Other page
 // sizes gather rows with plain loads.
+#include <mutex>
+#include <vector>
+
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
@@ -714,5 +717,143 @@ extern "C" kvq_status kvq_decode_attn(const kvq_pool* k_pools, const kvq_pool* v
   }
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "decode attention launch: %s",
                                     cudaGetErrorString(e));
+  return ok();
+}
+
+// ------------------------------------------------------------------------------------------------
+// Decode attention without a caller-provided workspace.
+//
+// Some callers cannot call cudaMalloc at the point where they run attention: code embedded in a
+// runtime whose own allocator owns all device memory, or a latency-critical serving loop that
+// must not allocate (cudaMalloc can synchronize the device) once it is running.  For them the
+// split partials live in a fixed array of device memory that belongs to this library: every GPU
+// that loads the library holds it (32 MiB) until the process exits.
+namespace kvq {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(32) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array for the current device.  The host-side name of the array
+// is only a stand-in, so the address is looked up once per device (with that device current)
+// and cached.
+kvq_status noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static std::vector<void*> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess)
+    return fail(KVQ_ERR_CUDA, "kvq_decode_attn_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+  std::lock_guard<std::mutex> lock(mu);
+  if (static_cast<int>(cache.size()) <= dev) cache.resize(dev + 1, nullptr);
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return fail(KVQ_ERR_CUDA, "kvq_decode_attn_noalloc: cudaGetSymbolAddress: %s",
+                  cudaGetErrorString(e));
+    cache[dev] = p;
+  }
+  *out = cache[dev];
+  return KVQ_OK;
+}
+
+}  // namespace
+}  // namespace kvq
+
+extern "C" kvq_status kvq_decode_attn_noalloc(const kvq_pool* k_pools, const kvq_pool* v_pools,
+                                              int n_layers, const uint16_t* q, int num_q_heads,
+                                              const int32_t* page_table, int max_pages,
+                                              const int32_t* seq_lens, int nseq, int max_seq_len,
+                                              float softmax_scale, float* out, int32_t* dev_err,
+                                              kvq_stream_t stream) {
+  using namespace kvq;
+  const char* fn = "kvq_decode_attn_noalloc";
+  if (n_layers < 1 || n_layers > KVQ_MAX_TENSORS)
+    return fail(KVQ_ERR_RANGE, "%s: n_layers %d not in [1, %d]", fn, n_layers, KVQ_MAX_TENSORS);
+  kvq_status st = check_pools_uniform(k_pools, n_layers, fn);
+  if (st != KVQ_OK) return st;
+  st = check_pools_uniform(v_pools, n_layers, fn);
+  if (st != KVQ_OK) return st;
+  const kvq_pool& k0 = k_pools[0];
+  const kvq_pool& v0 = v_pools[0];
+  if (v0.bits != k0.bits || v0.num_heads != k0.num_heads || v0.head_dim != k0.head_dim ||
+      v0.page_size != k0.page_size)
+    return fail(KVQ_ERR_SHAPE, "%s: K and V pools differ in shape", fn);
+  if (k0.head_dim != kD)
+    return fail(KVQ_ERR_SHAPE, "%s: head_dim %d unsupported (256 only)", fn, k0.head_dim);
+  const int H = k0.num_heads;
+  if (num_q_heads < H || num_q_heads % H || num_q_heads / H > 8)
+    return fail(KVQ_ERR_SHAPE, "%s: num_q_heads %d must be a multiple of %d, at most 8 per KV "
+                "head", fn, num_q_heads, H);
+  if (nseq < 1 || max_pages < 1 || max_seq_len < 0)
+    return fail(KVQ_ERR_RANGE, "%s: bad nseq/max_pages/max_seq_len", fn);
+  if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages) * k0.page_size)
+    return fail(KVQ_ERR_RANGE, "%s: max_seq_len exceeds max_pages * page_size", fn);
+  if (!q || !page_table || !seq_lens || !out) return fail(KVQ_ERR_NULL, "%s: NULL pointer", fn);
+  if (!aligned16(q) || !aligned16(out))
+    return fail(KVQ_ERR_ALIGN, "%s: q/out must be 16-byte aligned", fn);
+  if (static_cast<int64_t>(n_layers) * nseq > 65535)
+    return fail(KVQ_ERR_RANGE, "%s: n_layers * nseq > 65535", fn);
+
+  // One partial record per (layer, sequence, KV head, split); the split count is capped so that
+  // all records fit in the static scratch.
+  const size_t per_split = static_cast<size_t>(n_layers) * nseq * H * 8 * kRec * sizeof(float);
+  if (per_split > kNoAllocScratchBytes)
+    return fail(KVQ_ERR_RANGE, "%s: %d layers x %d sequences x %d KV heads need %zu bytes of "
+                "scratch, more than the %zu-byte static scratch; use kvq_decode_attn with a "
+                "workspace", fn, n_layers, nseq, H, per_split, kNoAllocScratchBytes);
+  const int tiles = (max_seq_len + kTile - 1) / kTile;
+  const int max_splits = static_cast<int>(kNoAllocScratchBytes / per_split);
+  int tpc = tiles_per_cta_for(n_layers, nseq, H, max_seq_len);
+  int n_splits = tiles > 0 ? (tiles + tpc - 1) / tpc : 1;
+  if (n_splits > max_splits) {
+    tpc = (tiles + max_splits - 1) / max_splits;
+    tpc = ((tpc + kWarps - 1) / kWarps) * kWarps;
+    n_splits = (tiles + tpc - 1) / tpc;
+  }
+  void* ws = nullptr;
+  st = noalloc_scratch(&ws);
+  if (st != KVQ_OK) return st;
+
+  AttnArgs a;
+  for (int i = 0; i < KVQ_MAX_TENSORS; ++i) {
+    if (i < n_layers)
+      a.L[i] = LayerPools{k_pools[i].codes, k_pools[i].scales, v_pools[i].codes,
+                          v_pools[i].scales, k_pools[i].num_pages, v_pools[i].num_pages};
+    else
+      a.L[i] = LayerPools{nullptr, nullptr, nullptr, nullptr, 0, 0};
+  }
+  a.q = q;
+  a.out = out;
+  a.ws = static_cast<float*>(ws);
+  a.pt = page_table;
+  a.lens = seq_lens;
+  a.err = dev_err;
+  a.n_layers = n_layers;
+  a.nseq = nseq;
+  a.H = H;
+  a.G = num_q_heads / H;
+  a.Hq = num_q_heads;
+  a.ps = k0.page_size;
+  a.max_pages = max_pages;
+  a.tiles_per_cta = tpc;
+  a.n_splits = n_splits;
+  a.qk_scale = softmax_scale * 1.4426950408889634f;
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const dim3 grid(a.n_splits, H, n_layers * nseq);
+  const bool tma = (k0.page_size % kTile) == 0;
+  cudaError_t e;
+  switch (k0.bits) {
+    case 8: e = launch_attn<8>(a, grid, tma, cs); break;
+    case 6: e = launch_attn<6>(a, grid, tma, cs); break;
+    default: e = launch_attn<4>(a, grid, tma, cs); break;
+  }
+  if (e == cudaSuccess) {
+    decode_merge_kernel<<<dim3(num_q_heads, n_layers * nseq), kD, 0, cs>>>(a);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "%s launch: %s", fn, cudaGetErrorString(e));
   return ok();
 }
