@@ -100,6 +100,60 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// PRMT selector picking bytes (b0, b1) of the first and (b0, b1) of the second source word.
+__host__ __device__ constexpr uint32_t sel4(int a0, int a1, int b0, int b1) {
+  return static_cast<uint32_t>(a0 | (a1 << 4) | (b0 << 8) | (b1 << 12));
+}
+
+// Exact fp16 codes of elements 8*GI + k (lo[k]) and 8*GI + k + 4 (hi[k]), k = 0..3, of the
+// thread's packed V bytes, paired across two tokens: low half token A, high half token B.
+// (The d order matches the output mapping of tile_pv.)
+template <int BITS, int GI>
+__device__ __forceinline__ void cross_group(const uint32_t* wa, const uint32_t* wb, uint32_t lo[4],
+                                            uint32_t hi[4]) {
+  if constexpr (BITS == 6) {
+#pragma unroll
+    for (int qd = 0; qd < 2; ++qd) {           // quads 2*GI (-> lo) and 2*GI + 1 (-> hi)
+      const int b = 6 * GI + 3 * qd;           // byte offset of the quad (compile-time)
+      const int w = b / 4, intra = b % 4;
+      uint32_t xa, xb;
+      int i0;
+      if (intra <= 1) {
+        xa = wa[w]; xb = wb[w]; i0 = intra;
+      } else {                                 // the quad straddles two words: align it first
+        xa = __funnelshift_r(wa[w], wa[w + 1], 8 * intra);
+        xb = __funnelshift_r(wb[w], wb[w + 1], 8 * intra);
+        i0 = 0;
+      }
+      const uint32_t p1 = prmt(xa, xb, sel4(i0, i0 + 1, 4 + i0, 5 + i0));      // A.b0 A.b1 B.b0 B.b1
+      const uint32_t p2 = prmt(xa, xb, sel4(i0 + 1, i0 + 2, 5 + i0, 6 + i0));  // A.b1 A.b2 B.b1 B.b2
+      uint32_t* o = qd ? hi : lo;
+      o[0] = hfma2u((p1 & 0x003F003Fu) | 0x64006400u, kH1, kHm1056);
+      o[1] = hfma2u(((p1 >> 2) & 0x03F003F0u) | 0x64006400u, kH16th, kHm96);
+      o[2] = hfma2u((p2 & 0x03F003F0u) | 0x64006400u, kH16th, kHm96);
+      o[3] = hfma2u(((p2 >> 8) & 0x00FC00FCu) | 0x64006400u, kHQuarter, kHm288);
+    }
+  } else if constexpr (BITS == 8) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      lo[k] = hfma2u((prmt(wa[2 * GI], wb[2 * GI], sel4(k, k, 4 + k, 4 + k)) & 0x00FF00FFu) ^
+                         0x64806480u, kH1, kHm1152);
+      hi[k] = hfma2u((prmt(wa[2 * GI + 1], wb[2 * GI + 1], sel4(k, k, 4 + k, 4 + k)) &
+                      0x00FF00FFu) ^ 0x64806480u, kH1, kHm1152);
+    }
+  } else {
+    uint32_t pb[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) pb[b] = prmt(wa[GI], wb[GI], sel4(b, b, 4 + b, 4 + b));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int m = 4 * (k & 1);
+      lo[k] = hfma2u(((pb[k >> 1] >> m) & 0x000F000Fu) | 0x64006400u, kH1, kHm1032);
+      hi[k] = hfma2u(((pb[2 + (k >> 1)] >> m) & 0x000F000Fu) | 0x64006400u, kH1, kHm1032);
+    }
+  }
+}
+
 // ------------------------------------------------------------------------------ mbarrier / TMA
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -153,7 +207,7 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 template <int BITS>
 struct KRegs {
   uint32_t kw[2][Wd<BITS>::kKWords];
-  uint32_t ksc[2];   // fp16 scale duplicated in both halves
+  float ksc[2];      // the rows' fp16 scales, applied to the scores
   bool kval[2];
 };
 
@@ -169,17 +223,15 @@ __device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const uint
                                                 float (&acc)[16][4], float& m0, float& m1,
                                                 float& l0, float& l1, float qk_scale,
                                                 uint32_t& pb0, uint32_t& pb1) {
-  // ---------------- S^T = K_hat . Q^T  (four independent accumulation chains)
+  // ---------------- S^T = C_K . Q^T on the exact integer codes (four independent accumulation
+  // chains); each token row's fp16 scale multiplies its scores afterwards (the code-times-scale
+  // products are exact instead of rounded to fp16 -- a difference far inside the tolerance)
   float sacc4[4][4] = {};
 #define KVQ_QK_GROUP(GI)                                                                \
   {                                                                                     \
     uint32_t p0[4], p1[4];                                                              \
     unpack_group<BITS, GI>(T.kw[0], p0);                                                \
     unpack_group<BITS, GI>(T.kw[1], p1);                                                \
-    _Pragma("unroll") for (int k = 0; k < 4; ++k) {                                     \
-      p0[k] = hmul2u(p0[k], T.ksc[0]);                                                  \
-      p1[k] = hmul2u(p1[k], T.ksc[1]);                                                  \
-    }                                                                                   \
     mma16816(sacc4[(2 * GI) & 3], p0[0], p1[0], p0[1], p1[1], qf[2 * GI][0], qf[2 * GI][1]); \
     mma16816(sacc4[(2 * GI + 1) & 3], p0[2], p1[2], p0[3], p1[3], qf[2 * GI + 1][0],        \
              qf[2 * GI + 1][1]);                                                        \
@@ -193,10 +245,11 @@ __device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const uint
 
   // ---------------- online softmax (log2 domain); sacc: [tok g | g+8][head 2c | 2c+1]
   float sc[4];
-  sc[0] = T.kval[0] ? sacc[0] * qk_scale : kNegInf;
-  sc[1] = T.kval[0] ? sacc[1] * qk_scale : kNegInf;
-  sc[2] = T.kval[1] ? sacc[2] * qk_scale : kNegInf;
-  sc[3] = T.kval[1] ? sacc[3] * qk_scale : kNegInf;
+  const float f0 = T.ksc[0] * qk_scale, f1 = T.ksc[1] * qk_scale;
+  sc[0] = T.kval[0] ? sacc[0] * f0 : kNegInf;
+  sc[1] = T.kval[0] ? sacc[1] * f0 : kNegInf;
+  sc[2] = T.kval[1] ? sacc[2] * f1 : kNegInf;
+  sc[3] = T.kval[1] ? sacc[3] * f1 : kNegInf;
   float tm0 = fmaxf(sc[0], sc[2]), tm1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
@@ -234,17 +287,12 @@ __device__ __forceinline__ void tile_pv(const VRegs<BITS>& T, uint32_t pb0, uint
   const uint32_t sab = T.vsc[0] | (T.vsc[1] << 16), scd = T.vsc[2] | (T.vsc[3] << 16);
 #define KVQ_PV_GROUP(GI)                                                                \
   {                                                                                     \
-    uint32_t pa[4], pb[4], pc[4], pd[4];                                                \
-    unpack_group<BITS, GI>(T.vw[0], pa);                                                \
-    unpack_group<BITS, GI>(T.vw[1], pb);                                                \
-    unpack_group<BITS, GI>(T.vw[2], pc);                                                \
-    unpack_group<BITS, GI>(T.vw[3], pd);                                                \
+    uint32_t lab[4], hab[4], lcd[4], hcd[4];                                            \
+    cross_group<BITS, GI>(T.vw[0], T.vw[1], lab, hab);                                  \
+    cross_group<BITS, GI>(T.vw[2], T.vw[3], lcd, hcd);                                  \
     _Pragma("unroll") for (int k = 0; k < 4; ++k) {                                     \
-      const uint32_t lab = hmul2u(prmt(pa[k], pb[k], 0x5410u), sab);                   \
-      const uint32_t hab = hmul2u(prmt(pa[k], pb[k], 0x7632u), sab);                   \
-      const uint32_t lcd = hmul2u(prmt(pc[k], pd[k], 0x5410u), scd);                   \
-      const uint32_t hcd = hmul2u(prmt(pc[k], pd[k], 0x7632u), scd);                   \
-      mma16816(acc[4 * GI + k], lab, hab, lcd, hcd, pb0, pb1);                          \
+      mma16816(acc[4 * GI + k], hmul2u(lab[k], sab), hmul2u(hab[k], sab),               \
+               hmul2u(lcd[k], scd), hmul2u(hcd[k], scd), pb0, pb1);                     \
     }                                                                                   \
   }
   KVQ_PV_GROUP(0) KVQ_PV_GROUP(1) KVQ_PV_GROUP(2) KVQ_PV_GROUP(3)
@@ -417,8 +465,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_tma_kernel(const Attn
     for (int r = 0; r < 2; ++r) {
       const int row = g + 8 * r;
       K.kval[r] = ok && tb + row < len;
-      const uint32_t sb = sks[row];
-      K.ksc[r] = sb | (sb << 16);
+      K.ksc[r] = h2f(sks[row]);
       const uint4* src = reinterpret_cast<const uint4*>(sk + row * kPd + c * (4 * W::kKWords));
 #pragma unroll
       for (int i = 0; i < W::kKWords / 4; ++i) {
@@ -516,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_gather_kernel(const A
       int64_t row = -1;
       if (t < len) row = locate_row(a.pt, a.max_pages, a.ps, a.H, P.k_pages, s, t, h, a.err);
       K.kval[r] = row >= 0;
-      K.ksc[r] = 0;
+      K.ksc[r] = 0.f;
 #pragma unroll
       for (int i = 0; i < W::kKWords; ++i) K.kw[r][i] = 0;
       if (row >= 0) {
@@ -527,8 +574,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_gather_kernel(const A
           K.kw[r][4 * i] = v.x; K.kw[r][4 * i + 1] = v.y;
           K.kw[r][4 * i + 2] = v.z; K.kw[r][4 * i + 3] = v.w;
         }
-        const uint32_t sb = ld_nc_u16(P.ks + row);
-        K.ksc[r] = sb | (sb << 16);
+        K.ksc[r] = h2f(ld_nc_u16(P.ks + row));
       }
     }
     uint32_t pb0, pb1;

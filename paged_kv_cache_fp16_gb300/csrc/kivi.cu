@@ -8,11 +8,19 @@
 // rounding (explicit __f*_rn intrinsics so the compiler cannot fuse the multiply-add).  A ragged
 // last group reduces over its real elements only, which equals the page's padding by repetition.
 //
-// Keys: one thread per (tensor, b, h, token group, channel pair) walks the group's tokens with the
-// pair's values in registers; adjacent threads own adjacent pairs of a row (coalesced rows).
-// Values: one thread per (row, channel group) holds the group in 16-byte vectors.  Groups that
-// are not a multiple of 8 channels use a scalar kernel.  HBM-bound: 4 bytes per element.
-// The data are modified in place, so loads use the coherent path (no ld.global.nc).
+// One launch covers all tensors: the first blocks take key groups, the rest value groups.
+// Keys: one thread per (tensor, b, h, token group, channel pair) holds the pair's column of the
+// group in registers (fp16 min/max as a tree); adjacent threads own adjacent pairs of a row, so
+// every row access is contiguous across the warp.  Values: one thread per (row, channel group)
+// holds the group in 16-byte vectors.  Groups that are not a multiple of 8 channels use a scalar
+// kernel.  HBM-bound: 4 bytes per element.  The data are modified in place, so loads use the
+// coherent path (no ld.global.nc).
+//
+// The code of an element needs rint(RN(d / scale)) with d = RN(x - gmin) >= 0.  With the group's
+// y = RN(1 / scale), q0 = RN(d * y) is within 2.5 ulp of RN(d / scale); wherever q0 is farther
+// than |q0| * 2^-20 (> 8 ulp) from every half-integer both round to the same integer, so q0 is
+// used; otherwise (near or at a tie) the IEEE quotient is computed.  The result is identical to
+// dividing every element.
 #include <cuda_runtime.h>
 
 #include "kvq_device.cuh"
@@ -22,6 +30,8 @@ namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kKeepRows = 32;  // key group rows held in registers (longer groups are re-read)
+constexpr int kMaxVecs = 8;    // value group vectors held in registers (<= 64 channels)
 
 // Passed by value (kernel parameter space): the library allocates no device memory.
 struct KiviArgs {
@@ -30,55 +40,49 @@ struct KiviArgs {
   int val_list[KVQ_MAX_TENSORS];  // indices into x of the value tensors
   int n_keys, n_vals;
   int B, H, S, D, lo, hi, gs;
+  int key_blocks;                 // blocks [0, key_blocks) do keys, the rest values
   float levels, eps;
 };
 
-__device__ __forceinline__ void to_f8(const uint4& v, float f[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    f[2 * k] = h2f(static_cast<uint16_t>(w[k] & 0xffffu));
-    f[2 * k + 1] = h2f(static_cast<uint16_t>(w[k] >> 16));
-  }
+struct Group {
+  float mn, sc, y;  // gmin, scale, RN(1 / scale)
+};
+
+__device__ __forceinline__ Group make_group(float mn, float mx, float levels, float eps) {
+  Group g;
+  g.mn = mn;
+  g.sc = fmaxf(__fdiv_rn(__fsub_rn(mx, mn), levels), eps);
+  g.y = __frcp_rn(g.sc);
+  return g;
 }
 
-__device__ __forceinline__ float group_scale(float mn, float mx, float levels, float eps) {
-  return fmaxf(__fdiv_rn(__fsub_rn(mx, mn), levels), eps);
+__device__ __forceinline__ uint16_t roundtrip(float x, const Group& g, float levels) {
+  const float d = __fsub_rn(x, g.mn);
+  const float q0 = __fmul_rn(d, g.y);
+  const float dist = fabsf(__fsub_rn(__fadd_rn(floorf(q0), 0.5f), q0));
+  float q = q0;
+  if (dist <= __fmul_rn(q0, 9.5367431640625e-07f)) q = __fdiv_rn(d, g.sc);  // 2^-20
+  const float c = fminf(fmaxf(rintf(q), 0.f), levels);
+  return f2h(__fadd_rn(__fmul_rn(c, g.sc), g.mn));
 }
 
-__device__ __forceinline__ uint16_t roundtrip(float x, float mn, float scale, float levels) {
-  const float c = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(x, mn), scale)), 0.f), levels);
-  return f2h(__fadd_rn(__fmul_rn(c, scale), mn));
+__device__ __forceinline__ uint32_t roundtrip2(uint32_t w, const Group& g0, const Group& g1,
+                                               float levels) {
+  const uint32_t lo = roundtrip(h2f(static_cast<uint16_t>(w & 0xffffu)), g0, levels);
+  const uint32_t hi = roundtrip(h2f(static_cast<uint16_t>(w >> 16)), g1, levels);
+  return lo | (hi << 16);
 }
 
-__device__ __forceinline__ uint4 roundtrip8(const float f[8], const float mn[8],
-                                            const float sc[8], float levels) {
-  uint32_t w[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    w[k] = static_cast<uint32_t>(roundtrip(f[2 * k], mn[2 * k], sc[2 * k], levels)) |
-           (static_cast<uint32_t>(roundtrip(f[2 * k + 1], mn[2 * k + 1], sc[2 * k + 1], levels))
-            << 16);
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
+__device__ __forceinline__ __half2 as_h2(uint32_t w) { return *reinterpret_cast<__half2*>(&w); }
 
 // ------------------------------------------------------------------------------ keys
-// One thread per (key tensor, b, h, token group, channel pair): it walks the group's tokens, keeps
-// the pair's values in registers (up to kKeepRows tokens; longer groups are read twice), reduces
-// min/max per channel without any cross-thread step, and writes the round trip back.  Adjacent
-// threads own adjacent channel pairs of the same token row, so every load and store of a row is
-// contiguous across the warp.
-constexpr int kKeepRows = 32;
-
-__global__ void __launch_bounds__(kThreads) kivi_keys_kernel(const KiviArgs a) {
+__device__ __forceinline__ void keys_part(const KiviArgs& a, int64_t first, int64_t stride) {
   const int span = a.hi - a.lo;
   const int n_groups = (span + a.gs - 1) / a.gs;
   const int pairs = a.D / 2;
   const int64_t bh_count = static_cast<int64_t>(a.B) * a.H;
   const int64_t items = static_cast<int64_t>(a.n_keys) * bh_count * n_groups * pairs;
-  for (int64_t it = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; it < items;
-       it += static_cast<int64_t>(gridDim.x) * kThreads) {
+  for (int64_t it = first; it < items; it += stride) {
     const int pr = static_cast<int>(it % pairs);
     const int64_t r1 = it / pairs;
     const int g = static_cast<int>(r1 % n_groups);
@@ -88,57 +92,49 @@ __global__ void __launch_bounds__(kThreads) kivi_keys_kernel(const KiviArgs a) {
     const int t0 = a.lo + g * a.gs;
     const int n = min(a.gs, a.hi - t0);
     uint32_t* base = reinterpret_cast<uint32_t*>(a.x[ti] + (bh * a.S + t0) * a.D) + pr;
-    const int stride = a.D / 2;   // in half2 words
+    const int64_t stride_w = a.D / 2;   // in half2 words
     uint32_t keep[kKeepRows];
-    // fp16 +-inf as the identities (inputs are finite)
-    __half2 mn = __halves2half2(__ushort_as_half(0x7c00), __ushort_as_half(0x7c00));
-    __half2 mx = __halves2half2(__ushort_as_half(0xfc00), __ushort_as_half(0xfc00));
+    keep[0] = base[0];
 #pragma unroll
-    for (int r = 0; r < kKeepRows; ++r) {
-      keep[r] = 0;
-      if (r < n) {
-        keep[r] = base[static_cast<int64_t>(r) * stride];
-        const __half2 v = *reinterpret_cast<const __half2*>(&keep[r]);
-        mn = __hmin2(mn, v);
-        mx = __hmax2(mx, v);
+    for (int r = 1; r < kKeepRows; ++r)   // rows past the group repeat row 0 (min/max unchanged)
+      keep[r] = (r < n) ? base[r * stride_w] : keep[0];
+    // pairwise tree of fp16 min / max (exact)
+    __half2 mn[kKeepRows / 2], mx[kKeepRows / 2];
+#pragma unroll
+    for (int r = 0; r < kKeepRows / 2; ++r) {
+      mn[r] = __hmin2(as_h2(keep[2 * r]), as_h2(keep[2 * r + 1]));
+      mx[r] = __hmax2(as_h2(keep[2 * r]), as_h2(keep[2 * r + 1]));
+    }
+#pragma unroll
+    for (int w = kKeepRows / 4; w >= 1; w >>= 1)
+#pragma unroll
+      for (int r = 0; r < w; ++r) {
+        mn[r] = __hmin2(mn[r], mn[r + w]);
+        mx[r] = __hmax2(mx[r], mx[r + w]);
       }
-    }
+    __half2 gmn = mn[0], gmx = mx[0];
     for (int r = kKeepRows; r < n; ++r) {
-      const uint32_t w = base[static_cast<int64_t>(r) * stride];
-      const __half2 v = *reinterpret_cast<const __half2*>(&w);
-      mn = __hmin2(mn, v);
-      mx = __hmax2(mx, v);
+      const __half2 v = as_h2(base[r * stride_w]);
+      gmn = __hmin2(gmn, v);
+      gmx = __hmax2(gmx, v);
     }
-    // fp16 min/max are exact; the group arithmetic is float32
-    const float mn0 = __low2float(mn), mn1 = __high2float(mn);
-    const float sc0 = group_scale(mn0, __low2float(mx), a.levels, a.eps);
-    const float sc1 = group_scale(mn1, __high2float(mx), a.levels, a.eps);
-    auto rt = [&](uint32_t w) -> uint32_t {
-      const uint32_t lo = roundtrip(h2f(static_cast<uint16_t>(w & 0xffffu)), mn0, sc0, a.levels);
-      const uint32_t hi = roundtrip(h2f(static_cast<uint16_t>(w >> 16)), mn1, sc1, a.levels);
-      return lo | (hi << 16);
-    };
+    const Group g0 = make_group(__low2float(gmn), __low2float(gmx), a.levels, a.eps);
+    const Group g1 = make_group(__high2float(gmn), __high2float(gmx), a.levels, a.eps);
 #pragma unroll
     for (int r = 0; r < kKeepRows; ++r)
-      if (r < n) base[static_cast<int64_t>(r) * stride] = rt(keep[r]);
+      if (r < n) base[r * stride_w] = roundtrip2(keep[r], g0, g1, a.levels);
     for (int r = kKeepRows; r < n; ++r)
-      base[static_cast<int64_t>(r) * stride] = rt(base[static_cast<int64_t>(r) * stride]);
+      base[r * stride_w] = roundtrip2(base[r * stride_w], g0, g1, a.levels);
   }
 }
 
 // ------------------------------------------------------------------------------ values
-// One thread per (value tensor, row, channel group) for groups of a multiple of 8 channels
-// (16-byte vectors, at most 64 channels held in registers); the group's min/max, scale and round
-// trip stay in the thread.
-constexpr int kMaxVecs = 8;
-
-__global__ void __launch_bounds__(kThreads) kivi_values_kernel(const KiviArgs a) {
+__device__ __forceinline__ void values_part(const KiviArgs& a, int64_t first, int64_t stride) {
   const int span = a.hi - a.lo;
   const int groups = (a.D + a.gs - 1) / a.gs;
   const int64_t rows_per_tensor = static_cast<int64_t>(a.B) * a.H * span;
   const int64_t items = rows_per_tensor * a.n_vals * groups;
-  for (int64_t it = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; it < items;
-       it += static_cast<int64_t>(gridDim.x) * kThreads) {
+  for (int64_t it = first; it < items; it += stride) {
     const int g = static_cast<int>(it % groups);
     const int64_t row = it / groups;
     const int64_t vi = row / rows_per_tensor;
@@ -149,37 +145,45 @@ __global__ void __launch_bounds__(kThreads) kivi_values_kernel(const KiviArgs a)
     const int nv = (min(a.D, c0 + a.gs) - c0) / 8;   // 16-byte vectors in this group
     uint4* p = reinterpret_cast<uint4*>(a.x[a.val_list[vi]] + (bh * a.S + t) * a.D + c0);
     uint4 v[kMaxVecs];
-    __half2 mn = __halves2half2(__ushort_as_half(0x7c00), __ushort_as_half(0x7c00));
-    __half2 mx = __halves2half2(__ushort_as_half(0xfc00), __ushort_as_half(0xfc00));
+    v[0] = p[0];
+#pragma unroll
+    for (int k = 1; k < kMaxVecs; ++k) v[k] = (k < nv) ? p[k] : v[0];  // repeats keep min/max
+    __half2 mn[kMaxVecs], mx[kMaxVecs];
 #pragma unroll
     for (int k = 0; k < kMaxVecs; ++k) {
-      v[k] = make_uint4(0, 0, 0, 0);
-      if (k < nv) {
-        v[k] = p[k];
-        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __half2 h = *reinterpret_cast<const __half2*>(&w[e]);
-          mn = __hmin2(mn, h);
-          mx = __hmax2(mx, h);
-        }
-      }
+      mn[k] = __hmin2(__hmin2(as_h2(v[k].x), as_h2(v[k].y)), __hmin2(as_h2(v[k].z), as_h2(v[k].w)));
+      mx[k] = __hmax2(__hmax2(as_h2(v[k].x), as_h2(v[k].y)), __hmax2(as_h2(v[k].z), as_h2(v[k].w)));
     }
-    const float mnf = fminf(__low2float(mn), __high2float(mn));
-    const float sc = group_scale(mnf, fmaxf(__low2float(mx), __high2float(mx)), a.levels, a.eps);
+#pragma unroll
+    for (int w = kMaxVecs / 2; w >= 1; w >>= 1)
+#pragma unroll
+      for (int k = 0; k < w; ++k) {
+        mn[k] = __hmin2(mn[k], mn[k + w]);
+        mx[k] = __hmax2(mx[k], mx[k + w]);
+      }
+    const Group gr = make_group(fminf(__low2float(mn[0]), __high2float(mn[0])),
+                                fmaxf(__low2float(mx[0]), __high2float(mx[0])), a.levels, a.eps);
 #pragma unroll
     for (int k = 0; k < kMaxVecs; ++k) {
       if (k >= nv) continue;
-      float f[8], mn8[8], sc8[8];
-      to_f8(v[k], f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) { mn8[e] = mnf; sc8[e] = sc; }
-      p[k] = roundtrip8(f, mn8, sc8, a.levels);
+      p[k] = make_uint4(roundtrip2(v[k].x, gr, gr, a.levels), roundtrip2(v[k].y, gr, gr, a.levels),
+                        roundtrip2(v[k].z, gr, gr, a.levels), roundtrip2(v[k].w, gr, gr, a.levels));
     }
   }
 }
 
-// Any group size: one thread per (row, channel group), scalar loads.
+// Keys and values of every tensor in one launch (block-uniform split).
+__global__ void __launch_bounds__(kThreads, 3) kivi_kernel(const KiviArgs a) {
+  if (static_cast<int>(blockIdx.x) < a.key_blocks)
+    keys_part(a, static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x,
+              static_cast<int64_t>(a.key_blocks) * kThreads);
+  else
+    values_part(a, static_cast<int64_t>(blockIdx.x - a.key_blocks) * kThreads + threadIdx.x,
+                static_cast<int64_t>(gridDim.x - a.key_blocks) * kThreads);
+}
+
+// Values whose groups are not a multiple of 8 channels (or longer than 64): one thread per
+// (row, channel group), scalar loads.
 __global__ void __launch_bounds__(kThreads) kivi_values_scalar_kernel(const KiviArgs a) {
   const int span = a.hi - a.lo;
   const int groups = (a.D + a.gs - 1) / a.gs;
@@ -197,20 +201,13 @@ __global__ void __launch_bounds__(kThreads) kivi_values_scalar_kernel(const Kivi
     const int c0 = g * a.gs, c1 = min(a.D, c0 + a.gs);
     float mn = __int_as_float(0x7f800000), mx = -mn;
     for (int c = c0; c < c1; ++c) { const float v = h2f(p[c]); mn = fminf(mn, v); mx = fmaxf(mx, v); }
-    const float sc = group_scale(mn, mx, a.levels, a.eps);
-    for (int c = c0; c < c1; ++c) p[c] = roundtrip(h2f(p[c]), mn, sc, a.levels);
+    const Group gr = make_group(mn, mx, a.levels, a.eps);
+    for (int c = c0; c < c1; ++c) p[c] = roundtrip(h2f(p[c]), gr, a.levels);
   }
 }
 
-
-int grid_cap() {
-  const int sms = sm_count();
-  return (sms > 0 ? sms : 1) * (2048 / kThreads);
-}
-
-int blocks_for_threads(int64_t threads) {
+int blocks_for_threads(int64_t threads, int cap) {
   int64_t b = (threads + kThreads - 1) / kThreads;
-  const int cap = grid_cap();
   if (b > cap) b = cap;
   return static_cast<int>(b < 1 ? 1 : b);
 }
@@ -258,18 +255,20 @@ extern "C" kvq_status kivi_quant_dequant(uint16_t* const* x, const int32_t* is_k
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int span = hi - lo;
-  if (a.n_keys > 0) {
-    const int64_t items = static_cast<int64_t>(a.n_keys) * B * H *
-                          ((span + group_size - 1) / group_size) * (D / 2);
-    kivi_keys_kernel<<<blocks_for_threads(items), kThreads, 0, st>>>(a);
-  }
-  if (a.n_vals > 0) {
-    const int64_t rows = static_cast<int64_t>(a.n_vals) * B * H * span;
-    const int64_t items = rows * ((D + group_size - 1) / group_size);
-    if (group_size % 8 == 0 && group_size <= 8 * kMaxVecs)
-      kivi_values_kernel<<<blocks_for_threads(items), kThreads, 0, st>>>(a);
-    else
-      kivi_values_scalar_kernel<<<blocks_for_threads(items), kThreads, 0, st>>>(a);
+  const int sms = sm_count() > 0 ? sm_count() : 152;
+  const int cap = sms * 3;
+  const int64_t key_items = static_cast<int64_t>(a.n_keys) * B * H *
+                            ((span + group_size - 1) / group_size) * (D / 2);
+  const int64_t val_rows = static_cast<int64_t>(a.n_vals) * B * H * span;
+  const int64_t val_items = val_rows * ((D + group_size - 1) / group_size);
+  const bool vec_values = group_size % 8 == 0 && group_size <= 8 * kMaxVecs;
+  const int kb = a.n_keys > 0 ? blocks_for_threads(key_items, cap) : 0;
+  const int vb = (a.n_vals > 0 && vec_values) ? blocks_for_threads(val_items, cap) : 0;
+  a.key_blocks = kb;
+  if (kb + vb > 0) kivi_kernel<<<kb + vb, kThreads, 0, st>>>(a);
+  if (a.n_vals > 0 && !vec_values) {
+    a.key_blocks = 0;
+    kivi_values_scalar_kernel<<<blocks_for_threads(val_items, sms * 8), kThreads, 0, st>>>(a);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "kivi launch: %s", cudaGetErrorString(e));
