@@ -63,6 +63,30 @@ def bytes_kivi(n_tensors, B, H, span, D):
     return n_tensors * B * H * span * D * 4
 
 
+def kernel_source_hash():
+    """sha256 of the CUDA sources: recorded ncu traffic is only valid for the code it measured."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_fp16_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(stage, bits):
+    """DRAM bytes per launch from the committed ncu record, or None if the kernels changed."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    if rec.get("source_sha256") != kernel_source_hash():
+        return None
+    e = rec.get("kernels", {}).get(f"{stage}/q{bits}")
+    return None if e is None else e.get("bytes_per_launch")
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -338,7 +362,7 @@ def run_gpu(args):
     total = max_over_ranks(total, world, dev)
     ms_per_step = total / args.steps * 1e3
     value = world * step_bytes * args.steps / total / 1e9
-    launches_per_step = 6   # quant, dequant, decode + merge, kivi keys + values
+    launches_per_step = 5   # quant, dequant, decode + merge, kivi (keys and values in one launch)
 
     stage = {}
     for n, ts in per.items():
@@ -352,7 +376,8 @@ def run_gpu(args):
     roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
-                "traffic": args.traffic}
+                "traffic": (args.traffic if args.traffic is not None
+                            else recorded_traffic(dom, bits))}
 
     # extras outside the timed step: 262,144-token decode, q8/q4 variants
     extras = {}
