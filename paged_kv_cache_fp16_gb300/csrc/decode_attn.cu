@@ -408,14 +408,28 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_tma_kernel(const Attn
   }
   __syncwarp();
 
-  // Issue the loads of this warp's j-th tile into stage j % S (lane 0 only).
-  auto issue = [&](int j) {
+  // Page ids of this warp's tiles, 32 at a time: lane i holds the id of tile 32 * blk + i, so
+  // the per-tile issue needs a shuffle instead of a dependent global load.  All lanes call it.
+  int pg_blk = -1, pg_val = -1;
+  auto page_of = [&](int j) -> int {
+    const int blk = j >> 5;
+    if (blk != pg_blk) {   // warp-uniform
+      pg_blk = blk;
+      pg_val = -1;
+      const int jl = blk * 32 + lane;
+      if (jl < n_mine) {
+        const int lp = (tile0 + warp + jl * kWarps) * kTile / a.ps;
+        if (lp < a.max_pages) pg_val = __ldg(a.pt + static_cast<int64_t>(s) * a.max_pages + lp);
+      }
+    }
+    return __shfl_sync(kFullMask, pg_val, j & 31);
+  };
+
+  // Issue the loads of this warp's j-th tile (page id `page`) into stage j % S (lane 0 only).
+  auto issue = [&](int j, int page) {
     const int st = j % S;
     const int tb = (tile0 + warp + j * kWarps) * kTile;
-    const int lp = tb / a.ps;
-    const int slot0 = tb - lp * a.ps;
-    int page = -1;
-    if (lp < a.max_pages) page = __ldg(a.pt + static_cast<int64_t>(s) * a.max_pages + lp);
+    const int slot0 = tb % a.ps;
     const bool ok = page >= 0 && page < P.k_pages && page < P.v_pages;
     flags[st] = ok ? 1 : 0;
     uint8_t* dst = wbase + st * kStageBytes;
@@ -432,8 +446,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_tma_kernel(const Attn
     }
   };
 
-  if (lane == 0)
-    for (int j = 0; j < S && j < n_mine; ++j) issue(j);
+  for (int j = 0; j < S && j < n_mine; ++j) {
+    const int page = page_of(j);
+    if (lane == 0) issue(j, page);
+  }
 
   uint32_t qf[16][2];
   load_q_frags(a, ls, h, g, c, len > 0, qf);
@@ -499,10 +515,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_tma_kernel(const Attn
       }
     }
     // the stage's bytes are in registers: hand it back to the copy engine
+    const int next_page = (j + S < n_mine) ? page_of(j + S) : -1;   // warp-uniform condition
     __syncwarp();
     if (lane == 0 && j + S < n_mine) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(j + S);
+      issue(j + S, next_page);
       ++issued;
     }
     tile_pv<BITS>(V, pb0, pb1, acc);

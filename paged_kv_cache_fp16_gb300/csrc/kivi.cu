@@ -56,12 +56,16 @@ __device__ __forceinline__ Group make_group(float mn, float mx, float levels, fl
   return g;
 }
 
+// The exact quotient, out of line: it runs only near ties, and keeping it out of the unrolled
+// loops keeps the kernel's code small.
+__device__ __noinline__ float exact_quotient(float d, float sc) { return __fdiv_rn(d, sc); }
+
 __device__ __forceinline__ uint16_t roundtrip(float x, const Group& g, float levels) {
   const float d = __fsub_rn(x, g.mn);
   const float q0 = __fmul_rn(d, g.y);
   const float dist = fabsf(__fsub_rn(__fadd_rn(floorf(q0), 0.5f), q0));
   float q = q0;
-  if (dist <= __fmul_rn(q0, 9.5367431640625e-07f)) q = __fdiv_rn(d, g.sc);  // 2^-20
+  if (dist <= __fmul_rn(q0, 9.5367431640625e-07f)) q = exact_quotient(d, g.sc);  // 2^-20
   const float c = fminf(fmaxf(rintf(q), 0.f), levels);
   return f2h(__fadd_rn(__fmul_rn(c, g.sc), g.mn));
 }
