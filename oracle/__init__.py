@@ -19,6 +19,9 @@ It is a plain, slow, obviously correct numpy restatement of what the pages compu
   Source: VeloxQuant-MLX source page "veloxquant_mlx.cache.kivi_cache"
   (``KIVIKVCache._quant_dequant_along``, ``_quantization_boundary``, ``update_and_fetch``,
   ``_rollback_frontier``, ``trim``).
+* ``kivi_packed`` -- the packed KIVI storage the page only estimates (b-bit codes plus an fp16
+  (scale, zero) per group) and decode attention over it with the fp16 residual window.
+  Source: the same page (module docstring, ``_quantized_bytes``, ``_account_bytes``).
 * ``attention``  -- decode attention as the reference path computes it: dequantize the packed
   cache to fp16, then plain softmax(q k^T * scale) v, here in float64.
   Source: MTPLX pull request #267, description ("plain KV quant dequantizes and runs MLX SDPA").
@@ -29,4 +32,4 @@ Readings taken where the pages are silent are listed in each module's docstring.
 Pins (checks against values and properties the pages and mathematics fix) live in
 ``tests/test_oracle_*.py`` and ``tests/golden/``.
 """
-from . import symmetric, kivi, attention, storage  # noqa: F401
+from . import symmetric, kivi, kivi_packed, attention, storage  # noqa: F401
