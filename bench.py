@@ -43,6 +43,10 @@ KV = kvgen.WORKLOADS["kivi_flush_16L_16x8x4096x64"]
 HQ = 24
 SOFTMAX_SCALE = 1.0 / 16.0
 KIVI_LO, KIVI_HI = 3840, 3968
+KIVI_HQ = 32                      # GQA 4:1 over the KIVI cache's 8 KV heads
+KIVI_BITS = 2
+KIVI_OFFSET = KV["S"]             # decode at a full 4096-token cache
+KIVI_NPACKED = KV["S"] - KV["residual"]   # 3968 packed tokens + a 128-token fp16 window
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -210,7 +214,7 @@ class Workload:
         self.bits = bits
         self.pools = {bits: self.make_pools(bits)}
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
-        self._deq = self._dec = self._dec1 = self._kivi = None
+        self._deq = self._dec = self._dec1 = self._kivi = self._kp = None
         self.kivi_layers = KV["n_layers"] if layers is None else layers
 
     @property
@@ -257,6 +261,38 @@ class Workload:
     @property
     def kivi_flags(self):
         return [k for _ in range(self.kivi_layers) for k in (True, False)]
+
+    def kivi_packed(self):
+        """(caches, ks, vs, q, out, workspace) of the packed KIVI cache (2-bit, group 32)."""
+        if self._kp is None:
+            L, B, H, S, D = self.kivi_layers, KV["B"], KV["H"], KV["S"], KV["D"]
+            caches = [self.kvq.KiviPacked.empty(KIVI_BITS, KV["group_size"], B, H, S, D, self.dev)
+                      for _ in range(L)]
+            q = kvgen.queries_torch(KV["seed"], L, B, KIVI_HQ, D, self.dev)
+            out = torch.empty((L, B, KIVI_HQ, D), dtype=torch.float32, device=self.dev)
+            ws = torch.empty(self.kvq.kivi_decode_attn_workspace(L, B, H, KIVI_HQ, D, KIVI_OFFSET),
+                             dtype=torch.uint8, device=self.dev)
+            self._kp = (caches, self.kivi[0::2], self.kivi[1::2], q, out, ws)
+        return self._kp
+
+    def kivi_pack(self):
+        caches, ks, vs = self.kivi_packed()[:3]
+        self.kvq.kivi_pack(caches, ks, vs, 0, KIVI_NPACKED, KV["eps"])
+
+    def kivi_attn(self, n_packed=KIVI_NPACKED):
+        caches, ks, vs, q, out, ws = self.kivi_packed()
+        self.kvq.kivi_decode_attn(caches, ks, vs, q, n_packed, KIVI_OFFSET,
+                                  1.0 / np.sqrt(KV["D"]), out, ws)
+
+    def kivi_packed_bytes(self):
+        """Algorithmic bytes of the pack and of the two attention launches (packed / all fp16)."""
+        L, B, H, D = self.kivi_layers, KV["B"], KV["H"], KV["D"]
+        kb, vb = self.kivi_packed()[0][0].nbytes(KIVI_NPACKED)
+        fp16_tok = B * H * D * 2 * 2            # K and V bytes of one token, all rows
+        qo = B * KIVI_HQ * D * (2 + 4)
+        return {"pack": L * (KIVI_NPACKED * fp16_tok + kb + vb),
+                "attn_packed": L * (kb + vb + (KIVI_OFFSET - KIVI_NPACKED) * fp16_tok + qo),
+                "attn_fp16": L * (KIVI_OFFSET * fp16_tok + qo)}
 
     def make_pools(self, bits):
         return [self.kvq.Pool.empty(bits, self.H, self.D, self.ps, self.pt_np.size, self.dev)
@@ -401,6 +437,24 @@ def run_gpu(args):
             del w.pools[b2]
             torch.cuda.empty_cache()
 
+    # packed KIVI: pack the aged tokens of all 16 layers, decode over packed + residual, and the
+    # same decode over the fp16 cache (n_packed = 0) for comparison
+    if not args.no_kivi_packed:
+        Bk = w.kivi_packed_bytes()
+        tp = time_fn(w.kivi_pack, args.steps, args.warmup, stream)
+        ta = time_fn(w.kivi_attn, args.steps, args.warmup, stream)
+        tf = time_fn(lambda: w.kivi_attn(0), args.steps, args.warmup, stream)
+        w.kivi_pack()
+        extras["kivi_packed_2bit_16L_16x8x4096x64"] = {
+            "pack_ms": tp * 1e3, "pack_GB_s": Bk["pack"] / tp / 1e9,
+            "attn_ms": ta * 1e3, "attn_tok_s": KV["B"] / ta,
+            "attn_GB_s": Bk["attn_packed"] / ta / 1e9,
+            "attn_fp16_cache_ms": tf * 1e3, "attn_fp16_cache_tok_s": KV["B"] / tf,
+            "attn_fp16_cache_GB_s": Bk["attn_fp16"] / tf / 1e9}
+        del w._kp
+        w._kp = None
+        torch.cuda.empty_cache()
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -440,7 +494,11 @@ def run_only(w, bits, args, stream):
     """Profiling aid: run one stage warmup + steps times on a (possibly reduced) workload."""
     fn = {"quant_pack": lambda: w.quant(bits), "dequant": lambda: w.dequant(bits),
           "decode_attn": lambda: w.decode(bits), "kivi": w.kivi_flush,
-          "decode_attn_262144": lambda: w.decode_full_context(bits)}[args.only]
+          "decode_attn_262144": lambda: w.decode_full_context(bits),
+          "kivi_pack": w.kivi_pack, "kivi_attn": w.kivi_attn,
+          "kivi_attn_fp16": lambda: w.kivi_attn(0)}[args.only]
+    if args.only.startswith("kivi_attn"):
+        w.kivi_pack()
     w.quant(bits)
     torch.cuda.synchronize()
     t = time_fn(fn, args.steps, args.warmup, stream)
@@ -586,8 +644,11 @@ def main():
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling only: fewer layers than the workload's 16")
     ap.add_argument("--only", default=None,
-                    choices=["quant_pack", "dequant", "decode_attn", "kivi", "decode_attn_262144"],
+                    choices=["quant_pack", "dequant", "decode_attn", "kivi", "decode_attn_262144",
+                             "kivi_pack", "kivi_attn", "kivi_attn_fp16"],
                     help="profiling only: run one stage and print its time, no bench line")
+    ap.add_argument("--no-kivi-packed", action="store_true",
+                    help="skip the packed KIVI pack/attention extras")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the dominant kernel, if captured")
     args = ap.parse_args()

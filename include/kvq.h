@@ -256,6 +256,74 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_pool* k_pools, const kvq_pool* v_po
                            float softmax_scale, float* out, void* workspace,
                            size_t workspace_bytes, int32_t* dev_err, kvq_stream_t stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * Packed KIVI storage and decode attention over it
+ * ------------------------------------------------------------------------------------------ */
+
+/*
+ * VeloxQuant-MLX source page "veloxquant_mlx.cache.kivi_cache": the page keeps the KIVI cache in
+ * fp16 and estimates the bytes of a packed form (module docstring, _quantized_bytes,
+ * _account_bytes): b-bit codes plus an fp16 (scale, zero) pair per group -- per (token group,
+ * channel) for keys, per (token, channel group) for values.  This is that packed form, for one
+ * layer of a [batch][heads][capacity][head_dim] cache:
+ *   k_codes [B][H][capacity][D*bits/8]   k_scale, k_zero fp16 [B][H][capacity/gs][D]
+ *   v_codes [B][H][capacity][D*bits/8]   v_scale, v_zero fp16 [B][H][capacity][D/gs]
+ * zero = the group minimum (an fp16 value), scale = fp16(max((max - min) / levels, eps)) with
+ * levels = 2^bits - 1, code = clamp(rint((x - zero) / scale), 0, levels) (0 when the fp16 scale
+ * is 0), stored LSB-first along the head dimension.  Its size is exactly the page's estimate.
+ * All arrays 16-byte aligned; bits in {2, 4, 8}; group_size in {8, 16, 32, 64}; head_dim a
+ * multiple of group_size, at most 256; capacity a multiple of group_size.
+ */
+typedef struct kivi_packed {
+  int32_t bits;
+  int32_t group_size;
+  int32_t batch;
+  int32_t num_heads;
+  int32_t capacity;
+  int32_t head_dim;
+  uint8_t* k_codes;
+  uint16_t* k_scale;
+  uint16_t* k_zero;
+  uint8_t* v_codes;
+  uint16_t* v_scale;
+  uint16_t* v_zero;
+} kivi_packed;
+
+/*
+ * Pack tokens [lo, hi) of every layer's fp16 K and V (k[l], v[l]: device fp16 [B][H][capacity]
+ * [D], 16-byte aligned; the same layout the in-place KIVI cache uses) into caches[l].  lo and hi
+ * are multiples of group_size (the residual boundary of kivi_boundary always is).  eps is the
+ * page's 1e-8.  Errors: KVQ_ERR_BITS, KVQ_ERR_SHAPE, KVQ_ERR_NULL, KVQ_ERR_ALIGN, KVQ_ERR_RANGE,
+ * KVQ_ERR_CUDA.
+ */
+KVQ_API kvq_status kivi_pack(const kivi_packed* caches, const uint16_t* const* k,
+                             const uint16_t* const* v, int n_layers, int lo, int hi, float eps,
+                             kvq_stream_t stream);
+
+/*
+ * Decode attention of one query per batch row over a KIVI cache whose tokens [0, n_packed) are
+ * packed in caches[l] and tokens [n_packed, offset) are still fp16 in k[l], v[l] (the residual
+ * window).  q device fp16 [n_layers][B][num_q_heads][D]; out device float32, same shape; query
+ * head j uses KV head j / (num_q_heads / H); the reconstruction of a packed element is
+ * c * scale + zero in fp16 (one fused rounding), accumulation in float32.  Supports bits 2,
+ * head_dim 64, group_size 16/32/64, at most 8 query heads per KV head; n_packed a multiple of
+ * group_size; 0 <= n_packed <= offset <= capacity.  workspace: kivi_decode_attn_workspace(...)
+ * bytes, 16-byte aligned, no initialisation needed.  dev_err (device int32, may be NULL) gets
+ * KVQ_DEVERR_TIMEOUT OR-ed in if a staged copy never completed (the affected split then counts
+ * no tokens).  Errors: KVQ_ERR_BITS, KVQ_ERR_SHAPE (bits, head_dim, group_size, num_q_heads),
+ * KVQ_ERR_NULL, KVQ_ERR_ALIGN, KVQ_ERR_RANGE (n_packed, offset, grid limits), KVQ_ERR_WORKSPACE,
+ * KVQ_ERR_CUDA.
+ */
+KVQ_API size_t kivi_decode_attn_workspace(int n_layers, int batch, int num_heads, int num_q_heads,
+                                          int head_dim, int offset);
+
+KVQ_API kvq_status kivi_decode_attn(const kivi_packed* caches, const uint16_t* const* k,
+                                    const uint16_t* const* v, int n_layers, const uint16_t* q,
+                                    int num_q_heads, int n_packed, int offset,
+                                    float softmax_scale, float* out, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_err,
+                                    kvq_stream_t stream);
+
 /*
  * Decode attention for callers that cannot allocate device memory (no counterpart on the pages:
  * it is an addition of this library).  Same arguments, semantics and errors as kvq_decode_attn,

@@ -43,6 +43,15 @@ class kvq_pool(ctypes.Structure):
                 ("scales", ctypes.c_void_p)]
 
 
+class kivi_packed(ctypes.Structure):
+    _fields_ = [("bits", ctypes.c_int32), ("group_size", ctypes.c_int32),
+                ("batch", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("capacity", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("k_codes", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("k_zero", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p), ("v_zero", ctypes.c_void_p)]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -68,6 +77,10 @@ def _load() -> ctypes.CDLL:
         "kvq_decode_attn_workspace": (S, [I, I, I, I, I, I, I]),
         "kvq_decode_attn": (I, [pool_p, pool_p, I, P, I, P, I, P, I, I, F, P, P, S, P, P]),
         "kvq_decode_attn_noalloc": (I, [pool_p, pool_p, I, P, I, P, I, P, I, I, F, P, P, P]),
+        "kivi_pack": (I, [ctypes.POINTER(kivi_packed), P, P, I, I, I, F, P]),
+        "kivi_decode_attn_workspace": (S, [I, I, I, I, I, I]),
+        "kivi_decode_attn": (I, [ctypes.POINTER(kivi_packed), P, P, I, P, I, I, I, F, P, P, S,
+                                 P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -337,6 +350,96 @@ def kvq_decode_attn_noalloc(k_pools: Sequence[Pool], v_pools: Sequence[Pool], q:
                                         _stream(stream)))
 
 
+@dataclass
+class KiviPacked:
+    """Packed KIVI storage of one layer (see include/kvq.h): b-bit codes plus fp16 scale/zero per
+    group, keys per (token group, channel), values per (token, channel group)."""
+    bits: int
+    group_size: int
+    batch: int
+    num_heads: int
+    capacity: int
+    head_dim: int
+    k_codes: torch.Tensor
+    k_scale: torch.Tensor
+    k_zero: torch.Tensor
+    v_codes: torch.Tensor
+    v_scale: torch.Tensor
+    v_zero: torch.Tensor
+
+    @staticmethod
+    def empty(bits, group_size, batch, num_heads, capacity, head_dim, device="cuda"):
+        B, H, S, D, gs = batch, num_heads, capacity, head_dim, group_size
+        cb = D * bits // 8
+        u8 = dict(dtype=torch.uint8, device=device)
+        f16 = dict(dtype=torch.float16, device=device)
+        return KiviPacked(bits, gs, B, H, S, D,
+                          torch.zeros((B, H, S, cb), **u8),
+                          torch.zeros((B, H, S // gs, D), **f16),
+                          torch.zeros((B, H, S // gs, D), **f16),
+                          torch.zeros((B, H, S, cb), **u8),
+                          torch.zeros((B, H, S, D // gs), **f16),
+                          torch.zeros((B, H, S, D // gs), **f16))
+
+    def nbytes(self, n_tokens: int) -> tuple[int, int]:
+        """(key, value) bytes this layout stores for the first n_tokens tokens."""
+        B, H, D, gs = self.batch, self.num_heads, self.head_dim, self.group_size
+        code = n_tokens * D * self.bits // 8 * H * B
+        return code + n_tokens // gs * D * 4 * H * B, code + n_tokens * (D // gs) * 4 * H * B
+
+    def as_c(self) -> kivi_packed:
+        return kivi_packed(self.bits, self.group_size, self.batch, self.num_heads, self.capacity,
+                           self.head_dim, self.k_codes.data_ptr(), self.k_scale.data_ptr(),
+                           self.k_zero.data_ptr(), self.v_codes.data_ptr(),
+                           self.v_scale.data_ptr(), self.v_zero.data_ptr())
+
+
+def _packed_array(caches: Sequence[KiviPacked]):
+    arr = (kivi_packed * len(caches))()
+    for i, c in enumerate(caches):
+        arr[i] = c.as_c()
+    return arr
+
+
+def kivi_pack(caches: Sequence[KiviPacked], ks: Sequence[torch.Tensor],
+              vs: Sequence[torch.Tensor], lo: int, hi: int, eps: float = 1e-8,
+              stream=None) -> None:
+    """Pack tokens [lo, hi) of every layer's fp16 K/V [B, H, capacity, D] into caches."""
+    if not (len(caches) == len(ks) == len(vs)):
+        raise ValueError("one K and one V tensor per cache")
+    for i, (k, v) in enumerate(zip(ks, vs)):
+        _cuda_tensor(k, torch.float16, f"ks[{i}]")
+        _cuda_tensor(v, torch.float16, f"vs[{i}]")
+    _check(_lib.kivi_pack(_packed_array(caches), _ptr_array(ks), _ptr_array(vs), len(caches), lo,
+                          hi, eps, _stream(stream)))
+
+
+def kivi_decode_attn_workspace(n_layers: int, batch: int, num_heads: int, num_q_heads: int,
+                               head_dim: int, offset: int) -> int:
+    return _lib.kivi_decode_attn_workspace(n_layers, batch, num_heads, num_q_heads, head_dim,
+                                           offset)
+
+
+def kivi_decode_attn(caches: Sequence[KiviPacked], ks: Sequence[torch.Tensor],
+                     vs: Sequence[torch.Tensor], q: torch.Tensor, n_packed: int, offset: int,
+                     softmax_scale: float, out: torch.Tensor, workspace: torch.Tensor,
+                     dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """Decode attention over packed tokens [0, n_packed) and fp16 residual tokens
+    [n_packed, offset): q fp16 [n_layers, B, Hq, D] -> out float32."""
+    _cuda_tensor(q, torch.float16, "q")
+    _cuda_tensor(out, torch.float32, "out")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    for i, (k, v) in enumerate(zip(ks, vs)):
+        _cuda_tensor(k, torch.float16, f"ks[{i}]")
+        _cuda_tensor(v, torch.float16, f"vs[{i}]")
+    _check(_lib.kivi_decode_attn(_packed_array(caches), _ptr_array(ks), _ptr_array(vs),
+                                 len(caches), q.data_ptr(), q.shape[2], n_packed, offset,
+                                 softmax_scale, out.data_ptr(), workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(),
+                                 _ptr(dev_err), _stream(stream)))
+
+
 def decode_workspace(k_pools: Sequence[Pool], nseq: int, num_q_heads: int, max_seq_len: int,
                      device="cuda") -> torch.Tensor:
     """A workspace tensor of the size kvq_decode_attn needs."""
@@ -349,4 +452,5 @@ def decode_workspace(k_pools: Sequence[Pool], nseq: int, num_q_heads: int, max_s
 __all__ = ["KVQError", "Pool", "Allocator", "parse_mode", "kvq_version", "kvq_packed_dim",
            "kivi_boundary", "kvq_quant_pack_paged", "kvq_dequant_paged", "kivi_quant_dequant",
            "kvq_decode_attn_workspace", "kvq_decode_attn", "kvq_decode_attn_noalloc",
+           "KiviPacked", "kivi_pack", "kivi_decode_attn_workspace", "kivi_decode_attn",
            "decode_workspace", "LIB_PATH"]

@@ -34,6 +34,7 @@
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 #include "kvq_math.cuh"
+#include "kvq_warp.cuh"
 
 namespace kvq {
 namespace {
@@ -43,7 +44,6 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 16;
 constexpr int kRec = kD + 4;   // workspace record per (split, head): O[256], m, l, pad, pad
-constexpr long long kWaitLimit = 1LL << 22;  // try_wait polls before giving up
 #define kNegInf (-__int_as_float(0x7f800000))
 
 struct LayerPools {
@@ -79,26 +79,6 @@ template <int BITS> __host__ __device__ constexpr int tma_smem_bytes() {
   return kWarps * warp_bytes<BITS>() + kWarps * Wd<BITS>::kStages * 16;  // + barriers, flags
 }
 constexpr int kMergeBytes = kWarps * 8 * kD * 4 + 2 * kWarps * 8 * 4;
-
-__device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t movtrans(uint32_t x) {
-  uint32_t r;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
 
 // PRMT selector picking bytes (b0, b1) of the first and (b0, b1) of the second source word.
 __host__ __device__ constexpr uint32_t sel4(int a0, int a1, int b0, int b1) {
@@ -152,52 +132,6 @@ __device__ __forceinline__ void cross_group(const uint32_t* wa, const uint32_t* 
       hi[k] = hfma2u(((pb[2 + (k >> 1)] >> m) & 0x000F000Fu) | 0x64006400u, kH1, kHm1032);
     }
   }
-}
-
-// ------------------------------------------------------------------------------ mbarrier / TMA
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for a phase; false if it did not complete within kWaitLimit polls.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (long long i = 0; i < kWaitLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
 }
 
 // ------------------------------------------------------------------------------ tile compute

@@ -194,3 +194,40 @@ def test_decode_attn_rejects_bad_arguments_before_launch(kvq):
     assert args(P(bits=7), P(bits=7)) == 1
     need = kvq.kvq_decode_attn_workspace(16, 1, 4, 24, 256, 16, 262144)
     assert need > 0 and need % 16 == 0
+
+
+def _kp(kvq, bits=2, gs=32, B=1, H=2, S=128, D=64, ptr=FAKE):
+    return kvq.kivi_packed(bits, gs, B, H, S, D, ptr, ptr, ptr, ptr, ptr, ptr)
+
+
+def test_kivi_packed_rejects_bad_arguments_before_launch(kvq):
+    C = lambda **kw: (kvq.kivi_packed * 1)(_kp(kvq, **kw))
+    xs = (ctypes.c_void_p * 1)(FAKE)
+    pack = lambda c, lo=0, hi=64, eps=1e-8, k=xs: kvq._lib.kivi_pack(c, k, xs, 1, lo, hi, eps, None)
+    assert pack(C(bits=3)) == 1
+    assert pack(C(gs=24)) == 2                      # group size not in {8, 16, 32, 64}
+    assert pack(C(D=72)) == 2                       # head_dim % group_size
+    assert pack(C(S=100)) == 5                      # capacity % group_size
+    assert pack(C(ptr=FAKE + 2)) == 4
+    assert pack(C(ptr=0)) == 3
+    assert pack(C(), lo=16) == 2                    # lo not on a group boundary
+    assert pack(C(), hi=160) == 2                   # beyond capacity
+    assert pack(C(), eps=-1.0) == 5
+    assert pack(C(), k=(ctypes.c_void_p * 1)(FAKE + 8)) == 4
+    assert pack(C(), lo=64, hi=64) == 0             # empty: no launch
+    two = (kvq.kivi_packed * 2)(_kp(kvq), _kp(kvq, H=3))
+    assert kvq._lib.kivi_pack(two, (ctypes.c_void_p * 2)(FAKE, FAKE),
+                              (ctypes.c_void_p * 2)(FAKE, FAKE), 2, 0, 64, 1e-8, None) == 2
+
+    attn = lambda c, hq=8, n_packed=64, offset=100, ws=1 << 30: kvq._lib.kivi_decode_attn(
+        c, xs, xs, 1, FAKE, hq, n_packed, offset, 0.125, FAKE, FAKE, ws, None, None)
+    assert attn(C(bits=4)) == 2                     # the attention kernel reads 2-bit codes
+    assert attn(C(D=128)) == 2                      # head_dim 64
+    assert attn(C(gs=8)) == 2                       # group size a multiple of the 16-token tile
+    assert attn(C(), hq=7) == 2                     # not a multiple of the 2 KV heads
+    assert attn(C(), hq=18) == 2                    # 9 query heads per KV head
+    assert attn(C(), n_packed=48) == 5              # not a whole group
+    assert attn(C(), offset=60) == 5                # offset < n_packed
+    assert attn(C(), offset=129) == 5               # beyond capacity
+    assert attn(C(), ws=16) == 8
+    assert kvq.kivi_decode_attn_workspace(1, 1, 2, 8, 64, 100) > 0
