@@ -23,7 +23,8 @@ It is a plain, slow, obviously correct numpy restatement of what the pages compu
   (scale, zero) per group) and decode attention over it with the fp16 residual window.
   Source: the same page (module docstring, ``_quantized_bytes``, ``_account_bytes``).
 * ``attention``  -- decode attention as the reference path computes it: dequantize the packed
-  cache to fp16, then plain softmax(q k^T * scale) v, here in float64.
+  cache to fp16, then plain softmax(q k^T * scale) v, here in float64; and one decode step
+  (write the new token, then attend over the grown window) in that order.
   Source: MTPLX pull request #267, description ("plain KV quant dequantizes and runs MLX SDPA").
 * ``storage``    -- the storage arithmetic (bytes per token per KV head, whole-cache GiB).
   Source: MTPLX pull request #267, description, storage paragraph.

@@ -70,6 +70,21 @@ def decode_attention_paged(q16: np.ndarray, k_pool: symmetric.PagedPool,
     return out
 
 
+def append_decode_paged(q16: np.ndarray, k_pool: symmetric.PagedPool,
+                        v_pool: symmetric.PagedPool, k_new16: np.ndarray, v_new16: np.ndarray,
+                        page_table: np.ndarray, seq_lens: np.ndarray, softmax_scale: float
+                        ) -> np.ndarray:
+    """One decode step as the pages run it, in their order: quantize-on-write of every sequence's
+    new token (k_new16, v_new16 [nseq, H, D]) at position seq_lens[s] through the page table,
+    then dequantize the active window of seq_lens[s] + 1 tokens and attend.  The pools are
+    updated in place.  q16 [nseq, Hq, D] -> float64 [nseq, Hq, D]."""
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    cu = np.arange(len(lens) + 1)
+    symmetric.quant_pack_paged(k_pool, k_new16, page_table, cu, lens)
+    symmetric.quant_pack_paged(v_pool, v_new16, page_table, cu, lens)
+    return decode_attention_paged(q16, k_pool, v_pool, page_table, lens + 1, softmax_scale)
+
+
 def decode_attention_fp16(q16: np.ndarray, k16: np.ndarray, v16: np.ndarray, bits: int,
                           softmax_scale: float) -> np.ndarray:
     """Quantize an fp16 cache k16, v16 [T, H, D] with the oracle, dequantize, attend -> [Hq, D]."""

@@ -85,3 +85,85 @@ def test_paged_equals_contiguous(bits):
     for s in range(len(lens)):
         ref = A.decode_attention_fp16(q[s], k[cu[s]:cu[s + 1]], v[cu[s]:cu[s + 1]], bits, 0.125)
         assert np.array_equal(out[s], ref)
+
+
+# ---------------------------------------------------------------- fused append + decode step
+def _pools(bits, H, D, ps, pages):
+    return S.PagedPool(bits, H, D, ps, pages), S.PagedPool(bits, H, D, ps, pages)
+
+
+@pytest.mark.parametrize("bits", [8, 6, 4])
+def test_append_decode_on_empty_caches_returns_the_new_value(bits):
+    """One cached token after the append: softmax of one score is 1, so every query head of KV
+    head h returns the dequantized new value row of h."""
+    nseq, H, G, D, ps = 3, 2, 3, 32, 16
+    kp, vp = _pools(bits, H, D, ps, 8)
+    pt = np.arange(nseq * 2).reshape(nseq, 2)
+    kn, vn, q = _fp16((nseq, H, D), 11), _fp16((nseq, H, D), 12), _fp16((nseq, H * G, D), 13)
+    out = A.append_decode_paged(q, kp, vp, kn, vn, pt, np.zeros(nseq, np.int64), 0.1)
+    v_hat = S.dequant_rows(*S.quant_pack_rows(vn, bits), bits, D)
+    for s in range(nseq):
+        for j in range(H * G):
+            assert np.array_equal(out[s, j], v_hat[s, j // G].astype(np.float64))
+
+
+@pytest.mark.parametrize("bits", [6, 4])
+def test_append_decode_writes_exactly_the_new_rows(bits):
+    """The pools change only at (page_table[s][len // ps], h, len % ps), where they hold the
+    quantizer's packed row and scale of the new token; a page boundary (len % ps == 0) is
+    crossed for one sequence."""
+    nseq, H, D, ps = 3, 2, 32, 16
+    lens = np.array([5, 16, 31])
+    pt = kvgen.random_page_table(4, nseq, 3)
+    kp, vp = _pools(bits, H, D, ps, nseq * 3)
+    kp.codes[:] = 0xA5
+    kp.scales[:] = np.float16(0.5)
+    before_c, before_s = kp.codes.copy(), kp.scales.copy()
+    kn, vn, q = _fp16((nseq, H, D), 21), _fp16((nseq, H, D), 22), _fp16((nseq, 2 * H, D), 23)
+    A.append_decode_paged(q, kp, vp, kn, vn, pt, lens, 0.2)
+    packed, scale = S.quant_pack_rows(kn, bits)
+    changed = np.zeros(kp.scales.shape, bool)
+    for s in range(nseq):
+        page, slot = pt[s, lens[s] // ps], lens[s] % ps
+        changed[page, :, slot] = True
+        assert np.array_equal(kp.codes[page, :, slot], packed[s])
+        assert np.array_equal(kp.scales[page, :, slot].view(np.uint16), scale[s].view(np.uint16))
+    assert np.array_equal(kp.codes[~changed], before_c[~changed])
+    assert np.array_equal(kp.scales[~changed].view(np.uint16), before_s[~changed].view(np.uint16))
+
+
+def test_append_decode_two_tokens_closed_form():
+    """A cache of one token plus the new one: the weight of the new token is the logistic
+    function of the score difference, o = v0 + (v1 - v0) / (1 + exp(s0 - s1))."""
+    bits, H, D, ps = 8, 1, 16, 16
+    kp, vp = _pools(bits, H, D, ps, 1)
+    pt = np.zeros((1, 1), np.int64)
+    k0, v0 = _fp16((1, H, D), 31), _fp16((1, H, D), 32)
+    S.quant_pack_paged(kp, k0, pt, np.array([0, 1]), np.array([0]))
+    S.quant_pack_paged(vp, v0, pt, np.array([0, 1]), np.array([0]))
+    k1, v1, q = _fp16((1, H, D), 33), _fp16((1, H, D), 34), _fp16((1, 2, D), 35)
+    out = A.append_decode_paged(q, kp, vp, k1, v1, pt, np.array([1]), 0.3)
+    deq = lambda x: S.dequant_rows(*S.quant_pack_rows(x, bits), bits, D)[0, 0].astype(np.float64)
+    kh0, kh1, vh0, vh1 = deq(k0), deq(k1), deq(v0), deq(v1)
+    for j in range(2):
+        qq = q[0, j].astype(np.float64)
+        s0, s1 = 0.3 * float(qq @ kh0), 0.3 * float(qq @ kh1)
+        ref = vh0 + (vh1 - vh0) / (1.0 + math.exp(s0 - s1))
+        assert np.allclose(out[0, j], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_append_decode_steps_equal_one_prefill_write():
+    """Appending T tokens one decode step at a time leaves the same pools as writing them in one
+    quant-pack call (the write is per row, independent of how the tokens are batched)."""
+    bits, H, D, ps, T = 6, 2, 32, 16, 40
+    pt = kvgen.random_page_table(5, 1, 3)
+    kp, vp = _pools(bits, H, D, ps, 3)
+    kq, vq = _pools(bits, H, D, ps, 3)
+    k, v = _fp16((T, H, D), 41), _fp16((T, H, D), 42)
+    q = _fp16((1, H, D), 43)
+    for t in range(T):
+        A.append_decode_paged(q, kp, vp, k[t:t + 1], v[t:t + 1], pt, np.array([t]), 0.2)
+    S.quant_pack_paged(kq, k, pt, np.array([0, T]), np.array([0]))
+    S.quant_pack_paged(vq, v, pt, np.array([0, T]), np.array([0]))
+    assert np.array_equal(kp.codes, kq.codes) and np.array_equal(vp.codes, vq.codes)
+    assert np.array_equal(kp.scales.view(np.uint16), kq.scales.view(np.uint16))
