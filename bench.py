@@ -192,6 +192,69 @@ def max_over_ranks(x: float, world: int, device) -> float:
 
 
 # ----------------------------------------------------------------------------- GPU arm
+def decode_step_extra(kvq, dev, steps, warmup, stream, bits=6):
+    """One decode step of 64 sequences with lengths uniform in [1024, 65536] over 16 layers
+    (4 KV heads x 256, 24 query heads, page 16): the fused kvq_append_decode_attn against the two
+    calls it replaces (kvq_quant_pack_paged of the 64 new tokens, then kvq_decode_attn).  The
+    cache pages hold seeded random codes and scales (the work does not depend on them); the new
+    tokens and queries come from the generator.  Each timed step rewrites the same tail slots."""
+    wl = kvgen.WORKLOADS["decode_append_16L_64seq_4x256"]
+    L, nseq, H, D, ps = wl["n_layers"], wl["n_seq"], wl["H"], wl["D"], wl["page_size"]
+    lens = kvgen.decode_append_lengths(wl["seed"], nseq).astype(np.int64)
+    ppseq = (lens + 1 + ps - 1) // ps
+    perm = kvgen.permutation(wl["seed"], 77, int(ppseq.sum()))
+    pt_np = np.full((nseq, int(ppseq.max())), -1, dtype=np.int32)
+    o = 0
+    for s_ in range(nseq):
+        pt_np[s_, :ppseq[s_]] = perm[o:o + ppseq[s_]]
+        o += ppseq[s_]
+    n_pages = int(ppseq.sum())
+    pools = []
+    for i in range(2 * L):
+        p = kvq.Pool.empty(bits, H, D, ps, n_pages, dev)
+        kvgen.fill_random_pool_(p.codes, p.scales, 1000 + i)
+        pools.append(p)
+    kps, vps = pools[0::2], pools[1::2]
+    kn = [kvgen.KVSpec(seed=wl["seed"], layer=l, is_key=True, n_seq=1, n_tok=nseq, num_heads=H,
+                       head_dim=D).full_torch(dev) for l in range(L)]
+    vn = [kvgen.KVSpec(seed=wl["seed"], layer=l, is_key=False, n_seq=1, n_tok=nseq, num_heads=H,
+                       head_dim=D).full_torch(dev) for l in range(L)]
+    q = kvgen.queries_torch(wl["seed"], L, nseq, HQ, D, dev)
+    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    pt = torch.from_numpy(pt_np).to(dev)
+    lens_d = torch.from_numpy(lens.astype(np.int32)).to(dev)
+    lens1_d = lens_d + 1
+    cu = torch.arange(nseq + 1, dtype=torch.int32, device=dev)
+    max_len = int(lens.max()) + 1
+    ws = kvq.decode_workspace(kps, nseq, HQ, max_len, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    new = [t for pair in zip(kn, vn) for t in pair]
+
+    def fused():
+        kvq.kvq_append_decode_attn(kps, vps, kn, vn, q, pt, lens_d, max_len, SOFTMAX_SCALE, out,
+                                   ws, err)
+
+    def separate():
+        kvq.kvq_quant_pack_paged(pools, new, pt, cu, lens_d, err)
+        kvq.kvq_decode_attn(kps, vps, q, pt, lens1_d, max_len, SOFTMAX_SCALE, out, ws, err)
+
+    tf = time_fn(fused, steps, warmup, stream)
+    ts = time_fn(separate, steps, warmup, stream)
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError("device error word set in the decode step")
+    pd = packed_dim(D, bits)
+    tok_heads = int((lens + 1).sum()) * L * H
+    nbytes = (tok_heads * 2 * (pd + 2) + L * nseq * H * 2 * (2 * D + pd + 2)
+              + L * nseq * HQ * D * (2 + 4))
+    res = {"ms": tf * 1e3, "tok_s": nseq / tf, "GB_s": nbytes / tf / 1e9,
+           "separate_ms": ts * 1e3, "separate_tok_s": nseq / ts, "bytes": nbytes,
+           "cached_tokens": int(lens.sum())}
+    del pools, kps, vps, kn, vn, new
+    torch.cuda.empty_cache()
+    return res
+
+
 class Workload:
     """Device-resident inputs and outputs of one replica (outputs allocated on first use)."""
 
@@ -455,6 +518,11 @@ def run_gpu(args):
         w._kp = None
         torch.cuda.empty_cache()
 
+    # one decode step (append + attend) of 64 ragged sequences
+    if not args.no_decode_step:
+        extras["decode_step_64seq_ragged_16L_q6"] = decode_step_extra(kvq, dev, args.steps,
+                                                                      args.warmup, stream)
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -647,6 +715,8 @@ def main():
                     choices=["quant_pack", "dequant", "decode_attn", "kivi", "decode_attn_262144",
                              "kivi_pack", "kivi_attn", "kivi_attn_fp16"],
                     help="profiling only: run one stage and print its time, no bench line")
+    ap.add_argument("--no-decode-step", action="store_true",
+                    help="skip the fused append + decode step extra")
     ap.add_argument("--no-kivi-packed", action="store_true",
                     help="skip the packed KIVI pack/attention extras")
     ap.add_argument("--traffic", type=float, default=None,

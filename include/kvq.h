@@ -6,6 +6,8 @@
  *   kvq_dequant_paged      gather + unpack + dequantize back to fp16
  *   kivi_quant_dequant     KIVI asymmetric group quantize->dequantize, in place
  *   kvq_decode_attn        decode attention that reads the packed pages directly
+ *   kvq_append_decode_attn one decode step: append the new token, then attend, in one launch
+ *   kivi_pack, kivi_decode_attn   packed KIVI storage and decode attention over it
  * plus host helpers: packed_dim, the KIVI residual boundary, and a page allocator.
  *
  * Conventions shared by every entry point
@@ -255,6 +257,28 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_pool* k_pools, const kvq_pool* v_po
                            int max_pages, const int32_t* seq_lens, int nseq, int max_seq_len,
                            float softmax_scale, float* out, void* workspace,
                            size_t workspace_bytes, int32_t* dev_err, kvq_stream_t stream);
+
+/*
+ * One decode step with the append fused in: for every sequence s, quantize its new token's K and
+ * V rows (k_new[l], v_new[l]: device fp16 [nseq][H][256] per layer, 16-byte aligned) exactly as
+ * kvq_quant_pack_paged would, store them at position seq_lens[s] of the pools (page
+ * page_table[s][seq_lens[s] / page_size], which the caller has mapped, e.g. with
+ * kvq_table_reserve), and attend over the seq_lens[s] + 1 tokens that result -- one launch (plus
+ * the split merge).  MTPLX pull request #267, description: quantize on write, and attention over
+ * the active window; the pages run the two as separate steps (write, then dequantize + SDPA).
+ * seq_lens holds the lengths BEFORE the append and is not modified: the caller advances it.
+ * max_seq_len bounds seq_lens[s] + 1.  The page size must be a multiple of 16.  Other arguments,
+ * the workspace (kvq_decode_attn_workspace with that max_seq_len) and the errors are those of
+ * kvq_decode_attn; the pools are written, so they must not be read by other work in flight.
+ */
+KVQ_API kvq_status kvq_append_decode_attn(const kvq_pool* k_pools, const kvq_pool* v_pools,
+                                          int n_layers, const uint16_t* const* k_new,
+                                          const uint16_t* const* v_new, const uint16_t* q,
+                                          int num_q_heads, const int32_t* page_table,
+                                          int max_pages, const int32_t* seq_lens, int nseq,
+                                          int max_seq_len, float softmax_scale, float* out,
+                                          void* workspace, size_t workspace_bytes,
+                                          int32_t* dev_err, kvq_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Packed KIVI storage and decode attention over it

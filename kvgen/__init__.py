@@ -324,6 +324,22 @@ def decode_append_lengths(seed: int, nseq: int, lo: int = 1024, hi: int = 65536)
     return uniform_ints(seed, TAG_SEQLEN, nseq, lo, hi).astype(np.int32)
 
 
+# ---------------------------------------------------------------- random packed cache contents
+def fill_random_pool_(codes, scales, seed: int) -> None:
+    """Fill a packed pool in place with seeded random bytes: codes uniform over all byte values
+    (every byte string is a valid packed row at every width) and fp16 scales log-uniform in
+    [2^-10, 2^-4] (the scales of N(0, 1) rows with a few outliers).  Used where a cache is too
+    large to produce by quantizing generated fp16 rows; the attention does the same work on any
+    contents."""
+    import torch
+    g = torch.Generator(device=codes.device)
+    g.manual_seed(seed)
+    codes.copy_(torch.randint(0, 256, codes.shape, dtype=torch.uint8, device=codes.device,
+                              generator=g))
+    e = torch.rand(scales.shape, device=scales.device, generator=g, dtype=torch.float32)
+    scales.copy_(torch.exp2(-10.0 + 6.0 * e).to(torch.float16))
+
+
 # ---------------------------------------------------------------- the workloads
 WORKLOADS = {
     # one layer, contiguous: K and V each [1 seq, 4 heads, 1024 tokens, D=256]

@@ -77,6 +77,8 @@ def _load() -> ctypes.CDLL:
         "kvq_decode_attn_workspace": (S, [I, I, I, I, I, I, I]),
         "kvq_decode_attn": (I, [pool_p, pool_p, I, P, I, P, I, P, I, I, F, P, P, S, P, P]),
         "kvq_decode_attn_noalloc": (I, [pool_p, pool_p, I, P, I, P, I, P, I, I, F, P, P, P]),
+        "kvq_append_decode_attn": (I, [pool_p, pool_p, I, P, P, P, I, P, I, P, I, I, F, P, P, S,
+                                       P, P]),
         "kivi_pack": (I, [ctypes.POINTER(kivi_packed), P, P, I, I, I, F, P]),
         "kivi_decode_attn_workspace": (S, [I, I, I, I, I, I]),
         "kivi_decode_attn": (I, [ctypes.POINTER(kivi_packed), P, P, I, P, I, I, I, F, P, P, S,
@@ -324,6 +326,42 @@ def kvq_decode_attn(k_pools: Sequence[Pool], v_pools: Sequence[Pool], q: torch.T
                                 _stream(stream)))
 
 
+def kvq_append_decode_attn(k_pools: Sequence[Pool], v_pools: Sequence[Pool],
+                           k_new: Sequence[torch.Tensor], v_new: Sequence[torch.Tensor],
+                           q: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                           max_seq_len: int, softmax_scale: float, out: torch.Tensor,
+                           workspace: torch.Tensor, dev_err: torch.Tensor | None = None,
+                           stream=None) -> None:
+    """One decode step: write each sequence's new token (k_new[l], v_new[l] fp16 [nseq, H, D])
+    at position seq_lens[s] of the pools, then attend over seq_lens[s] + 1 tokens.  seq_lens is
+    not advanced; max_seq_len bounds seq_lens + 1."""
+    if not (len(k_pools) == len(v_pools) == len(k_new) == len(v_new)):
+        raise ValueError("one V pool and one new K/V tensor per K pool")
+    _cuda_tensor(q, torch.float16, "q")
+    _cuda_tensor(out, torch.float32, "out")
+    _cuda_tensor(page_table, torch.int32, "page_table")
+    _cuda_tensor(seq_lens, torch.int32, "seq_lens")
+    n_layers, nseq, hq, D = q.shape
+    for i, (k, v) in enumerate(zip(k_new, v_new)):
+        _cuda_tensor(k, torch.float16, f"k_new[{i}]")
+        _cuda_tensor(v, torch.float16, f"v_new[{i}]")
+        if k.numel() < nseq * k_pools[i].num_heads * D or v.numel() != k.numel():
+            raise ValueError("k_new/v_new need [nseq, H, D] rows")
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous CUDA tensor")
+    if page_table.dim() != 2 or page_table.shape[0] < nseq or seq_lens.numel() < nseq:
+        raise ValueError("page_table needs a row and seq_lens an entry per sequence")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    _check(_lib.kvq_append_decode_attn(_pool_array(k_pools), _pool_array(v_pools), n_layers,
+                                       _ptr_array(k_new), _ptr_array(v_new), q.data_ptr(), hq,
+                                       page_table.data_ptr(), page_table.shape[1],
+                                       seq_lens.data_ptr(), nseq, max_seq_len, softmax_scale,
+                                       out.data_ptr(), workspace.data_ptr(),
+                                       workspace.numel() * workspace.element_size(),
+                                       _ptr(dev_err), _stream(stream)))
+
+
 def kvq_decode_attn_noalloc(k_pools: Sequence[Pool], v_pools: Sequence[Pool], q: torch.Tensor,
                             page_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
                             softmax_scale: float, out: torch.Tensor,
@@ -452,5 +490,6 @@ def decode_workspace(k_pools: Sequence[Pool], nseq: int, num_q_heads: int, max_s
 __all__ = ["KVQError", "Pool", "Allocator", "parse_mode", "kvq_version", "kvq_packed_dim",
            "kivi_boundary", "kvq_quant_pack_paged", "kvq_dequant_paged", "kivi_quant_dequant",
            "kvq_decode_attn_workspace", "kvq_decode_attn", "kvq_decode_attn_noalloc",
+           "kvq_append_decode_attn",
            "KiviPacked", "kivi_pack", "kivi_decode_attn_workspace", "kivi_decode_attn",
            "decode_workspace", "LIB_PATH"]

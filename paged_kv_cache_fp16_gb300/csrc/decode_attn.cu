@@ -62,6 +62,9 @@ struct AttnArgs {
   const int32_t* pt;
   const int32_t* lens;
   int32_t* err;
+  // fused append: the new token of every sequence, fp16 [nseq][H][D] per layer (else unused)
+  const uint16_t* knew[KVQ_MAX_TENSORS];
+  const uint16_t* vnew[KVQ_MAX_TENSORS];
   int n_layers, nseq, H, G, Hq, ps, max_pages, n_splits, tiles_per_cta;
   float qk_scale;  // softmax_scale * log2(e)
 };
@@ -306,7 +309,56 @@ __device__ __forceinline__ void cta_merge_write(const AttnArgs& a, float* sm, in
 }
 
 // ------------------------------------------------------------------------------ TMA kernel
+// Fused append: quantize the new K and V rows of (layer, sequence s, KV head h) exactly as
+// kvq_quant_pack_paged does, store them at position `pos` of the pools (physical row `prow`) and
+// over row `slot` of the warp's shared-memory stage, whose copy of that slot predates the write.
+// Lanes 0-15 take the K row, lanes 16-31 the V row, 16 elements (one unit) per lane.
 template <int BITS>
+__device__ __forceinline__ void append_rows(const AttnArgs& a, const LayerPools& P, int layer,
+                                            int s, int h, int64_t prow, int slot, uint8_t* sk,
+                                            uint8_t* sv, uint16_t* sks, uint16_t* svs, int lane) {
+  constexpr int kQm = SymQ<BITS>::kQmax;
+  constexpr int kB = SymQ<BITS>::kBias;
+  constexpr int kM = SymQ<BITS>::kMask;
+  constexpr int kPd = Wd<BITS>::kPd;
+  const bool is_v = lane >= 16;
+  const int u = lane & 15;
+  const uint16_t* src = (is_v ? a.vnew[layer] : a.knew[layer]) +
+                        (static_cast<int64_t>(s) * a.H + h) * kD + u * 16;
+  const uint4 x0 = ld_nc_v4(src), x1 = ld_nc_v4(src + 8);
+  const __half2 m2 = __hmax2(absmax8(x0), absmax8(x1));
+  float amax = fmaxf(__low2float(m2), __high2float(m2));
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, o));
+  const uint16_t sbits = f2h(row_scale_f32<kQm>(amax));
+  const float sc = h2f(sbits);
+  const float y = (sc == 0.f) ? 0.f : __frcp_rn(sc);
+  const float se = (sc == 0.f) ? 1.f : sc;
+  const bool clip = sc < 6.103515625e-05f;   // 2^-14, smallest normal fp16
+  uint32_t pk[4];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const uint4& vv = hh ? x1 : x0;
+    const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+    uint32_t f[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      f[e] = quant_field<kQm, kB, kM>(h2f(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)))),
+                                      se, y, clip);
+    pack8<BITS>(f, pk[2 * hh], pk[2 * hh + 1]);
+  }
+  uint8_t* gcodes = const_cast<uint8_t*>(is_v ? P.vc : P.kc);
+  uint16_t* gscales = const_cast<uint16_t*>(is_v ? P.vs : P.ks);
+  const int off = u * SymQ<BITS>::kUnitBytes;
+  store_unit<BITS>(gcodes + prow * kPd + off, pk[0], pk[1], pk[2], pk[3]);
+  store_unit<BITS>((is_v ? sv : sk) + slot * kPd + off, pk[0], pk[1], pk[2], pk[3]);
+  if (u == 0) {
+    gscales[prow] = sbits;
+    (is_v ? svs : sks)[slot] = sbits;
+  }
+}
+
+template <int BITS, bool APPEND>
 __global__ void __launch_bounds__(kThreads, 3) decode_attn_tma_kernel(const AttnArgs a) {
   using W = Wd<BITS>;
   constexpr int S = W::kStages;
@@ -324,7 +376,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_tma_kernel(const Attn
   const int layer = ls / a.nseq;
   const int s = ls - layer * a.nseq;
   const LayerPools P = a.L[layer];
-  const int len = __ldg(a.lens + s);
+  // with APPEND the new token at position lens[s] is attended too
+  const int len = __ldg(a.lens + s) + (APPEND ? 1 : 0);
   const int n_tiles = (len + kTile - 1) / kTile;
   const int tile0 = split * a.tiles_per_cta;
   const int tile1 = min(n_tiles, tile0 + a.tiles_per_cta);
@@ -404,12 +457,21 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_tma_kernel(const Attn
       timed_out = true;
       break;
     }
-    const uint8_t* sk = wbase + st * kStageBytes;
-    const uint8_t* sv = sk + kTile * kPd;
-    const uint16_t* sks = reinterpret_cast<const uint16_t*>(sk + 2 * kTile * kPd);
-    const uint16_t* svs = sks + kTile;
+    uint8_t* sk = wbase + st * kStageBytes;
+    uint8_t* sv = sk + kTile * kPd;
+    uint16_t* sks = reinterpret_cast<uint16_t*>(sk + 2 * kTile * kPd);
+    uint16_t* svs = sks + kTile;
     const bool ok = flags[st] != 0;
     const int tb = (tile0 + warp + j * kWarps) * kTile;
+    if constexpr (APPEND) {
+      const int pos = len - 1;   // the new token; exactly one warp of the grid owns its tile
+      if (ok && pos >= tb && pos < tb + kTile) {   // warp-uniform
+        const int page = page_of(j);
+        const int64_t prow = (static_cast<int64_t>(page) * a.H + h) * a.ps + (pos % a.ps);
+        append_rows<BITS>(a, P, layer, s, h, prow, pos - tb, sk, sv, sks, svs, lane);
+        __syncwarp();
+      }
+    }
     KRegs<BITS> K;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
@@ -600,15 +662,15 @@ int tiles_per_cta_for(int n_layers, int nseq, int H, int max_seq_len) {
   return static_cast<int>(t);
 }
 
-template <int BITS>
+template <int BITS, bool APPEND = false>
 cudaError_t launch_attn(const AttnArgs& a, dim3 grid, bool tma, cudaStream_t cs) {
   if (tma) {
     constexpr int smem = tma_smem_bytes<BITS>();
     static_assert(smem >= kMergeBytes, "merge buffer must fit in the stage ring");
-    cudaError_t e = cudaFuncSetAttribute(decode_attn_tma_kernel<BITS>,
+    cudaError_t e = cudaFuncSetAttribute(decode_attn_tma_kernel<BITS, APPEND>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    decode_attn_tma_kernel<BITS><<<grid, kThreads, smem, cs>>>(a);
+    decode_attn_tma_kernel<BITS, APPEND><<<grid, kThreads, smem, cs>>>(a);
   } else {
     decode_attn_gather_kernel<BITS><<<grid, kThreads, 0, cs>>>(a);
   }
@@ -630,48 +692,60 @@ extern "C" size_t kvq_decode_attn_workspace(int n_layers, int nseq, int num_kv_h
          sizeof(float);
 }
 
-extern "C" kvq_status kvq_decode_attn(const kvq_pool* k_pools, const kvq_pool* v_pools,
-                                      int n_layers, const uint16_t* q, int num_q_heads,
-                                      const int32_t* page_table, int max_pages,
-                                      const int32_t* seq_lens, int nseq, int max_seq_len,
-                                      float softmax_scale, float* out, void* workspace,
-                                      size_t workspace_bytes, int32_t* dev_err,
-                                      kvq_stream_t stream) {
-  using namespace kvq;
+namespace kvq {
+namespace {
+
+// Validation, arguments and launches shared by kvq_decode_attn and kvq_append_decode_attn
+// (knew/vnew non-NULL: the fused append).
+kvq_status decode_attn_entry(const char* fn, const kvq_pool* k_pools, const kvq_pool* v_pools,
+                             int n_layers, const uint16_t* const* knew,
+                             const uint16_t* const* vnew, const uint16_t* q, int num_q_heads,
+                             const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                             int nseq, int max_seq_len, float softmax_scale, float* out,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                             cudaStream_t cs) {
+  const bool append = knew != nullptr || vnew != nullptr;
   if (n_layers < 1 || n_layers > KVQ_MAX_TENSORS)
-    return fail(KVQ_ERR_RANGE, "kvq_decode_attn: n_layers %d not in [1, %d]", n_layers,
-                KVQ_MAX_TENSORS);
-  kvq_status st = check_pools_uniform(k_pools, n_layers, "kvq_decode_attn(k)");
+    return fail(KVQ_ERR_RANGE, "%s: n_layers %d not in [1, %d]", fn, n_layers, KVQ_MAX_TENSORS);
+  kvq_status st = check_pools_uniform(k_pools, n_layers, fn);
   if (st != KVQ_OK) return st;
-  st = check_pools_uniform(v_pools, n_layers, "kvq_decode_attn(v)");
+  st = check_pools_uniform(v_pools, n_layers, fn);
   if (st != KVQ_OK) return st;
   const kvq_pool& k0 = k_pools[0];
   const kvq_pool& v0 = v_pools[0];
   if (v0.bits != k0.bits || v0.num_heads != k0.num_heads || v0.head_dim != k0.head_dim ||
       v0.page_size != k0.page_size)
-    return fail(KVQ_ERR_SHAPE, "kvq_decode_attn: K and V pools differ in shape");
+    return fail(KVQ_ERR_SHAPE, "%s: K and V pools differ in shape", fn);
   if (k0.head_dim != kD)
-    return fail(KVQ_ERR_SHAPE, "kvq_decode_attn: head_dim %d unsupported (256 only)",
-                k0.head_dim);
+    return fail(KVQ_ERR_SHAPE, "%s: head_dim %d unsupported (256 only)", fn, k0.head_dim);
   const int H = k0.num_heads;
   if (num_q_heads < H || num_q_heads % H || num_q_heads / H > 8)
-    return fail(KVQ_ERR_SHAPE, "kvq_decode_attn: num_q_heads %d must be a multiple of %d, "
-                "at most 8 per KV head", num_q_heads, H);
+    return fail(KVQ_ERR_SHAPE, "%s: num_q_heads %d must be a multiple of %d, at most 8 per KV "
+                "head", fn, num_q_heads, H);
+  if (append && k0.page_size % kTile)
+    return fail(KVQ_ERR_SHAPE, "%s: page_size %d must be a multiple of 16", fn, k0.page_size);
   if (nseq < 1 || max_pages < 1 || max_seq_len < 0)
-    return fail(KVQ_ERR_RANGE, "kvq_decode_attn: bad nseq/max_pages/max_seq_len");
+    return fail(KVQ_ERR_RANGE, "%s: bad nseq/max_pages/max_seq_len", fn);
   if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages) * k0.page_size)
-    return fail(KVQ_ERR_RANGE, "kvq_decode_attn: max_seq_len exceeds max_pages * page_size");
+    return fail(KVQ_ERR_RANGE, "%s: max_seq_len exceeds max_pages * page_size", fn);
   if (!q || !page_table || !seq_lens || !out || !workspace)
-    return fail(KVQ_ERR_NULL, "kvq_decode_attn: NULL pointer");
+    return fail(KVQ_ERR_NULL, "%s: NULL pointer", fn);
   if (!aligned16(q) || !aligned16(out) || !aligned16(workspace))
-    return fail(KVQ_ERR_ALIGN, "kvq_decode_attn: q/out/workspace must be 16-byte aligned");
+    return fail(KVQ_ERR_ALIGN, "%s: q/out/workspace must be 16-byte aligned", fn);
+  if (append) {
+    if (!knew || !vnew) return fail(KVQ_ERR_NULL, "%s: NULL new-token array", fn);
+    for (int i = 0; i < n_layers; ++i) {
+      if (!knew[i] || !vnew[i]) return fail(KVQ_ERR_NULL, "%s: new K/V of layer %d is NULL", fn, i);
+      if (!aligned16(knew[i]) || !aligned16(vnew[i]))
+        return fail(KVQ_ERR_ALIGN, "%s: new K/V rows must be 16-byte aligned", fn);
+    }
+  }
   const size_t need = kvq_decode_attn_workspace(n_layers, nseq, H, num_q_heads, kD,
                                                 k0.page_size, max_seq_len);
   if (workspace_bytes < need)
-    return fail(KVQ_ERR_WORKSPACE, "kvq_decode_attn: workspace %zu < %zu bytes",
-                workspace_bytes, need);
+    return fail(KVQ_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, workspace_bytes, need);
   if (static_cast<int64_t>(n_layers) * nseq > 65535)
-    return fail(KVQ_ERR_RANGE, "kvq_decode_attn: n_layers * nseq > 65535");
+    return fail(KVQ_ERR_RANGE, "%s: n_layers * nseq > 65535", fn);
 
   AttnArgs a;
   for (int i = 0; i < KVQ_MAX_TENSORS; ++i) {
@@ -680,6 +754,8 @@ extern "C" kvq_status kvq_decode_attn(const kvq_pool* k_pools, const kvq_pool* v
                           v_pools[i].scales, k_pools[i].num_pages, v_pools[i].num_pages};
     else
       a.L[i] = LayerPools{nullptr, nullptr, nullptr, nullptr, 0, 0};
+    a.knew[i] = (append && i < n_layers) ? knew[i] : nullptr;
+    a.vnew[i] = (append && i < n_layers) ? vnew[i] : nullptr;
   }
   a.q = q;
   a.out = out;
@@ -699,22 +775,52 @@ extern "C" kvq_status kvq_decode_attn(const kvq_pool* k_pools, const kvq_pool* v
   a.n_splits = tiles > 0 ? (tiles + a.tiles_per_cta - 1) / a.tiles_per_cta : 1;
   a.qk_scale = softmax_scale * 1.4426950408889634f;
 
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const dim3 grid(a.n_splits, H, n_layers * nseq);
   const bool tma = (k0.page_size % kTile) == 0;
   cudaError_t e;
   switch (k0.bits) {
-    case 8: e = launch_attn<8>(a, grid, tma, cs); break;
-    case 6: e = launch_attn<6>(a, grid, tma, cs); break;
-    default: e = launch_attn<4>(a, grid, tma, cs); break;
+    case 8: e = append ? launch_attn<8, true>(a, grid, tma, cs) : launch_attn<8>(a, grid, tma, cs); break;
+    case 6: e = append ? launch_attn<6, true>(a, grid, tma, cs) : launch_attn<6>(a, grid, tma, cs); break;
+    default: e = append ? launch_attn<4, true>(a, grid, tma, cs) : launch_attn<4>(a, grid, tma, cs); break;
   }
   if (e == cudaSuccess) {
     decode_merge_kernel<<<dim3(num_q_heads, n_layers * nseq), kD, 0, cs>>>(a);
     e = cudaGetLastError();
   }
-  if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "decode attention launch: %s",
-                                    cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "%s launch: %s", fn, cudaGetErrorString(e));
   return ok();
+}
+
+}  // namespace
+}  // namespace kvq
+
+extern "C" kvq_status kvq_decode_attn(const kvq_pool* k_pools, const kvq_pool* v_pools,
+                                      int n_layers, const uint16_t* q, int num_q_heads,
+                                      const int32_t* page_table, int max_pages,
+                                      const int32_t* seq_lens, int nseq, int max_seq_len,
+                                      float softmax_scale, float* out, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_err,
+                                      kvq_stream_t stream) {
+  return kvq::decode_attn_entry("kvq_decode_attn", k_pools, v_pools, n_layers, nullptr, nullptr,
+                                q, num_q_heads, page_table, max_pages, seq_lens, nseq,
+                                max_seq_len, softmax_scale, out, workspace, workspace_bytes,
+                                dev_err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" kvq_status kvq_append_decode_attn(const kvq_pool* k_pools, const kvq_pool* v_pools,
+                                             int n_layers, const uint16_t* const* k_new,
+                                             const uint16_t* const* v_new, const uint16_t* q,
+                                             int num_q_heads, const int32_t* page_table,
+                                             int max_pages, const int32_t* seq_lens, int nseq,
+                                             int max_seq_len, float softmax_scale, float* out,
+                                             void* workspace, size_t workspace_bytes,
+                                             int32_t* dev_err, kvq_stream_t stream) {
+  if (!k_new || !v_new)
+    return kvq::fail(KVQ_ERR_NULL, "kvq_append_decode_attn: NULL new-token array");
+  return kvq::decode_attn_entry("kvq_append_decode_attn", k_pools, v_pools, n_layers, k_new,
+                                v_new, q, num_q_heads, page_table, max_pages, seq_lens, nseq,
+                                max_seq_len, softmax_scale, out, workspace, workspace_bytes,
+                                dev_err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------------------------------------

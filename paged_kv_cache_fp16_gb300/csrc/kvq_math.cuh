@@ -118,4 +118,56 @@ __device__ __forceinline__ void unpack_group(const uint32_t* w, uint32_t p[4]) {
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Symmetric row quantizer: per width the clip bound, field bias and mask, and the packed bytes of
+// one 16-element unit.
+template <int BITS> struct SymQ;
+template <> struct SymQ<8> { static constexpr int kQmax = 127, kBias = 0, kMask = 0xff, kUnitBytes = 16; };
+template <> struct SymQ<6> { static constexpr int kQmax = 31, kBias = 32, kMask = 0x3f, kUnitBytes = 12; };
+template <> struct SymQ<4> { static constexpr int kQmax = 7, kBias = 8, kMask = 0x0f, kUnitBytes = 8; };
+
+
+__device__ __forceinline__ __half2 habs2u(uint32_t w) {
+  return __habs2(*reinterpret_cast<const __half2*>(&w));
+}
+
+__device__ __forceinline__ __half2 absmax8(const uint4& v) {
+  return __hmax2(__hmax2(habs2u(v.x), habs2u(v.y)), __hmax2(habs2u(v.z), habs2u(v.w)));
+}
+
+// 8 fields (each < 2^BITS) -> packed little-endian bits: q6 two 24-bit words, q4 one word,
+// q8 two words.
+template <int BITS>
+__device__ __forceinline__ void pack8(const uint32_t f[8], uint32_t& a, uint32_t& b) {
+  if constexpr (BITS == 6) {
+    a = f[0] | (f[1] << 6) | (f[2] << 12) | (f[3] << 18);
+    b = f[4] | (f[5] << 6) | (f[6] << 12) | (f[7] << 18);
+  } else if constexpr (BITS == 4) {
+    a = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a |= f[k] << (4 * k);
+    b = 0;
+  } else {
+    a = f[0] | (f[1] << 8) | (f[2] << 16) | (f[3] << 24);
+    b = f[4] | (f[5] << 8) | (f[6] << 16) | (f[7] << 24);
+  }
+}
+
+// Store one unit (16 elements) of packed codes.  With D % 16 == 0 the row stride packed_dim is
+// a multiple of 12 / 16 / 8 bytes (q6 / q8 / q4), so a unit is 4- / 16- / 8-byte aligned.
+template <int BITS>
+__device__ __forceinline__ void store_unit(uint8_t* p, const uint32_t a0, const uint32_t b0,
+                                           const uint32_t a1, const uint32_t b1) {
+  if constexpr (BITS == 6) {
+    // fields 0..7 -> 24-bit words a0, b0; fields 8..15 -> a1, b1; 12 bytes = 3 words
+    *reinterpret_cast<uint32_t*>(p) = a0 | (b0 << 24);
+    *reinterpret_cast<uint32_t*>(p + 4) = (b0 >> 8) | (a1 << 16);
+    *reinterpret_cast<uint32_t*>(p + 8) = (a1 >> 16) | (b1 << 8);
+  } else if constexpr (BITS == 4) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(a0, a1);
+  } else {
+    *reinterpret_cast<uint4*>(p) = make_uint4(a0, b0, a1, b1);
+  }
+}
+
 }  // namespace kvq

@@ -42,11 +42,6 @@ struct PackArgs {
   int lpr_log2;  // lanes per row = 1 << lpr_log2 = min(next_pow2(units), 8)
 };
 
-template <int BITS> struct Q;
-template <> struct Q<8> { static constexpr int kQmax = 127, kBias = 0, kMask = 0xff, kUnitBytes = 16; };
-template <> struct Q<6> { static constexpr int kQmax = 31, kBias = 32, kMask = 0x3f, kUnitBytes = 12; };
-template <> struct Q<4> { static constexpr int kQmax = 7, kBias = 8, kMask = 0x0f, kUnitBytes = 8; };
-
 // Physical row of head 0 of new token `tok` ((page * H) * page_size + slot), or -1.
 __device__ __forceinline__ long long token_base(const PackArgs& a, int64_t num_pages, int tok) {
   const int s = find_seq(a.cu, a.nseq, tok);
@@ -58,49 +53,6 @@ __device__ __forceinline__ long long shfl_ll(long long v, int src) {
   const int lo = __shfl_sync(kFullMask, static_cast<int>(v & 0xffffffffLL), src);
   const int hi = __shfl_sync(kFullMask, static_cast<int>(v >> 32), src);
   return (static_cast<long long>(hi) << 32) | static_cast<unsigned int>(lo);
-}
-
-__device__ __forceinline__ __half2 habs2u(uint32_t w) {
-  return __habs2(*reinterpret_cast<const __half2*>(&w));
-}
-
-__device__ __forceinline__ __half2 absmax8(const uint4& v) {
-  return __hmax2(__hmax2(habs2u(v.x), habs2u(v.y)), __hmax2(habs2u(v.z), habs2u(v.w)));
-}
-
-// 8 fields (each < 2^BITS) -> packed little-endian bits: q6 two 24-bit words, q4 one word,
-// q8 two words.
-template <int BITS>
-__device__ __forceinline__ void pack8(const uint32_t f[8], uint32_t& a, uint32_t& b) {
-  if constexpr (BITS == 6) {
-    a = f[0] | (f[1] << 6) | (f[2] << 12) | (f[3] << 18);
-    b = f[4] | (f[5] << 6) | (f[6] << 12) | (f[7] << 18);
-  } else if constexpr (BITS == 4) {
-    a = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) a |= f[k] << (4 * k);
-    b = 0;
-  } else {
-    a = f[0] | (f[1] << 8) | (f[2] << 16) | (f[3] << 24);
-    b = f[4] | (f[5] << 8) | (f[6] << 16) | (f[7] << 24);
-  }
-}
-
-// Store one unit (16 elements) of packed codes.  With D % 16 == 0 the row stride packed_dim is
-// a multiple of 12 / 16 / 8 bytes (q6 / q8 / q4), so a unit is 4- / 16- / 8-byte aligned.
-template <int BITS>
-__device__ __forceinline__ void store_unit(uint8_t* p, const uint32_t a0, const uint32_t b0,
-                                           const uint32_t a1, const uint32_t b1) {
-  if constexpr (BITS == 6) {
-    // fields 0..7 -> 24-bit words a0, b0; fields 8..15 -> a1, b1; 12 bytes = 3 words
-    *reinterpret_cast<uint32_t*>(p) = a0 | (b0 << 24);
-    *reinterpret_cast<uint32_t*>(p + 4) = (b0 >> 8) | (a1 << 16);
-    *reinterpret_cast<uint32_t*>(p + 8) = (a1 >> 16) | (b1 << 8);
-  } else if constexpr (BITS == 4) {
-    *reinterpret_cast<uint2*>(p) = make_uint2(a0, a1);
-  } else {
-    *reinterpret_cast<uint4*>(p) = make_uint4(a0, b0, a1, b1);
-  }
 }
 
 // Load one unit of packed codes (words for unpack_group<BITS, 0> and <BITS, 1>).
@@ -122,9 +74,9 @@ __device__ __forceinline__ void load_unit(const uint8_t* p, uint32_t w[4]) {
 
 template <int BITS, int UPL>
 __global__ void __launch_bounds__(kThreads) quant_pack_kernel(const PackArgs a) {
-  constexpr int kQm = Q<BITS>::kQmax;
-  constexpr int kB = Q<BITS>::kBias;
-  constexpr int kM = Q<BITS>::kMask;
+  constexpr int kQm = SymQ<BITS>::kQmax;
+  constexpr int kB = SymQ<BITS>::kBias;
+  constexpr int kM = SymQ<BITS>::kMask;
   const int t = blockIdx.y;
   const uint16_t* __restrict__ x = a.x[t];
   const PoolRef pool = a.pool[t];
@@ -200,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) quant_pack_kernel(const PackArgs a) 
             }
             pack8<BITS>(f, pk[2 * hh], pk[2 * hh + 1]);
           }
-          store_unit<BITS>(crow + unit * Q<BITS>::kUnitBytes, pk[0], pk[1], pk[2], pk[3]);
+          store_unit<BITS>(crow + unit * SymQ<BITS>::kUnitBytes, pk[0], pk[1], pk[2], pk[3]);
         }
         if (lr == 0) pool.scales[prow] = sbits;
       }
@@ -249,7 +201,7 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const PackArgs a) {
 #pragma unroll
           for (int j = 0; j < UPL; ++j) {
             const int unit = lr + j * lpr;
-            if (unit * 16 < D) load_unit<BITS>(crow + unit * Q<BITS>::kUnitBytes, w[u][j]);
+            if (unit * 16 < D) load_unit<BITS>(crow + unit * SymQ<BITS>::kUnitBytes, w[u][j]);
           }
           sc[u] = ld_nc_u16(pool.scales + prow);
         }

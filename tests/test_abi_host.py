@@ -231,3 +231,17 @@ def test_kivi_packed_rejects_bad_arguments_before_launch(kvq):
     assert attn(C(), offset=129) == 5               # beyond capacity
     assert attn(C(), ws=16) == 8
     assert kvq.kivi_decode_attn_workspace(1, 1, 2, 8, 64, 100) > 0
+
+
+def test_append_decode_rejects_bad_arguments_before_launch(kvq):
+    f = kvq._lib.kvq_append_decode_attn
+    P = lambda **kw: (kvq.kvq_pool * 1)(_pool(kvq, **kw))
+    xs = (ctypes.c_void_p * 1)(FAKE)
+    call = lambda kp, vp, kn=xs, vn=xs, ws=1 << 30: f(kp, vp, 1, kn, vn, FAKE, 24, FAKE, 4, FAKE,
+                                                     1, 64, 0.0625, FAKE, FAKE, ws, None, None)
+    assert call(P(ps=8), P(ps=8)) == 2              # page size not a multiple of 16
+    assert call(P(), P(), kn=None) == 3
+    assert call(P(), P(), vn=(ctypes.c_void_p * 1)(0)) == 3
+    assert call(P(), P(), kn=(ctypes.c_void_p * 1)(FAKE + 2)) == 4
+    assert call(P(), P(), ws=16) == 8
+    assert call(P(D=128), P(D=128)) == 2
