@@ -147,3 +147,84 @@ def decode_attention(q16: np.ndarray, k_packed, v_packed, k_res16: np.ndarray,
         out[b] = attention.attend(q16[b], np.transpose(k_all[b], (1, 0, 2)),
                                   np.transpose(v_all[b], (1, 0, 2)), softmax_scale)
     return out
+
+
+class KiviPackedCache:
+    """The KIVI cache protocol of the page (``update_and_fetch``, ``trim`` with
+    ``_rollback_frontier``) with the quantized region held in the packed form above.
+
+    Tokens [0, n_quantized) are packed; tokens [n_quantized, offset) are the fp16 residual
+    window.  A flush packs [n_quantized, boundary) from the fp16 rows (``update_and_fetch``).
+    A trim pulls the frontier down to a group multiple; the rows between the new frontier and the
+    new offset leave the packed region carrying their round-tripped values into the fp16 window
+    (on the page they were round-tripped in place), so the next flush quantizes them a second time
+    -- the double rounding the page bounds by one quantization step.
+    """
+
+    def __init__(self, batch: int, num_heads: int, head_dim: int, capacity: int,
+                 bit_width: int = 2, group_size: int = 32, residual_length: int = 128,
+                 eps: float = 1e-8):
+        from . import kivi
+        self._kivi = kivi
+        B, H, D, S, gs = batch, num_heads, head_dim, capacity, group_size
+        if S % gs:
+            raise ValueError("capacity must be a multiple of group_size")
+        self.bits, self.gs, self.residual_length, self.eps = bit_width, gs, residual_length, eps
+        self.keys = np.zeros((B, H, S, D), np.float16)
+        self.values = np.zeros((B, H, S, D), np.float16)
+        cb = D * bit_width // 8
+        G = -(-D // gs)
+        self.k_codes = np.zeros((B, H, S, cb), np.uint8)
+        self.k_scale = np.zeros((B, H, S // gs, D), np.float16)
+        self.k_zero = np.zeros((B, H, S // gs, D), np.float16)
+        self.v_codes = np.zeros((B, H, S, cb), np.uint8)
+        self.v_scale = np.zeros((B, H, S, G), np.float16)
+        self.v_zero = np.zeros((B, H, S, G), np.float16)
+        self.offset = 0
+        self.n_quantized = 0
+
+    def update(self, keys: np.ndarray, values: np.ndarray) -> None:
+        n = keys.shape[2]
+        self.keys[:, :, self.offset:self.offset + n] = keys
+        self.values[:, :, self.offset:self.offset + n] = values
+        self.offset += n
+        hi = self._kivi.quantization_boundary(self.offset, self.residual_length, self.gs)
+        lo = self.n_quantized
+        if hi > lo:
+            gs = self.gs
+            c, s, z = pack_keys(self.keys[:, :, lo:hi], self.bits, gs, self.eps)
+            self.k_codes[:, :, lo:hi], self.k_scale[:, :, lo // gs:hi // gs] = c, s
+            self.k_zero[:, :, lo // gs:hi // gs] = z
+            c, s, z = pack_values(self.values[:, :, lo:hi], self.bits, gs, self.eps)
+            self.v_codes[:, :, lo:hi], self.v_scale[:, :, lo:hi], self.v_zero[:, :, lo:hi] = c, s, z
+            self.n_quantized = hi
+
+    def _unpacked(self, lo: int, hi: int):
+        D, gs = self.keys.shape[3], self.gs
+        g0 = lo // gs
+        g1 = -(-hi // gs)
+        k = unpack_keys(self.k_codes[:, :, g0 * gs:g1 * gs], self.k_scale[:, :, g0:g1],
+                        self.k_zero[:, :, g0:g1], self.bits, gs, D)[:, :, lo - g0 * gs:hi - g0 * gs]
+        v = unpack_values(self.v_codes[:, :, lo:hi], self.v_scale[:, :, lo:hi],
+                          self.v_zero[:, :, lo:hi], self.bits, gs, D)
+        return k, v
+
+    def trim(self, n: int) -> int:
+        trimmed = min(self.offset, n)
+        self.offset -= trimmed
+        if trimmed:
+            gs = self.gs
+            new_nq = min(self.n_quantized, (max(self.offset, 0) // gs) * gs)
+            hi = min(self.n_quantized, self.offset)
+            if hi > new_nq:   # rows leaving the packed region keep their round-tripped values
+                k, v = self._unpacked(new_nq, hi)
+                self.keys[:, :, new_nq:hi], self.values[:, :, new_nq:hi] = k, v
+            self.n_quantized = new_nq
+        return trimmed
+
+    def fetch(self):
+        """The cache as attention sees it: unpacked [0, n_quantized) then the fp16 window."""
+        nq, off = self.n_quantized, self.offset
+        k, v = self._unpacked(0, nq)
+        return (np.concatenate([k, self.keys[:, :, nq:off]], axis=2),
+                np.concatenate([v, self.values[:, :, nq:off]], axis=2))

@@ -153,3 +153,83 @@ def test_attention_special_cases():
     out = P.decode_attention(q, kp2, vp2, kk[:, :, 32:], vv[:, :, 32:], 2, 32, 0.125)
     vh = np.concatenate([P.unpack_values(*vp2, 2, 32, D), vv[:, :, 32:]], axis=2)
     assert np.allclose(out[0], vh[0, 0].astype(np.float64).mean(0), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- the cache protocol, packed
+def _exact_scale_tokens(rng, B, H, n, D, gs):
+    """Tokens whose every key group (gs tokens of a channel) and value group (gs channels of a
+    token) spans exactly 3 * 2^e: range / 3 is an fp16 value, so the packed and the in-place
+    round trips use the same scale and give the same fp16 values."""
+    e = rng.integers(-4, 2, size=(B, H, n // gs, 1, 1))
+    base = rng.integers(-6, 6, size=(B, H, n // gs, 1, 1)) * 2.0 ** e
+    frac = rng.integers(0, 13, size=(B, H, n // gs, gs, D)) / 4.0
+    frac[:, :, :, 0, :] = 0          # every key group holds its min and max
+    frac[:, :, :, 1, :] = 3
+    frac[..., 0::gs] = 0             # every value group holds its min and max
+    frac[..., 1::gs] = 3
+    x = (base + frac * 2.0 ** e).reshape(B, H, n, D)
+    assert np.all(x.astype(np.float16).astype(np.float64) == x)
+    return x.astype(np.float16)
+
+
+def test_packed_protocol_equals_the_in_place_protocol_on_exact_scale_data():
+    """update_and_fetch in chunks of 1..70 tokens: the packed cache's view equals the page's
+    in-place fp16 cache bit for bit (same flush windows, same round-tripped values)."""
+    rng = np.random.default_rng(11)
+    B, H, D, gs, R, S = 2, 2, 64, 32, 128, 640
+    k = _exact_scale_tokens(rng, B, H, S, D, gs)
+    v = _exact_scale_tokens(rng, B, H, S, D, gs)
+    ref = K.KiviCache(B, H, D, S, bit_width=2, group_size=gs, residual_length=R)
+    pc = P.KiviPackedCache(B, H, D, S, bit_width=2, group_size=gs, residual_length=R)
+    t = 0
+    for n in [1, 5, 70, 31, 64, 1, 1, 128, 40, 200]:
+        kr, vr = ref.update_and_fetch(k[:, :, t:t + n], v[:, :, t:t + n])
+        pc.update(k[:, :, t:t + n], v[:, :, t:t + n])
+        t += n
+        assert pc.offset == ref.offset and pc.n_quantized == ref.n_quantized
+        kp, vp = pc.fetch()
+        assert np.array_equal(kp.view(np.uint16), kr.view(np.uint16))
+        assert np.array_equal(vp.view(np.uint16), vr.view(np.uint16))
+
+
+def test_packed_trim_rolls_back_like_the_page_and_keeps_round_tripped_rows():
+    """Frontier after a trim = min(old, floor(offset / gs) * gs) (``_rollback_frontier``); the
+    rows between the new frontier and the new offset hold their round-tripped values in the fp16
+    window, and the view is unchanged on the kept tokens."""
+    B, H, D, gs, R, S = 1, 2, 64, 32, 128, 512
+    x = kvgen.KiviSpec(seed=8, layer=0, is_key=True, batch=B, num_heads=H, seq=S, head_dim=D)
+    y = kvgen.KiviSpec(seed=8, layer=0, is_key=False, batch=B, num_heads=H, seq=S, head_dim=D)
+    k, v = x.full_np(), y.full_np()
+    pc = P.KiviPackedCache(B, H, D, S, group_size=gs, residual_length=R)
+    pc.update(k[:, :, :400], v[:, :, :400])
+    assert pc.n_quantized == 256
+    before_k, before_v = pc.fetch()
+    assert pc.trim(150) == 150 and pc.offset == 250 and pc.n_quantized == 224
+    kk, vv = pc.fetch()
+    assert np.array_equal(kk.view(np.uint16), before_k[:, :, :250].view(np.uint16))
+    assert np.array_equal(vv.view(np.uint16), before_v[:, :, :250].view(np.uint16))
+    assert not np.array_equal(pc.keys[:, :, 224:250], k[:, :, 224:250])   # round-tripped now
+    assert pc.trim(1000) == 250 and pc.offset == 0 and pc.n_quantized == 0
+
+
+def test_packed_requantize_after_trim_moves_values_by_at_most_one_step():
+    """The page's bound on the double rounding: a row quantized, rolled back by a trim and
+    quantized again differs from its first round trip by at most one step of the new group
+    (plus half an fp16 ulp of each stored value)."""
+    B, H, D, gs, R, S = 1, 2, 64, 32, 128, 640
+    x = kvgen.KiviSpec(seed=9, layer=1, is_key=True, batch=B, num_heads=H, seq=S, head_dim=D)
+    y = kvgen.KiviSpec(seed=9, layer=1, is_key=False, batch=B, num_heads=H, seq=S, head_dim=D)
+    k, v = x.full_np(), y.full_np()
+    pc = P.KiviPackedCache(B, H, D, S, group_size=gs, residual_length=R)
+    pc.update(k[:, :, :420], v[:, :, :420])            # frontier 288
+    first_k, first_v = (a.astype(np.float64) for a in pc.fetch())
+    pc.trim(140)                                       # offset 280, frontier 256
+    pc.update(k[:, :, 280:600], v[:, :, 280:600])      # re-flushes [256, 448)
+    again_k, again_v = (a.astype(np.float64) for a in pc.fetch())
+    rows = slice(256, 280)
+    ks = np.repeat(pc.k_scale.astype(np.float64), gs, axis=2)[:, :, rows]
+    vs = pc.v_scale.astype(np.float64)[:, :, rows][..., np.arange(D) // gs]
+    for a, b, s in ((again_k, first_k, ks), (again_v, first_v, vs)):
+        d = np.abs(a[:, :, rows] - b[:, :, rows])
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(b[:, :, rows]), 2 ** -14))) - 10)
+        assert np.all(d <= s + ulp)
