@@ -8,6 +8,7 @@
  *   kvq_decode_attn        decode attention that reads the packed pages directly
  *   kvq_append_decode_attn one decode step: append the new token, then attend, in one launch
  *   kivi_pack, kivi_decode_attn   packed KIVI storage and decode attention over it
+ *   kivi_update, kivi_trim, kivi_packed_update, kivi_packed_trim   the KIVI cache protocol
  * plus host helpers: packed_dim, the KIVI residual boundary, and a page allocator.
  *
  * Conventions shared by every entry point
@@ -347,6 +348,83 @@ KVQ_API kvq_status kivi_decode_attn(const kivi_packed* caches, const uint16_t* c
                                     float softmax_scale, float* out, void* workspace,
                                     size_t workspace_bytes, int32_t* dev_err,
                                     kvq_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * The KIVI cache protocol: update (append + flush) and trim (frontier rollback)
+ * ------------------------------------------------------------------------------------------ */
+
+/*
+ * VeloxQuant-MLX source page "veloxquant_mlx.cache.kivi_cache": KIVIKVCache.update_and_fetch,
+ * _quantization_boundary, trim and _rollback_frontier.  A kivi_state (host memory, owned by the
+ * caller) tracks one cache of n_layers layers that append and trim together: `offset` tokens
+ * held in [B][H][capacity][D] fp16 K and V caches, the first `n_quantized` of them quantized.
+ * bits 2/4/8 give levels 2^bits - 1; eps is the page's 1e-8.  Fill it with kivi_state_init
+ * (offset 0); the calls below advance it only when they succeed.
+ */
+typedef struct kivi_state {
+  int32_t batch;
+  int32_t num_heads;
+  int32_t head_dim;         /* multiple of 8, <= 256 */
+  int32_t capacity;
+  int32_t bits;             /* 2, 4 or 8 */
+  int32_t group_size;
+  int32_t residual_length;  /* the page's residual window R (128 by default) */
+  float eps;
+  int32_t offset;           /* tokens held */
+  int32_t n_quantized;      /* the quantization frontier */
+} kivi_state;
+
+KVQ_API kvq_status kivi_state_init(kivi_state* st, int batch, int num_heads, int head_dim,
+                                   int capacity, int bits, int group_size, int residual_length);
+
+/*
+ * update_and_fetch for the page's in-place cache: copy the n_new new tokens of every layer
+ * (k_new[l], v_new[l]: device fp16 [B][H][n_new][D], 16-byte aligned) into k_cache[l],
+ * v_cache[l] at st->offset (one launch for all layers), then round-trip the tokens
+ * [n_quantized, kivi_boundary(offset + n_new)) in place (kivi_quant_dequant, one launch), and
+ * advance the state.  n_layers <= 32.  Errors: those of kivi_quant_dequant, KVQ_ERR_RANGE if the
+ * tokens do not fit.  The "fetch" is the caches' first st->offset tokens.
+ */
+KVQ_API kvq_status kivi_update(kivi_state* st, uint16_t* const* k_cache, uint16_t* const* v_cache,
+                               const uint16_t* const* k_new, const uint16_t* const* v_new,
+                               int n_layers, int n_new, kvq_stream_t stream);
+
+/*
+ * trim for the page's in-place cache: drop the last n tokens (at most offset) and pull the
+ * frontier down to min(n_quantized, (offset / group_size) * group_size).  Host only: the rows
+ * between the new frontier and the new offset keep their round-tripped values in the cache and
+ * are quantized again by the next flush (the double rounding the page bounds by one step).
+ * Returns the number of tokens dropped.
+ */
+KVQ_API int kivi_trim(kivi_state* st, int n);
+
+/*
+ * update_and_fetch with the quantized region packed (kivi_packed, one per layer, matching the
+ * state): append as kivi_update, then kivi_pack tokens [n_quantized, boundary) from the fp16
+ * caches.  Attention: kivi_decode_attn(n_packed = st->n_quantized, offset = st->offset).
+ */
+KVQ_API kvq_status kivi_packed_update(kivi_state* st, const kivi_packed* caches,
+                                      uint16_t* const* k_cache, uint16_t* const* v_cache,
+                                      const uint16_t* const* k_new, const uint16_t* const* v_new,
+                                      int n_layers, int n_new, kvq_stream_t stream);
+
+/*
+ * trim with the quantized region packed: as kivi_trim, and the rows that leave the packed region
+ * ([new frontier, min(old frontier, new offset))) get their round-tripped values written into
+ * the fp16 caches (kivi_unpack), as the page's in-place cache holds them.  *trimmed (may be
+ * NULL) receives the number of tokens dropped.
+ */
+KVQ_API kvq_status kivi_packed_trim(kivi_state* st, const kivi_packed* caches,
+                                    uint16_t* const* k_cache, uint16_t* const* v_cache,
+                                    int n_layers, int n, int* trimmed, kvq_stream_t stream);
+
+/*
+ * Write the reconstruction fp16(float32(c * scale) + zero) of packed tokens [lo, hi) of every
+ * layer into k[l], v[l] (device fp16 [B][H][capacity][D]).  Errors: KVQ_ERR_BITS, KVQ_ERR_SHAPE,
+ * KVQ_ERR_NULL, KVQ_ERR_ALIGN, KVQ_ERR_RANGE, KVQ_ERR_CUDA.
+ */
+KVQ_API kvq_status kivi_unpack(const kivi_packed* caches, uint16_t* const* k, uint16_t* const* v,
+                               int n_layers, int lo, int hi, kvq_stream_t stream);
 
 /*
  * Decode attention for callers that cannot allocate device memory (no counterpart on the pages:

@@ -52,6 +52,14 @@ class kivi_packed(ctypes.Structure):
                 ("v_scale", ctypes.c_void_p), ("v_zero", ctypes.c_void_p)]
 
 
+class kivi_state(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("capacity", ctypes.c_int32),
+                ("bits", ctypes.c_int32), ("group_size", ctypes.c_int32),
+                ("residual_length", ctypes.c_int32), ("eps", ctypes.c_float),
+                ("offset", ctypes.c_int32), ("n_quantized", ctypes.c_int32)]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -80,6 +88,14 @@ def _load() -> ctypes.CDLL:
         "kvq_append_decode_attn": (I, [pool_p, pool_p, I, P, P, P, I, P, I, P, I, I, F, P, P, S,
                                        P, P]),
         "kivi_pack": (I, [ctypes.POINTER(kivi_packed), P, P, I, I, I, F, P]),
+        "kivi_state_init": (I, [ctypes.POINTER(kivi_state), I, I, I, I, I, I, I]),
+        "kivi_update": (I, [ctypes.POINTER(kivi_state), P, P, P, P, I, I, P]),
+        "kivi_trim": (I, [ctypes.POINTER(kivi_state), I]),
+        "kivi_packed_update": (I, [ctypes.POINTER(kivi_state), ctypes.POINTER(kivi_packed), P, P,
+                                   P, P, I, I, P]),
+        "kivi_packed_trim": (I, [ctypes.POINTER(kivi_state), ctypes.POINTER(kivi_packed), P, P,
+                                 I, I, ctypes.POINTER(ctypes.c_int), P]),
+        "kivi_unpack": (I, [ctypes.POINTER(kivi_packed), P, P, I, I, I, P]),
         "kivi_decode_attn_workspace": (S, [I, I, I, I, I, I]),
         "kivi_decode_attn": (I, [ctypes.POINTER(kivi_packed), P, P, I, P, I, I, I, F, P, P, S,
                                  P, P]),
@@ -452,6 +468,87 @@ def kivi_pack(caches: Sequence[KiviPacked], ks: Sequence[torch.Tensor],
                           hi, eps, _stream(stream)))
 
 
+def kivi_state_new(batch: int, num_heads: int, head_dim: int, capacity: int, bits: int = 2,
+                   group_size: int = 32, residual_length: int = 128) -> kivi_state:
+    """An empty KIVI cache state (offset 0, frontier 0)."""
+    st = kivi_state()
+    _check(_lib.kivi_state_init(ctypes.byref(st), batch, num_heads, head_dim, capacity, bits,
+                                group_size, residual_length))
+    return st
+
+
+def _new_tokens(ks, vs, st):
+    n = None
+    for i, (k, v) in enumerate(zip(ks, vs)):
+        _cuda_tensor(k, torch.float16, f"k_new[{i}]")
+        _cuda_tensor(v, torch.float16, f"v_new[{i}]")
+        if k.dim() != 4 or k.shape != v.shape or k.shape[0] != st.batch or \
+                k.shape[1] != st.num_heads or k.shape[3] != st.head_dim:
+            raise ValueError("new tokens are [B, H, n, D] per layer, K and V alike")
+        if n is not None and k.shape[2] != n:
+            raise ValueError("every layer appends the same number of tokens")
+        n = k.shape[2]
+    return n or 0
+
+
+def _caches(kc, vc, st):
+    for i, (k, v) in enumerate(zip(kc, vc)):
+        _cuda_tensor(k, torch.float16, f"k_cache[{i}]")
+        _cuda_tensor(v, torch.float16, f"v_cache[{i}]")
+        if k.shape != (st.batch, st.num_heads, st.capacity, st.head_dim) or v.shape != k.shape:
+            raise ValueError("caches are [B, H, capacity, D] per layer")
+
+
+def kivi_update(st: kivi_state, k_cache, v_cache, k_new, v_new, stream=None) -> None:
+    """update_and_fetch on the in-place fp16 cache (all layers); advances `st`."""
+    if not (len(k_cache) == len(v_cache) == len(k_new) == len(v_new)):
+        raise ValueError("one cache and one new-token tensor per layer, K and V")
+    _caches(k_cache, v_cache, st)
+    n = _new_tokens(k_new, v_new, st)
+    _check(_lib.kivi_update(ctypes.byref(st), _ptr_array(k_cache), _ptr_array(v_cache),
+                            _ptr_array(k_new), _ptr_array(v_new), len(k_cache), n,
+                            _stream(stream)))
+
+
+def kivi_trim(st: kivi_state, n: int) -> int:
+    """trim on the in-place cache (host only); returns the number of tokens dropped."""
+    return _lib.kivi_trim(ctypes.byref(st), n)
+
+
+def kivi_packed_update(st: kivi_state, caches: Sequence["KiviPacked"], k_cache, v_cache, k_new,
+                       v_new, stream=None) -> None:
+    """update_and_fetch with the quantized region packed; advances `st`."""
+    if not (len(caches) == len(k_cache) == len(v_cache) == len(k_new) == len(v_new)):
+        raise ValueError("one packed cache, cache and new-token tensor per layer")
+    _caches(k_cache, v_cache, st)
+    n = _new_tokens(k_new, v_new, st)
+    _check(_lib.kivi_packed_update(ctypes.byref(st), _packed_array(caches), _ptr_array(k_cache),
+                                   _ptr_array(v_cache), _ptr_array(k_new), _ptr_array(v_new),
+                                   len(caches), n, _stream(stream)))
+
+
+def kivi_packed_trim(st: kivi_state, caches: Sequence["KiviPacked"], k_cache, v_cache, n: int,
+                     stream=None) -> int:
+    """trim with the quantized region packed; returns the number of tokens dropped."""
+    if not (len(caches) == len(k_cache) == len(v_cache)):
+        raise ValueError("one packed cache and one cache per layer")
+    _caches(k_cache, v_cache, st)
+    out = ctypes.c_int(0)
+    _check(_lib.kivi_packed_trim(ctypes.byref(st), _packed_array(caches), _ptr_array(k_cache),
+                                 _ptr_array(v_cache), len(caches), n, ctypes.byref(out),
+                                 _stream(stream)))
+    return out.value
+
+
+def kivi_unpack(caches: Sequence["KiviPacked"], k, v, lo: int, hi: int, stream=None) -> None:
+    """Write the reconstruction of packed tokens [lo, hi) into fp16 k[l], v[l]."""
+    for i, (a, b) in enumerate(zip(k, v)):
+        _cuda_tensor(a, torch.float16, f"k[{i}]")
+        _cuda_tensor(b, torch.float16, f"v[{i}]")
+    _check(_lib.kivi_unpack(_packed_array(caches), _ptr_array(k), _ptr_array(v), len(caches), lo,
+                            hi, _stream(stream)))
+
+
 def kivi_decode_attn_workspace(n_layers: int, batch: int, num_heads: int, num_q_heads: int,
                                head_dim: int, offset: int) -> int:
     return _lib.kivi_decode_attn_workspace(n_layers, batch, num_heads, num_q_heads, head_dim,
@@ -492,4 +589,6 @@ __all__ = ["KVQError", "Pool", "Allocator", "parse_mode", "kvq_version", "kvq_pa
            "kvq_decode_attn_workspace", "kvq_decode_attn", "kvq_decode_attn_noalloc",
            "kvq_append_decode_attn",
            "KiviPacked", "kivi_pack", "kivi_decode_attn_workspace", "kivi_decode_attn",
+           "kivi_state", "kivi_state_new", "kivi_update", "kivi_trim", "kivi_packed_update",
+           "kivi_packed_trim", "kivi_unpack",
            "decode_workspace", "LIB_PATH"]

@@ -245,3 +245,56 @@ def test_append_decode_rejects_bad_arguments_before_launch(kvq):
     assert call(P(), P(), kn=(ctypes.c_void_p * 1)(FAKE + 2)) == 4
     assert call(P(), P(), ws=16) == 8
     assert call(P(D=128), P(D=128)) == 2
+
+
+def test_kivi_state_and_trim_follow_the_page_rollback(kvq):
+    """kivi_trim is host arithmetic: offsets and frontiers follow the oracle's cache (the page's
+    trim with _rollback_frontier) over a seeded sequence of appends and trims."""
+    from oracle import kivi as K
+    with pytest.raises(kvq.KVQError):
+        kvq.kivi_state_new(1, 1, 12, 64)              # head_dim % 8
+    with pytest.raises(kvq.KVQError):
+        kvq.kivi_state_new(1, 1, 64, 64, bits=3)
+    rng = np.random.default_rng(5)
+    st = kvq.kivi_state_new(1, 1, 64, 4096, bits=2, group_size=32, residual_length=128)
+    ref = K.KiviCache(1, 1, 8, 4096, bit_width=2, group_size=32, residual_length=128)
+    for _ in range(300):
+        if rng.random() < 0.7:
+            n = int(rng.integers(1, 90))
+            if ref.offset + n > 4096:
+                continue
+            ref.offset += n                            # the state part of update_and_fetch
+            b = K.quantization_boundary(ref.offset, 128, 32)
+            ref.n_quantized = max(ref.n_quantized, b)
+            st.offset, st.n_quantized = ref.offset, ref.n_quantized
+        else:
+            n = int(rng.integers(0, 200))
+            assert kvq.kivi_trim(st, n) == ref.trim(n)
+            assert (st.offset, st.n_quantized) == (ref.offset, ref.n_quantized)
+
+
+def test_kivi_protocol_rejects_bad_arguments_before_launch(kvq):
+    st = kvq.kivi_state_new(1, 2, 64, 128, bits=2, group_size=32, residual_length=16)
+    xs = (ctypes.c_void_p * 1)(FAKE)
+    sp = ctypes.byref(st)
+    f = kvq._lib.kivi_update
+    assert f(sp, xs, xs, xs, xs, 1, 129, None) == 5                 # does not fit
+    assert f(sp, xs, xs, None, xs, 1, 4, None) == 3
+    assert f(sp, xs, (ctypes.c_void_p * 1)(FAKE + 2), xs, xs, 1, 4, None) == 4
+    assert f(sp, xs, xs, xs, xs, 33, 4, None) == 5                  # at most 32 layers
+    assert f(sp, xs, xs, xs, xs, 1, 0, None) == 0                   # nothing to do
+    assert (st.offset, st.n_quantized) == (0, 0)
+    C = (kvq.kivi_packed * 1)(kvq.kivi_packed(2, 32, 1, 2, 128, 64, FAKE, FAKE, FAKE, FAKE,
+                                              FAKE, FAKE))
+    bad = (kvq.kivi_packed * 1)(kvq.kivi_packed(2, 32, 1, 2, 256, 64, FAKE, FAKE, FAKE, FAKE,
+                                                FAKE, FAKE))
+    g = kvq._lib.kivi_packed_update
+    assert g(sp, bad, xs, xs, xs, xs, 1, 4, None) == 2              # capacity differs
+    assert g(sp, C, xs, xs, xs, xs, 1, 200, None) == 5
+    out = ctypes.c_int(-1)
+    assert kvq._lib.kivi_packed_trim(sp, C, xs, xs, 1, 5, ctypes.byref(out), None) == 0
+    assert out.value == 0                                           # empty cache: nothing cut
+    u = kvq._lib.kivi_unpack
+    assert u(C, xs, xs, 1, 0, 129, None) == 2
+    assert u(C, xs, xs, 1, 10, 5, None) == 2
+    assert u(C, xs, xs, 1, 7, 7, None) == 0                         # empty: no launch
