@@ -255,6 +255,64 @@ def decode_step_extra(kvq, dev, steps, warmup, stream, bits=6):
     return res
 
 
+def kivi_loop_extra(kvq, dev, warmup, stream, passes=3):
+    """The KIVI serving loop on the [16, 8, 4096, 64] x 16-layer cache (2-bit, group 32, residual
+    128): from a prefill of 3,936 tokens (3,808 packed), 32 decode steps, each appending one token
+    to every layer (kivi_packed_update; one flush of 32 tokens falls in the 32 steps) and running
+    kivi_decode_attn for 32 query heads over the packed tokens and the fp16 window.  The state
+    is restored to the post-prefill point before every pass (a pass rewrites the same bytes)."""
+    L, B, H, S, D, gs = KV["n_layers"], KV["B"], KV["H"], KV["S"], KV["D"], KV["group_size"]
+    prefill, steps = 3936, 32
+    kc = [kvgen.KiviSpec(seed=KV["seed"], layer=l, is_key=True, batch=B, num_heads=H, seq=S,
+                         head_dim=D).full_torch(dev) for l in range(L)]
+    vc = [kvgen.KiviSpec(seed=KV["seed"], layer=l, is_key=False, batch=B, num_heads=H, seq=S,
+                         head_dim=D).full_torch(dev) for l in range(L)]
+    caches = [kvq.KiviPacked.empty(KIVI_BITS, gs, B, H, S, D, dev) for _ in range(L)]
+    st = kvq.kivi_state_new(B, H, D, S, bits=KIVI_BITS, group_size=gs,
+                            residual_length=KV["residual"])
+    st.offset = prefill                      # the caches hold the prefill tokens already
+    kvq.kivi_packed_update(st, caches, kc, vc)   # pack the aged prefill tokens
+    nq0 = st.n_quantized
+    # new tokens of each step, [B, H, 1, D] per layer (the generator's tokens 3936..3967)
+    kn = [[kc[l][:, :, prefill + i:prefill + i + 1].clone() for l in range(L)] for i in range(steps)]
+    vn = [[vc[l][:, :, prefill + i:prefill + i + 1].clone() for l in range(L)] for i in range(steps)]
+    q = kvgen.queries_torch(KV["seed"] + 1, L, B, KIVI_HQ, D, dev)
+    out = torch.empty((L, B, KIVI_HQ, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(kvq.kivi_decode_attn_workspace(L, B, H, KIVI_HQ, D, S), dtype=torch.uint8,
+                     device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    scale = 1.0 / np.sqrt(D)
+
+    def one_pass():
+        st.offset, st.n_quantized = prefill, nq0
+        for i in range(steps):
+            kvq.kivi_packed_update(st, caches, kc, vc, kn[i], vn[i])
+            kvq.kivi_decode_attn(caches, kc, vc, q, st.n_quantized, st.offset, scale, out, ws, err)
+
+    for _ in range(warmup):
+        one_pass()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(passes):
+        st.offset, st.n_quantized = prefill, nq0
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(steps):
+            kvq.kivi_packed_update(st, caches, kc, vc, kn[i], vn[i])
+            kvq.kivi_decode_attn(caches, kc, vc, q, st.n_quantized, st.offset, scale, out, ws, err)
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / 1e3)
+    if int(err.item()) != 0:
+        raise RuntimeError("device error word set in the KIVI loop")
+    t = sum(times) / len(times)
+    res = {"ms_per_step": t / steps * 1e3, "tok_s": B * steps / t, "steps": steps,
+           "flushes": 1, "first_offset": prefill + 1}
+    del kc, vc, caches, kn, vn
+    torch.cuda.empty_cache()
+    return res
+
+
 class Workload:
     """Device-resident inputs and outputs of one replica (outputs allocated on first use)."""
 
@@ -518,6 +576,10 @@ def run_gpu(args):
         w._kp = None
         torch.cuda.empty_cache()
 
+    # the KIVI serving loop: append one token, flush every 32, attend over packed + window
+    if not args.no_kivi_packed:
+        extras["kivi_decode_loop_16L_16x8_2bit"] = kivi_loop_extra(kvq, dev, args.warmup, stream)
+
     # one decode step (append + attend) of 64 ragged sequences
     if not args.no_decode_step:
         extras["decode_step_64seq_ragged_16L_q6"] = decode_step_extra(kvq, dev, args.steps,
@@ -548,7 +610,8 @@ def run_gpu(args):
                        "l2": "inputs larger than L2 (no flush)",
                        "bytes_per_step": step_bytes, "parallelism": f"replicas x{world}"},
             "stages": {k: {kk: round(vv, 3) for kk, vv in v.items()} for k, v in stage.items()},
-            "extras": {k: {kk: round(vv, 3) for kk, vv in v.items()} for k, v in extras.items()},
+            "extras": {k: {kk: (round(vv, 3) if isinstance(vv, float) else vv)
+                           for kk, vv in v.items()} for k, v in extras.items()},
             "roofline": roofline,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,

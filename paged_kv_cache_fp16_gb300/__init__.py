@@ -499,15 +499,25 @@ def _caches(kc, vc, st):
             raise ValueError("caches are [B, H, capacity, D] per layer")
 
 
-def kivi_update(st: kivi_state, k_cache, v_cache, k_new, v_new, stream=None) -> None:
-    """update_and_fetch on the in-place fp16 cache (all layers); advances `st`."""
-    if not (len(k_cache) == len(v_cache) == len(k_new) == len(v_new)):
-        raise ValueError("one cache and one new-token tensor per layer, K and V")
-    _caches(k_cache, v_cache, st)
+def _new_arrays(k_new, v_new, n_layers, st):
+    """(k array, v array, n) for the C call; None, None means no new tokens (flush only)."""
+    if k_new is None and v_new is None:
+        return None, None, 0
+    if not (len(k_new) == len(v_new) == n_layers):
+        raise ValueError("one new-token tensor per layer, K and V")
     n = _new_tokens(k_new, v_new, st)
-    _check(_lib.kivi_update(ctypes.byref(st), _ptr_array(k_cache), _ptr_array(v_cache),
-                            _ptr_array(k_new), _ptr_array(v_new), len(k_cache), n,
-                            _stream(stream)))
+    return _ptr_array(k_new), _ptr_array(v_new), n
+
+
+def kivi_update(st: kivi_state, k_cache, v_cache, k_new=None, v_new=None, stream=None) -> None:
+    """update_and_fetch on the in-place fp16 cache (all layers); advances `st`.  k_new / v_new:
+    [B, H, n, D] per layer, or None to flush without appending."""
+    if len(k_cache) != len(v_cache):
+        raise ValueError("one K and one V cache per layer")
+    _caches(k_cache, v_cache, st)
+    ka, va, n = _new_arrays(k_new, v_new, len(k_cache), st)
+    _check(_lib.kivi_update(ctypes.byref(st), _ptr_array(k_cache), _ptr_array(v_cache), ka, va,
+                            len(k_cache), n, _stream(stream)))
 
 
 def kivi_trim(st: kivi_state, n: int) -> int:
@@ -515,16 +525,16 @@ def kivi_trim(st: kivi_state, n: int) -> int:
     return _lib.kivi_trim(ctypes.byref(st), n)
 
 
-def kivi_packed_update(st: kivi_state, caches: Sequence["KiviPacked"], k_cache, v_cache, k_new,
-                       v_new, stream=None) -> None:
-    """update_and_fetch with the quantized region packed; advances `st`."""
-    if not (len(caches) == len(k_cache) == len(v_cache) == len(k_new) == len(v_new)):
-        raise ValueError("one packed cache, cache and new-token tensor per layer")
+def kivi_packed_update(st: kivi_state, caches: Sequence["KiviPacked"], k_cache, v_cache,
+                       k_new=None, v_new=None, stream=None) -> None:
+    """update_and_fetch with the quantized region packed; advances `st`.  k_new / v_new as in
+    kivi_update."""
+    if not (len(caches) == len(k_cache) == len(v_cache)):
+        raise ValueError("one packed cache and one K and V cache per layer")
     _caches(k_cache, v_cache, st)
-    n = _new_tokens(k_new, v_new, st)
+    ka, va, n = _new_arrays(k_new, v_new, len(caches), st)
     _check(_lib.kivi_packed_update(ctypes.byref(st), _packed_array(caches), _ptr_array(k_cache),
-                                   _ptr_array(v_cache), _ptr_array(k_new), _ptr_array(v_new),
-                                   len(caches), n, _stream(stream)))
+                                   _ptr_array(v_cache), ka, va, len(caches), n, _stream(stream)))
 
 
 def kivi_packed_trim(st: kivi_state, caches: Sequence["KiviPacked"], k_cache, v_cache, n: int,
