@@ -67,28 +67,34 @@ def bytes_kivi(n_tensors, B, H, span, D):
     return n_tensors * B * H * span * D * 4
 
 
-def kernel_source_hash():
-    """sha256 of the CUDA sources: recorded ncu traffic is only valid for the code it measured."""
-    import glob
+def kernel_source_hash(sources):
+    """sha256 over the files a kernel is built from (paths relative to the repository): recorded
+    ncu traffic is only valid for the code it measured."""
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_fp16_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    for rel in sorted(sources):
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(rel.encode() + b"\0" + fh.read())
     return h.hexdigest()
 
 
 def recorded_traffic(stage, bits):
-    """DRAM bytes per launch from the committed ncu record, or None if the kernels changed."""
+    """DRAM bytes per launch from the committed ncu record, or None if the kernel's sources
+    changed since it was captured."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         rec = json.load(f)
-    if rec.get("source_sha256") != kernel_source_hash():
-        return None
     e = rec.get("kernels", {}).get(f"{stage}/q{bits}")
-    return None if e is None else e.get("bytes_per_launch")
+    if e is None:
+        return None
+    try:
+        if e.get("source_sha256") != kernel_source_hash(e.get("sources", [])):
+            return None
+    except OSError:
+        return None
+    return e.get("bytes_per_launch")
 
 
 def measured_peaks():
