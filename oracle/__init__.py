@@ -26,6 +26,10 @@ It is a plain, slow, obviously correct numpy restatement of what the pages compu
   cache to fp16, then plain softmax(q k^T * scale) v, here in float64; and one decode step
   (write the new token, then attend over the grown window) in that order.
   Source: MTPLX pull request #267, description ("plain KV quant dequantizes and runs MLX SDPA").
+* ``side``       -- fp16 side channels on the symmetric quantizer: attention sinks kept exactly and
+  each row's largest-magnitude elements kept as (fp16 value, position) pairs.
+  Source: VeloxQuant-MLX API docs, "veloxquant_mlx.cache.kvquant_cache module" (byte
+  accounting: the fp16 outlier side channel; Attention Sink-Aware quantization).
 * ``storage``    -- the storage arithmetic (bytes per token per KV head, whole-cache GiB).
   Source: MTPLX pull request #267, description, storage paragraph.
 
@@ -33,4 +37,4 @@ Readings taken where the pages are silent are listed in each module's docstring.
 Pins (checks against values and properties the pages and mathematics fix) live in
 ``tests/test_oracle_*.py`` and ``tests/golden/``.
 """
-from . import symmetric, kivi, kivi_packed, attention, storage  # noqa: F401
+from . import symmetric, kivi, kivi_packed, attention, storage, side  # noqa: F401
