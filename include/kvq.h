@@ -9,6 +9,7 @@
  *   kvq_append_decode_attn one decode step: append the new token, then attend, in one launch
  *   kivi_pack, kivi_decode_attn   packed KIVI storage and decode attention over it
  *   kivi_update, kivi_trim, kivi_packed_update, kivi_packed_trim   the KIVI cache protocol
+ *   kvq_*_side             fp16 attention sinks and outlier side channel on the symmetric path
  * plus host helpers: packed_dim, the KIVI residual boundary, and a page allocator.
  *
  * Conventions shared by every entry point
@@ -280,6 +281,56 @@ KVQ_API kvq_status kvq_append_decode_attn(const kvq_pool* k_pools, const kvq_poo
                                           int max_seq_len, float softmax_scale, float* out,
                                           void* workspace, size_t workspace_bytes,
                                           int32_t* dev_err, kvq_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * fp16 side channels: attention sinks and dense-and-sparse outliers
+ * ------------------------------------------------------------------------------------------ */
+
+#define KVQ_MAX_OUTLIERS 8
+#define KVQ_MAX_SINKS 16
+
+/*
+ * VeloxQuant-MLX API docs, "veloxquant_mlx.cache.kvquant_cache module": per-vector
+ * dense-and-sparse outlier isolation with an fp16 side channel (value + position index), and
+ * Attention Sink-Aware quantization (the first n_sink tokens of a sequence restored to exact
+ * fp16), applied to the symmetric quantizer above.  One kvq_side accompanies one kvq_pool:
+ *   a row's n_outlier largest-magnitude elements (ties: the lower position) are stored as fp16
+ *   value + uint8 position, ascending by position, in out_val / out_idx at the row's physical
+ *   index; the rest of the row (outliers set to 0) is quantized as usual -- its scale comes from
+ *   the (n_outlier + 1)-th largest magnitude and the outlier positions hold code 0;
+ *   rows at positions < n_sink are also copied exactly into sink, which dequantization and
+ *   attention read instead of the pages.
+ * The page's fraction 0.01 gives n_outlier = ceil(0.01 * head_dim) (3 at 256).
+ */
+typedef struct kvq_side {
+  int32_t n_outlier;  /* outliers per row, 0..KVQ_MAX_OUTLIERS, < head_dim */
+  int32_t n_sink;     /* sink tokens per sequence, 0..KVQ_MAX_SINKS */
+  int32_t max_seqs;   /* sequences the sink buffer holds (>= nseq of every call) */
+  uint16_t* out_val;  /* fp16 [num_pages][H][page_size][n_outlier], 16-byte aligned */
+  uint8_t* out_idx;   /* uint8 [num_pages][H][page_size][n_outlier], 16-byte aligned */
+  uint16_t* sink;     /* fp16 [max_seqs][n_sink][H][D], 16-byte aligned */
+} kvq_side;
+
+/*
+ * kvq_quant_pack_paged with the side channels: same arguments plus sides[i] for pools[i]
+ * (uniform n_outlier and n_sink).  head_dim a multiple of 16, <= 256.  Errors: those of
+ * kvq_quant_pack_paged, KVQ_ERR_RANGE (n_outlier, n_sink, max_seqs < nseq).
+ */
+KVQ_API kvq_status kvq_quant_pack_paged_side(const kvq_pool* pools, const kvq_side* sides,
+                                             const uint16_t* const* x, int n_tensors,
+                                             const int32_t* page_table, int max_pages,
+                                             const int32_t* cu_new_tokens,
+                                             const int32_t* start_pos, int nseq,
+                                             int total_new_tokens, int32_t* dev_err,
+                                             kvq_stream_t stream);
+
+/* kvq_dequant_paged with the side channels: outliers written back, sink rows exact. */
+KVQ_API kvq_status kvq_dequant_paged_side(const kvq_pool* pools, const kvq_side* sides,
+                                          uint16_t* const* out, int n_tensors,
+                                          const int32_t* page_table, int max_pages,
+                                          const int32_t* cu_tokens, const int32_t* start_pos,
+                                          int nseq, int total_tokens, int32_t* dev_err,
+                                          kvq_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Packed KIVI storage and decode attention over it

@@ -52,6 +52,12 @@ class kivi_packed(ctypes.Structure):
                 ("v_scale", ctypes.c_void_p), ("v_zero", ctypes.c_void_p)]
 
 
+class kvq_side(ctypes.Structure):
+    _fields_ = [("n_outlier", ctypes.c_int32), ("n_sink", ctypes.c_int32),
+                ("max_seqs", ctypes.c_int32), ("out_val", ctypes.c_void_p),
+                ("out_idx", ctypes.c_void_p), ("sink", ctypes.c_void_p)]
+
+
 class kivi_state(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("num_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("capacity", ctypes.c_int32),
@@ -88,6 +94,10 @@ def _load() -> ctypes.CDLL:
         "kvq_append_decode_attn": (I, [pool_p, pool_p, I, P, P, P, I, P, I, P, I, I, F, P, P, S,
                                        P, P]),
         "kivi_pack": (I, [ctypes.POINTER(kivi_packed), P, P, I, I, I, F, P]),
+        "kvq_quant_pack_paged_side": (I, [pool_p, ctypes.POINTER(kvq_side), P, I, P, I, P, P,
+                                          I, I, P, P]),
+        "kvq_dequant_paged_side": (I, [pool_p, ctypes.POINTER(kvq_side), P, I, P, I, P, P, I, I,
+                                       P, P]),
         "kivi_state_init": (I, [ctypes.POINTER(kivi_state), I, I, I, I, I, I, I]),
         "kivi_update": (I, [ctypes.POINTER(kivi_state), P, P, P, P, I, I, P]),
         "kivi_trim": (I, [ctypes.POINTER(kivi_state), I]),
@@ -585,6 +595,76 @@ def kivi_decode_attn(caches: Sequence[KiviPacked], ks: Sequence[torch.Tensor],
                                  _ptr(dev_err), _stream(stream)))
 
 
+@dataclass
+class Side:
+    """fp16 side channels of one pool (see kvq_side in include/kvq.h)."""
+    n_outlier: int
+    n_sink: int
+    out_val: torch.Tensor | None
+    out_idx: torch.Tensor | None
+    sink: torch.Tensor | None
+
+    @staticmethod
+    def empty(pool: "Pool", n_outlier: int, n_sink: int, max_seqs: int, device="cuda") -> "Side":
+        P, H, ps = pool.num_pages, pool.num_heads, pool.page_size
+        k = max(n_outlier, 1)
+        val = torch.zeros((P, H, ps, k), dtype=torch.float16, device=device) if n_outlier else None
+        idx = torch.zeros((P, H, ps, k), dtype=torch.uint8, device=device) if n_outlier else None
+        sink = (torch.zeros((max_seqs, n_sink, H, pool.head_dim), dtype=torch.float16,
+                            device=device) if n_sink else None)
+        return Side(n_outlier, n_sink, val, idx, sink)
+
+    @property
+    def max_seqs(self) -> int:
+        return self.sink.shape[0] if self.sink is not None else 0
+
+    def as_c(self) -> kvq_side:
+        return kvq_side(self.n_outlier, self.n_sink, self.max_seqs, _ptr(self.out_val),
+                        _ptr(self.out_idx), _ptr(self.sink))
+
+
+def _side_array(sides):
+    arr = (kvq_side * len(sides))()
+    for i, sd in enumerate(sides):
+        arr[i] = sd.as_c()
+    return arr
+
+
+def kvq_quant_pack_paged_side(pools: Sequence[Pool], sides: Sequence[Side],
+                              x: Sequence[torch.Tensor], page_table: torch.Tensor,
+                              cu_new_tokens: torch.Tensor, start_pos: torch.Tensor,
+                              dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """kvq_quant_pack_paged with outliers split off and sink rows kept exactly."""
+    if not (len(pools) == len(sides) == len(x)):
+        raise ValueError("one side and one input per pool")
+    for i, t in enumerate(x):
+        _cuda_tensor(t, torch.float16, f"x[{i}]")
+    _cuda_tensor(page_table, torch.int32, "page_table")
+    total = x[0].shape[0]
+    _check(_lib.kvq_quant_pack_paged_side(_pool_array(pools), _side_array(sides), _ptr_array(x),
+                                          len(pools), page_table.data_ptr(), page_table.shape[1],
+                                          cu_new_tokens.data_ptr(), start_pos.data_ptr(),
+                                          start_pos.numel(), total, _ptr(dev_err),
+                                          _stream(stream)))
+
+
+def kvq_dequant_paged_side(pools: Sequence[Pool], sides: Sequence[Side],
+                           out: Sequence[torch.Tensor], page_table: torch.Tensor,
+                           cu_tokens: torch.Tensor, start_pos: torch.Tensor,
+                           dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """kvq_dequant_paged with the outliers written back and sink rows exact."""
+    if not (len(pools) == len(sides) == len(out)):
+        raise ValueError("one side and one output per pool")
+    for i, t in enumerate(out):
+        _cuda_tensor(t, torch.float16, f"out[{i}]")
+    _cuda_tensor(page_table, torch.int32, "page_table")
+    total = out[0].shape[0]
+    _check(_lib.kvq_dequant_paged_side(_pool_array(pools), _side_array(sides), _ptr_array(out),
+                                       len(pools), page_table.data_ptr(), page_table.shape[1],
+                                       cu_tokens.data_ptr(), start_pos.data_ptr(),
+                                       start_pos.numel(), total, _ptr(dev_err), _stream(stream)))
+
+
 def decode_workspace(k_pools: Sequence[Pool], nseq: int, num_q_heads: int, max_seq_len: int,
                      device="cuda") -> torch.Tensor:
     """A workspace tensor of the size kvq_decode_attn needs."""
@@ -597,7 +677,8 @@ def decode_workspace(k_pools: Sequence[Pool], nseq: int, num_q_heads: int, max_s
 __all__ = ["KVQError", "Pool", "Allocator", "parse_mode", "kvq_version", "kvq_packed_dim",
            "kivi_boundary", "kvq_quant_pack_paged", "kvq_dequant_paged", "kivi_quant_dequant",
            "kvq_decode_attn_workspace", "kvq_decode_attn", "kvq_decode_attn_noalloc",
-           "kvq_append_decode_attn",
+           "kvq_append_decode_attn", "Side", "kvq_quant_pack_paged_side",
+           "kvq_dequant_paged_side",
            "KiviPacked", "kivi_pack", "kivi_decode_attn_workspace", "kivi_decode_attn",
            "kivi_state", "kivi_state_new", "kivi_update", "kivi_trim", "kivi_packed_update",
            "kivi_packed_trim", "kivi_unpack",

@@ -1,0 +1,164 @@
+"""GPU parity for the fp16 side channels on the symmetric path (attention sinks, dense-and-sparse
+outliers): kvq_quant_pack_paged_side / kvq_dequant_paged_side against oracle/side.py bit for bit
+(codes, scales, outlier values and positions, sink rows, dequantized rows)."""
+import numpy as np
+import pytest
+import torch
+
+import kvgen
+from oracle import side as osd
+from oracle import symmetric as osym
+from _gpu_util import cu_of, dev_tensor, i32, u16
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows(seed, is_key, n, H, D):
+    x = kvgen.KVSpec(seed=seed, layer=0, is_key=is_key, n_seq=1, n_tok=n, num_heads=H,
+                     head_dim=D).full_np()
+    if n > 3:   # magnitude ties: a row of +-1 (ties everywhere) and one with two equal maxima
+        x[1, 0] = np.where(np.arange(D) % 3 == 0, -1.0, 1.0).astype(np.float16)
+        x[2, 0, 5] = x[2, 0, 9] = np.float16(-7.5)
+        x[2, 0, 200 % D] = np.float16(7.5)
+    return x
+
+
+def _setup(kvq, dev, bits, H, D, ps, k, n_sink, lens, starts, seed=1):
+    lens, starts = np.asarray(lens), np.asarray(starts)
+    nseq = len(lens)
+    pps = int(((starts + lens).max() + ps - 1) // ps)
+    pt_np = kvgen.random_page_table(seed, nseq, pps)
+    n_pages = pt_np.size
+    pools, sides, opools, osides = [], [], [], []
+    for _ in range(2):
+        p = kvq.Pool.empty(bits, H, D, ps, n_pages, dev)
+        p.codes.zero_()
+        p.scales.zero_()
+        pools.append(p)
+        sides.append(kvq.Side.empty(p, k, n_sink, nseq, dev))
+        op = osym.PagedPool(bits, H, D, ps, n_pages)
+        opools.append(op)
+        osides.append(osd.SidePool(op, k, n_sink, nseq))
+    return pt_np, pools, sides, opools, osides
+
+
+def _compare_state(pools, sides, opools, osides, n_sink):
+    for p, sd, op, osp in zip(pools, sides, opools, osides):
+        assert np.array_equal(p.codes.cpu().numpy(), op.codes)
+        assert np.array_equal(u16(p.scales), op.scales.view(np.uint16))
+        if sd.n_outlier:
+            assert np.array_equal(sd.out_idx.cpu().numpy(), osp.out_idx)
+            assert np.array_equal(u16(sd.out_val), osp.out_val.view(np.uint16))
+        if n_sink:
+            assert np.array_equal(u16(sd.sink), osp.sink.view(np.uint16))
+
+
+@pytest.mark.parametrize("bits", [8, 6, 4])
+@pytest.mark.parametrize("D,k,n_sink", [(256, 3, 4), (256, 8, 16), (128, 2, 0), (64, 0, 4),
+                                        (256, 1, 1), (16, 8, 2)])
+def test_quant_dequant_side_bit_exact(kvq, cuda_dev, bits, D, k, n_sink):
+    H, ps = 4, 16
+    lens, starts = [1, 5, 40, 100], [0, 0, 0, 0]
+    pt_np, pools, sides, opools, osides = _setup(kvq, cuda_dev, bits, H, D, ps, k, n_sink,
+                                                 lens, starts)
+    tot = int(sum(lens))
+    xs = [_rows(3, True, tot, H, D), _rows(3, False, tot, H, D)]
+    cu = cu_of(lens)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    kvq.kvq_quant_pack_paged_side(pools, sides, [dev_tensor(x, cuda_dev) for x in xs],
+                                  i32(pt_np, cuda_dev), i32(cu, cuda_dev), i32(starts, cuda_dev),
+                                  err)
+    for x, osp in zip(xs, osides):
+        osd.quant_pack_paged_side(osp, x, pt_np, cu, np.asarray(starts))
+    outs = [torch.full((tot, H, D), float("nan"), dtype=torch.float16, device=cuda_dev)
+            for _ in range(2)]
+    kvq.kvq_dequant_paged_side(pools, sides, outs, i32(pt_np, cuda_dev), i32(cu, cuda_dev),
+                               i32(starts, cuda_dev), err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    _compare_state(pools, sides, opools, osides, n_sink)
+    for o, osp in zip(outs, osides):
+        want = osd.dequant_paged_side(osp, pt_np, cu, np.asarray(starts))
+        assert np.array_equal(u16(o), want.view(np.uint16))
+
+
+def test_append_across_the_sink_boundary(kvq, cuda_dev):
+    """Appending to sequences at positions below and above n_sink: the sink buffer takes exactly
+    the positions < n_sink, in place, and the rest of the state is untouched."""
+    bits, H, D, ps, k, n_sink = 6, 2, 256, 16, 3, 4
+    first, second = [2, 0, 30], [5, 3, 2]
+    pt_np, pools, sides, opools, osides = _setup(kvq, cuda_dev, bits, H, D, ps, k, n_sink,
+                                                 second, np.asarray(first))
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    seed = 10
+    for lens, starts in ((first, [0, 0, 0]), (second, first)):
+        tot = int(sum(lens))
+        xs = [_rows(seed, True, tot, H, D), _rows(seed, False, tot, H, D)]
+        seed += 1
+        cu = cu_of(lens)
+        kvq.kvq_quant_pack_paged_side(pools, sides, [dev_tensor(x, cuda_dev) for x in xs],
+                                      i32(pt_np, cuda_dev), i32(cu, cuda_dev),
+                                      i32(starts, cuda_dev), err)
+        for x, osp in zip(xs, osides):
+            osd.quant_pack_paged_side(osp, x, pt_np, cu, np.asarray(starts))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    _compare_state(pools, sides, opools, osides, n_sink)
+
+
+def test_side_rejects_bad_arguments(kvq, cuda_dev):
+    p = kvq.Pool.empty(6, 2, 256, 16, 4, cuda_dev)
+    x = torch.zeros((4, 2, 256), dtype=torch.float16, device=cuda_dev)
+    pt, cu, st = i32([[0, 1, 2, 3]], cuda_dev), i32([0, 4], cuda_dev), i32([0], cuda_dev)
+    with pytest.raises(kvq.KVQError):   # 9 outliers
+        kvq.kvq_quant_pack_paged_side([p], [kvq.Side.empty(p, 9, 0, 1, cuda_dev)], [x], pt, cu, st)
+    with pytest.raises(kvq.KVQError):   # 17 sinks
+        kvq.kvq_quant_pack_paged_side([p], [kvq.Side.empty(p, 3, 17, 1, cuda_dev)], [x], pt, cu, st)
+    sd = kvq.Side.empty(p, 3, 4, 1, cuda_dev)
+    sd.out_val = None
+    with pytest.raises(kvq.KVQError):
+        kvq.kvq_quant_pack_paged_side([p], [sd], [x], pt, cu, st)
+
+
+def test_full_size_prefill_sampled(kvq, cuda_dev):
+    """The paged-prefill workload (16 layers x K/V x 8 seqs x 32,768 tokens x 4 heads x 256, page
+    16), q6, 3 outliers per row (the page's 1 %), 4 sinks: sampled rows of every tensor are
+    checked bit for bit -- packed codes, scale, outliers, and the dequantized row."""
+    w = kvgen.WORKLOADS["paged_prefill_16L_8x32768_4x256"]
+    L, nseq, ntok, H, D, ps = w["n_layers"], w["n_seq"], w["n_tok"], w["H"], w["D"], w["page_size"]
+    bits, k, n_sink = 6, osd.outlier_count(D, 0.01), 4
+    pt_np = kvgen.random_page_table(1, nseq, ntok // ps)
+    pt = i32(pt_np, cuda_dev)
+    cu = i32(np.arange(nseq + 1) * ntok, cuda_dev)
+    st = i32(np.zeros(nseq), cuda_dev)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    rng = np.random.default_rng(4)
+    for layer in (0, 15):   # two layers x K/V through the full-size launch shape
+        specs = [kvgen.KVSpec(seed=w["seed"], layer=layer, is_key=kk, n_seq=nseq, n_tok=ntok,
+                              num_heads=H, head_dim=D) for kk in (True, False)]
+        xs = [s.full_torch(cuda_dev) for s in specs]
+        pools = [kvq.Pool.empty(bits, H, D, ps, pt_np.size, cuda_dev) for _ in range(2)]
+        sides = [kvq.Side.empty(p, k, n_sink, nseq, cuda_dev) for p in pools]
+        kvq.kvq_quant_pack_paged_side(pools, sides, xs, pt, cu, st, err)
+        outs = [torch.empty_like(x) for x in xs]
+        kvq.kvq_dequant_paged_side(pools, sides, outs, pt, cu, st, err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        tok = np.concatenate([rng.integers(0, nseq * ntok, 300), [0, 1, 3, 4, ntok, ntok + 3]])
+        for spec, p, sd, out in zip(specs, pools, sides, outs):
+            head = rng.integers(0, H, tok.size)
+            x = spec.rows_np(tok * H + head)
+            s, pos = tok // ntok, tok % ntok
+            page, slot = pt_np[s, pos // ps], pos % ps
+            packed, scale, opos, oval = osd.quant_pack_rows_side(x, bits, k)
+            idx = [torch.from_numpy(a.astype(np.int64)).to(cuda_dev) for a in (page, head, slot)]
+            assert np.array_equal(p.codes[idx[0], idx[1], idx[2]].cpu().numpy(), packed)
+            assert np.array_equal(u16(p.scales[idx[0], idx[1], idx[2]]), scale.view(np.uint16))
+            assert np.array_equal(sd.out_idx[idx[0], idx[1], idx[2]].cpu().numpy(), opos)
+            assert np.array_equal(u16(sd.out_val[idx[0], idx[1], idx[2]]), oval.view(np.uint16))
+            deq = osd.dequant_rows_side(packed, scale, opos, oval, bits, D)
+            deq[pos < n_sink] = x[pos < n_sink]
+            rows = out.view(-1, D)[torch.from_numpy(tok * H + head).to(cuda_dev)]
+            assert np.array_equal(u16(rows), deq.view(np.uint16))
+        del xs, pools, sides, outs
+        torch.cuda.empty_cache()
