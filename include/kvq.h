@@ -332,6 +332,22 @@ KVQ_API kvq_status kvq_dequant_paged_side(const kvq_pool* pools, const kvq_side*
                                           int nseq, int total_tokens, int32_t* dev_err,
                                           kvq_stream_t stream);
 
+/*
+ * kvq_decode_attn over pools with side channels: the keys and values of a row are the dense
+ * reconstruction with its outliers written back, and the sink positions (< n_sink) use the exact
+ * fp16 rows of the sink buffer.  k_sides[l] / v_sides[l] accompany k_pools[l] / v_pools[l]
+ * (uniform n_outlier and n_sink; max_seqs >= nseq).  The page size must be a multiple of 16.
+ * Other arguments, the workspace and the errors are those of kvq_decode_attn.
+ */
+KVQ_API kvq_status kvq_decode_attn_side(const kvq_pool* k_pools, const kvq_pool* v_pools,
+                                        const kvq_side* k_sides, const kvq_side* v_sides,
+                                        int n_layers, const uint16_t* q, int num_q_heads,
+                                        const int32_t* page_table, int max_pages,
+                                        const int32_t* seq_lens, int nseq, int max_seq_len,
+                                        float softmax_scale, float* out, void* workspace,
+                                        size_t workspace_bytes, int32_t* dev_err,
+                                        kvq_stream_t stream);
+
 /* ---------------------------------------------------------------------------------------------
  * Packed KIVI storage and decode attention over it
  * ------------------------------------------------------------------------------------------ */

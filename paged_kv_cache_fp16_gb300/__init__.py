@@ -96,6 +96,9 @@ def _load() -> ctypes.CDLL:
         "kivi_pack": (I, [ctypes.POINTER(kivi_packed), P, P, I, I, I, F, P]),
         "kvq_quant_pack_paged_side": (I, [pool_p, ctypes.POINTER(kvq_side), P, I, P, I, P, P,
                                           I, I, P, P]),
+        "kvq_decode_attn_side": (I, [pool_p, pool_p, ctypes.POINTER(kvq_side),
+                                     ctypes.POINTER(kvq_side), I, P, I, P, I, P, I, I, F, P, P, S,
+                                     P, P]),
         "kvq_dequant_paged_side": (I, [pool_p, ctypes.POINTER(kvq_side), P, I, P, I, P, P, I, I,
                                        P, P]),
         "kivi_state_init": (I, [ctypes.POINTER(kivi_state), I, I, I, I, I, I, I]),
@@ -665,6 +668,30 @@ def kvq_dequant_paged_side(pools: Sequence[Pool], sides: Sequence[Side],
                                        start_pos.numel(), total, _ptr(dev_err), _stream(stream)))
 
 
+def kvq_decode_attn_side(k_pools: Sequence[Pool], v_pools: Sequence[Pool],
+                         k_sides: Sequence[Side], v_sides: Sequence[Side], q: torch.Tensor,
+                         page_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                         softmax_scale: float, out: torch.Tensor, workspace: torch.Tensor,
+                         dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """Decode attention over pools with sinks and outlier side channels."""
+    if not (len(k_pools) == len(v_pools) == len(k_sides) == len(v_sides)):
+        raise ValueError("one V pool and one side per pool")
+    _cuda_tensor(q, torch.float16, "q")
+    _cuda_tensor(out, torch.float32, "out")
+    _cuda_tensor(page_table, torch.int32, "page_table")
+    _cuda_tensor(seq_lens, torch.int32, "seq_lens")
+    n_layers, nseq, hq, _ = q.shape
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    _check(_lib.kvq_decode_attn_side(_pool_array(k_pools), _pool_array(v_pools),
+                                     _side_array(k_sides), _side_array(v_sides), n_layers,
+                                     q.data_ptr(), hq, page_table.data_ptr(), page_table.shape[1],
+                                     seq_lens.data_ptr(), nseq, max_seq_len, softmax_scale,
+                                     out.data_ptr(), workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(), _ptr(dev_err),
+                                     _stream(stream)))
+
+
 def decode_workspace(k_pools: Sequence[Pool], nseq: int, num_q_heads: int, max_seq_len: int,
                      device="cuda") -> torch.Tensor:
     """A workspace tensor of the size kvq_decode_attn needs."""
@@ -678,7 +705,7 @@ __all__ = ["KVQError", "Pool", "Allocator", "parse_mode", "kvq_version", "kvq_pa
            "kivi_boundary", "kvq_quant_pack_paged", "kvq_dequant_paged", "kivi_quant_dequant",
            "kvq_decode_attn_workspace", "kvq_decode_attn", "kvq_decode_attn_noalloc",
            "kvq_append_decode_attn", "Side", "kvq_quant_pack_paged_side",
-           "kvq_dequant_paged_side",
+           "kvq_dequant_paged_side", "kvq_decode_attn_side",
            "KiviPacked", "kivi_pack", "kivi_decode_attn_workspace", "kivi_decode_attn",
            "kivi_state", "kivi_state_new", "kivi_update", "kivi_trim", "kivi_packed_update",
            "kivi_packed_trim", "kivi_unpack",

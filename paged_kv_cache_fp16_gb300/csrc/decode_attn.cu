@@ -69,6 +69,17 @@ struct AttnArgs {
   float qk_scale;  // softmax_scale * log2(e)
 };
 
+// Side channels of the decode attention (fp16 sinks and outliers), per layer; zero when unused.
+struct AttnSide {
+  const uint16_t* kov[KVQ_MAX_TENSORS];   // K outlier values, fp16 [pages][H][ps][k]
+  const uint8_t* koi[KVQ_MAX_TENSORS];    // K outlier positions
+  const uint16_t* vov[KVQ_MAX_TENSORS];
+  const uint8_t* voi[KVQ_MAX_TENSORS];
+  const uint16_t* ksink[KVQ_MAX_TENSORS]; // fp16 [max_seqs][n_sink][H][D]
+  const uint16_t* vsink[KVQ_MAX_TENSORS];
+  int k, n_sink;
+};
+
 template <int BITS> struct Wd;
 // Stage counts keep three CTAs (12 warps) resident per SM within 228 KB of shared memory.
 template <> struct Wd<8> { static constexpr int kPd = 256, kKWords = 16, kVWords = 8, kStages = 2; };
@@ -81,6 +92,27 @@ template <int BITS> __host__ __device__ constexpr int warp_bytes() { return Wd<B
 template <int BITS> __host__ __device__ constexpr int tma_smem_bytes() {
   return kWarps * warp_bytes<BITS>() + kWarps * Wd<BITS>::kStages * 16;  // + barriers, flags
 }
+
+// Shared-memory layout of the staged kernel.  Without side channels it is the layout above.  With
+// them a stage also holds the tile's K and V outlier values (fp16 [16][k], 256 B reserved each)
+// and positions (uint8 [16][k], 128 B each); two stages per warp; then the warps' sparse output
+// accumulators (fp32 [8 heads][256]), the KV head's queries (fp16 [8][256]) and per-warp sink-row
+// weights (fp32 [16][8]).
+template <int BITS, bool SIDE>
+struct Lay {
+  static constexpr int kStages = SIDE ? 2 : Wd<BITS>::kStages;
+  static constexpr int kBase = stage_bytes<BITS>();   // bytes of the four page copies
+  static constexpr int kOffKov = kBase, kOffVov = kBase + 256;
+  static constexpr int kOffKoi = kBase + 512, kOffVoi = kBase + 640;
+  static constexpr int kStage = SIDE ? kBase + 768 : kBase;
+  static constexpr int kWarpBytes = kStages * kStage;
+  static constexpr int kRing = kWarps * kWarpBytes;
+  static constexpr int kOsp = kRing + kWarps * kStages * 16;
+  static constexpr int kQs = kOsp + kWarps * 8 * kD * 4;
+  static constexpr int kPs = kQs + 8 * kD * 2;
+  static constexpr int kTotal = SIDE ? kPs + kWarps * 16 * 8 * 4 : kOsp;
+};
+static_assert(Lay<6, false>::kTotal == tma_smem_bytes<6>(), "side-free layout is the base layout");
 constexpr int kMergeBytes = kWarps * 8 * kD * 4 + 2 * kWarps * 8 * 4;
 
 // PRMT selector picking bytes (b0, b1) of the first and (b0, b1) of the second source word.
@@ -155,11 +187,15 @@ struct VRegs {
 };
 
 // Q.K^T of one tile and the online-softmax update; returns P^T as the two B-operand registers.
-template <int BITS>
+// With SIDE, kc[4] (same layout as the scores) is added after the row scale -- the outlier and
+// sink terms of the keys -- and p[4] and the rescale factors are returned for the side outputs.
+template <int BITS, bool SIDE = false>
 __device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const uint32_t (&qf)[16][2],
                                                 float (&acc)[16][4], float& m0, float& m1,
                                                 float& l0, float& l1, float qk_scale,
-                                                uint32_t& pb0, uint32_t& pb1) {
+                                                uint32_t& pb0, uint32_t& pb1,
+                                                const float* kc = nullptr, float* p_out = nullptr,
+                                                float* al_out = nullptr) {
   // ---------------- S^T = C_K . Q^T on the exact integer codes (four independent accumulation
   // chains); each token row's fp16 scale multiplies its scores afterwards (the code-times-scale
   // products are exact instead of rounded to fp16 -- a difference far inside the tolerance)
@@ -182,11 +218,18 @@ __device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const uint
 
   // ---------------- online softmax (log2 domain); sacc: [tok g | g+8][head 2c | 2c+1]
   float sc[4];
-  const float f0 = T.ksc[0] * qk_scale, f1 = T.ksc[1] * qk_scale;
-  sc[0] = T.kval[0] ? sacc[0] * f0 : kNegInf;
-  sc[1] = T.kval[0] ? sacc[1] * f0 : kNegInf;
-  sc[2] = T.kval[1] ? sacc[2] * f1 : kNegInf;
-  sc[3] = T.kval[1] ? sacc[3] * f1 : kNegInf;
+  if constexpr (SIDE) {
+    sc[0] = T.kval[0] ? fmaf(sacc[0], T.ksc[0], kc[0]) * qk_scale : kNegInf;
+    sc[1] = T.kval[0] ? fmaf(sacc[1], T.ksc[0], kc[1]) * qk_scale : kNegInf;
+    sc[2] = T.kval[1] ? fmaf(sacc[2], T.ksc[1], kc[2]) * qk_scale : kNegInf;
+    sc[3] = T.kval[1] ? fmaf(sacc[3], T.ksc[1], kc[3]) * qk_scale : kNegInf;
+  } else {
+    const float f0 = T.ksc[0] * qk_scale, f1 = T.ksc[1] * qk_scale;
+    sc[0] = T.kval[0] ? sacc[0] * f0 : kNegInf;
+    sc[1] = T.kval[0] ? sacc[1] * f0 : kNegInf;
+    sc[2] = T.kval[1] ? sacc[2] * f1 : kNegInf;
+    sc[3] = T.kval[1] ? sacc[3] * f1 : kNegInf;
+  }
   float tm0 = fmaxf(sc[0], sc[2]), tm1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
@@ -213,6 +256,12 @@ __device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const uint
   }
   pb0 = movtrans(pack_h2(p[0], p[1]));   // tokens 2c, 2c+1 ; head g
   pb1 = movtrans(pack_h2(p[2], p[3]));   // tokens 8+2c, 8+2c+1 ; head g
+  if constexpr (SIDE) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) p_out[k] = p[k];
+    al_out[0] = al0;
+    al_out[1] = al1;
+  }
 }
 
 
@@ -358,12 +407,15 @@ __device__ __forceinline__ void append_rows(const AttnArgs& a, const LayerPools&
   }
 }
 
-template <int BITS, bool APPEND>
-__global__ void __launch_bounds__(kThreads, 3) decode_attn_tma_kernel(const AttnArgs a) {
+// Side channels need more shared memory (2 CTAs per SM), so that variant may use more registers.
+template <int BITS, bool APPEND, bool SIDE>
+__global__ void __launch_bounds__(kThreads, SIDE ? 2 : 3) decode_attn_tma_kernel(const AttnArgs a,
+                                                                      const AttnSide sd) {
   using W = Wd<BITS>;
-  constexpr int S = W::kStages;
+  using Ly = Lay<BITS, SIDE>;
+  constexpr int S = Ly::kStages;
   constexpr int kPd = W::kPd;
-  constexpr uint32_t kStageBytes = stage_bytes<BITS>();
+  constexpr uint32_t kStageBytes = Ly::kStage;
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5;
@@ -384,10 +436,26 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_tma_kernel(const Attn
   const int n_mine = (tile1 - tile0 - warp + kWarps - 1) > 0
                          ? (tile1 - tile0 - warp + kWarps - 1) / kWarps : 0;
 
-  uint8_t* wbase = smem + warp * warp_bytes<BITS>();
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * warp_bytes<BITS>()) + warp * S;
-  int* flags = reinterpret_cast<int*>(smem + kWarps * warp_bytes<BITS>() + kWarps * S * 8) +
-               warp * S;
+  uint8_t* wbase = smem + warp * Ly::kWarpBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kRing) + warp * S;
+  int* flags = reinterpret_cast<int*>(smem + Ly::kRing + kWarps * S * 8) + warp * S;
+  float* osp = nullptr;          // SIDE: this warp's sparse output accumulator [8][256]
+  const uint16_t* qs = nullptr;  // SIDE: the KV head's queries, fp16 [8][256]
+  float* psk = nullptr;          // SIDE: sink-row weights [16][8]
+  if constexpr (SIDE) {
+    osp = reinterpret_cast<float*>(smem + Ly::kOsp) + warp * 8 * kD;
+    uint16_t* qw = reinterpret_cast<uint16_t*>(smem + Ly::kQs);
+    qs = qw;
+    psk = reinterpret_cast<float*>(smem + Ly::kPs) + warp * 16 * 8;
+    for (int i = threadIdx.x; i < 8 * kD / 8; i += kThreads) {
+      const int jh = i / (kD / 8), v = i - jh * (kD / 8);
+      uint4 x = make_uint4(0, 0, 0, 0);
+      if (jh < a.G) x = ld_nc_v4(a.q + ((static_cast<int64_t>(ls) * a.Hq) + h * a.G + jh) * kD + 8 * v);
+      reinterpret_cast<uint4*>(qw)[i] = x;
+    }
+    for (int i = lane; i < 8 * kD; i += 32) osp[i] = 0.f;
+    __syncthreads();
+  }
 
   if (lane == 0) {
     for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
@@ -422,11 +490,20 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_tma_kernel(const Attn
     uint8_t* dst = wbase + st * kStageBytes;
     if (ok) {
       const int64_t row = (static_cast<int64_t>(page) * a.H + h) * a.ps + slot0;
-      mbar_expect_tx(&bars[st], kStageBytes);
+      const int nk = SIDE ? sd.k : 0;
+      mbar_expect_tx(&bars[st], Ly::kBase + 96 * nk);
       bulk_g2s(dst, P.kc + row * kPd, kTile * kPd, &bars[st]);
       bulk_g2s(dst + kTile * kPd, P.vc + row * kPd, kTile * kPd, &bars[st]);
       bulk_g2s(dst + 2 * kTile * kPd, P.ks + row, 2 * kTile, &bars[st]);
       bulk_g2s(dst + 2 * kTile * kPd + 2 * kTile, P.vs + row, 2 * kTile, &bars[st]);
+      if constexpr (SIDE) {
+        if (nk > 0) {   // the tile's outliers: 16 rows x k values (fp16) and positions (uint8)
+          bulk_g2s(dst + Ly::kOffKov, sd.kov[layer] + row * nk, 32 * nk, &bars[st]);
+          bulk_g2s(dst + Ly::kOffVov, sd.vov[layer] + row * nk, 32 * nk, &bars[st]);
+          bulk_g2s(dst + Ly::kOffKoi, sd.koi[layer] + row * nk, 16 * nk, &bars[st]);
+          bulk_g2s(dst + Ly::kOffVoi, sd.voi[layer] + row * nk, 16 * nk, &bars[st]);
+        }
+      }
     } else {
       report(a.err, KVQ_DEVERR_PAGE_RANGE);
       mbar_arrive(&bars[st]);
@@ -477,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_tma_kernel(const Attn
     for (int r = 0; r < 2; ++r) {
       const int row = g + 8 * r;
       K.kval[r] = ok && tb + row < len;
-      K.ksc[r] = h2f(sks[row]);
+      K.ksc[r] = (SIDE && tb + row < sd.n_sink) ? 0.f : h2f(sks[row]);   // sinks: exact below
       const uint4* src = reinterpret_cast<const uint4*>(sk + row * kPd + c * (4 * W::kKWords));
 #pragma unroll
       for (int i = 0; i < W::kKWords / 4; ++i) {
@@ -487,12 +564,95 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_tma_kernel(const Attn
       }
     }
     uint32_t pb0, pb1;
-    tile_qk_softmax<BITS>(K, qf, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1);
+    if constexpr (SIDE) {
+      // key terms the codes do not carry: for a sink row the exact fp16 dot product (its dense
+      // scale was zeroed above), for any other row the outliers' q[pos] * value
+      float kc[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint16_t* kov = reinterpret_cast<const uint16_t*>(sk + Ly::kOffKov);
+      const uint8_t* koi = sk + Ly::kOffKoi;
+      const uint16_t* q0 = qs + (2 * c) * kD;
+      const uint16_t* q1 = q0 + kD;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int row = g + 8 * r;
+        if (!K.kval[r]) continue;
+        float c0 = 0.f, c1 = 0.f;
+        if (tb + row < sd.n_sink) {
+          const uint16_t* kr = sd.ksink[layer] +
+                               ((static_cast<int64_t>(s) * sd.n_sink + tb + row) * a.H + h) * kD;
+          for (int d = 0; d < kD; d += 8) {
+            const uint4 kv = ld_nc_v4(kr + d);
+            const uint32_t kw4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float kx = h2f(static_cast<uint16_t>(kw4[e >> 1] >> (16 * (e & 1))));
+              c0 = fmaf(h2f(q0[d + e]), kx, c0);
+              c1 = fmaf(h2f(q1[d + e]), kx, c1);
+            }
+          }
+        } else {
+          for (int jj = 0; jj < sd.k; ++jj) {
+            const int pos = koi[row * sd.k + jj];
+            const float v = h2f(kov[row * sd.k + jj]);
+            c0 = fmaf(h2f(q0[pos]), v, c0);
+            c1 = fmaf(h2f(q1[pos]), v, c1);
+          }
+        }
+        kc[2 * r] = c0;
+        kc[2 * r + 1] = c1;
+      }
+      float p[4], al[2];
+      tile_qk_softmax<BITS, true>(K, qf, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1, kc, p, al);
+      // the value terms the codes do not carry, into the warp's sparse accumulator (same
+      // running-max domain as acc: rescaled with it)
+      if (__any_sync(kFullMask, al[0] != 1.f || al[1] != 1.f)) {
+        float* o0 = osp + (2 * c) * kD + 32 * g;
+        float* o1 = o0 + kD;
+        for (int d = 0; d < 32; ++d) {
+          o0[d] *= al[0];
+          o1[d] *= al[1];
+        }
+      }
+      __syncwarp();
+      const uint16_t* vov = reinterpret_cast<const uint16_t*>(sk + Ly::kOffVov);
+      const uint8_t* voi = sk + Ly::kOffVoi;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int row = g + 8 * r;
+        if (!K.kval[r] || tb + row < sd.n_sink) continue;
+        for (int jj = 0; jj < sd.k; ++jj) {
+          const int pos = voi[row * sd.k + jj];
+          const float v = h2f(vov[row * sd.k + jj]);
+          atomicAdd(osp + (2 * c) * kD + pos, p[2 * r] * v);
+          atomicAdd(osp + (2 * c + 1) * kD + pos, p[2 * r + 1] * v);
+        }
+      }
+      if (tb < sd.n_sink) {   // warp-uniform: the tile holds the sink rows
+        if (g < sd.n_sink) { psk[g * 8 + 2 * c] = p[0]; psk[g * 8 + 2 * c + 1] = p[1]; }
+        if (g + 8 < sd.n_sink) { psk[(g + 8) * 8 + 2 * c] = p[2]; psk[(g + 8) * 8 + 2 * c + 1] = p[3]; }
+        __syncwarp();
+        const int ns = min(sd.n_sink, len);
+        for (int d = lane; d < kD; d += 32) {
+          float add[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          for (int t = 0; t < ns; ++t) {
+            const float vx = h2f(sd.vsink[layer][((static_cast<int64_t>(s) * sd.n_sink + t) * a.H +
+                                                  h) * kD + d]);
+#pragma unroll
+            for (int hh = 0; hh < 8; ++hh) add[hh] = fmaf(psk[t * 8 + hh], vx, add[hh]);
+          }
+#pragma unroll
+          for (int hh = 0; hh < 8; ++hh) osp[hh * kD + d] += add[hh];
+        }
+      }
+      __syncwarp();
+    } else {
+      tile_qk_softmax<BITS>(K, qf, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1);
+    }
     VRegs<BITS> V;
 #pragma unroll
     for (int qi = 0; qi < 4; ++qi) {
       const int row = 2 * c + (qi & 1) + 8 * (qi >> 1);
-      const bool v_ok = ok && tb + row < len;
+      const bool v_ok = ok && tb + row < len && !(SIDE && tb + row < sd.n_sink);
       V.vsc[qi] = v_ok ? svs[row] : 0u;
       const uint8_t* src = sv + row * kPd + g * (4 * W::kVWords);
       if constexpr (W::kVWords % 4 == 0) {
@@ -531,6 +691,17 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_tma_kernel(const Attn
     }
     m0 = m1 = kNegInf;
     l0 = l1 = 0.f;
+  }
+  if constexpr (SIDE) {   // fold the warp's sparse accumulator into acc (the merge's layout)
+    __syncwarp();
+#pragma unroll
+    for (int mt = 0; mt < 16; ++mt) {
+      const int d = 32 * g + 8 * (mt >> 2) + (mt & 3);
+      acc[mt][0] += osp[(2 * c) * kD + d];
+      acc[mt][1] += osp[(2 * c + 1) * kD + d];
+      acc[mt][2] += osp[(2 * c) * kD + d + 4];
+      acc[mt][3] += osp[(2 * c + 1) * kD + d + 4];
+    }
   }
   __syncthreads();  // every warp is done with its stages: reuse them for the merge
   cta_merge_write(a, reinterpret_cast<float*>(smem), ls, h, split, warp, g, c, acc, m0, m1, l0,
@@ -662,15 +833,16 @@ int tiles_per_cta_for(int n_layers, int nseq, int H, int max_seq_len) {
   return static_cast<int>(t);
 }
 
-template <int BITS, bool APPEND = false>
-cudaError_t launch_attn(const AttnArgs& a, dim3 grid, bool tma, cudaStream_t cs) {
+template <int BITS, bool APPEND = false, bool SIDE = false>
+cudaError_t launch_attn(const AttnArgs& a, dim3 grid, bool tma, cudaStream_t cs,
+                        const AttnSide& sd = AttnSide{}) {
   if (tma) {
-    constexpr int smem = tma_smem_bytes<BITS>();
-    static_assert(smem >= kMergeBytes, "merge buffer must fit in the stage ring");
-    cudaError_t e = cudaFuncSetAttribute(decode_attn_tma_kernel<BITS, APPEND>,
+    constexpr int smem = Lay<BITS, SIDE>::kTotal;
+    static_assert(Lay<BITS, SIDE>::kRing >= kMergeBytes, "merge buffer must fit in the stage ring");
+    cudaError_t e = cudaFuncSetAttribute(decode_attn_tma_kernel<BITS, APPEND, SIDE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    decode_attn_tma_kernel<BITS, APPEND><<<grid, kThreads, smem, cs>>>(a);
+    decode_attn_tma_kernel<BITS, APPEND, SIDE><<<grid, kThreads, smem, cs>>>(a, sd);
   } else {
     decode_attn_gather_kernel<BITS><<<grid, kThreads, 0, cs>>>(a);
   }
@@ -699,12 +871,14 @@ namespace {
 // (knew/vnew non-NULL: the fused append).
 kvq_status decode_attn_entry(const char* fn, const kvq_pool* k_pools, const kvq_pool* v_pools,
                              int n_layers, const uint16_t* const* knew,
-                             const uint16_t* const* vnew, const uint16_t* q, int num_q_heads,
+                             const uint16_t* const* vnew, const kvq_side* k_sides,
+                             const kvq_side* v_sides, const uint16_t* q, int num_q_heads,
                              const int32_t* page_table, int max_pages, const int32_t* seq_lens,
                              int nseq, int max_seq_len, float softmax_scale, float* out,
                              void* workspace, size_t workspace_bytes, int32_t* dev_err,
                              cudaStream_t cs) {
   const bool append = knew != nullptr || vnew != nullptr;
+  const bool side = k_sides != nullptr || v_sides != nullptr;
   if (n_layers < 1 || n_layers > KVQ_MAX_TENSORS)
     return fail(KVQ_ERR_RANGE, "%s: n_layers %d not in [1, %d]", fn, n_layers, KVQ_MAX_TENSORS);
   kvq_status st = check_pools_uniform(k_pools, n_layers, fn);
@@ -722,8 +896,39 @@ kvq_status decode_attn_entry(const char* fn, const kvq_pool* k_pools, const kvq_
   if (num_q_heads < H || num_q_heads % H || num_q_heads / H > 8)
     return fail(KVQ_ERR_SHAPE, "%s: num_q_heads %d must be a multiple of %d, at most 8 per KV "
                 "head", fn, num_q_heads, H);
-  if (append && k0.page_size % kTile)
+  if ((append || side) && k0.page_size % kTile)
     return fail(KVQ_ERR_SHAPE, "%s: page_size %d must be a multiple of 16", fn, k0.page_size);
+  AttnSide sd{};
+  if (side) {
+    if (!k_sides || !v_sides) return fail(KVQ_ERR_NULL, "%s: NULL side array", fn);
+    const int k = k_sides[0].n_outlier, ns = k_sides[0].n_sink;
+    if (k < 0 || k > KVQ_MAX_OUTLIERS || ns < 0 || ns > KVQ_MAX_SINKS)
+      return fail(KVQ_ERR_RANGE, "%s: n_outlier %d / n_sink %d out of range", fn, k, ns);
+    for (int i = 0; i < n_layers; ++i) {
+      for (const kvq_side* sp : {&k_sides[i], &v_sides[i]}) {
+        if (sp->n_outlier != k || sp->n_sink != ns)
+          return fail(KVQ_ERR_SHAPE, "%s: sides differ in n_outlier/n_sink", fn);
+        if (k > 0 && (!sp->out_val || !sp->out_idx))
+          return fail(KVQ_ERR_NULL, "%s: side of layer %d has no outlier arrays", fn, i);
+        if (ns > 0 && !sp->sink)
+          return fail(KVQ_ERR_NULL, "%s: side of layer %d has no sink buffer", fn, i);
+        if ((k > 0 && (!aligned16(sp->out_val) || !aligned16(sp->out_idx))) ||
+            (ns > 0 && !aligned16(sp->sink)))
+          return fail(KVQ_ERR_ALIGN, "%s: side arrays must be 16-byte aligned", fn);
+        if (ns > 0 && sp->max_seqs < nseq)
+          return fail(KVQ_ERR_RANGE, "%s: sink buffer holds %d sequences, call has %d", fn,
+                      sp->max_seqs, nseq);
+      }
+      sd.kov[i] = k_sides[i].out_val;
+      sd.koi[i] = k_sides[i].out_idx;
+      sd.vov[i] = v_sides[i].out_val;
+      sd.voi[i] = v_sides[i].out_idx;
+      sd.ksink[i] = k_sides[i].sink;
+      sd.vsink[i] = v_sides[i].sink;
+    }
+    sd.k = k;
+    sd.n_sink = ns;
+  }
   if (nseq < 1 || max_pages < 1 || max_seq_len < 0)
     return fail(KVQ_ERR_RANGE, "%s: bad nseq/max_pages/max_seq_len", fn);
   if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages) * k0.page_size)
@@ -779,9 +984,18 @@ kvq_status decode_attn_entry(const char* fn, const kvq_pool* k_pools, const kvq_
   const bool tma = (k0.page_size % kTile) == 0;
   cudaError_t e;
   switch (k0.bits) {
-    case 8: e = append ? launch_attn<8, true>(a, grid, tma, cs) : launch_attn<8>(a, grid, tma, cs); break;
-    case 6: e = append ? launch_attn<6, true>(a, grid, tma, cs) : launch_attn<6>(a, grid, tma, cs); break;
-    default: e = append ? launch_attn<4, true>(a, grid, tma, cs) : launch_attn<4>(a, grid, tma, cs); break;
+    case 8:
+      e = side ? launch_attn<8, false, true>(a, grid, tma, cs, sd)
+               : append ? launch_attn<8, true>(a, grid, tma, cs) : launch_attn<8>(a, grid, tma, cs);
+      break;
+    case 6:
+      e = side ? launch_attn<6, false, true>(a, grid, tma, cs, sd)
+               : append ? launch_attn<6, true>(a, grid, tma, cs) : launch_attn<6>(a, grid, tma, cs);
+      break;
+    default:
+      e = side ? launch_attn<4, false, true>(a, grid, tma, cs, sd)
+               : append ? launch_attn<4, true>(a, grid, tma, cs) : launch_attn<4>(a, grid, tma, cs);
+      break;
   }
   if (e == cudaSuccess) {
     decode_merge_kernel<<<dim3(num_q_heads, n_layers * nseq), kD, 0, cs>>>(a);
@@ -802,7 +1016,7 @@ extern "C" kvq_status kvq_decode_attn(const kvq_pool* k_pools, const kvq_pool* v
                                       size_t workspace_bytes, int32_t* dev_err,
                                       kvq_stream_t stream) {
   return kvq::decode_attn_entry("kvq_decode_attn", k_pools, v_pools, n_layers, nullptr, nullptr,
-                                q, num_q_heads, page_table, max_pages, seq_lens, nseq,
+                                nullptr, nullptr, q, num_q_heads, page_table, max_pages, seq_lens, nseq,
                                 max_seq_len, softmax_scale, out, workspace, workspace_bytes,
                                 dev_err, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -818,9 +1032,25 @@ extern "C" kvq_status kvq_append_decode_attn(const kvq_pool* k_pools, const kvq_
   if (!k_new || !v_new)
     return kvq::fail(KVQ_ERR_NULL, "kvq_append_decode_attn: NULL new-token array");
   return kvq::decode_attn_entry("kvq_append_decode_attn", k_pools, v_pools, n_layers, k_new,
-                                v_new, q, num_q_heads, page_table, max_pages, seq_lens, nseq,
+                                v_new, nullptr, nullptr, q, num_q_heads, page_table, max_pages, seq_lens, nseq,
                                 max_seq_len, softmax_scale, out, workspace, workspace_bytes,
                                 dev_err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" kvq_status kvq_decode_attn_side(const kvq_pool* k_pools, const kvq_pool* v_pools,
+                                           const kvq_side* k_sides, const kvq_side* v_sides,
+                                           int n_layers, const uint16_t* q, int num_q_heads,
+                                           const int32_t* page_table, int max_pages,
+                                           const int32_t* seq_lens, int nseq, int max_seq_len,
+                                           float softmax_scale, float* out, void* workspace,
+                                           size_t workspace_bytes, int32_t* dev_err,
+                                           kvq_stream_t stream) {
+  if (!k_sides || !v_sides)
+    return kvq::fail(KVQ_ERR_NULL, "kvq_decode_attn_side: NULL side array");
+  return kvq::decode_attn_entry("kvq_decode_attn_side", k_pools, v_pools, n_layers, nullptr,
+                                nullptr, k_sides, v_sides, q, num_q_heads, page_table, max_pages,
+                                seq_lens, nseq, max_seq_len, softmax_scale, out, workspace,
+                                workspace_bytes, dev_err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------------------------------------

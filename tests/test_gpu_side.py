@@ -162,3 +162,98 @@ def test_full_size_prefill_sampled(kvq, cuda_dev):
             assert np.array_equal(u16(rows), deq.view(np.uint16))
         del xs, pools, sides, outs
         torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- decode attention
+ATOL, RTOL = 2e-3, 1e-3
+
+
+def _close(got, ref):
+    bad = np.abs(got - ref) > ATOL + RTOL * np.abs(ref)
+    assert not bad.any(), (f"{int(bad.sum())} outside tol; max abs err "
+                           f"{float(np.abs(got - ref).max()):.3e}")
+
+
+@pytest.mark.parametrize("bits", [8, 6, 4])
+@pytest.mark.parametrize("k,n_sink,ps", [(3, 4, 16), (0, 4, 16), (3, 0, 16), (8, 16, 32),
+                                         (1, 1, 16)])
+def test_decode_attn_side(kvq, cuda_dev, bits, k, n_sink, ps):
+    H, G, D, L = 4, 6, 256, 2
+    lens = [1, 3, 16, 17, 100, 1000, 0]
+    nseq = len(lens)
+    starts = [0] * nseq
+    pt_np = None
+    kps, vps, kss, vss, oks, ovs = [], [], [], [], [], []
+    for layer in range(L):
+        pt_np, pools, sides, opools, osides = _setup(kvq, cuda_dev, bits, H, D, ps, k, n_sink,
+                                                     lens, starts)
+        tot = int(sum(lens))
+        xs = [_rows(20 + layer, True, tot, H, D), _rows(20 + layer, False, tot, H, D)]
+        cu = cu_of(lens)
+        kvq.kvq_quant_pack_paged_side(pools, sides, [dev_tensor(x, cuda_dev) for x in xs],
+                                      i32(pt_np, cuda_dev), i32(cu, cuda_dev),
+                                      i32(starts, cuda_dev))
+        for x, osp in zip(xs, osides):
+            osd.quant_pack_paged_side(osp, x, pt_np, cu, np.asarray(starts))
+        kps.append(pools[0]); vps.append(pools[1]); kss.append(sides[0]); vss.append(sides[1])
+        oks.append(osides[0]); ovs.append(osides[1])
+    q = kvgen.queries_np(30, L, nseq, H * G, D)
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device=cuda_dev)
+    ws = kvq.decode_workspace(kps, nseq, H * G, max(lens), cuda_dev)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    kvq.kvq_decode_attn_side(kps, vps, kss, vss, dev_tensor(q, cuda_dev), i32(pt_np, cuda_dev),
+                             i32(lens, cuda_dev), max(lens), 1.0 / 16, out, ws, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    for layer in range(L):
+        ref = osd.decode_attention_paged_side(q[layer], oks[layer], ovs[layer], pt_np,
+                                              np.asarray(lens), 1.0 / 16)
+        _close(got[layer], ref)
+
+
+def test_decode_attn_side_full_size_sampled(kvq, cuda_dev):
+    """The bench's decode shape with side channels: 16 layers, 8 sequences x 32,768 tokens, 4 KV
+    heads x 256, 24 query heads, q6, page 16, 3 outliers per row, 4 sinks; sampled (layer,
+    sequence) outputs against the oracle's own quantization of those sequences."""
+    w = kvgen.WORKLOADS["paged_prefill_16L_8x32768_4x256"]
+    L, nseq, ntok, H, D, ps = w["n_layers"], w["n_seq"], w["n_tok"], w["H"], w["D"], w["page_size"]
+    bits, k, n_sink, Hq = 6, 3, 4, 24
+    pt_np = kvgen.random_page_table(1, nseq, ntok // ps)
+    pt = i32(pt_np, cuda_dev)
+    cu = i32(np.arange(nseq + 1) * ntok, cuda_dev)
+    st = i32(np.zeros(nseq), cuda_dev)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    kps, vps, kss, vss, specs = [], [], [], [], []
+    for layer in range(L):
+        sp = [kvgen.KVSpec(seed=w["seed"], layer=layer, is_key=kk, n_seq=nseq, n_tok=ntok,
+                           num_heads=H, head_dim=D) for kk in (True, False)]
+        pools = [kvq.Pool.empty(bits, H, D, ps, pt_np.size, cuda_dev) for _ in range(2)]
+        sides = [kvq.Side.empty(p, k, n_sink, nseq, cuda_dev) for p in pools]
+        xs = [s.full_torch(cuda_dev) for s in sp]
+        kvq.kvq_quant_pack_paged_side(pools, sides, xs, pt, cu, st, err)
+        del xs
+        kps.append(pools[0]); vps.append(pools[1]); kss.append(sides[0]); vss.append(sides[1])
+        specs.append(sp)
+    q = kvgen.queries_torch(w["seed"], L, nseq, Hq, D, cuda_dev)
+    out = torch.empty(q.shape, dtype=torch.float32, device=cuda_dev)
+    ws = kvq.decode_workspace(kps, nseq, Hq, ntok, cuda_dev)
+    lens = i32(np.full(nseq, ntok), cuda_dev)
+    kvq.kvq_decode_attn_side(kps, vps, kss, vss, q, pt, lens, ntok, 1.0 / 16, out, ws, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    qn, got = q.cpu().numpy(), out.cpu().numpy().astype(np.float64)
+    for layer, s in ((0, 0), (15, 7)):
+        rows = np.arange(s * ntok * H, (s + 1) * ntok * H, dtype=np.int64)
+        kx = specs[layer][0].rows_np(rows).reshape(ntok, H, D)
+        vx = specs[layer][1].rows_np(rows).reshape(ntok, H, D)
+        ops = [osd.SidePool(osym.PagedPool(bits, H, D, ps, ntok // ps), k, n_sink, 1)
+               for _ in range(2)]
+        table = np.arange(ntok // ps)[None, :]
+        for x, op in zip((kx, vx), ops):
+            osd.quant_pack_paged_side(op, x, table, np.array([0, ntok]), np.array([0]))
+        ref = osd.decode_attention_paged_side(qn[layer, s:s + 1], ops[0], ops[1], table,
+                                              np.array([ntok]), 1.0 / 16)
+        _close(got[layer, s:s + 1], ref)
+    del kps, vps, kss, vss
+    torch.cuda.empty_cache()
