@@ -319,6 +319,46 @@ def kivi_loop_extra(kvq, dev, warmup, stream, passes=3):
     return res
 
 
+def side_extra(w, kvq, dev, steps, warmup, stream, bits=6, n_sink=4, fraction=0.01):
+    """The symmetric path with fp16 side channels on the paged-prefill workload: quant-pack with
+    k = ceil(0.01 * D) = 3 outliers per row and 4 sink tokens per sequence, dequant, and decode
+    attention (8 sequences x 24 query heads) over the result."""
+    k = int(np.ceil(fraction * w.D))
+    pools = w.make_pools(bits)
+    sides = [kvq.Side.empty(p, k, n_sink, w.nseq, dev) for p in pools]
+    q, out, ws = w.dec_buffers()
+
+    def quant():
+        kvq.kvq_quant_pack_paged_side(pools, sides, w.x, w.pt, w.cu, w.start, w.err)
+
+    def deq():
+        kvq.kvq_dequant_paged_side(pools, sides, w.deq, w.pt, w.cu, w.start, w.err)
+
+    def attn():
+        kvq.kvq_decode_attn_side(pools[0::2], pools[1::2], sides[0::2], sides[1::2], q, w.pt,
+                                 w.lens, w.ntok, SOFTMAX_SCALE, out, ws, w.err)
+
+    tq = time_fn(quant, steps, warmup, stream)
+    td = time_fn(deq, steps, warmup, stream)
+    ta = time_fn(attn, steps, warmup, stream)
+    torch.cuda.synchronize()
+    if int(w.err.item()) != 0:
+        raise RuntimeError("device error word set in the side-channel extra")
+    rows = w.L * 2 * w.nseq * w.ntok * w.H
+    side_b = 3 * k                                       # fp16 value + uint8 position per outlier
+    bq = rows * (2 * w.D + packed_dim(w.D, bits) + 2 + side_b)
+    ba = (w.L * w.nseq * w.ntok * w.H * 2 * (packed_dim(w.D, bits) + 2 + side_b)
+          + w.L * w.nseq * HQ * w.D * (2 + 4))
+    res = {"outliers_per_row": k, "sinks": n_sink,
+           "quant_pack_ms": tq * 1e3, "quant_pack_GB_s": bq / tq / 1e9,
+           "dequant_ms": td * 1e3, "dequant_GB_s": bq / td / 1e9,
+           "decode_attn_ms": ta * 1e3, "decode_attn_GB_s": ba / ta / 1e9,
+           "decode_attn_tok_s": w.nseq / ta}
+    del pools, sides
+    torch.cuda.empty_cache()
+    return res
+
+
 class Workload:
     """Device-resident inputs and outputs of one replica (outputs allocated on first use)."""
 
@@ -582,6 +622,10 @@ def run_gpu(args):
         w._kp = None
         torch.cuda.empty_cache()
 
+    # the symmetric path with fp16 sinks and outlier side channels
+    if not args.no_side:
+        extras["side_q6_k3_sink4"] = side_extra(w, kvq, dev, args.steps, args.warmup, stream)
+
     # the KIVI serving loop: append one token, flush every 32, attend over packed + window
     if not args.no_kivi_packed:
         extras["kivi_decode_loop_16L_16x8_2bit"] = kivi_loop_extra(kvq, dev, args.warmup, stream)
@@ -784,6 +828,8 @@ def main():
                     choices=["quant_pack", "dequant", "decode_attn", "kivi", "decode_attn_262144",
                              "kivi_pack", "kivi_attn", "kivi_attn_fp16"],
                     help="profiling only: run one stage and print its time, no bench line")
+    ap.add_argument("--no-side", action="store_true",
+                    help="skip the side-channel (sinks + outliers) extra")
     ap.add_argument("--no-decode-step", action="store_true",
                     help="skip the fused append + decode step extra")
     ap.add_argument("--no-kivi-packed", action="store_true",
