@@ -99,6 +99,17 @@ KVQ_API const char* kvq_last_error(void);
 KVQ_API const char* kvq_status_string(kvq_status status);
 
 /*
+ * The address under which kernels read page-locked host memory (cudaHostAlloc, or
+ * cudaHostRegister with the mapped flag; on systems with unified addressing all page-locked memory
+ * is mapped).  Any entry point documented to take "device" input may be given this address: its
+ * kernels then read the host memory directly over the host link (NVLink-C2C on Grace systems)
+ * instead of the caller copying it to the device first.  A device or managed pointer is returned
+ * as is; other memory is refused with KVQ_ERR_RANGE (no kernel ever sees an unmapped address).
+ * No counterpart on the pages: a host-memory convenience of this library.
+ */
+KVQ_API kvq_status kvq_host_device_view(const void* host_ptr, void** device_ptr);
+
+/*
  * Bytes per packed row.  MTPLX pull request #267, "feat(kv-cache): add q6 paged KV
  * quantization", description, packed_dim sentence: packed_dim(D, 6) = D*3/4 and q6 needs
  * D % 4 == 0; q8 stores one code per byte, q4 two per byte (D % 2 == 0).

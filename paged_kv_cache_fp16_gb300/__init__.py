@@ -101,6 +101,7 @@ def _load() -> ctypes.CDLL:
                                      P, P]),
         "kvq_dequant_paged_side": (I, [pool_p, ctypes.POINTER(kvq_side), P, I, P, I, P, P, I, I,
                                        P, P]),
+        "kvq_host_device_view": (I, [P, ctypes.POINTER(ctypes.c_void_p)]),
         "kivi_state_init": (I, [ctypes.POINTER(kivi_state), I, I, I, I, I, I, I]),
         "kivi_update": (I, [ctypes.POINTER(kivi_state), P, P, P, P, I, I, P]),
         "kivi_trim": (I, [ctypes.POINTER(kivi_state), I]),
@@ -147,7 +148,11 @@ def _ptr_array(tensors: Sequence[torch.Tensor]):
     return arr
 
 
-def _cuda_tensor(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
+def _cuda_tensor(t, dtype, name: str):
+    if isinstance(t, HostView):   # page-locked host memory read in place by the kernel
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}")
+        return t
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
@@ -690,6 +695,28 @@ def kvq_decode_attn_side(k_pools: Sequence[Pool], v_pools: Sequence[Pool],
                                      out.data_ptr(), workspace.data_ptr(),
                                      workspace.numel() * workspace.element_size(), _ptr(dev_err),
                                      _stream(stream)))
+
+
+class HostView:
+    """A page-locked host tensor seen through its device address (kvq_host_device_view): pass it
+    where an entry point takes device input and the kernel reads the host memory directly."""
+
+    def __init__(self, t: torch.Tensor):
+        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+            raise TypeError("HostView needs a contiguous page-locked host tensor")
+        out = ctypes.c_void_p()
+        _check(_lib.kvq_host_device_view(t.data_ptr(), ctypes.byref(out)))
+        self.tensor, self.ptr = t, out.value
+        self.shape, self.dtype = t.shape, t.dtype
+
+    def data_ptr(self) -> int:
+        return self.ptr
+
+    def numel(self) -> int:
+        return self.tensor.numel()
+
+    def element_size(self) -> int:
+        return self.tensor.element_size()
 
 
 def decode_workspace(k_pools: Sequence[Pool], nseq: int, num_q_heads: int, max_seq_len: int,

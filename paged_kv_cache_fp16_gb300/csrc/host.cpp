@@ -1,5 +1,6 @@
 // Host side of libkvq: error state, validation helpers, packed_dim, the KIVI boundary and the
-// page allocator.  No CUDA call here except the SM-count query.
+// page allocator.  The only CUDA calls here are the SM-count query and the pointer queries of
+// kvq_host_device_view.
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -97,6 +98,30 @@ const char* kvq_status_string(kvq_status status) {
     case KVQ_ERR_WORKSPACE: return "KVQ_ERR_WORKSPACE";
   }
   return "KVQ_ERR_UNKNOWN";
+}
+
+kvq_status kvq_host_device_view(const void* host_ptr, void** device_ptr) {
+  using namespace kvq;
+  if (!host_ptr || !device_ptr) return fail(KVQ_ERR_NULL, "kvq_host_device_view: NULL pointer");
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, host_ptr);
+  if (e != cudaSuccess)
+    return fail(KVQ_ERR_CUDA, "kvq_host_device_view: cudaPointerGetAttributes: %s",
+                cudaGetErrorString(e));
+  if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged) {
+    *device_ptr = const_cast<void*>(host_ptr);
+    return ok();
+  }
+  if (attr.type != cudaMemoryTypeHost)
+    return fail(KVQ_ERR_RANGE, "kvq_host_device_view: not page-locked host memory (allocate it "
+                "with cudaHostAlloc or register it with cudaHostRegister)");
+  void* d = nullptr;
+  e = cudaHostGetDevicePointer(&d, const_cast<void*>(host_ptr), 0);
+  if (e != cudaSuccess || d == nullptr)
+    return fail(KVQ_ERR_CUDA, "kvq_host_device_view: cudaHostGetDevicePointer: %s",
+                cudaGetErrorString(e));
+  *device_ptr = d;
+  return ok();
 }
 
 int kvq_packed_dim(int head_dim, int bits) {
