@@ -28,7 +28,10 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarpsPerBlock = kThreads / 32;
 constexpr int kTok = 8;     // tokens per warp work item (all heads of each)
-constexpr int kUnroll = 2;  // warp steps with loads in flight
+constexpr int kUnroll = 2;  // warp steps with loads in flight (quant-pack)
+// dequant: its loads are smaller than the quantizer's, so more warp steps stay in flight -- 4 for
+// q6/q4 (measured +12 % at q6); q8 keeps 2 (its 16-byte units at 4 steps cost occupancy)
+template <int BITS> constexpr int dq_unroll() { return BITS == 8 ? 2 : 4; }
 
 struct PackArgs {
   const uint16_t* x[KVQ_MAX_TENSORS];  // quant: inputs; dequant: outputs (cast back)
@@ -162,6 +165,7 @@ __global__ void __launch_bounds__(kThreads) quant_pack_kernel(const PackArgs a) 
 
 template <int BITS, int UPL>
 __global__ void __launch_bounds__(kThreads) dequant_kernel(const PackArgs a) {
+  constexpr int kDqU = dq_unroll<BITS>();
   const int t = blockIdx.y;
   uint16_t* __restrict__ out = const_cast<uint16_t*>(a.x[t]);
   const PoolRef pool = a.pool[t];
@@ -182,12 +186,12 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const PackArgs a) {
     if (lane < ntok) base = token_base(a, pool.num_pages, tok0 + lane);
     const int nrows = ntok * H;
     uint16_t* oi = out + static_cast<int64_t>(tok0) * H * D;
-    for (int r0 = 0; r0 < nrows; r0 += rps * kUnroll) {
-      uint32_t w[kUnroll][UPL][4];
-      uint32_t sc[kUnroll];
-      bool act[kUnroll];
+    for (int r0 = 0; r0 < nrows; r0 += rps * kDqU) {
+      uint32_t w[kDqU][UPL][4];
+      uint32_t sc[kDqU];
+      bool act[kDqU];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
+      for (int u = 0; u < kDqU; ++u) {
         const int row = r0 + u * rps + sub;
         const int k = row / H;
         const long long b = shfl_ll(base, k < kTok ? k : 0);
@@ -207,7 +211,7 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const PackArgs a) {
         }
       }
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
+      for (int u = 0; u < kDqU; ++u) {
         if (!act[u]) continue;
         const int row = r0 + u * rps + sub;
         const uint32_t s2 = sc[u] | (sc[u] << 16);
