@@ -52,6 +52,15 @@ __device__ __forceinline__ uint32_t quant_field(float x, float se, float y, bool
   return rint_biased_bits<BIAS>(q) & static_cast<uint32_t>(MASK);
 }
 
+// The same with the clamp decided at compile time: a row with a normal fp16 scale never needs it,
+// so a kernel can branch once per row instead of testing per element.
+template <int QMAX, int BIAS, int MASK, bool CLIP>
+__device__ __forceinline__ uint32_t quant_field_c(float x, float se, float y) {
+  float q = div_by_row_scale(x, se, y);
+  if constexpr (CLIP) q = fminf(fmaxf(q, -static_cast<float>(QMAX)), static_cast<float>(QMAX));
+  return rint_biased_bits<BIAS>(q) & static_cast<uint32_t>(MASK);
+}
+
 // ---------------------------------------------------------------------------------------------
 // Packed fields -> exact fp16 codes.  A field u placed in the low mantissa bits of 1024 (fp16
 // 0x6400) reads as 1024 + u (or 1024 + 16u / 1024 + 4u when it sits higher); one half2 FMA then

@@ -16,6 +16,8 @@
 // plus a segmented shuffle, and codes are packed in registers.  Per element: the quotient by the row's scale from a per-row
 // reciprocal with one Markstein correction (exact), then one add that rounds half to even and
 // leaves the biased field in the low bits.  HBM-bound: per row 2D bytes in, packed_dim + 2 out.
+#include <type_traits>
+
 #include <cuda_runtime.h>
 
 #include "kvq_device.cuh"
@@ -138,25 +140,31 @@ __global__ void __launch_bounds__(kThreads) quant_pack_kernel(const PackArgs a) 
         const float se = (s == 0.f) ? 1.f : s;
         const bool clip = s < 6.103515625e-05f;   // 2^-14, smallest normal fp16
         uint8_t* crow = pool.codes + prow * a.pd;
+        // the clamp only matters for a subnormal scale: decide it once per row
+        auto units = [&](auto clip_tag) {
+          constexpr bool kClip = decltype(clip_tag)::value;
 #pragma unroll
-        for (int j = 0; j < UPL; ++j) {
-          const int unit = lr + j * lpr;
-          if (unit * 16 >= D) continue;
-          uint32_t pk[4];
+          for (int j = 0; j < UPL; ++j) {
+            const int unit = lr + j * lpr;
+            if (unit * 16 >= D) continue;
+            uint32_t pk[4];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint4& vv = v[u][j][hh];
-            const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
-            uint32_t f[8];
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint4& vv = v[u][j][hh];
+              const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+              uint32_t f[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float xe = h2f(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
-              f[e] = quant_field<kQm, kB, kM>(xe, se, y, clip);
+              for (int e = 0; e < 8; ++e) {
+                const float xe = h2f(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
+                f[e] = quant_field_c<kQm, kB, kM, kClip>(xe, se, y);
+              }
+              pack8<BITS>(f, pk[2 * hh], pk[2 * hh + 1]);
             }
-            pack8<BITS>(f, pk[2 * hh], pk[2 * hh + 1]);
+            store_unit<BITS>(crow + unit * SymQ<BITS>::kUnitBytes, pk[0], pk[1], pk[2], pk[3]);
           }
-          store_unit<BITS>(crow + unit * SymQ<BITS>::kUnitBytes, pk[0], pk[1], pk[2], pk[3]);
-        }
+        };
+        if (clip) units(std::true_type{});
+        else units(std::false_type{});
         if (lr == 0) pool.scales[prow] = sbits;
       }
     }
