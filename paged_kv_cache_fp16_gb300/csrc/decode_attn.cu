@@ -177,13 +177,13 @@ template <int BITS>
 struct KRegs {
   uint32_t kw[2][Wd<BITS>::kKWords];
   float ksc[2];      // the rows' fp16 scales, applied to the scores
+  float vsc[2];      // the rows' V scales (0 if masked), folded into P for the P.V product
   bool kval[2];
 };
 
 template <int BITS>
 struct VRegs {
   uint32_t vw[4][Wd<BITS>::kVWords];
-  uint32_t vsc[4];   // fp16 scale bits (0 if the token is masked)
 };
 
 // Q.K^T of one tile and the online-softmax update; returns P^T as the two B-operand registers.
@@ -254,8 +254,10 @@ __device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const uint
       acc[mt][0] *= al0; acc[mt][1] *= al1; acc[mt][2] *= al0; acc[mt][3] *= al1;
     }
   }
-  pb0 = movtrans(pack_h2(p[0], p[1]));   // tokens 2c, 2c+1 ; head g
-  pb1 = movtrans(pack_h2(p[2], p[3]));   // tokens 8+2c, 8+2c+1 ; head g
+  // P times each token's V scale: O = sum_t (p_t s_t) c_t, so the V operand is the exact integer
+  // codes (the normaliser l keeps the unscaled p)
+  pb0 = movtrans(pack_h2(p[0] * T.vsc[0], p[1] * T.vsc[0]));   // tokens 2c, 2c+1 ; head g
+  pb1 = movtrans(pack_h2(p[2] * T.vsc[1], p[3] * T.vsc[1]));   // tokens 8+2c, 8+2c+1 ; head g
   if constexpr (SIDE) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) p_out[k] = p[k];
@@ -269,16 +271,14 @@ __device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const uint
 template <int BITS>
 __device__ __forceinline__ void tile_pv(const VRegs<BITS>& T, uint32_t pb0, uint32_t pb1,
                                         float (&acc)[16][4]) {
-  // ---------------- O^T += V_hat^T . P^T
-  const uint32_t sab = T.vsc[0] | (T.vsc[1] << 16), scd = T.vsc[2] | (T.vsc[3] << 16);
+  // ---------------- O^T += C_V^T . (P S_V)^T on the exact integer codes
 #define KVQ_PV_GROUP(GI)                                                                \
   {                                                                                     \
     uint32_t lab[4], hab[4], lcd[4], hcd[4];                                            \
     cross_group<BITS, GI>(T.vw[0], T.vw[1], lab, hab);                                  \
     cross_group<BITS, GI>(T.vw[2], T.vw[3], lcd, hcd);                                  \
     _Pragma("unroll") for (int k = 0; k < 4; ++k) {                                     \
-      mma16816(acc[4 * GI + k], hmul2u(lab[k], sab), hmul2u(hab[k], sab),               \
-               hmul2u(lcd[k], scd), hmul2u(hcd[k], scd), pb0, pb1);                     \
+      mma16816(acc[4 * GI + k], lab[k], hab[k], lcd[k], hcd[k], pb0, pb1);              \
     }                                                                                   \
   }
   KVQ_PV_GROUP(0) KVQ_PV_GROUP(1) KVQ_PV_GROUP(2) KVQ_PV_GROUP(3)
@@ -555,6 +555,7 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : 3) decode_attn_tma_kernel
       const int row = g + 8 * r;
       K.kval[r] = ok && tb + row < len;
       K.ksc[r] = (SIDE && tb + row < sd.n_sink) ? 0.f : h2f(sks[row]);   // sinks: exact below
+      K.vsc[r] = (K.kval[r] && !(SIDE && tb + row < sd.n_sink)) ? h2f(svs[row]) : 0.f;
       const uint4* src = reinterpret_cast<const uint4*>(sk + row * kPd + c * (4 * W::kKWords));
 #pragma unroll
       for (int i = 0; i < W::kKWords / 4; ++i) {
@@ -652,8 +653,6 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : 3) decode_attn_tma_kernel
 #pragma unroll
     for (int qi = 0; qi < 4; ++qi) {
       const int row = 2 * c + (qi & 1) + 8 * (qi >> 1);
-      const bool v_ok = ok && tb + row < len && !(SIDE && tb + row < sd.n_sink);
-      V.vsc[qi] = v_ok ? svs[row] : 0u;
       const uint8_t* src = sv + row * kPd + g * (4 * W::kVWords);
       if constexpr (W::kVWords % 4 == 0) {
 #pragma unroll
@@ -748,6 +747,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_gather_kernel(const A
       if (t < len) row = locate_row(a.pt, a.max_pages, a.ps, a.H, P.k_pages, s, t, h, a.err);
       K.kval[r] = row >= 0;
       K.ksc[r] = 0.f;
+      K.vsc[r] = 0.f;
+      if (t < len) {
+        const int64_t vrow = locate_row(a.pt, a.max_pages, a.ps, a.H, P.v_pages, s, t, h, a.err);
+        if (vrow >= 0) K.vsc[r] = h2f(ld_nc_u16(P.vs + vrow));
+      }
 #pragma unroll
       for (int i = 0; i < W::kKWords; ++i) K.kw[r][i] = 0;
       if (row >= 0) {
@@ -769,7 +773,6 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_gather_kernel(const A
       const int t = tb + 2 * c + (qi & 1) + 8 * (qi >> 1);
       int64_t row = -1;
       if (t < len) row = locate_row(a.pt, a.max_pages, a.ps, a.H, P.v_pages, s, t, h, a.err);
-      V.vsc[qi] = 0;
 #pragma unroll
       for (int i = 0; i < W::kVWords; ++i) V.vw[qi][i] = 0;
       if (row >= 0) {
@@ -788,7 +791,6 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_gather_kernel(const A
             V.vw[qi][2 * i] = v.x; V.vw[qi][2 * i + 1] = v.y;
           }
         }
-        V.vsc[qi] = ld_nc_u16(P.vs + row);
       }
     }
     tile_pv<BITS>(V, pb0, pb1, acc);
