@@ -28,6 +28,8 @@
 #include <mutex>
 #include <vector>
 
+#include <type_traits>
+
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
@@ -81,9 +83,11 @@ struct AttnSide {
 };
 
 template <int BITS> struct Wd;
-// Stage counts keep three CTAs (12 warps) resident per SM within 228 KB of shared memory.
+// Stage counts: with the query fragments in shared memory (q6, q4) the staged kernel holds 128
+// registers, so shared memory decides the CTAs per SM: 4 for q6 (2 stages) and q4 (3); q8 (2
+// stages, fragments in registers) runs 3.
 template <> struct Wd<8> { static constexpr int kPd = 256, kKWords = 16, kVWords = 8, kStages = 2; };
-template <> struct Wd<6> { static constexpr int kPd = 192, kKWords = 12, kVWords = 6, kStages = 3; };
+template <> struct Wd<6> { static constexpr int kPd = 192, kKWords = 12, kVWords = 6, kStages = 2; };
 template <> struct Wd<4> { static constexpr int kPd = 128, kKWords = 8, kVWords = 4, kStages = 3; };
 
 // shared-memory stage: [K codes 16 x pd][V codes 16 x pd][K scales 16 x 2][V scales 16 x 2]
@@ -93,8 +97,9 @@ template <int BITS> __host__ __device__ constexpr int tma_smem_bytes() {
   return kWarps * warp_bytes<BITS>() + kWarps * Wd<BITS>::kStages * 16;  // + barriers, flags
 }
 
-// Shared-memory layout of the staged kernel.  Without side channels it is the layout above.  With
-// them a stage also holds the tile's K and V outlier values (fp16 [16][k], 256 B reserved each)
+// Shared-memory layout of the staged kernel: the stage ring, the barriers and flags, and the query
+// B fragments every warp of the CTA shares (4 KB: 32 registers per thread saved).  With side
+// channels a stage also holds the tile's K and V outlier values (fp16 [16][k], 256 B reserved each)
 // and positions (uint8 [16][k], 128 B each); two stages per warp; then the warps' sparse output
 // accumulators (fp32 [8 heads][256]), the KV head's queries (fp16 [8][256]) and per-warp sink-row
 // weights (fp32 [16][8]).
@@ -107,12 +112,13 @@ struct Lay {
   static constexpr int kStage = SIDE ? kBase + 768 : kBase;
   static constexpr int kWarpBytes = kStages * kStage;
   static constexpr int kRing = kWarps * kWarpBytes;
-  static constexpr int kOsp = kRing + kWarps * kStages * 16;
+  static constexpr int kQf = kRing + kWarps * kStages * 16;   // query B fragments [16][32] uint2
+  static constexpr int kOsp = kQf + 16 * 32 * 8;
   static constexpr int kQs = kOsp + kWarps * 8 * kD * 4;
   static constexpr int kPs = kQs + 8 * kD * 2;
   static constexpr int kTotal = SIDE ? kPs + kWarps * 16 * 8 * 4 : kOsp;
 };
-static_assert(Lay<6, false>::kTotal == tma_smem_bytes<6>(), "side-free layout is the base layout");
+
 constexpr int kMergeBytes = kWarps * 8 * kD * 4 + 2 * kWarps * 8 * 4;
 
 // PRMT selector picking bytes (b0, b1) of the first and (b0, b1) of the second source word.
@@ -187,10 +193,24 @@ struct VRegs {
 };
 
 // Q.K^T of one tile and the online-softmax update; returns P^T as the two B-operand registers.
+// Where a thread's query B fragments come from: registers, or the CTA's shared copy.
+struct QFragRegs {
+  const uint32_t (*qf)[2];
+  __device__ __forceinline__ uint2 pair(int ks) const { return make_uint2(qf[ks][0], qf[ks][1]); }
+};
+struct QFragSmem {
+  uint32_t addr;   // shared address of this lane's fragments; k-step ks at addr + 256 * ks
+  __device__ __forceinline__ uint2 pair(int ks) const {
+    uint2 r;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(addr + 256 * ks));
+    return r;
+  }
+};
+
 // With SIDE, kc[4] (same layout as the scores) is added after the row scale -- the outlier and
 // sink terms of the keys -- and p[4] and the rescale factors are returned for the side outputs.
-template <int BITS, bool SIDE = false>
-__device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const uint32_t (&qf)[16][2],
+template <int BITS, bool SIDE = false, typename QF>
+__device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const QF& Q,
                                                 float (&acc)[16][4], float& m0, float& m1,
                                                 float& l0, float& l1, float qk_scale,
                                                 uint32_t& pb0, uint32_t& pb1,
@@ -205,9 +225,9 @@ __device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const uint
     uint32_t p0[4], p1[4];                                                              \
     unpack_group<BITS, GI>(T.kw[0], p0);                                                \
     unpack_group<BITS, GI>(T.kw[1], p1);                                                \
-    mma16816(sacc4[(2 * GI) & 3], p0[0], p1[0], p0[1], p1[1], qf[2 * GI][0], qf[2 * GI][1]); \
-    mma16816(sacc4[(2 * GI + 1) & 3], p0[2], p1[2], p0[3], p1[3], qf[2 * GI + 1][0],        \
-             qf[2 * GI + 1][1]);                                                        \
+    const uint2 qa = Q.pair(2 * GI), qb = Q.pair(2 * GI + 1);                           \
+    mma16816(sacc4[(2 * GI) & 3], p0[0], p1[0], p0[1], p1[1], qa.x, qa.y);              \
+    mma16816(sacc4[(2 * GI + 1) & 3], p0[2], p1[2], p0[3], p1[3], qb.x, qb.y);          \
   }
   KVQ_QK_GROUP(0) KVQ_QK_GROUP(1) KVQ_QK_GROUP(2) KVQ_QK_GROUP(3)
   KVQ_QK_GROUP(4) KVQ_QK_GROUP(5) KVQ_QK_GROUP(6) KVQ_QK_GROUP(7)
@@ -409,7 +429,7 @@ __device__ __forceinline__ void append_rows(const AttnArgs& a, const LayerPools&
 
 // Side channels need more shared memory (2 CTAs per SM), so that variant may use more registers.
 template <int BITS, bool APPEND, bool SIDE>
-__global__ void __launch_bounds__(kThreads, SIDE ? 2 : 3) decode_attn_tma_kernel(const AttnArgs a,
+__global__ void __launch_bounds__(kThreads, SIDE ? 2 : (BITS == 8 ? 3 : 4)) decode_attn_tma_kernel(const AttnArgs a,
                                                                       const AttnSide sd) {
   using W = Wd<BITS>;
   using Ly = Lay<BITS, SIDE>;
@@ -515,8 +535,30 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : 3) decode_attn_tma_kernel
     if (lane == 0) issue(j, page);
   }
 
-  uint32_t qf[16][2];
-  load_q_frags(a, ls, h, g, c, len > 0, qf);
+  // The query fragments: for q6/q4 computed once per CTA (warp 0) into shared memory, which
+  // frees the registers for a fourth CTA per SM; q8's stages allow only three, so it keeps them
+  // in registers.
+  constexpr bool kQShared = BITS != 8;
+  using QSrc = typename std::conditional<kQShared, QFragSmem, QFragRegs>::type;
+  const uint32_t qaddr = smem_u32(smem + Ly::kQf) + 8 * lane;
+  uint32_t qf[kQShared ? 1 : 16][2];
+  if constexpr (kQShared) {
+    if (warp == 0) {
+      uint32_t qt[16][2];
+      load_q_frags(a, ls, h, g, c, len > 0, qt);
+#pragma unroll
+      for (int ks = 0; ks < 16; ++ks)
+        asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(qaddr + 256 * ks), "r"(qt[ks][0]),
+                     "r"(qt[ks][1])
+                     : "memory");
+    }
+    __syncthreads();
+  } else {
+    load_q_frags(a, ls, h, g, c, len > 0, reinterpret_cast<uint32_t (&)[16][2]>(qf));
+  }
+  QSrc Q;
+  if constexpr (kQShared) Q = QFragSmem{qaddr};
+  else Q = QFragRegs{qf};
   float acc[16][4];
 #pragma unroll
   for (int mt = 0; mt < 16; ++mt)
@@ -603,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : 3) decode_attn_tma_kernel
         kc[2 * r + 1] = c1;
       }
       float p[4], al[2];
-      tile_qk_softmax<BITS, true>(K, qf, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1, kc, p, al);
+      tile_qk_softmax<BITS, true>(K, Q, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1, kc, p, al);
       // the value terms the codes do not carry, into the warp's sparse accumulator (same
       // running-max domain as acc: rescaled with it)
       if (__any_sync(kFullMask, al[0] != 1.f || al[1] != 1.f)) {
@@ -647,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : 3) decode_attn_tma_kernel
       }
       __syncwarp();
     } else {
-      tile_qk_softmax<BITS>(K, qf, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1);
+      tile_qk_softmax<BITS>(K, Q, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1);
     }
     VRegs<BITS> V;
 #pragma unroll
@@ -766,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_gather_kernel(const A
       }
     }
     uint32_t pb0, pb1;
-    tile_qk_softmax<BITS>(K, qf, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1);
+    tile_qk_softmax<BITS>(K, QFragRegs{qf}, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1);
     VRegs<BITS> V;
 #pragma unroll
     for (int qi = 0; qi < 4; ++qi) {
