@@ -10,11 +10,14 @@
 //   hold code 0; dequantization writes the values back.  Rows at positions < n_sink are also
 //   copied exactly into a [seq][n_sink][H][D] fp16 buffer that dequantization reads instead.
 //
-// One warp per row, lane l holding elements [8l, 8l + 8).  Selection: each element's key is
-// ((|x| bits << 8) | (255 - position)) + 1 -- unique within the row, larger for a larger
-// magnitude and, among equal magnitudes, for the lower position; padding lanes hold 0 -- and
-// k + 1 rounds of a warp max (redux) pick the outliers, then the largest remaining magnitude,
-// which is the dense row's amax.  The scale and code arithmetic are the quant-pack kernel's.
+// A warp takes 32 consecutive rows: lane i locates row i (page-table lookups in parallel), then
+// the warp walks them one row at a time, lane l holding elements [8l, 8l + 8).  Selection: each
+// element's key is ((|x| bits << 8) | (255 - position)) + 1 -- unique within the row, larger for
+// a larger magnitude and, among equal magnitudes, for the lower position; padding lanes hold 0 --
+// and k + 1 rounds of a warp max (redux) pick the outliers, then the largest remaining magnitude,
+// which is the dense row's amax; lane j keeps the j-th outlier and stores it at its rank among
+// the k positions (ascending order without a sort).  The scale and code arithmetic are the
+// quant-pack kernel's.
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
@@ -76,6 +79,12 @@ __device__ __forceinline__ uint64_t load_lane(const uint8_t* p) {
   }
 }
 
+__device__ __forceinline__ int64_t shfl_i64(int64_t v, int src) {
+  const int lo = __shfl_sync(kFullMask, static_cast<int>(v & 0xffffffffLL), src);
+  const int hi = __shfl_sync(kFullMask, static_cast<int>(v >> 32), src);
+  return (static_cast<int64_t>(hi) << 32) | static_cast<uint32_t>(lo);
+}
+
 // Row r of the call's [total_tokens][H] rows -> (sequence, position, physical row or -1).
 __device__ __forceinline__ int64_t row_place(const SideArgs& a, int64_t num_pages, int r, int& s,
                                              int64_t& pos) {
@@ -96,89 +105,88 @@ __global__ void __launch_bounds__(kThreads) quant_pack_side_kernel(const SideArg
   const int lane = threadIdx.x & 31;
   const int rows = a.total_tokens * a.H;
   const bool live = 8 * lane < a.D;
-  for (int r = blockIdx.x * kWarps + (threadIdx.x >> 5); r < rows; r += gridDim.x * kWarps) {
-    int s;
-    int64_t pos;
-    const int64_t prow = row_place(a, pool.num_pages, r, s, pos);
-    if (prow < 0) continue;   // warp-uniform
-    const int h = r % a.H;
-    uint4 xv = make_uint4(0, 0, 0, 0);
-    if (live) xv = ld_stream_v4(a.x[t] + static_cast<int64_t>(r) * a.D + 8 * lane);
-    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-    uint32_t key[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint32_t bits = (xw[e >> 1] >> (16 * (e & 1))) & 0xffffu;
-      key[e] = live ? ((((bits & 0x7fffu) << 8) | (255u - (8 * lane + e))) + 1u) : 0u;
-    }
-    uint32_t opos[8], oval[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) { opos[j] = 0xffffu; oval[j] = 0; }
-    float amax = 0.f;
-    for (int j = 0; j <= a.k; ++j) {   // k outliers, then the dense amax
-      uint32_t m = key[0];
-#pragma unroll
-      for (int e = 1; e < 8; ++e) m = max(m, key[e]);
-      const uint32_t w = __reduce_max_sync(kFullMask, m);
-      if (j == a.k) {
-        amax = (w == 0u) ? 0.f : h2f(static_cast<uint16_t>((w - 1u) >> 8));
-        break;
-      }
-      uint32_t v = 0;
+  const int n_blocks = (rows + 31) / 32;
+  for (int blk = blockIdx.x * kWarps + (threadIdx.x >> 5); blk < n_blocks;
+       blk += gridDim.x * kWarps) {
+    // lane i locates row 32 * blk + i; the warp then walks the 32 rows
+    int my_s = 0;
+    int64_t my_pos = 0, my_prow = -1;
+    if (32 * blk + lane < rows)
+      my_prow = row_place(a, pool.num_pages, 32 * blk + lane, my_s, my_pos);
+    const int nr = min(32, rows - 32 * blk);
+    for (int i = 0; i < nr; ++i) {
+      const int r = 32 * blk + i;
+      const int64_t prow = shfl_i64(my_prow, i);
+      if (prow < 0) continue;   // warp-uniform
+      const int s = __shfl_sync(kFullMask, my_s, i);
+      const int64_t pos = shfl_i64(my_pos, i);
+      const int h = r % a.H;
+      uint4 xv = make_uint4(0, 0, 0, 0);
+      if (live) xv = ld_stream_v4(a.x[t] + static_cast<int64_t>(r) * a.D + 8 * lane);
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      uint32_t key[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        if (key[e] == w) {
-          v = (xw[e >> 1] >> (16 * (e & 1))) & 0xffffu;
-          key[e] = 0u;   // taken: it also leaves the dense row
+        const uint32_t bits = (xw[e >> 1] >> (16 * (e & 1))) & 0xffffu;
+        key[e] = live ? ((((bits & 0x7fffu) << 8) | (255u - (8 * lane + e))) + 1u) : 0u;
+      }
+      // k rounds of a warp max pick the outliers (lane j keeps the j-th), round k the dense amax
+      uint32_t my_opos = 0xffffu, my_oval = 0;
+      float amax = 0.f;
+      for (int j = 0; j <= a.k; ++j) {
+        uint32_t m = key[0];
+#pragma unroll
+        for (int e = 1; e < 8; ++e) m = max(m, key[e]);
+        const uint32_t w = __reduce_max_sync(kFullMask, m);
+        if (j == a.k) {
+          amax = (w == 0u) ? 0.f : h2f(static_cast<uint16_t>((w - 1u) >> 8));
+          break;
+        }
+        uint32_t v = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (key[e] == w) {
+            v = (xw[e >> 1] >> (16 * (e & 1))) & 0xffffu;
+            key[e] = 0u;   // taken: it also leaves the dense row
+          }
+        }
+        const uint32_t val = __reduce_or_sync(kFullMask, v);
+        if (lane == j) {
+          my_opos = 255u - ((w - 1u) & 0xffu);
+          my_oval = val;
         }
       }
-      const uint32_t val = __reduce_or_sync(kFullMask, v);
-      const uint32_t d = 255u - ((w - 1u) & 0xffu);
+      const uint16_t sbits = f2h(row_scale_f32<kQm>(amax));
+      const float sc = h2f(sbits);
+      const float y = (sc == 0.f) ? 0.f : __frcp_rn(sc);
+      const float se = (sc == 0.f) ? 1.f : sc;
+      const bool clip = sc < 6.103515625e-05f;   // 2^-14, smallest normal fp16
+      if (live) {
+        uint32_t f[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (q == j) { opos[q] = d; oval[q] = val; }
-      }
-    }
-    const uint16_t sbits = f2h(row_scale_f32<kQm>(amax));
-    const float sc = h2f(sbits);
-    const float y = (sc == 0.f) ? 0.f : __frcp_rn(sc);
-    const float se = (sc == 0.f) ? 1.f : sc;
-    const bool clip = sc < 6.103515625e-05f;   // 2^-14, smallest normal fp16
-    if (live) {
-      uint32_t f[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const bool dense = key[e] != 0u;
-        const float xe = dense ? h2f(static_cast<uint16_t>(xw[e >> 1] >> (16 * (e & 1)))) : 0.f;
-        f[e] = quant_field<kQm, kB, kM>(xe, se, y, clip);
-      }
-      uint32_t pa, pb;
-      pack8<BITS>(f, pa, pb);
-      store_lane<BITS>(pool.codes + prow * a.pd + lane * lane_bytes<BITS>(), pa, pb);
-    }
-    if (lane == 0) pool.scales[prow] = sbits;
-    if (a.k > 0) {
-      // ascending positions: a sorting network over the 8 slots (unused slots sort last)
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 7 - i; ++j) {
-          const bool sw = opos[j] > opos[j + 1];
-          const uint32_t p0 = sw ? opos[j + 1] : opos[j], p1 = sw ? opos[j] : opos[j + 1];
-          const uint32_t v0 = sw ? oval[j + 1] : oval[j], v1 = sw ? oval[j] : oval[j + 1];
-          opos[j] = p0; opos[j + 1] = p1; oval[j] = v0; oval[j + 1] = v1;
+        for (int e = 0; e < 8; ++e) {
+          const bool dense = key[e] != 0u;
+          const float xe = dense ? h2f(static_cast<uint16_t>(xw[e >> 1] >> (16 * (e & 1)))) : 0.f;
+          f[e] = quant_field<kQm, kB, kM>(xe, se, y, clip);
         }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (lane == j && j < a.k) {
-          sd.out_idx[prow * a.k + j] = static_cast<uint8_t>(opos[j]);
-          sd.out_val[prow * a.k + j] = static_cast<uint16_t>(oval[j]);
+        uint32_t pa, pb;
+        pack8<BITS>(f, pa, pb);
+        store_lane<BITS>(pool.codes + prow * a.pd + lane * lane_bytes<BITS>(), pa, pb);
+      }
+      if (lane == 0) pool.scales[prow] = sbits;
+      if (a.k > 0) {
+        // ascending positions: lane j < k stores its outlier at its rank among the k positions
+        uint32_t rank = 0;
+        for (int j = 0; j < a.k; ++j) rank += __shfl_sync(kFullMask, my_opos, j) < my_opos ? 1u : 0u;
+        if (lane < a.k) {
+          sd.out_idx[prow * a.k + rank] = static_cast<uint8_t>(my_opos);
+          sd.out_val[prow * a.k + rank] = static_cast<uint16_t>(my_oval);
         }
       }
+      if (pos < a.n_sink && live)
+        *reinterpret_cast<uint4*>(sd.sink + ((static_cast<int64_t>(s) * a.n_sink + pos) * a.H + h) *
+                                                a.D + 8 * lane) = xv;
     }
-    if (pos < a.n_sink && live)
-      *reinterpret_cast<uint4*>(sd.sink + ((static_cast<int64_t>(s) * a.n_sink + pos) * a.H + h) *
-                                              a.D + 8 * lane) = xv;
   }
 }
 
@@ -193,38 +201,49 @@ __global__ void __launch_bounds__(kThreads) dequant_side_kernel(const SideArgs a
   const int lane = threadIdx.x & 31;
   const int rows = a.total_tokens * a.H;
   const bool live = 8 * lane < a.D;
-  for (int r = blockIdx.x * kWarps + (threadIdx.x >> 5); r < rows; r += gridDim.x * kWarps) {
-    int s;
-    int64_t pos;
-    const int64_t prow = row_place(a, pool.num_pages, r, s, pos);
-    if (prow < 0 || !live) continue;
-    const int h = r % a.H;
-    uint4 res;
-    if (pos < a.n_sink) {
-      res = *reinterpret_cast<const uint4*>(
-          sd.sink + ((static_cast<int64_t>(s) * a.n_sink + pos) * a.H + h) * a.D + 8 * lane);
-    } else {
-      const uint64_t fw = load_lane<BITS>(pool.codes + prow * a.pd + lane * lane_bytes<BITS>());
-      const float sc = h2f(pool.scales[prow]);
-      uint32_t o[8];
+  const int n_blocks = (rows + 31) / 32;
+  for (int blk = blockIdx.x * kWarps + (threadIdx.x >> 5); blk < n_blocks;
+       blk += gridDim.x * kWarps) {
+    int my_s = 0;
+    int64_t my_pos = 0, my_prow = -1;
+    if (32 * blk + lane < rows)
+      my_prow = row_place(a, pool.num_pages, 32 * blk + lane, my_s, my_pos);
+    const int nr = min(32, rows - 32 * blk);
+    for (int i = 0; i < nr; ++i) {
+      const int r = 32 * blk + i;
+      const int64_t prow = shfl_i64(my_prow, i);
+      if (prow < 0) continue;   // warp-uniform
+      const int s = __shfl_sync(kFullMask, my_s, i);
+      const int64_t pos = shfl_i64(my_pos, i);
+      if (!live) continue;
+      const int h = r % a.H;
+      uint4 res;
+      if (pos < a.n_sink) {
+        res = *reinterpret_cast<const uint4*>(
+            sd.sink + ((static_cast<int64_t>(s) * a.n_sink + pos) * a.H + h) * a.D + 8 * lane);
+      } else {
+        const uint64_t fw = load_lane<BITS>(pool.codes + prow * a.pd + lane * lane_bytes<BITS>());
+        const float sc = h2f(pool.scales[prow]);
+        uint32_t o[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint32_t fld = static_cast<uint32_t>(fw >> (BITS * e)) & kM;
-        const int c = (BITS == 8) ? static_cast<int>(static_cast<int8_t>(fld))
-                                  : static_cast<int>(fld) - kB;
-        o[e] = f2h(static_cast<float>(c) * sc);   // exact product, one rounding to fp16
-      }
-      for (int j = 0; j < a.k; ++j) {
-        const uint32_t d = sd.out_idx[prow * a.k + j];
-        const uint32_t v = sd.out_val[prow * a.k + j];
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t fld = static_cast<uint32_t>(fw >> (BITS * e)) & kM;
+          const int c = (BITS == 8) ? static_cast<int>(static_cast<int8_t>(fld))
+                                    : static_cast<int>(fld) - kB;
+          o[e] = f2h(static_cast<float>(c) * sc);   // exact product, one rounding to fp16
+        }
+        for (int j = 0; j < a.k; ++j) {
+          const uint32_t d = sd.out_idx[prow * a.k + j];
+          const uint32_t v = sd.out_val[prow * a.k + j];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (d == static_cast<uint32_t>(8 * lane + e)) o[e] = v;
+          for (int e = 0; e < 8; ++e)
+            if (d == static_cast<uint32_t>(8 * lane + e)) o[e] = v;
+        }
+        res = make_uint4(o[0] | (o[1] << 16), o[2] | (o[3] << 16), o[4] | (o[5] << 16),
+                         o[6] | (o[7] << 16));
       }
-      res = make_uint4(o[0] | (o[1] << 16), o[2] | (o[3] << 16), o[4] | (o[5] << 16),
-                       o[6] | (o[7] << 16));
+      *reinterpret_cast<uint4*>(out + static_cast<int64_t>(r) * a.D + 8 * lane) = res;
     }
-    *reinterpret_cast<uint4*>(out + static_cast<int64_t>(r) * a.D + 8 * lane) = res;
   }
 }
 
@@ -301,7 +320,7 @@ kvq_status side_call(bool quant, const kvq_pool* pools, const kvq_side* sides,
   a.n_sink = sides[0].n_sink;
   const int sms = sm_count() > 0 ? sm_count() : 152;
   const int64_t rows = static_cast<int64_t>(total) * a.H;
-  int64_t blocks = (rows + kWarps - 1) / kWarps;
+  int64_t blocks = ((rows + 31) / 32 + kWarps - 1) / kWarps;
   const int64_t cap = (8LL * sms + n_tensors - 1) / n_tensors;
   if (blocks > cap) blocks = cap;
   const dim3 grid(static_cast<unsigned>(blocks), n_tensors);
