@@ -370,7 +370,7 @@ class Workload:
         self.specs = [kvgen.KVSpec(seed=WL["seed"], layer=l, is_key=k, n_seq=nseq, n_tok=ntok,
                                    num_heads=H, head_dim=D)
                       for l in range(L) for k in (True, False)]
-        self.x = [s.full_torch(dev) for s in self.specs]
+        self._x = None
         self.pt_np = kvgen.random_page_table(1, nseq, ntok // ps)
         self.pt = torch.from_numpy(self.pt_np).to(dev)
         self.pt1 = self.pt.reshape(1, -1).contiguous()      # one 262,144-token sequence
@@ -379,10 +379,23 @@ class Workload:
         self.lens = torch.full((nseq,), ntok, dtype=torch.int32, device=dev)
         self.lens1 = torch.tensor([nseq * ntok], dtype=torch.int32, device=dev)
         self.bits = bits
-        self.pools = {bits: self.make_pools(bits)}
+        self._pools = None
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self._deq = self._dec = self._dec1 = self._kivi = self._kp = None
         self.kivi_layers = KV["n_layers"] if layers is None else layers
+
+    @property
+    def x(self):
+        """The paged-prefill fp16 inputs (16 GiB at 16 layers), generated on first use."""
+        if self._x is None:
+            self._x = [s.full_torch(self.dev) for s in self.specs]
+        return self._x
+
+    @property
+    def pools(self):
+        if self._pools is None:
+            self._pools = {self.bits: self.make_pools(self.bits)}
+        return self._pools
 
     @property
     def deq(self):
@@ -463,7 +476,7 @@ class Workload:
 
     def make_pools(self, bits):
         return [self.kvq.Pool.empty(bits, self.H, self.D, self.ps, self.pt_np.size, self.dev)
-                for _ in self.x]
+                for _ in range(2 * self.L)]
 
     # the four stages of one step
     def quant(self, bits):
@@ -582,6 +595,12 @@ def run_gpu(args):
                 "traffic": (args.traffic if args.traffic is not None
                             else recorded_traffic(dom, bits))}
 
+    # end to end through the public API with host buffers (before the extras, which allocate and
+    # free tens of GB)
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(w, kvq, bits, args, stream, world, dev, step_bytes)
+
     # extras outside the timed step: 262,144-token decode, q8/q4 variants
     extras = {}
     t = time_fn(lambda: w.decode_full_context(bits), args.steps, args.warmup, stream)
@@ -635,10 +654,6 @@ def run_gpu(args):
         extras["decode_step_64seq_ragged_16L_q6"] = decode_step_extra(kvq, dev, args.steps,
                                                                       args.warmup, stream)
 
-    # end to end through the public API with host buffers
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(w, kvq, bits, args, stream, world, dev, step_bytes)
 
     if int(w.err.item()) != 0:
         raise RuntimeError("device error word set")
@@ -678,9 +693,11 @@ def run_only(w, bits, args, stream):
           "decode_attn_262144": lambda: w.decode_full_context(bits),
           "kivi_pack": w.kivi_pack, "kivi_attn": w.kivi_attn,
           "kivi_attn_fp16": lambda: w.kivi_attn(0)}[args.only]
-    if args.only.startswith("kivi_attn"):
-        w.kivi_pack()
-    w.quant(bits)
+    if args.only.startswith("kivi"):   # the KIVI stages need none of the paged workload
+        if args.only.startswith("kivi_attn"):
+            w.kivi_pack()
+    else:
+        w.quant(bits)
     torch.cuda.synchronize()
     t = time_fn(fn, args.steps, args.warmup, stream)
     print(json.dumps({"profile_only": args.only, "layers": w.L, "bits": bits,
