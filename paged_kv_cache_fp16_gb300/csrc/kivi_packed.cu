@@ -262,11 +262,22 @@ struct KAArgs {
   float qk_scale;
 };
 
-__device__ __forceinline__ uint32_t lds_u32(const uint8_t* p) {
-  return *reinterpret_cast<const uint32_t*>(p);
+// Shared-memory loads at 32-bit shared-window addresses (no generic-address arithmetic).
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t r;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(a));
+  return r;
 }
-__device__ __forceinline__ uint32_t lds_u16(const uint8_t* p) {
-  return *reinterpret_cast<const uint16_t*>(p);
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+  uint16_t r;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(r) : "r"(a));
+  return r;
+}
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a));
+  return r;
 }
 
 // Exact fp16 codes {e_k, e_(k + 8)} of a word of sixteen 2-bit fields.
@@ -378,7 +389,7 @@ __global__ void __launch_bounds__(kAThreads, 4) kivi_attn_kernel(const KAArgs a)
       timed_out = true;
       break;
     }
-    const uint8_t* sb = wbase + st * kStageBytes;
+    const uint32_t sb = smem_u32(wbase + st * kStageBytes);   // the stage, shared window
     const int ctile = tile0 + 4 * (warp + j * kAWarps);
     const int t0 = ctile * kATile;
 #pragma unroll 1
@@ -395,11 +406,11 @@ __global__ void __launch_bounds__(kAThreads, 4) kivi_attn_kernel(const KAArgs a)
         const int grp = tb / gs;
         if (grp != kgroup) {   // group parameters of the thread's 16 channels (warp-uniform)
           kgroup = grp;
-          const uint8_t* sp = sb + kOffKS + ((tb - t0) / gs) * (kAD * 2) + 32 * c;
-          const uint4 s0 = *reinterpret_cast<const uint4*>(sp);
-          const uint4 s1 = *reinterpret_cast<const uint4*>(sp + 16);
-          const uint4 z0 = *reinterpret_cast<const uint4*>(sp + (kOffKZ - kOffKS));
-          const uint4 z1 = *reinterpret_cast<const uint4*>(sp + (kOffKZ - kOffKS) + 16);
+          const uint32_t sp = sb + kOffKS + ((tb - t0) / gs) * (kAD * 2) + 32 * c;
+          const uint4 s0 = lds_v4(sp);
+          const uint4 s1 = lds_v4(sp + 16);
+          const uint4 z0 = lds_v4(sp + (kOffKZ - kOffKS));
+          const uint4 z1 = lds_v4(sp + (kOffKZ - kOffKS) + 16);
           const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
           const uint32_t zw[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
 #pragma unroll
