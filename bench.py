@@ -692,10 +692,23 @@ def run_only(w, bits, args, stream):
           "decode_attn": lambda: w.decode(bits), "kivi": w.kivi_flush,
           "decode_attn_262144": lambda: w.decode_full_context(bits),
           "kivi_pack": w.kivi_pack, "kivi_attn": w.kivi_attn,
-          "kivi_attn_fp16": lambda: w.kivi_attn(0)}[args.only]
+          "kivi_attn_fp16": lambda: w.kivi_attn(0)}.get(args.only)
     if args.only.startswith("kivi"):   # the KIVI stages need none of the paged workload
         if args.only.startswith("kivi_attn"):
             w.kivi_pack()
+    elif args.only.startswith("side_"):   # side channels: 3 outliers per row, 4 sinks
+        kvq = w.kvq
+        pools = w.pools[bits]
+        sides = [kvq.Side.empty(p, int(np.ceil(0.01 * w.D)), 4, w.nseq, w.dev) for p in pools]
+        q, out, ws = w.dec_buffers()
+        fn = {"side_quant": lambda: kvq.kvq_quant_pack_paged_side(pools, sides, w.x, w.pt, w.cu,
+                                                                  w.start, w.err),
+              "side_dequant": lambda: kvq.kvq_dequant_paged_side(pools, sides, w.deq, w.pt, w.cu,
+                                                                 w.start, w.err),
+              "side_attn": lambda: kvq.kvq_decode_attn_side(pools[0::2], pools[1::2], sides[0::2],
+                                                            sides[1::2], q, w.pt, w.lens, w.ntok,
+                                                            SOFTMAX_SCALE, out, ws, w.err)}[args.only]
+        kvq.kvq_quant_pack_paged_side(pools, sides, w.x, w.pt, w.cu, w.start, w.err)
     else:
         w.quant(bits)
     torch.cuda.synchronize()
@@ -874,7 +887,8 @@ def main():
                     help="profiling only: fewer layers than the workload's 16")
     ap.add_argument("--only", default=None,
                     choices=["quant_pack", "dequant", "decode_attn", "kivi", "decode_attn_262144",
-                             "kivi_pack", "kivi_attn", "kivi_attn_fp16"],
+                             "kivi_pack", "kivi_attn", "kivi_attn_fp16", "side_quant",
+                             "side_dequant", "side_attn"],
                     help="profiling only: run one stage and print its time, no bench line")
     ap.add_argument("--no-side", action="store_true",
                     help="skip the side-channel (sinks + outliers) extra")

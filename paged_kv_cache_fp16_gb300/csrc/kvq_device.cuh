@@ -82,6 +82,24 @@ __device__ __forceinline__ int64_t locate_row(const int32_t* __restrict__ page_t
   return (static_cast<int64_t>(page) * num_heads + h) * page_size + slot;
 }
 
+// Load one 16-element unit of packed codes (12 / 8 / 16 bytes for q6 / q4 / q8) into the words
+// that unpack_group<BITS, 0> and <BITS, 1> read.
+template <int BITS>
+__device__ __forceinline__ void load_unit(const uint8_t* p, uint32_t w[4]) {
+  if constexpr (BITS == 6) {
+    w[0] = ld_nc_u32(p);
+    w[1] = ld_nc_u32(p + 4);
+    w[2] = ld_nc_u32(p + 8);
+    w[3] = 0;
+  } else if constexpr (BITS == 4) {
+    const uint2 v = ld_nc_v2(p);
+    w[0] = v.x; w[1] = v.y; w[2] = w[3] = 0;
+  } else {
+    const uint4 v = ld_nc_v4(p);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  }
+}
+
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 __device__ __forceinline__ uint16_t f2h(float f) { return __half_as_ushort(__float2half_rn(f)); }
 

@@ -60,23 +60,6 @@ __device__ __forceinline__ long long shfl_ll(long long v, int src) {
   return (static_cast<long long>(hi) << 32) | static_cast<unsigned int>(lo);
 }
 
-// Load one unit of packed codes (words for unpack_group<BITS, 0> and <BITS, 1>).
-template <int BITS>
-__device__ __forceinline__ void load_unit(const uint8_t* p, uint32_t w[4]) {
-  if constexpr (BITS == 6) {
-    w[0] = ld_nc_u32(p);
-    w[1] = ld_nc_u32(p + 4);
-    w[2] = ld_nc_u32(p + 8);
-    w[3] = 0;
-  } else if constexpr (BITS == 4) {
-    const uint2 v = ld_nc_v2(p);
-    w[0] = v.x; w[1] = v.y; w[2] = w[3] = 0;
-  } else {
-    const uint4 v = ld_nc_v4(p);
-    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-  }
-}
-
 template <int BITS, int UPL>
 __global__ void __launch_bounds__(kThreads) quant_pack_kernel(const PackArgs a) {
   constexpr int kQm = SymQ<BITS>::kQmax;

@@ -10,14 +10,26 @@
 //   hold code 0; dequantization writes the values back.  Rows at positions < n_sink are also
 //   copied exactly into a [seq][n_sink][H][D] fp16 buffer that dequantization reads instead.
 //
-// A warp takes 32 consecutive rows: lane i locates row i (page-table lookups in parallel), then
-// the warp walks them one row at a time, lane l holding elements [8l, 8l + 8).  Selection: each
-// element's key is ((|x| bits << 8) | (255 - position)) + 1 -- unique within the row, larger for
-// a larger magnitude and, among equal magnitudes, for the lower position; padding lanes hold 0 --
-// and k + 1 rounds of a warp max (redux) pick the outliers, then the largest remaining magnitude,
-// which is the dense row's amax; lane j keeps the j-th outlier and stores it at its rank among
-// the k positions (ascending order without a sort).  The scale and code arithmetic are the
-// quant-pack kernel's.
+// Thread layout (the plain quant-pack kernel's): a warp takes a block of 8 new tokens (all their
+// heads); lanes 0..7 locate one token each and broadcast it by shuffle.  A row is cut into
+// 16-element units, 8 lanes share a row (fewer for short rows) and lane j of a row holds units j
+// and j + 8, so one warp instruction serves 4 rows.
+//
+// Selection.  Element x at position p of a row has the key (|x| bits << 8) | (255 - p): unique
+// within the row, larger for a larger magnitude and, among equal magnitudes, for the lower
+// position (one byte permute per element builds it).  Each lane sorts the keys of its elements
+// with small sorting networks into a descending list of its DEPTH largest (DEPTH >= k + 1, or
+// the lane's own remaining maximum is recomputed for the last round); k + 1 rounds of a max over
+// the row's lanes pick the k outlier keys and then the (k+1)-th largest key, whose magnitude T
+// is the dense row's amax, the lane that held each winner popping it from its list.  An element
+// is an outlier iff its key exceeds that last key; unless the k-th outlier's magnitude equals T
+// (a tie at the threshold), that is simply |x| > T, one half2 compare per pair of elements,
+// else the keys are rebuilt and compared.  Outliers are zeroed in the dense row, whose scale and
+// codes are the quant-pack kernel's arithmetic; the row's lane j < k stores the outlier whose
+// key is the j-th largest at its rank among the k positions (ascending order without a sort),
+// its fp16 value (with its sign) read back from the input row.
+#include <type_traits>
+
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
@@ -30,6 +42,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kTok = 8;   // new tokens per warp work item (all their heads)
+constexpr int kQU = 1;    // quant-pack: warp steps with loads in flight
+constexpr int kDU = 2;    // dequant: warp steps with loads in flight
 
 struct SideRef {
   uint16_t* out_val;
@@ -46,204 +61,450 @@ struct SideArgs {
   const int32_t* start;
   int32_t* err;
   int n_tensors, total_tokens, H, D, page_size, pd, max_pages, nseq, k, n_sink;
+  int units;     // 16-element units per row: D / 16
+  int lpr_log2;  // lanes per row = 1 << lpr_log2 = min(next_pow2(units), 8)
 };
 
-// Bytes of the packed fields of 8 consecutive elements (lane l's share of a row).
-template <int BITS> constexpr int lane_bytes() { return BITS; }
-
-template <int BITS>
-__device__ __forceinline__ void store_lane(uint8_t* p, uint32_t a, uint32_t b) {
-  if constexpr (BITS == 6) {   // two 24-bit words -> 6 bytes, 2-byte aligned
-    uint16_t* q = reinterpret_cast<uint16_t*>(p);
-    q[0] = static_cast<uint16_t>(a & 0xffffu);
-    q[1] = static_cast<uint16_t>((a >> 16) | ((b & 0xffu) << 8));
-    q[2] = static_cast<uint16_t>(b >> 8);
-  } else if constexpr (BITS == 4) {
-    *reinterpret_cast<uint32_t*>(p) = a;
-  } else {
-    *reinterpret_cast<uint2*>(p) = make_uint2(a, b);
-  }
+// New token `tok` -> physical row of its head 0 ((page * H) * page_size + slot) or -1, with its
+// sequence and position (the position clamped to int: it is only compared with n_sink).
+__device__ __forceinline__ long long token_place(const SideArgs& a, int64_t num_pages, int tok,
+                                                 int& s, int& pos) {
+  s = find_seq(a.cu, a.nseq, tok);
+  const int64_t p = static_cast<int64_t>(__ldg(a.start + s)) + (tok - __ldg(a.cu + s));
+  pos = p > 0x7fffffffLL ? 0x7fffffff : static_cast<int>(p);
+  return locate_row(a.page_table, a.max_pages, a.page_size, a.H, num_pages, s, p, 0, a.err);
 }
 
-template <int BITS>
-__device__ __forceinline__ uint64_t load_lane(const uint8_t* p) {
-  if constexpr (BITS == 6) {
-    const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
-    return static_cast<uint64_t>(q[0]) | (static_cast<uint64_t>(q[1]) << 16) |
-           (static_cast<uint64_t>(q[2]) << 32);
-  } else if constexpr (BITS == 4) {
-    return *reinterpret_cast<const uint32_t*>(p);
-  } else {
-    const uint2 w = *reinterpret_cast<const uint2*>(p);
-    return static_cast<uint64_t>(w.x) | (static_cast<uint64_t>(w.y) << 32);
-  }
-}
-
-__device__ __forceinline__ int64_t shfl_i64(int64_t v, int src) {
+__device__ __forceinline__ long long shfl_ll(long long v, int src) {
   const int lo = __shfl_sync(kFullMask, static_cast<int>(v & 0xffffffffLL), src);
   const int hi = __shfl_sync(kFullMask, static_cast<int>(v >> 32), src);
-  return (static_cast<int64_t>(hi) << 32) | static_cast<uint32_t>(lo);
+  return (static_cast<long long>(hi) << 32) | static_cast<unsigned int>(lo);
 }
 
-// Row r of the call's [total_tokens][H] rows -> (sequence, position, physical row or -1).
-__device__ __forceinline__ int64_t row_place(const SideArgs& a, int64_t num_pages, int r, int& s,
-                                             int64_t& pos) {
-  const int tok = r / a.H, h = r - tok * a.H;
-  s = find_seq(a.cu, a.nseq, tok);
-  pos = static_cast<int64_t>(__ldg(a.start + s)) + (tok - __ldg(a.cu + s));
-  return locate_row(a.page_table, a.max_pages, a.page_size, a.H, num_pages, s, pos, h, a.err);
+// ---------------------------------------------------------------------------- selection keys
+// Compare-exchange: a >= b afterwards.
+__device__ __forceinline__ void cx(uint32_t& a, uint32_t& b) {
+  const uint32_t hi = max(a, b);
+  b = min(a, b);
+  a = hi;
 }
 
-template <int BITS>
-__global__ void __launch_bounds__(kThreads) quant_pack_side_kernel(const SideArgs a) {
+__device__ __forceinline__ void sort4(uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+  cx(a, b); cx(c, d); cx(a, c); cx(b, d); cx(b, c);
+}
+
+// A bitonic sequence t[0..N) -> descending (half-cleaners of Batcher's bitonic sorter).
+template <int N>
+__device__ __forceinline__ void bitonic_desc(uint32_t* t) {
+#pragma unroll
+  for (int len = N / 2; len >= 1; len /= 2) {
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if ((i & len) == 0) cx(t[i], t[i + len]);
+  }
+}
+
+// Keys of 8 consecutive elements (4 words of fp16 pairs); cb = 255 - position of the first.
+__device__ __forceinline__ void keys8(const uint4& v, uint32_t cb, uint32_t k[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const uint32_t c0 = cb | ((cb - 1u) << 16);   // bytes [255-p, 0, 255-(p+1), 0]
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t m = w[i] & 0x7fff7fffu;       // |x| of both halves
+    const uint32_t c = c0 - 0x00020002u * static_cast<uint32_t>(i);
+    k[2 * i] = prmt(m, c, 0x5104u);              // [255-p, |x| lo byte, |x| hi byte, 0]
+    k[2 * i + 1] = prmt(m, c, 0x7326u);
+  }
+}
+
+// k[0..8) -> k[0..DEPTH) = its DEPTH largest, descending (DEPTH 4 or 8).
+template <int DEPTH>
+__device__ __forceinline__ void top_of8(uint32_t k[8]) {
+  sort4(k[0], k[1], k[2], k[3]);
+  sort4(k[4], k[5], k[6], k[7]);
+  if constexpr (DEPTH == 4) {
+    // the 4 largest of two descending lists: max(a_i, b_{3-i}) is bitonic
+#pragma unroll
+    for (int i = 0; i < 4; ++i) k[i] = max(k[i], k[7 - i]);
+    bitonic_desc<4>(k);
+  } else {
+    uint32_t t[8] = {k[0], k[1], k[2], k[3], k[7], k[6], k[5], k[4]};   // down then up
+    bitonic_desc<8>(t);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) k[i] = t[i];
+  }
+}
+
+// run = the DEPTH largest of two descending lists run, g.
+template <int DEPTH>
+__device__ __forceinline__ void merge_top(uint32_t* run, const uint32_t* g) {
+#pragma unroll
+  for (int i = 0; i < DEPTH; ++i) run[i] = max(run[i], g[DEPTH - 1 - i]);
+  bitonic_desc<DEPTH>(run);
+}
+
+// ------------------------------------------------------------------------------ quant-pack
+template <int BITS, int UPL, int DEPTH>
+__global__ void __launch_bounds__(kThreads, 3) quant_pack_side_kernel(const SideArgs a) {
   constexpr int kQm = SymQ<BITS>::kQmax;
   constexpr int kB = SymQ<BITS>::kBias;
   constexpr int kM = SymQ<BITS>::kMask;
-  const int t = blockIdx.y;
-  const PoolRef pool = a.pool[t];
-  const SideRef sd = a.side[t];
   const int lane = threadIdx.x & 31;
-  const int rows = a.total_tokens * a.H;
-  const bool live = 8 * lane < a.D;
-  const int n_blocks = (rows + 31) / 32;
-  for (int blk = blockIdx.x * kWarps + (threadIdx.x >> 5); blk < n_blocks;
-       blk += gridDim.x * kWarps) {
-    // lane i locates row 32 * blk + i; the warp then walks the 32 rows
-    int my_s = 0;
-    int64_t my_pos = 0, my_prow = -1;
-    if (32 * blk + lane < rows)
-      my_prow = row_place(a, pool.num_pages, 32 * blk + lane, my_s, my_pos);
-    const int nr = min(32, rows - 32 * blk);
-    for (int i = 0; i < nr; ++i) {
-      const int r = 32 * blk + i;
-      const int64_t prow = shfl_i64(my_prow, i);
-      if (prow < 0) continue;   // warp-uniform
-      const int s = __shfl_sync(kFullMask, my_s, i);
-      const int64_t pos = shfl_i64(my_pos, i);
-      const int h = r % a.H;
-      uint4 xv = make_uint4(0, 0, 0, 0);
-      if (live) xv = ld_stream_v4(a.x[t] + static_cast<int64_t>(r) * a.D + 8 * lane);
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-      uint32_t key[8];
+  const int lpr = 1 << a.lpr_log2;
+  const int rps = 32 >> a.lpr_log2;
+  const int lr = lane & (lpr - 1);
+  const int sub = lane >> a.lpr_log2;
+  const int H = a.H, D = a.D, k = a.k;
+  const int n_items = (a.total_tokens + kTok - 1) / kTok;
+  const int64_t n_work = static_cast<int64_t>(a.n_tensors) * n_items;
+  const int n_warps = gridDim.x * kWarps;
+
+  for (int64_t g = blockIdx.x * kWarps + (threadIdx.x >> 5); g < n_work; g += n_warps) {
+    const int t = static_cast<int>(g / n_items);
+    const int item = static_cast<int>(g - static_cast<int64_t>(t) * n_items);
+    const uint16_t* __restrict__ x = a.x[t];
+    const PoolRef pool = a.pool[t];
+    const SideRef sd = a.side[t];
+    const int tok0 = item * kTok;
+    const int ntok = min(kTok, a.total_tokens - tok0);
+    long long base = -1;
+    int my_s = 0, my_pos = 0;
+    if (lane < ntok) base = token_place(a, pool.num_pages, tok0 + lane, my_s, my_pos);
+    const int nrows = ntok * H;
+    const uint16_t* xi = x + static_cast<int64_t>(tok0) * H * D;
+    for (int r0 = 0; r0 < nrows; r0 += rps * kQU) {
+      uint4 v[kQU][UPL][2];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint32_t bits = (xw[e >> 1] >> (16 * (e & 1))) & 0xffffu;
-        key[e] = live ? ((((bits & 0x7fffu) << 8) | (255u - (8 * lane + e))) + 1u) : 0u;
-      }
-      // k rounds of a warp max pick the outliers (lane j keeps the j-th), round k the dense amax
-      uint32_t my_opos = 0xffffu, my_oval = 0;
-      float amax = 0.f;
-      for (int j = 0; j <= a.k; ++j) {
-        uint32_t m = key[0];
+      for (int u = 0; u < kQU; ++u) {
+        const int row = r0 + u * rps + sub;
 #pragma unroll
-        for (int e = 1; e < 8; ++e) m = max(m, key[e]);
-        const uint32_t w = __reduce_max_sync(kFullMask, m);
-        if (j == a.k) {
-          amax = (w == 0u) ? 0.f : h2f(static_cast<uint16_t>((w - 1u) >> 8));
-          break;
-        }
-        uint32_t v = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (key[e] == w) {
-            v = (xw[e >> 1] >> (16 * (e & 1))) & 0xffffu;
-            key[e] = 0u;   // taken: it also leaves the dense row
+        for (int j = 0; j < UPL; ++j) {
+          const int e0 = (lr + j * lpr) * 16;
+          v[u][j][0] = v[u][j][1] = make_uint4(0, 0, 0, 0);
+          if (row < nrows && e0 < D) {
+            const uint16_t* src = xi + static_cast<int64_t>(row) * D + e0;
+            v[u][j][0] = ld_stream_v4(src);
+            v[u][j][1] = ld_stream_v4(src + 8);
           }
         }
-        const uint32_t val = __reduce_or_sync(kFullMask, v);
-        if (lane == j) {
-          my_opos = 255u - ((w - 1u) & 0xffu);
-          my_oval = val;
-        }
       }
-      const uint16_t sbits = f2h(row_scale_f32<kQm>(amax));
-      const float sc = h2f(sbits);
-      const float y = (sc == 0.f) ? 0.f : __frcp_rn(sc);
-      const float se = (sc == 0.f) ? 1.f : sc;
-      const bool clip = sc < 6.103515625e-05f;   // 2^-14, smallest normal fp16
-      if (live) {
-        uint32_t f[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const bool dense = key[e] != 0u;
-          const float xe = dense ? h2f(static_cast<uint16_t>(xw[e >> 1] >> (16 * (e & 1)))) : 0.f;
-          f[e] = quant_field<kQm, kB, kM>(xe, se, y, clip);
+      for (int u = 0; u < kQU; ++u) {
+        const int row = r0 + u * rps + sub;
+        const int kt = row / H;
+        const int src = kt < kTok ? kt : 0;
+        const long long b = shfl_ll(base, src);
+        const int s = __shfl_sync(kFullMask, my_s, src);
+        const int pos = __shfl_sync(kFullMask, my_pos, src);
+        // the lane's DEPTH largest keys
+        uint32_t top[DEPTH];
+#pragma unroll
+        for (int i = 0; i < DEPTH; ++i) top[i] = 0u;
+#pragma unroll
+        for (int j = 0; j < UPL; ++j) {
+          const int unit = lr + j * lpr;
+          if (unit * 16 >= D) continue;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t g[8];
+            keys8(v[u][j][hh], 255u - static_cast<uint32_t>(16 * unit + 8 * hh), g);
+            top_of8<DEPTH>(g);
+            if (j == 0 && hh == 0) {
+#pragma unroll
+              for (int i = 0; i < DEPTH; ++i) top[i] = g[i];
+            } else {
+              merge_top<DEPTH>(top, g);
+            }
+          }
         }
-        uint32_t pa, pb;
-        pack8<BITS>(f, pa, pb);
-        store_lane<BITS>(pool.codes + prow * a.pd + lane * lane_bytes<BITS>(), pa, pb);
-      }
-      if (lane == 0) pool.scales[prow] = sbits;
-      if (a.k > 0) {
-        // ascending positions: lane j < k stores its outlier at its rank among the k positions
-        uint32_t rank = 0;
-        for (int j = 0; j < a.k; ++j) rank += __shfl_sync(kFullMask, my_opos, j) < my_opos ? 1u : 0u;
-        if (lane < a.k) {
-          sd.out_idx[prow * a.k + rank] = static_cast<uint8_t>(my_opos);
-          sd.out_val[prow * a.k + rank] = static_cast<uint16_t>(my_oval);
+        // k + 1 rounds of a max over the row's lanes (all lanes take part in the shuffles)
+        uint32_t okey[KVQ_MAX_OUTLIERS];
+        uint32_t thr = 0u, last = 0u;
+#pragma unroll
+        for (int j = 0; j <= KVQ_MAX_OUTLIERS; ++j) {
+          if (j > k) break;
+          uint32_t m = top[0];
+          if (j >= DEPTH && j == k) {
+            // this lane may have given all DEPTH listed keys: its largest key below the last
+            // outlier's, rebuilt from the elements
+            m = 0u;
+#pragma unroll
+            for (int jj = 0; jj < UPL; ++jj) {
+              const int unit = lr + jj * lpr;
+              if (unit * 16 >= D) continue;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                uint32_t g[8];
+                keys8(v[u][jj][hh], 255u - static_cast<uint32_t>(16 * unit + 8 * hh), g);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) m = max(m, g[e] < last ? g[e] : 0u);
+              }
+            }
+          }
+#pragma unroll
+          for (int o = 4; o >= 1; o >>= 1)
+            if (o < lpr) m = max(m, __shfl_xor_sync(kFullMask, m, o));
+          if (j == k) {
+            thr = m;
+            break;
+          }
+          if (j < KVQ_MAX_OUTLIERS) okey[j] = m;
+          last = m;
+          const bool pop = top[0] == m;
+#pragma unroll
+          for (int i = 0; i + 1 < DEPTH; ++i) top[i] = pop ? top[i + 1] : top[i];
+          top[DEPTH - 1] = pop ? 0u : top[DEPTH - 1];
+        }
+        if (row >= nrows || b < 0) continue;
+        const int h = row - kt * H;
+        const int64_t prow = b + static_cast<int64_t>(h) * a.page_size;
+        const uint32_t T = thr >> 8;   // the dense row's amax, fp16 bits
+        const bool tie = k > 0 && (last >> 8) == T;
+        const uint16_t sbits = f2h(row_scale_f32<kQm>(h2f(static_cast<uint16_t>(T))));
+        const float sc = h2f(sbits);
+        const float y = (sc == 0.f) ? 0.f : __frcp_rn(sc);
+        const float se = (sc == 0.f) ? 1.f : sc;
+        const bool clip = sc < 6.103515625e-05f;   // 2^-14, smallest normal fp16
+        const uint32_t T2 = T | (T << 16);
+        uint8_t* crow = pool.codes + prow * a.pd;
+        auto units = [&](auto clip_tag) {
+          constexpr bool kClip = decltype(clip_tag)::value;
+#pragma unroll
+          for (int j = 0; j < UPL; ++j) {
+            const int unit = lr + j * lpr;
+            if (unit * 16 >= D) continue;
+            uint32_t pk[4];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint4& vv = v[u][j][hh];
+              uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+              // zero the outliers: |x| > T, or (tie at T) key > thr
+              if (!tie) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const uint32_t m = w[i] & 0x7fff7fffu;
+                  const uint32_t gt = __hgt2_mask(*reinterpret_cast<const __half2*>(&m),
+                                                  *reinterpret_cast<const __half2*>(&T2));
+                  w[i] &= ~gt;
+                }
+              } else {
+                uint32_t g[8];
+                keys8(vv, 255u - static_cast<uint32_t>(16 * unit + 8 * hh), g);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  w[i] &= (g[2 * i] > thr ? 0xffff0000u : 0xffffffffu) &
+                          (g[2 * i + 1] > thr ? 0x0000ffffu : 0xffffffffu);
+              }
+              uint32_t f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float xe = h2f(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
+                f[e] = quant_field_c<kQm, kB, kM, kClip>(xe, se, y);
+              }
+              pack8<BITS>(f, pk[2 * hh], pk[2 * hh + 1]);
+            }
+            store_unit<BITS>(crow + unit * SymQ<BITS>::kUnitBytes, pk[0], pk[1], pk[2], pk[3]);
+          }
+        };
+        if (clip) units(std::true_type{});
+        else units(std::false_type{});
+        if (lr == 0) pool.scales[prow] = sbits;
+        // outliers, ascending by position: lane j of the row stores the j-th largest key at its
+        // rank among the k positions (a larger low byte = a lower position)
+        for (int j = lr; j < k; j += lpr) {
+          uint32_t kj = 0u;
+#pragma unroll
+          for (int i = 0; i < KVQ_MAX_OUTLIERS; ++i)
+            if (i == j) kj = okey[i];
+          uint32_t rank = 0;
+#pragma unroll
+          for (int i = 0; i < KVQ_MAX_OUTLIERS; ++i)
+            if (i < k) rank += (okey[i] & 0xffu) > (kj & 0xffu) ? 1u : 0u;
+          const uint32_t p = 255u - (kj & 0xffu);
+          const uint16_t val = __ldg(xi + static_cast<int64_t>(row) * D + p);
+          sd.out_idx[prow * k + rank] = static_cast<uint8_t>(p);
+          sd.out_val[prow * k + rank] = val;
+        }
+        if (pos < a.n_sink) {
+          uint16_t* dst = sd.sink + ((static_cast<int64_t>(s) * a.n_sink + pos) * H + h) * D;
+#pragma unroll
+          for (int j = 0; j < UPL; ++j) {
+            const int e0 = (lr + j * lpr) * 16;
+            if (e0 >= D) continue;
+            *reinterpret_cast<uint4*>(dst + e0) = v[u][j][0];
+            *reinterpret_cast<uint4*>(dst + e0 + 8) = v[u][j][1];
+          }
         }
       }
-      if (pos < a.n_sink && live)
-        *reinterpret_cast<uint4*>(sd.sink + ((static_cast<int64_t>(s) * a.n_sink + pos) * a.H + h) *
-                                                a.D + 8 * lane) = xv;
     }
   }
 }
 
-template <int BITS>
+// -------------------------------------------------------------------------------- dequant
+// The plain dequant kernel's layout and arithmetic (fp16(c * scale), one rounding); then, after a
+// warp barrier that orders the stores, the row's lane j < k writes outlier j over its position.
+// Rows at positions < n_sink are copied from the sink buffer instead.
+template <int BITS, int UPL>
 __global__ void __launch_bounds__(kThreads) dequant_side_kernel(const SideArgs a) {
-  constexpr int kB = SymQ<BITS>::kBias;
-  constexpr uint32_t kM = SymQ<BITS>::kMask;
-  const int t = blockIdx.y;
-  uint16_t* out = const_cast<uint16_t*>(a.x[t]);
-  const PoolRef pool = a.pool[t];
-  const SideRef sd = a.side[t];
   const int lane = threadIdx.x & 31;
-  const int rows = a.total_tokens * a.H;
-  const bool live = 8 * lane < a.D;
-  const int n_blocks = (rows + 31) / 32;
-  for (int blk = blockIdx.x * kWarps + (threadIdx.x >> 5); blk < n_blocks;
-       blk += gridDim.x * kWarps) {
-    int my_s = 0;
-    int64_t my_pos = 0, my_prow = -1;
-    if (32 * blk + lane < rows)
-      my_prow = row_place(a, pool.num_pages, 32 * blk + lane, my_s, my_pos);
-    const int nr = min(32, rows - 32 * blk);
-    for (int i = 0; i < nr; ++i) {
-      const int r = 32 * blk + i;
-      const int64_t prow = shfl_i64(my_prow, i);
-      if (prow < 0) continue;   // warp-uniform
-      const int s = __shfl_sync(kFullMask, my_s, i);
-      const int64_t pos = shfl_i64(my_pos, i);
-      if (!live) continue;
-      const int h = r % a.H;
-      uint4 res;
-      if (pos < a.n_sink) {
-        res = *reinterpret_cast<const uint4*>(
-            sd.sink + ((static_cast<int64_t>(s) * a.n_sink + pos) * a.H + h) * a.D + 8 * lane);
-      } else {
-        const uint64_t fw = load_lane<BITS>(pool.codes + prow * a.pd + lane * lane_bytes<BITS>());
-        const float sc = h2f(pool.scales[prow]);
-        uint32_t o[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint32_t fld = static_cast<uint32_t>(fw >> (BITS * e)) & kM;
-          const int c = (BITS == 8) ? static_cast<int>(static_cast<int8_t>(fld))
-                                    : static_cast<int>(fld) - kB;
-          o[e] = f2h(static_cast<float>(c) * sc);   // exact product, one rounding to fp16
-        }
-        for (int j = 0; j < a.k; ++j) {
-          const uint32_t d = sd.out_idx[prow * a.k + j];
-          const uint32_t v = sd.out_val[prow * a.k + j];
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (d == static_cast<uint32_t>(8 * lane + e)) o[e] = v;
-        }
-        res = make_uint4(o[0] | (o[1] << 16), o[2] | (o[3] << 16), o[4] | (o[5] << 16),
-                         o[6] | (o[7] << 16));
-      }
-      *reinterpret_cast<uint4*>(out + static_cast<int64_t>(r) * a.D + 8 * lane) = res;
+  const int lpr = 1 << a.lpr_log2;
+  const int rps = 32 >> a.lpr_log2;
+  const int lr = lane & (lpr - 1);
+  const int sub = lane >> a.lpr_log2;
+  const int H = a.H, D = a.D, k = a.k;
+  const int n_items = (a.total_tokens + kTok - 1) / kTok;
+  const int64_t n_work = static_cast<int64_t>(a.n_tensors) * n_items;
+  const int n_warps = gridDim.x * kWarps;
+
+  for (int64_t g = blockIdx.x * kWarps + (threadIdx.x >> 5); g < n_work; g += n_warps) {
+    const int t = static_cast<int>(g / n_items);
+    const int item = static_cast<int>(g - static_cast<int64_t>(t) * n_items);
+    uint16_t* __restrict__ out = const_cast<uint16_t*>(a.x[t]);
+    const PoolRef pool = a.pool[t];
+    const SideRef sd = a.side[t];
+    const int tok0 = item * kTok;
+    const int ntok = min(kTok, a.total_tokens - tok0);
+    long long base = -1, sink_row = -1;   // sink_row: index of head 0's row in the sink buffer
+    if (lane < ntok) {
+      int s, pos;
+      base = token_place(a, pool.num_pages, tok0 + lane, s, pos);
+      if (pos < a.n_sink) sink_row = (static_cast<long long>(s) * a.n_sink + pos) * H;
     }
+    const int nrows = ntok * H;
+    uint16_t* oi = out + static_cast<int64_t>(tok0) * H * D;
+    for (int r0 = 0; r0 < nrows; r0 += rps * kDU) {
+      uint32_t w[kDU][UPL][4];
+      uint32_t sc[kDU], ov[kDU];   // scale; outlier lr: position | value << 16
+      bool act[kDU], dense[kDU];
+#pragma unroll
+      for (int u = 0; u < kDU; ++u) {
+        const int row = r0 + u * rps + sub;
+        const int kt = row / H;
+        const int src = kt < kTok ? kt : 0;
+        const long long b = shfl_ll(base, src);
+        const bool snk = __shfl_sync(kFullMask, static_cast<int>(sink_row >= 0), src) != 0;
+        act[u] = row < nrows && b >= 0;
+        dense[u] = act[u] && !snk;
+        sc[u] = ov[u] = 0;
+#pragma unroll
+        for (int j = 0; j < UPL; ++j) w[u][j][0] = w[u][j][1] = w[u][j][2] = w[u][j][3] = 0;
+        if (dense[u]) {
+          const int64_t prow = b + static_cast<int64_t>(row - kt * H) * a.page_size;
+          const uint8_t* crow = pool.codes + prow * a.pd;
+#pragma unroll
+          for (int j = 0; j < UPL; ++j) {
+            const int unit = lr + j * lpr;
+            if (unit * 16 < D) load_unit<BITS>(crow + unit * SymQ<BITS>::kUnitBytes, w[u][j]);
+          }
+          sc[u] = ld_nc_u16(pool.scales + prow);
+          if (lr < k)
+            ov[u] = __ldg(sd.out_idx + prow * k + lr) |
+                    (static_cast<uint32_t>(ld_nc_u16(sd.out_val + prow * k + lr)) << 16);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kDU; ++u) {
+        const int row = r0 + u * rps + sub;
+        const int kt = row / H;
+        const long long srow = shfl_ll(sink_row, kt < kTok ? kt : 0);
+        if (!act[u]) continue;
+        uint16_t* orow = oi + static_cast<int64_t>(row) * D;
+        if (!dense[u]) {
+          const uint16_t* sp = sd.sink + (srow + (row - kt * H)) * D;
+#pragma unroll
+          for (int j = 0; j < UPL; ++j) {
+            const int e0 = (lr + j * lpr) * 16;
+            if (e0 >= D) continue;
+            *reinterpret_cast<uint4*>(orow + e0) = ld_nc_v4(sp + e0);
+            *reinterpret_cast<uint4*>(orow + e0 + 8) = ld_nc_v4(sp + e0 + 8);
+          }
+          continue;
+        }
+        const uint32_t s2 = sc[u] | (sc[u] << 16);
+#pragma unroll
+        for (int j = 0; j < UPL; ++j) {
+          const int unit = lr + j * lpr;
+          if (unit * 16 >= D) continue;
+          uint32_t p[4], q[4];
+          unpack_group<BITS, 0>(w[u][j], p);
+          unpack_group<BITS, 1>(w[u][j], q);
+          const uint4 o0 = make_uint4(hmul2u(prmt(p[0], p[1], 0x5410u), s2),
+                                      hmul2u(prmt(p[2], p[3], 0x5410u), s2),
+                                      hmul2u(prmt(p[0], p[1], 0x7632u), s2),
+                                      hmul2u(prmt(p[2], p[3], 0x7632u), s2));
+          const uint4 o1 = make_uint4(hmul2u(prmt(q[0], q[1], 0x5410u), s2),
+                                      hmul2u(prmt(q[2], q[3], 0x5410u), s2),
+                                      hmul2u(prmt(q[0], q[1], 0x7632u), s2),
+                                      hmul2u(prmt(q[2], q[3], 0x7632u), s2));
+          *reinterpret_cast<uint4*>(orow + unit * 16) = o0;
+          *reinterpret_cast<uint4*>(orow + unit * 16 + 8) = o1;
+        }
+      }
+      // the dense stores of every lane come before the outlier stores over them
+      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < kDU; ++u) {
+        const int row = r0 + u * rps + sub;
+        uint16_t* orow = oi + static_cast<int64_t>(row) * D;
+        if (dense[u] && lr < k) {
+          const uint32_t d = ov[u] & 0xffu;
+          if (d < static_cast<uint32_t>(D)) orow[d] = static_cast<uint16_t>(ov[u] >> 16);
+        }
+        if (k > lpr) {   // more outliers than lanes per row (short rows): lane lr also takes lr + lpr, ...
+          const int kt = row / H;
+          const long long b = shfl_ll(base, kt < kTok ? kt : 0);
+          if (dense[u]) {
+            const int64_t prow = b + static_cast<int64_t>(row - kt * H) * a.page_size;
+            for (int j = lr + lpr; j < k; j += lpr) {
+              const uint32_t d = __ldg(sd.out_idx + prow * k + j);
+              if (d < static_cast<uint32_t>(D)) orow[d] = ld_nc_u16(sd.out_val + prow * k + j);
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+// Persistent 1-D grid over all (tensor, token block) work items: at most the blocks that are
+// resident on the SMs at once, so no block waits for a second wave.
+template <typename K>
+unsigned side_grid(K kernel, int& cache, int n_tensors, int total_tokens) {
+  if (cache == 0) {
+    int b = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0);
+    cache = (e != cudaSuccess || b < 1) ? 1 : b;
+  }
+  const int64_t items = (static_cast<int64_t>(total_tokens) + kTok - 1) / kTok * n_tensors;
+  const int64_t need = (items + kWarps - 1) / kWarps;
+  const int sms = sm_count();
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * cache;
+  return static_cast<unsigned>(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
+template <int BITS, int UPL, int DEPTH>
+void launch_quant(const SideArgs& a, cudaStream_t cs) {
+  static int cache = 0;
+  auto kern = quant_pack_side_kernel<BITS, UPL, DEPTH>;
+  kern<<<side_grid(kern, cache, a.n_tensors, a.total_tokens), kThreads, 0, cs>>>(a);
+}
+
+template <int BITS, int UPL>
+void launch_dequant(const SideArgs& a, cudaStream_t cs) {
+  static int cache = 0;
+  auto kern = dequant_side_kernel<BITS, UPL>;
+  kern<<<side_grid(kern, cache, a.n_tensors, a.total_tokens), kThreads, 0, cs>>>(a);
+}
+
+template <int BITS>
+void launch_side(bool quant, const SideArgs& a, cudaStream_t cs) {
+  const int upl = (a.units + (1 << a.lpr_log2) - 1) >> a.lpr_log2;   // 1 or 2 for D <= 256
+  if (quant) {
+    const bool deep = a.k > 3;
+    if (upl == 1) deep ? launch_quant<BITS, 1, 8>(a, cs) : launch_quant<BITS, 1, 4>(a, cs);
+    else deep ? launch_quant<BITS, 2, 8>(a, cs) : launch_quant<BITS, 2, 4>(a, cs);
+  } else {
+    upl == 1 ? launch_dequant<BITS, 1>(a, cs) : launch_dequant<BITS, 2>(a, cs);
   }
 }
 
@@ -318,26 +579,14 @@ kvq_status side_call(bool quant, const kvq_pool* pools, const kvq_side* sides,
   a.nseq = nseq;
   a.k = sides[0].n_outlier;
   a.n_sink = sides[0].n_sink;
-  const int sms = sm_count() > 0 ? sm_count() : 152;
-  const int64_t rows = static_cast<int64_t>(total) * a.H;
-  int64_t blocks = ((rows + 31) / 32 + kWarps - 1) / kWarps;
-  const int64_t cap = (8LL * sms + n_tensors - 1) / n_tensors;
-  if (blocks > cap) blocks = cap;
-  const dim3 grid(static_cast<unsigned>(blocks), n_tensors);
+  a.units = p0.head_dim / 16;
+  a.lpr_log2 = 0;
+  while ((1 << a.lpr_log2) < a.units && a.lpr_log2 < 3) ++a.lpr_log2;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   switch (p0.bits) {
-    case 8:
-      if (quant) quant_pack_side_kernel<8><<<grid, kThreads, 0, cs>>>(a);
-      else dequant_side_kernel<8><<<grid, kThreads, 0, cs>>>(a);
-      break;
-    case 6:
-      if (quant) quant_pack_side_kernel<6><<<grid, kThreads, 0, cs>>>(a);
-      else dequant_side_kernel<6><<<grid, kThreads, 0, cs>>>(a);
-      break;
-    default:
-      if (quant) quant_pack_side_kernel<4><<<grid, kThreads, 0, cs>>>(a);
-      else dequant_side_kernel<4><<<grid, kThreads, 0, cs>>>(a);
-      break;
+    case 8: launch_side<8>(quant, a, cs); break;
+    case 6: launch_side<6>(quant, a, cs); break;
+    default: launch_side<4>(quant, a, cs); break;
   }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "%s launch: %s", fn, cudaGetErrorString(e));

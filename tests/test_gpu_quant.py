@@ -3,13 +3,16 @@
 Codes, scales and dequantized fp16 must be identical (the arithmetic is fixed: IEEE float32
 divide, round-half-even, fp16 rounding).  Small cases span several tiles, ragged tails and the
 degenerate rows; the full-size prefill and decode-append workloads run in the launch
-configuration the benchmark times, checked on sampled rows (and on every appended row).
+configuration the benchmark times, checked on sampled rows (and on every appended row).  The
+full-size prefill test also runs kvq_decode_attn over the pools it wrote, in the benchmark's
+decode launch, against the oracle's attention on sampled (layer, sequence, head) triples.
 """
 import numpy as np
 import pytest
 import torch
 
 import kvgen
+from oracle import attention as oa
 from oracle import symmetric as osym
 from _gpu_util import (check_rows_against_oracle, cu_of, dev_tensor, i32, random_rows, u16)
 
@@ -159,6 +162,40 @@ def prefill_inputs(cuda_dev):
     torch.cuda.empty_cache()
 
 
+def _decode_on_prefill_pools(kvq, dev, w, specs, pools, pt, bits):
+    """kvq_decode_attn over the 16 packed layers, 8 sequences x 32,768 tokens, 24 query heads
+    (GQA 6:1), softmax scale 1/16 -- the decode launch the benchmark times on these pools --
+    against the oracle for sampled (layer, sequence, KV head) triples, within the decode
+    tolerance |got - ref| <= 2e-3 + 1e-3 |ref|; every output must be finite."""
+    H, D, nseq, ntok, L = w["H"], w["D"], w["n_seq"], w["n_tok"], w["n_layers"]
+    hq, G, scale = 24, 24 // w["H"], 1.0 / 16.0
+    q = kvgen.queries_torch(w["seed"], L, nseq, hq, D, dev)
+    out = torch.full((L, nseq, hq, D), float("nan"), dtype=torch.float32, device=dev)
+    ws = kvq.decode_workspace(pools[0::2], nseq, hq, ntok, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kvq.kvq_decode_attn(pools[0::2], pools[1::2], q, pt, i32([ntok] * nseq, dev), ntok, scale,
+                        out, ws, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    qn = q.cpu().numpy()
+    rng = np.random.default_rng(100 + bits)
+    triples = [(0, 0, 0), (L - 1, nseq - 1, H - 1)] + [
+        (int(rng.integers(L)), int(rng.integers(nseq)), int(rng.integers(H))) for _ in range(2)]
+    for layer, s, h in triples:
+        rows = (s * ntok + np.arange(ntok, dtype=np.int64)) * H + h
+        ks, vs = specs[2 * layer], specs[2 * layer + 1]
+        k_hat = osym.dequant_rows(*osym.quant_pack_rows(ks.rows_np(rows), bits), bits, D)
+        v_hat = osym.dequant_rows(*osym.quant_pack_rows(vs.rows_np(rows), bits), bits, D)
+        ref = oa.attend(qn[layer, s, h * G:(h + 1) * G], k_hat[:, None, :], v_hat[:, None, :],
+                        scale)
+        g = got[layer, s, h * G:(h + 1) * G]
+        bad = np.abs(g - ref) > 2e-3 + 1e-3 * np.abs(ref)
+        assert not bad.any(), (layer, s, h, float(np.abs(g - ref).max()))
+    del out, ws
+
+
 @pytest.mark.parametrize("bits", [8, 6, 4])
 def test_paged_prefill_full_size_sampled(kvq, cuda_dev, prefill_inputs, bits):
     """16 layers x {K,V} x 8 seqs x 32,768 tokens x 4 heads x 256, page 16, random table: one
@@ -183,6 +220,7 @@ def test_paged_prefill_full_size_sampled(kvq, cuda_dev, prefill_inputs, bits):
         tok, head = rows // H, rows % H
         seq, pos = tok // ntok, tok % ntok
         check_rows_against_oracle(pool, spec.rows_np(rows), pt_np, seq, pos, head, bits)
+    _decode_on_prefill_pools(kvq, cuda_dev, w, specs, pools, pt, bits)
     # dequant back (chunked in pairs of tensors to bound memory) and compare the sampled rows
     for i0 in range(0, len(xs), 8):
         outs = [torch.empty_like(xs[i]) for i in range(i0, i0 + 8)]
