@@ -100,9 +100,9 @@ template <int BITS> __host__ __device__ constexpr int tma_smem_bytes() {
 // Shared-memory layout of the staged kernel: the stage ring, the barriers and flags, and the query
 // B fragments every warp of the CTA shares (4 KB: 32 registers per thread saved).  With side
 // channels a stage also holds the tile's K and V outlier values (fp16 [16][k], 256 B reserved each)
-// and positions (uint8 [16][k], 128 B each); two stages per warp; then the warps' sparse output
-// accumulators (fp32 [8 heads][256]), the KV head's queries (fp16 [8][256]) and per-warp sink-row
-// weights (fp32 [16][8]).
+// and positions (uint8 [16][k], 128 B each); two stages per warp; then each warp's sparse residual
+// tile: fp16 [16 tokens][256] with a 528-byte row stride (conflict-free ldmatrix), all zero
+// between uses.
 template <int BITS, bool SIDE>
 struct Lay {
   static constexpr int kStages = SIDE ? 2 : Wd<BITS>::kStages;
@@ -113,10 +113,10 @@ struct Lay {
   static constexpr int kWarpBytes = kStages * kStage;
   static constexpr int kRing = kWarps * kWarpBytes;
   static constexpr int kQf = kRing + kWarps * kStages * 16;   // query B fragments [16][32] uint2
-  static constexpr int kOsp = kQf + 16 * 32 * 8;
-  static constexpr int kQs = kOsp + kWarps * 8 * kD * 4;
-  static constexpr int kPs = kQs + 8 * kD * 2;
-  static constexpr int kTotal = SIDE ? kPs + kWarps * 16 * 8 * 4 : kOsp;
+  static constexpr int kQfEnd = kQf + 16 * 32 * 8;
+  static constexpr int kOtStride = 2 * kD + 16;              // bytes per residual-tile row
+  static constexpr int kOt = kQfEnd;                         // residual tiles [warp][16][stride]
+  static constexpr int kTotal = SIDE ? kOt + kWarps * kTile * kOtStride : kQfEnd;
 };
 
 constexpr int kMergeBytes = kWarps * 8 * kD * 4 + 2 * kWarps * 8 * 4;
@@ -208,14 +208,14 @@ struct QFragSmem {
 };
 
 // With SIDE, kc[4] (same layout as the scores) is added after the row scale -- the outlier and
-// sink terms of the keys -- and p[4] and the rescale factors are returned for the side outputs.
+// sink terms of the keys -- and p[4] is returned for the value side terms.
 template <int BITS, bool SIDE = false, typename QF>
 __device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const QF& Q,
                                                 float (&acc)[16][4], float& m0, float& m1,
                                                 float& l0, float& l1, float qk_scale,
                                                 uint32_t& pb0, uint32_t& pb1,
-                                                const float* kc = nullptr, float* p_out = nullptr,
-                                                float* al_out = nullptr) {
+                                                const float* kc = nullptr,
+                                                float* p_out = nullptr) {
   // ---------------- S^T = C_K . Q^T on the exact integer codes (four independent accumulation
   // chains); each token row's fp16 scale multiplies its scores afterwards (the code-times-scale
   // products are exact instead of rounded to fp16 -- a difference far inside the tolerance)
@@ -281,8 +281,6 @@ __device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const QF& 
   if constexpr (SIDE) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) p_out[k] = p[k];
-    al_out[0] = al0;
-    al_out[1] = al1;
   }
 }
 
@@ -428,6 +426,68 @@ __device__ __forceinline__ void append_rows(const AttnArgs& a, const LayerPools&
 }
 
 // Side channels need more shared memory (2 CTAs per SM), so that variant may use more registers.
+// Column of element d in a residual tile.  Keys follow the score product's k-order: the dense
+// path's k-step 2*GI + h pairs, for thread c, elements 64c + 8*GI + {0, 4, 1, 5} (h = 0) or
+// {2, 6, 3, 7} (h = 1) at k = 2c, 2c+1, 2c+8, 2c+9.  Values follow the value product's m-order:
+// block 4*GI + k holds d = 32*m' + 8*GI + k at row m' and d + 4 at row m' + 8.
+template <bool KEY>
+__device__ __forceinline__ int side_col(int d) {
+  const int o = d & 7;
+  if constexpr (KEY)
+    return 16 * (2 * ((d & 63) >> 3) + ((o >> 1) & 1)) + 2 * (d >> 6) + ((o >> 2) & 1) +
+           8 * (o & 1);
+  else
+    return 16 * (4 * ((d & 31) >> 3) + (o & 3)) + (d >> 5) + 8 * (o >> 2);
+}
+
+// Write one tile's K or V side terms into the warp's residual tile: the outliers of every live
+// row that is not a sink (lanes 2r and 2r + 1 take row r's entries; positions are bytes, so always
+// < 256), and in the sequence's first tile the sink rows' exact fp16 rows from the sink buffer
+// [seq][n_sink][H][256].  The lane keeps the offsets it wrote in `at` (the stage may be refilled
+// before the tile is cleared).
+template <bool KEY>
+__device__ __forceinline__ void side_write(uint16_t* ot, const uint8_t* idx, const uint16_t* val,
+                                           int k, int n_sink, const uint16_t* sink, int s, int H,
+                                           int h, int tb, int len, int lane,
+                                           int (&at)[KVQ_MAX_OUTLIERS / 2]) {
+  constexpr int kRowH = (2 * kD + 16) / 2;   // halves per residual-tile row
+  const int row = lane >> 1;
+  const bool live = tb + row < len && tb + row >= n_sink;
+#pragma unroll
+  for (int i = 0; i < KVQ_MAX_OUTLIERS / 2; ++i) {
+    const int j = (lane & 1) + 2 * i;
+    at[i] = -1;
+    if (live && j < k) {
+      at[i] = row * kRowH + side_col<KEY>(idx[row * k + j]);
+      ot[at[i]] = val[row * k + j];
+    }
+  }
+  if (tb < n_sink) {   // only the first tile: n_sink <= 16 = kTile
+    const int nr = min(min(n_sink - tb, kTile), len - tb);
+    for (int e = lane; e < nr * kD; e += 32) {
+      const int r = e / kD, d = e - r * kD;
+      ot[r * kRowH + side_col<KEY>(d)] =
+          sink[((static_cast<int64_t>(s) * n_sink + tb + r) * H + h) * kD + d];
+    }
+  }
+}
+
+// Zero what side_write wrote.
+__device__ __forceinline__ void side_clear(uint16_t* ot, int n_sink, int tb, int len, int lane,
+                                           const int (&at)[KVQ_MAX_OUTLIERS / 2]) {
+  constexpr int kRowH = (2 * kD + 16) / 2;
+#pragma unroll
+  for (int i = 0; i < KVQ_MAX_OUTLIERS / 2; ++i)
+    if (at[i] >= 0) ot[at[i]] = 0;
+  if (tb < n_sink) {
+    const int nr = min(min(n_sink - tb, kTile), len - tb);
+    for (int e = lane; e < nr * kD; e += 32) {
+      const int r = e / kD;
+      ot[r * kRowH + (e - r * kD)] = 0;
+    }
+  }
+}
+
 template <int BITS, bool APPEND, bool SIDE>
 __global__ void __launch_bounds__(kThreads, SIDE ? 2 : (BITS == 8 ? 3 : 4)) decode_attn_tma_kernel(const AttnArgs a,
                                                                       const AttnSide sd) {
@@ -459,22 +519,14 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : (BITS == 8 ? 3 : 4)) deco
   uint8_t* wbase = smem + warp * Ly::kWarpBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kRing) + warp * S;
   int* flags = reinterpret_cast<int*>(smem + Ly::kRing + kWarps * S * 8) + warp * S;
-  float* osp = nullptr;          // SIDE: this warp's sparse output accumulator [8][256]
-  const uint16_t* qs = nullptr;  // SIDE: the KV head's queries, fp16 [8][256]
-  float* psk = nullptr;          // SIDE: sink-row weights [16][8]
+  // SIDE: this warp's residual tile (fp16 [16][256], stride Ly::kOtStride), zeroed once; each
+  // tile's side terms are written into it, consumed by tensor-core products and cleared again
+  uint16_t* ot = nullptr;
   if constexpr (SIDE) {
-    osp = reinterpret_cast<float*>(smem + Ly::kOsp) + warp * 8 * kD;
-    uint16_t* qw = reinterpret_cast<uint16_t*>(smem + Ly::kQs);
-    qs = qw;
-    psk = reinterpret_cast<float*>(smem + Ly::kPs) + warp * 16 * 8;
-    for (int i = threadIdx.x; i < 8 * kD / 8; i += kThreads) {
-      const int jh = i / (kD / 8), v = i - jh * (kD / 8);
-      uint4 x = make_uint4(0, 0, 0, 0);
-      if (jh < a.G) x = ld_nc_v4(a.q + ((static_cast<int64_t>(ls) * a.Hq) + h * a.G + jh) * kD + 8 * v);
-      reinterpret_cast<uint4*>(qw)[i] = x;
-    }
-    for (int i = lane; i < 8 * kD; i += 32) osp[i] = 0.f;
-    __syncthreads();
+    ot = reinterpret_cast<uint16_t*>(smem + Ly::kOt + warp * kTile * Ly::kOtStride);
+    for (int i = lane; i < kTile * Ly::kOtStride / 16; i += 32)
+      reinterpret_cast<uint4*>(ot)[i] = make_uint4(0, 0, 0, 0);
+    __syncwarp();
   }
 
   if (lane == 0) {
@@ -607,87 +659,33 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : (BITS == 8 ? 3 : 4)) deco
       }
     }
     uint32_t pb0, pb1;
+    float sp[4];   // SIDE: the tile's probabilities (unscaled), for the value side terms
+    int side_at[KVQ_MAX_OUTLIERS / 2];   // SIDE: residual-tile offsets this lane wrote
+    const bool side_work = SIDE && (sd.k > 0 || (tb == 0 && sd.n_sink > 0));   // warp-uniform
     if constexpr (SIDE) {
-      // key terms the codes do not carry: for a sink row the exact fp16 dot product (its dense
-      // scale was zeroed above), for any other row the outliers' q[pos] * value
-      float kc[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint16_t* kov = reinterpret_cast<const uint16_t*>(sk + Ly::kOffKov);
-      const uint8_t* koi = sk + Ly::kOffKoi;
-      const uint16_t* q0 = qs + (2 * c) * kD;
-      const uint16_t* q1 = q0 + kD;
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int row = g + 8 * r;
-        if (!K.kval[r]) continue;
-        float c0 = 0.f, c1 = 0.f;
-        if (tb + row < sd.n_sink) {
-          const uint16_t* kr = sd.ksink[layer] +
-                               ((static_cast<int64_t>(s) * sd.n_sink + tb + row) * a.H + h) * kD;
-          for (int d = 0; d < kD; d += 8) {
-            const uint4 kv = ld_nc_v4(kr + d);
-            const uint32_t kw4[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float kx = h2f(static_cast<uint16_t>(kw4[e >> 1] >> (16 * (e & 1))));
-              c0 = fmaf(h2f(q0[d + e]), kx, c0);
-              c1 = fmaf(h2f(q1[d + e]), kx, c1);
-            }
-          }
-        } else {
-          for (int jj = 0; jj < sd.k; ++jj) {
-            const int pos = koi[row * sd.k + jj];
-            const float v = h2f(kov[row * sd.k + jj]);
-            c0 = fmaf(h2f(q0[pos]), v, c0);
-            c1 = fmaf(h2f(q1[pos]), v, c1);
-          }
-        }
-        kc[2 * r] = c0;
-        kc[2 * r + 1] = c1;
-      }
-      float p[4], al[2];
-      tile_qk_softmax<BITS, true>(K, Q, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1, kc, p, al);
-      // the value terms the codes do not carry, into the warp's sparse accumulator (same
-      // running-max domain as acc: rescaled with it)
-      if (__any_sync(kFullMask, al[0] != 1.f || al[1] != 1.f)) {
-        float* o0 = osp + (2 * c) * kD + 32 * g;
-        float* o1 = o0 + kD;
-        for (int d = 0; d < 32; ++d) {
-          o0[d] *= al[0];
-          o1[d] *= al[1];
-        }
-      }
-      __syncwarp();
-      const uint16_t* vov = reinterpret_cast<const uint16_t*>(sk + Ly::kOffVov);
-      const uint8_t* voi = sk + Ly::kOffVoi;
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int row = g + 8 * r;
-        if (!K.kval[r] || tb + row < sd.n_sink) continue;
-        for (int jj = 0; jj < sd.k; ++jj) {
-          const int pos = voi[row * sd.k + jj];
-          const float v = h2f(vov[row * sd.k + jj]);
-          atomicAdd(osp + (2 * c) * kD + pos, p[2 * r] * v);
-          atomicAdd(osp + (2 * c + 1) * kD + pos, p[2 * r + 1] * v);
-        }
-      }
-      if (tb < sd.n_sink) {   // warp-uniform: the tile holds the sink rows
-        if (g < sd.n_sink) { psk[g * 8 + 2 * c] = p[0]; psk[g * 8 + 2 * c + 1] = p[1]; }
-        if (g + 8 < sd.n_sink) { psk[(g + 8) * 8 + 2 * c] = p[2]; psk[(g + 8) * 8 + 2 * c + 1] = p[3]; }
+      // Key terms the codes do not carry, as a tensor-core product with the query fragments: the
+      // outliers (q[pos] * value) and, for sink rows, the whole exact fp16 row (their dense scale
+      // is zeroed above).  Columns follow the dense path's MMA k-order.
+      float so[4] = {0.f, 0.f, 0.f, 0.f};
+      if (side_work) {
+        side_write<true>(ot, sk + Ly::kOffKoi, reinterpret_cast<const uint16_t*>(sk + Ly::kOffKov),
+                         sd.k, sd.n_sink, sd.ksink[layer], s, a.H, h, tb, len, lane, side_at);
         __syncwarp();
-        const int ns = min(sd.n_sink, len);
-        for (int d = lane; d < kD; d += 32) {
-          float add[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          for (int t = 0; t < ns; ++t) {
-            const float vx = h2f(sd.vsink[layer][((static_cast<int64_t>(s) * sd.n_sink + t) * a.H +
-                                                  h) * kD + d]);
+        const uint32_t ob = smem_u32(ot) + (lane & 15) * Ly::kOtStride + 16 * (lane >> 4);
 #pragma unroll
-            for (int hh = 0; hh < 8; ++hh) add[hh] = fmaf(psk[t * 8 + hh], vx, add[hh]);
-          }
-#pragma unroll
-          for (int hh = 0; hh < 8; ++hh) osp[hh * kD + d] += add[hh];
+        for (int ks = 0; ks < 16; ++ks) {
+          uint32_t af[4];
+          ldsm_x4(ob + 32 * ks, af);
+          const uint2 qb = Q.pair(ks);
+          mma16816(so, af[0], af[1], af[2], af[3], qb.x, qb.y);
         }
+        __syncwarp();
+        side_clear(ot, sd.n_sink, tb, len, lane, side_at);
+        __syncwarp();
+        side_write<false>(ot, sk + Ly::kOffVoi, reinterpret_cast<const uint16_t*>(sk + Ly::kOffVov),
+                          sd.k, sd.n_sink, sd.vsink[layer], s, a.H, h, tb, len, lane, side_at);
       }
-      __syncwarp();
+      tile_qk_softmax<BITS, true>(K, Q, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1, so, sp);
     } else {
       tile_qk_softmax<BITS>(K, Q, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1);
     }
@@ -720,6 +718,26 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : (BITS == 8 ? 3 : 4)) deco
       ++issued;
     }
     tile_pv<BITS>(V, pb0, pb1, acc);
+    if constexpr (SIDE) {
+      if (side_work) {
+        // value terms: O^T += R_V^T . P^T with the unscaled probabilities (the residual tile holds
+        // real fp16 values), into the same accumulators and running-max domain as the codes
+        __syncwarp();
+        const uint32_t pv0 = movtrans(pack_h2(sp[0], sp[1]));
+        const uint32_t pv1 = movtrans(pack_h2(sp[2], sp[3]));
+        const uint32_t ob = smem_u32(ot) + ((lane & 7) + 8 * (lane >> 4)) * Ly::kOtStride +
+                            16 * ((lane >> 3) & 1);
+#pragma unroll
+        for (int b = 0; b < 16; ++b) {
+          uint32_t af[4];
+          ldsm_x4_trans(ob + 32 * b, af);
+          mma16816(acc[b], af[0], af[1], af[2], af[3], pv0, pv1);
+        }
+        __syncwarp();
+        side_clear(ot, sd.n_sink, tb, len, lane, side_at);
+        __syncwarp();
+      }
+    }
   }
 
   if (timed_out) {
@@ -732,17 +750,6 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : (BITS == 8 ? 3 : 4)) deco
     }
     m0 = m1 = kNegInf;
     l0 = l1 = 0.f;
-  }
-  if constexpr (SIDE) {   // fold the warp's sparse accumulator into acc (the merge's layout)
-    __syncwarp();
-#pragma unroll
-    for (int mt = 0; mt < 16; ++mt) {
-      const int d = 32 * g + 8 * (mt >> 2) + (mt & 3);
-      acc[mt][0] += osp[(2 * c) * kD + d];
-      acc[mt][1] += osp[(2 * c + 1) * kD + d];
-      acc[mt][2] += osp[(2 * c) * kD + d + 4];
-      acc[mt][3] += osp[(2 * c + 1) * kD + d + 4];
-    }
   }
   __syncthreads();  // every warp is done with its stages: reuse them for the merge
   cta_merge_write(a, reinterpret_cast<float*>(smem), ls, h, split, warp, g, c, acc, m0, m1, l0,
