@@ -446,10 +446,11 @@ __device__ __forceinline__ int side_col(int d) {
 // [seq][n_sink][H][256].  The lane keeps the offsets it wrote in `at` (the stage may be refilled
 // before the tile is cleared).
 template <bool KEY>
-__device__ __forceinline__ void side_write(uint16_t* ot, const uint8_t* idx, const uint16_t* val,
-                                           int k, int n_sink, const uint16_t* sink, int s, int H,
-                                           int h, int tb, int len, int lane,
-                                           int (&at)[KVQ_MAX_OUTLIERS / 2]) {
+__device__ __forceinline__ void side_write(uint16_t* ot, const uint8_t* idx,
+                                               const uint16_t* val, int k, int n_sink,
+                                               const uint16_t* sink, int s, int H, int h, int tb,
+                                               int len, int lane,
+                                               int (&at)[KVQ_MAX_OUTLIERS / 2]) {
   constexpr int kRowH = (2 * kD + 16) / 2;   // halves per residual-tile row
   const int row = lane >> 1;
   const bool live = tb + row < len && tb + row >= n_sink;
@@ -458,7 +459,8 @@ __device__ __forceinline__ void side_write(uint16_t* ot, const uint8_t* idx, con
     const int j = (lane & 1) + 2 * i;
     at[i] = -1;
     if (live && j < k) {
-      at[i] = row * kRowH + side_col<KEY>(idx[row * k + j]);
+      const int col = side_col<KEY>(idx[row * k + j]);
+      at[i] = row * kRowH + col;
       ot[at[i]] = val[row * k + j];
     }
   }
@@ -672,13 +674,16 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : (BITS == 8 ? 3 : 4)) deco
                          sd.k, sd.n_sink, sd.ksink[layer], s, a.H, h, tb, len, lane, side_at);
         __syncwarp();
         const uint32_t ob = smem_u32(ot) + (lane & 15) * Ly::kOtStride + 16 * (lane >> 4);
+        float so4[4][4] = {};   // four independent accumulation chains
 #pragma unroll
         for (int ks = 0; ks < 16; ++ks) {
           uint32_t af[4];
           ldsm_x4(ob + 32 * ks, af);
           const uint2 qb = Q.pair(ks);
-          mma16816(so, af[0], af[1], af[2], af[3], qb.x, qb.y);
+          mma16816(so4[ks & 3], af[0], af[1], af[2], af[3], qb.x, qb.y);
         }
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) so[k4] = (so4[0][k4] + so4[1][k4]) + (so4[2][k4] + so4[3][k4]);
         __syncwarp();
         side_clear(ot, sd.n_sink, tb, len, lane, side_at);
         __syncwarp();
