@@ -425,7 +425,6 @@ __device__ __forceinline__ void append_rows(const AttnArgs& a, const LayerPools&
   }
 }
 
-// Side channels need more shared memory (2 CTAs per SM), so that variant may use more registers.
 // Column of element d in a residual tile.  Keys follow the score product's k-order: the dense
 // path's k-step 2*GI + h pairs, for thread c, elements 64c + 8*GI + {0, 4, 1, 5} (h = 0) or
 // {2, 6, 3, 7} (h = 1) at k = 2c, 2c+1, 2c+8, 2c+9.  Values follow the value product's m-order:
@@ -490,6 +489,7 @@ __device__ __forceinline__ void side_clear(uint16_t* ot, int n_sink, int tb, int
   }
 }
 
+// Side channels need more shared memory (2 CTAs per SM), so that variant may use more registers.
 template <int BITS, bool APPEND, bool SIDE>
 __global__ void __launch_bounds__(kThreads, SIDE ? 2 : (BITS == 8 ? 3 : 4)) decode_attn_tma_kernel(const AttnArgs a,
                                                                       const AttnSide sd) {
