@@ -166,11 +166,17 @@ __device__ __forceinline__ void cross_group(const uint32_t* wa, const uint32_t* 
     uint32_t pb[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) pb[b] = prmt(wa[GI], wb[GI], sel4(b, b, 4 + b, 4 + b));
+    // each 16-bit lane holds the byte twice: its low nibble at bits 0-3 (1024 + u) and its high
+    // nibble at bits 4-7 (1024 + 16u, scale 1/16) -- no shifts
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int m = 4 * (k & 1);
-      lo[k] = hfma2u(((pb[k >> 1] >> m) & 0x000F000Fu) | 0x64006400u, kH1, kHm1032);
-      hi[k] = hfma2u(((pb[2 + (k >> 1)] >> m) & 0x000F000Fu) | 0x64006400u, kH1, kHm1032);
+      if (k & 1) {
+        lo[k] = hfma2u((pb[k >> 1] & 0x00F000F0u) | 0x64006400u, kH16th, kHm72);
+        hi[k] = hfma2u((pb[2 + (k >> 1)] & 0x00F000F0u) | 0x64006400u, kH16th, kHm72);
+      } else {
+        lo[k] = hfma2u((pb[k >> 1] & 0x000F000Fu) | 0x64006400u, kH1, kHm1032);
+        hi[k] = hfma2u((pb[2 + (k >> 1)] & 0x000F000Fu) | 0x64006400u, kH1, kHm1032);
+      }
     }
   }
 }

@@ -92,6 +92,7 @@ constexpr uint32_t kHm1056 = 0xE420E420u;    // -1056 = -(1024 + 32)
 constexpr uint32_t kHm96 = 0xD600D600u;      // -96   = -(64 + 32)
 constexpr uint32_t kHm288 = 0xDC80DC80u;     // -288  = -(256 + 32)
 constexpr uint32_t kHm1032 = 0xE408E408u;    // -1032 = -(1024 + 8)
+constexpr uint32_t kHm72 = 0xD480D480u;      // -72   = -(64 + 8)
 constexpr uint32_t kHm1152 = 0xE480E480u;    // -1152 = -(1024 + 128)
 
 // Eight consecutive elements e0..e7 of a packed row -> four half2 holding the exact signed codes
@@ -113,10 +114,13 @@ __device__ __forceinline__ void unpack_group(const uint32_t* w, uint32_t p[4]) {
     p[2] = hfma2u((p2 & 0x03F003F0u) | 0x64006400u, kH16th, kHm96);            // 1024 + 16 u2
     p[3] = hfma2u(((p2 >> 8) & 0x00FC00FCu) | 0x64006400u, kHQuarter, kHm288); // 1024 + 4 u3
   } else if constexpr (BITS == 4) {
-    const uint32_t x = w[GI];  // nibble n = element n
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      p[k] = hfma2u(((x >> (4 * k)) & 0x000F000Fu) | 0x64006400u, kH1, kHm1032);
+    // nibble n = element n; nibbles 1 and 5 (3 and 7 after one shift) already sit at mantissa
+    // bits 4-7, where they read as 1024 + 16u (scale 1/16), so one shift serves all four pairs
+    const uint32_t x = w[GI], y = w[GI] >> 8;
+    p[0] = hfma2u((x & 0x000F000Fu) | 0x64006400u, kH1, kHm1032);      // 1024 + u
+    p[1] = hfma2u((x & 0x00F000F0u) | 0x64006400u, kH16th, kHm72);     // 1024 + 16 u
+    p[2] = hfma2u((y & 0x000F000Fu) | 0x64006400u, kH1, kHm1032);
+    p[3] = hfma2u((y & 0x00F000F0u) | 0x64006400u, kH16th, kHm72);
   } else {
     const uint32_t x = w[2 * GI], y = w[2 * GI + 1];  // int8 bytes e0..e3, e4..e7
 #pragma unroll
