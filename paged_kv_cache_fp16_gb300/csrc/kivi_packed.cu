@@ -280,9 +280,18 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t a) {
   return r;
 }
 
-// Exact fp16 codes {e_k, e_(k + 8)} of a word of sixteen 2-bit fields.
-__device__ __forceinline__ uint32_t code_pair2(uint32_t w, int k) {
-  return hfma2u(((w >> (2 * k)) & 0x00030003u) | 0x64006400u, kH1, 0xE400E400u);  // - 1024
+// Exact fp16 codes {e_k, e_(k + 8)} of a word of sixteen 2-bit fields, k = 0..7 (the callers
+// unroll k).  Fields 0-4 of each half already sit at mantissa bits 2k, 2k + 1 of fp16 1024, where
+// they read as 1024 + 4^k u, so one fp16 FMA with scale 4^-k and offset -1024 * 4^-k gives u
+// exactly; fields 5-7 are read the same way from w10 = w >> 10 (one shift per word).
+__device__ __forceinline__ uint32_t code_pair2(uint32_t w, uint32_t w10, int k) {
+  constexpr uint32_t kScale[5] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u,
+                                  0x1C001C00u};   // 1, 1/4, 1/16, 1/64, 1/256
+  constexpr uint32_t kOff[5] = {0xE400E400u, 0xDC00DC00u, 0xD400D400u, 0xCC00CC00u,
+                                0xC400C400u};     // -1024, -256, -64, -16, -4
+  const int j = k < 5 ? k : k - 5;
+  const uint32_t src = k < 5 ? w : w10;
+  return hfma2u((src & (0x00030003u << (2 * j))) | 0x64006400u, kScale[j], kOff[j]);
 }
 
 // One CTA: split `blockIdx.x` of KV head blockIdx.y of (layer, batch row) blockIdx.z, four warps.
@@ -423,8 +432,9 @@ __global__ void __launch_bounds__(kAThreads, 4) kivi_attn_kernel(const KAArgs a)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const uint32_t w = lds_u32(sb + (lt + g + 8 * r) * 16 + 4 * c);
+          const uint32_t w10 = w >> 10;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) kf[r][k] = hfma2u(code_pair2(w, k), ks2[k], kz2[k]);
+          for (int k = 0; k < 8; ++k) kf[r][k] = hfma2u(code_pair2(w, w10, k), ks2[k], kz2[k]);
         }
       } else {
 #pragma unroll
@@ -493,8 +503,9 @@ __global__ void __launch_bounds__(kAThreads, 4) kivi_attn_kernel(const KAArgs a)
                               (lds_u16(sb + kOffVS + ((ta + 1) * G + gi) * 2) << 16);
           const uint32_t z2 = lds_u16(sb + kOffVZ + (ta * G + gi) * 2) |
                               (lds_u16(sb + kOffVZ + ((ta + 1) * G + gi) * 2) << 16);
+          const uint32_t w10 = w >> 10;
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) vf[pr][jj] = hfma2u(code_pair2(w, jj), s2, z2);
+          for (int jj = 0; jj < 8; ++jj) vf[pr][jj] = hfma2u(code_pair2(w, w10, jj), s2, z2);
         }
       } else {
 #pragma unroll
