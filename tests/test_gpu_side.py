@@ -212,6 +212,46 @@ def test_decode_attn_side(kvq, cuda_dev, bits, k, n_sink, ps):
         _close(got[layer], ref)
 
 
+@pytest.mark.parametrize("bits", [6, 4])
+def test_decode_attn_side_stage_reuse(kvq, cuda_dev, bits):
+    """2 layers x 8 sequences x 4 KV heads of up to 2,048 tokens: the split sizing gives each
+    warp three or more tiles, so every stage is refilled by the copy engine while the residual
+    tile of its previous tile is still in use -- the side terms must not read the stage after
+    it is handed back.  Ragged lengths; every output checked against the oracle."""
+    H, G, D, L, ps, k, n_sink = 4, 6, 256, 2, 16, 3, 4
+    lens = [2048, 1900, 2047, 64, 2048, 1500, 1024, 2000]
+    nseq = len(lens)
+    starts = [0] * nseq
+    kps, vps, kss, vss, oks, ovs = [], [], [], [], [], []
+    pt_np = None
+    for layer in range(L):
+        pt_np, pools, sides, opools, osides = _setup(kvq, cuda_dev, bits, H, D, ps, k, n_sink,
+                                                     lens, starts, seed=3)
+        tot = int(sum(lens))
+        xs = [_rows(40 + layer, True, tot, H, D), _rows(40 + layer, False, tot, H, D)]
+        cu = cu_of(lens)
+        kvq.kvq_quant_pack_paged_side(pools, sides, [dev_tensor(x, cuda_dev) for x in xs],
+                                      i32(pt_np, cuda_dev), i32(cu, cuda_dev),
+                                      i32(starts, cuda_dev))
+        for x, osp in zip(xs, osides):
+            osd.quant_pack_paged_side(osp, x, pt_np, cu, np.asarray(starts))
+        kps.append(pools[0]); vps.append(pools[1]); kss.append(sides[0]); vss.append(sides[1])
+        oks.append(osides[0]); ovs.append(osides[1])
+    q = kvgen.queries_np(41, L, nseq, H * G, D)
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device=cuda_dev)
+    ws = kvq.decode_workspace(kps, nseq, H * G, max(lens), cuda_dev)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    kvq.kvq_decode_attn_side(kps, vps, kss, vss, dev_tensor(q, cuda_dev), i32(pt_np, cuda_dev),
+                             i32(lens, cuda_dev), max(lens), 1.0 / 16, out, ws, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    for layer in range(L):
+        ref = osd.decode_attention_paged_side(q[layer], oks[layer], ovs[layer], pt_np,
+                                              np.asarray(lens), 1.0 / 16)
+        _close(got[layer], ref)
+
+
 def test_decode_attn_side_full_size_sampled(kvq, cuda_dev):
     """The bench's decode shape with side channels: 16 layers, 8 sequences x 32,768 tokens, 4 KV
     heads x 256, 24 query heads, q6, page 16, 3 outliers per row, 4 sinks; sampled (layer,
