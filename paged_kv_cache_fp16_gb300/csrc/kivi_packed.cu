@@ -50,6 +50,7 @@ __device__ __forceinline__ __half2 as_h2(uint32_t w) { return *reinterpret_cast<
 // Group parameters as the pack uses them: zero, the stored fp16 scale and RN(1 / scale).
 struct GP {
   float z, s, y;
+  float t1, t2, t3;   // 2-bit fields: the thresholds of codes 1, 2, 3 on RN(x - zero)
 };
 
 __device__ __forceinline__ GP make_gp(float z, uint16_t s16) {
@@ -75,6 +76,29 @@ __device__ __forceinline__ uint32_t field(float x, const GP& g, float levels) {
   const float dist = fabsf(__fsub_rn(__fadd_rn(floorf(q), 0.5f), q));
   if (dist <= __fmul_rn(q, 9.5367431640625e-07f)) q = exact_quotient(d, g.s);  // 2^-20
   return static_cast<uint32_t>(fminf(fmaxf(rintf(q), 0.f), levels));
+}
+
+// 2-bit fields (levels = 3) as three compares.  With d = RN(x - zero) and q = RN(d / s), the code
+// clamp(rint_half_even(q), 0, 3) is >= 1 iff q > 0.5, >= 2 iff q >= 1.5, >= 3 iff q > 2.5, i.e.
+// (ties going to the even neighbour) iff the real quotient d / s exceeds 0.5 + 2^-25, reaches
+// 1.5 - 2^-24, exceeds 2.5 + 2^-23.  None of s * (0.5 + 2^-25), s * (1.5 - 2^-24),
+// s * (2.5 + 2^-23) is an fp32 value (the odd parts of the multipliers exceed 2^24), so each
+// condition is d >= RU(s * m), and one fused multiply-add rounded upward gives RU(s * m) exactly
+// from the exact power-of-two product s * 2^-k.  A zero scale gives code 0 everywhere.
+__device__ __forceinline__ void set_thresholds3(GP& g) {
+  if (g.s == 0.f) {
+    g.t1 = g.t2 = g.t3 = __int_as_float(0x7f800000);
+    return;
+  }
+  g.t1 = __fmaf_ru(g.s, 0.5f, g.s * 2.98023223876953125e-08f);      // s (0.5 + 2^-25)
+  g.t2 = __fmaf_ru(g.s, 1.5f, -(g.s * 5.9604644775390625e-08f));    // s (1.5 - 2^-24)
+  g.t3 = __fmaf_ru(g.s, 2.5f, g.s * 1.1920928955078125e-07f);       // s (2.5 + 2^-23)
+}
+
+__device__ __forceinline__ uint32_t field3(float x, const GP& g) {
+  const float d = __fsub_rn(x, g.z);
+  return static_cast<uint32_t>(d >= g.t1) + static_cast<uint32_t>(d >= g.t2) +
+         static_cast<uint32_t>(d >= g.t3);
 }
 
 // 8 fields of `bits` bits -> packed LSB-first (2 bits: 16 bits, 4 bits: 32 bits, 8: 64 bits).
@@ -155,6 +179,10 @@ __device__ void pack_keys_part(const KPArgs& a, int64_t first, int64_t stride) {
       const uint16_t s1 = scale16(z1, __high2float(mx[k]), a.levels, a.eps);
       gp[2 * k] = make_gp(z0, s0);
       gp[2 * k + 1] = make_gp(z1, s1);
+      if constexpr (BITS == 2) {
+        set_thresholds3(gp[2 * k]);
+        set_thresholds3(gp[2 * k + 1]);
+      }
       sw[k] = s0 | (static_cast<uint32_t>(s1) << 16);
       zw[k] = *reinterpret_cast<const uint32_t*>(&mn[k]);
     }
@@ -167,7 +195,8 @@ __device__ void pack_keys_part(const KPArgs& a, int64_t first, int64_t stride) {
       f8(src[static_cast<int64_t>(t) * row_v], x);
       uint32_t f[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = field(x[e], gp[e], a.levels);
+      for (int e = 0; e < 8; ++e)
+        f[e] = BITS == 2 ? field3(x[e], gp[e]) : field(x[e], gp[e], a.levels);
       store_fields8<BITS>(dst + static_cast<int64_t>(t) * cb, f);
     }
   }
@@ -205,7 +234,8 @@ __device__ void pack_values_part(const KPArgs& a, int64_t first, int64_t stride)
     }
     const float z = fminf(__low2float(mn), __high2float(mn));
     const uint16_t sb = scale16(z, fmaxf(__low2float(mx), __high2float(mx)), a.levels, a.eps);
-    const GP gp = make_gp(z, sb);
+    GP gp = make_gp(z, sb);
+    if constexpr (BITS == 2) set_thresholds3(gp);
     const int64_t pidx = (bh * S + t) * G + g;                      // params [B][H][S][G]
     C.v_scale[pidx] = sb;
     C.v_zero[pidx] = f2h(z);
@@ -217,7 +247,8 @@ __device__ void pack_values_part(const KPArgs& a, int64_t first, int64_t stride)
       f8(vv[k], x);
       uint32_t f[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = field(x[e], gp, a.levels);
+      for (int e = 0; e < 8; ++e)
+        f[e] = BITS == 2 ? field3(x[e], gp) : field(x[e], gp, a.levels);
       store_fields8<BITS>(dst + k * BITS, f);
     }
   }

@@ -30,8 +30,12 @@ def test_pack_bit_exact(kvq, cuda_dev, bits, gs, D):
     for layer in range(L):
         k, v = _layer(11, layer, B, H, S, D)
         k[0, 0, gs:2 * gs, 5] = 1.25            # a constant channel group (scale underflows to 0)
-        # exact ties (x - min) / scale = n + 1/2 under 2 bits: min 0, max 2.25, scale 0.75
-        ties = np.array([0.0, 2.25, 0.375, 1.125, 1.875, 0.75, 1.5], np.float16)
+        # exact ties (x - min) / scale = n + 1/2 under 2 bits: min 0, max 2.25, scale 0.75, and
+        # the fp16 neighbours on both sides of each tie
+        t3 = np.array([0.375, 1.125, 1.875], np.float16)
+        ties = np.concatenate([np.array([0.0, 2.25], np.float16), t3,
+                               np.nextafter(t3, np.float16(4)), np.nextafter(t3, np.float16(0)),
+                               np.array([0.75, 1.5], np.float16)])
         k[1, 1, gs:2 * gs, 7] = np.resize(ties, gs)
         v[1, 2, gs + 3, :gs] = np.resize(ties, gs)
         caches.append(kvq.KiviPacked.empty(bits, gs, B, H, S, D, cuda_dev))
