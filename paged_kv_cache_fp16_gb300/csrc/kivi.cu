@@ -20,7 +20,11 @@
 // y = RN(1 / scale), q0 = RN(d * y) is within 2.5 ulp of RN(d / scale); wherever q0 is farther
 // than |q0| * 2^-20 (> 8 ulp) from every half-integer both round to the same integer, so q0 is
 // used; otherwise (near or at a tie) the IEEE quotient is computed.  The result is identical to
-// dividing every element.
+// dividing every element.  With levels = 3 (2 bits) the code is three compares instead: it is
+// >= 1, 2, 3 iff d / scale exceeds 0.5 + 2^-25, reaches 1.5 - 2^-24, exceeds 2.5 + 2^-23 (ties
+// of RN(d / scale) at 0.5, 1.5, 2.5 go to the even neighbour), and since no scale * m is an
+// fp32 value (the multipliers' odd parts exceed 2^24) each condition is d >= RU(scale * m),
+// one upward-rounded FMA per group from the exact product scale * 2^-k.
 #include <cuda_runtime.h>
 
 #include "kvq_device.cuh"
@@ -45,14 +49,25 @@ struct KiviArgs {
 };
 
 struct Group {
-  float mn, sc, y;  // gmin, scale, RN(1 / scale)
+  float mn, sc, y;   // gmin, scale, RN(1 / scale)
+  float t1, t2, t3;  // levels = 3: thresholds of codes 1, 2, 3 on d = RN(x - gmin)
 };
 
+template <bool L3>
 __device__ __forceinline__ Group make_group(float mn, float mx, float levels, float eps) {
   Group g;
   g.mn = mn;
   g.sc = fmaxf(__fdiv_rn(__fsub_rn(mx, mn), levels), eps);
   g.y = __frcp_rn(g.sc);
+  if constexpr (L3) {
+    if (g.sc == 0.f) {   // eps = 0 and a constant group: every code is 0
+      g.t1 = g.t2 = g.t3 = __int_as_float(0x7f800000);
+    } else {
+      g.t1 = __fmaf_ru(g.sc, 0.5f, g.sc * 2.98023223876953125e-08f);    // sc (0.5 + 2^-25)
+      g.t2 = __fmaf_ru(g.sc, 1.5f, -(g.sc * 5.9604644775390625e-08f));  // sc (1.5 - 2^-24)
+      g.t3 = __fmaf_ru(g.sc, 2.5f, g.sc * 1.1920928955078125e-07f);     // sc (2.5 + 2^-23)
+    }
+  }
   return g;
 }
 
@@ -60,26 +75,34 @@ __device__ __forceinline__ Group make_group(float mn, float mx, float levels, fl
 // loops keeps the kernel's code small.
 __device__ __noinline__ float exact_quotient(float d, float sc) { return __fdiv_rn(d, sc); }
 
+template <bool L3>
 __device__ __forceinline__ uint16_t roundtrip(float x, const Group& g, float levels) {
   const float d = __fsub_rn(x, g.mn);
-  const float q0 = __fmul_rn(d, g.y);
-  const float dist = fabsf(__fsub_rn(__fadd_rn(floorf(q0), 0.5f), q0));
-  float q = q0;
-  if (dist <= __fmul_rn(q0, 9.5367431640625e-07f)) q = exact_quotient(d, g.sc);  // 2^-20
-  const float c = fminf(fmaxf(rintf(q), 0.f), levels);
+  float c;
+  if constexpr (L3) {
+    c = d >= g.t3 ? 3.f : (d >= g.t2 ? 2.f : (d >= g.t1 ? 1.f : 0.f));
+  } else {
+    const float q0 = __fmul_rn(d, g.y);
+    const float dist = fabsf(__fsub_rn(__fadd_rn(floorf(q0), 0.5f), q0));
+    float q = q0;
+    if (dist <= __fmul_rn(q0, 9.5367431640625e-07f)) q = exact_quotient(d, g.sc);  // 2^-20
+    c = fminf(fmaxf(rintf(q), 0.f), levels);
+  }
   return f2h(__fadd_rn(__fmul_rn(c, g.sc), g.mn));
 }
 
+template <bool L3>
 __device__ __forceinline__ uint32_t roundtrip2(uint32_t w, const Group& g0, const Group& g1,
                                                float levels) {
-  const uint32_t lo = roundtrip(h2f(static_cast<uint16_t>(w & 0xffffu)), g0, levels);
-  const uint32_t hi = roundtrip(h2f(static_cast<uint16_t>(w >> 16)), g1, levels);
+  const uint32_t lo = roundtrip<L3>(h2f(static_cast<uint16_t>(w & 0xffffu)), g0, levels);
+  const uint32_t hi = roundtrip<L3>(h2f(static_cast<uint16_t>(w >> 16)), g1, levels);
   return lo | (hi << 16);
 }
 
 __device__ __forceinline__ __half2 as_h2(uint32_t w) { return *reinterpret_cast<__half2*>(&w); }
 
 // ------------------------------------------------------------------------------ keys
+template <bool L3>
 __device__ __forceinline__ void keys_part(const KiviArgs& a, int64_t first, int64_t stride) {
   const int span = a.hi - a.lo;
   const int n_groups = (span + a.gs - 1) / a.gs;
@@ -122,17 +145,18 @@ __device__ __forceinline__ void keys_part(const KiviArgs& a, int64_t first, int6
       gmn = __hmin2(gmn, v);
       gmx = __hmax2(gmx, v);
     }
-    const Group g0 = make_group(__low2float(gmn), __low2float(gmx), a.levels, a.eps);
-    const Group g1 = make_group(__high2float(gmn), __high2float(gmx), a.levels, a.eps);
+    const Group g0 = make_group<L3>(__low2float(gmn), __low2float(gmx), a.levels, a.eps);
+    const Group g1 = make_group<L3>(__high2float(gmn), __high2float(gmx), a.levels, a.eps);
 #pragma unroll
     for (int r = 0; r < kKeepRows; ++r)
-      if (r < n) base[r * stride_w] = roundtrip2(keep[r], g0, g1, a.levels);
+      if (r < n) base[r * stride_w] = roundtrip2<L3>(keep[r], g0, g1, a.levels);
     for (int r = kKeepRows; r < n; ++r)
-      base[r * stride_w] = roundtrip2(base[r * stride_w], g0, g1, a.levels);
+      base[r * stride_w] = roundtrip2<L3>(base[r * stride_w], g0, g1, a.levels);
   }
 }
 
 // ------------------------------------------------------------------------------ values
+template <bool L3>
 __device__ __forceinline__ void values_part(const KiviArgs& a, int64_t first, int64_t stride) {
   const int span = a.hi - a.lo;
   const int groups = (a.D + a.gs - 1) / a.gs;
@@ -165,29 +189,33 @@ __device__ __forceinline__ void values_part(const KiviArgs& a, int64_t first, in
         mn[k] = __hmin2(mn[k], mn[k + w]);
         mx[k] = __hmax2(mx[k], mx[k + w]);
       }
-    const Group gr = make_group(fminf(__low2float(mn[0]), __high2float(mn[0])),
+    const Group gr = make_group<L3>(fminf(__low2float(mn[0]), __high2float(mn[0])),
                                 fmaxf(__low2float(mx[0]), __high2float(mx[0])), a.levels, a.eps);
 #pragma unroll
     for (int k = 0; k < kMaxVecs; ++k) {
       if (k >= nv) continue;
-      p[k] = make_uint4(roundtrip2(v[k].x, gr, gr, a.levels), roundtrip2(v[k].y, gr, gr, a.levels),
-                        roundtrip2(v[k].z, gr, gr, a.levels), roundtrip2(v[k].w, gr, gr, a.levels));
+      p[k] = make_uint4(roundtrip2<L3>(v[k].x, gr, gr, a.levels),
+                        roundtrip2<L3>(v[k].y, gr, gr, a.levels),
+                        roundtrip2<L3>(v[k].z, gr, gr, a.levels),
+                        roundtrip2<L3>(v[k].w, gr, gr, a.levels));
     }
   }
 }
 
 // Keys and values of every tensor in one launch (block-uniform split).
+template <bool L3>
 __global__ void __launch_bounds__(kThreads, 3) kivi_kernel(const KiviArgs a) {
   if (static_cast<int>(blockIdx.x) < a.key_blocks)
-    keys_part(a, static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x,
+    keys_part<L3>(a, static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x,
               static_cast<int64_t>(a.key_blocks) * kThreads);
   else
-    values_part(a, static_cast<int64_t>(blockIdx.x - a.key_blocks) * kThreads + threadIdx.x,
+    values_part<L3>(a, static_cast<int64_t>(blockIdx.x - a.key_blocks) * kThreads + threadIdx.x,
                 static_cast<int64_t>(gridDim.x - a.key_blocks) * kThreads);
 }
 
 // Values whose groups are not a multiple of 8 channels (or longer than 64): one thread per
 // (row, channel group), scalar loads.
+template <bool L3>
 __global__ void __launch_bounds__(kThreads) kivi_values_scalar_kernel(const KiviArgs a) {
   const int span = a.hi - a.lo;
   const int groups = (a.D + a.gs - 1) / a.gs;
@@ -205,8 +233,8 @@ __global__ void __launch_bounds__(kThreads) kivi_values_scalar_kernel(const Kivi
     const int c0 = g * a.gs, c1 = min(a.D, c0 + a.gs);
     float mn = __int_as_float(0x7f800000), mx = -mn;
     for (int c = c0; c < c1; ++c) { const float v = h2f(p[c]); mn = fminf(mn, v); mx = fmaxf(mx, v); }
-    const Group gr = make_group(mn, mx, a.levels, a.eps);
-    for (int c = c0; c < c1; ++c) p[c] = roundtrip(h2f(p[c]), gr, a.levels);
+    const Group gr = make_group<L3>(mn, mx, a.levels, a.eps);
+    for (int c = c0; c < c1; ++c) p[c] = roundtrip<L3>(h2f(p[c]), gr, a.levels);
   }
 }
 
@@ -269,10 +297,16 @@ extern "C" kvq_status kivi_quant_dequant(uint16_t* const* x, const int32_t* is_k
   const int kb = a.n_keys > 0 ? blocks_for_threads(key_items, cap) : 0;
   const int vb = (a.n_vals > 0 && vec_values) ? blocks_for_threads(val_items, cap) : 0;
   a.key_blocks = kb;
-  if (kb + vb > 0) kivi_kernel<<<kb + vb, kThreads, 0, st>>>(a);
+  const bool l3 = levels == 3;   // 2 bits: codes by thresholds
+  if (kb + vb > 0) {
+    if (l3) kivi_kernel<true><<<kb + vb, kThreads, 0, st>>>(a);
+    else kivi_kernel<false><<<kb + vb, kThreads, 0, st>>>(a);
+  }
   if (a.n_vals > 0 && !vec_values) {
     a.key_blocks = 0;
-    kivi_values_scalar_kernel<<<blocks_for_threads(val_items, sms * 8), kThreads, 0, st>>>(a);
+    const int nb = blocks_for_threads(val_items, sms * 8);
+    if (l3) kivi_values_scalar_kernel<true><<<nb, kThreads, 0, st>>>(a);
+    else kivi_values_scalar_kernel<false><<<nb, kThreads, 0, st>>>(a);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "kivi launch: %s", cudaGetErrorString(e));

@@ -30,6 +30,13 @@ def test_small_shapes_bit_exact(kvq, cuda_dev, D, gs, lo, hi):
     k, v = _pair(B, H, S, D, 1)
     k[0, 0, lo:hi, 3] = 2.5          # a constant channel and a row with ties
     v[1, 2, lo, :] = np.float16(np.arange(D) % 4 / 2.0)
+    # exact ties of (x - min) / scale at 0.5, 1.5, 2.5 under 2 bits (min 0, max 2.25, scale
+    # 0.75) and the fp16 neighbours on both sides, along a key channel and a value row
+    t3 = np.array([0.375, 1.125, 1.875], np.float16)
+    ties = np.concatenate([np.array([0.0, 2.25], np.float16), t3, np.nextafter(t3, np.float16(4)),
+                           np.nextafter(t3, np.float16(0))])
+    k[1, 1, lo:hi, 5 % D] = np.resize(ties, hi - lo)
+    v[0, 1, (lo + hi) // 2, :] = np.resize(ties, D)
     kt, vt = dev_tensor(k, cuda_dev), dev_tensor(v, cuda_dev)
     kvq.kivi_quant_dequant([kt, vt], [True, False], lo, hi, gs, 3, 1e-8)
     torch.cuda.synchronize()
