@@ -99,25 +99,39 @@ template <int BITS> __host__ __device__ constexpr int tma_smem_bytes() {
 
 // Shared-memory layout of the staged kernel: the stage ring, the barriers and flags, and the query
 // B fragments every warp of the CTA shares (4 KB: 32 registers per thread saved).  With side
-// channels a stage also holds the tile's K and V outlier values (fp16 [16][k], 256 B reserved each)
-// and positions (uint8 [16][k], 128 B each); two stages per warp; then each warp's sparse residual
-// tile: fp16 [16 tokens][256] with a 528-byte row stride (conflict-free ldmatrix), all zero
-// between uses.
+// channels a stage also holds the tile's K and V outlier values (fp16 [16][k]) and positions
+// (uint8 [16][k]), sized by k at launch (side_stage_extra); two stages per warp; then each warp's
+// sparse residual tile: half a tile's columns, fp16 [16 tokens][128] with a 272-byte row stride
+// (conflict-free ldmatrix), all zero between uses.  At q6/q4 and k = 3 a CTA takes 74 KB, so
+// three CTAs fit on an SM.
 template <int BITS, bool SIDE>
 struct Lay {
   static constexpr int kStages = SIDE ? 2 : Wd<BITS>::kStages;
   static constexpr int kBase = stage_bytes<BITS>();   // bytes of the four page copies
-  static constexpr int kOffKov = kBase, kOffVov = kBase + 256;
-  static constexpr int kOffKoi = kBase + 512, kOffVoi = kBase + 640;
-  static constexpr int kStage = SIDE ? kBase + 768 : kBase;
+  // without side channels (with them the stages grow by side_stage_extra(k) at run time, and
+  // kRing is the smallest ring, k = 0)
+  static constexpr int kStage = kBase;
   static constexpr int kWarpBytes = kStages * kStage;
   static constexpr int kRing = kWarps * kWarpBytes;
   static constexpr int kQf = kRing + kWarps * kStages * 16;   // query B fragments [16][32] uint2
   static constexpr int kQfEnd = kQf + 16 * 32 * 8;
-  static constexpr int kOtStride = 2 * kD + 16;              // bytes per residual-tile row
-  static constexpr int kOt = kQfEnd;                         // residual tiles [warp][16][stride]
-  static constexpr int kTotal = SIDE ? kOt + kWarps * kTile * kOtStride : kQfEnd;
+  static constexpr int kOtStride = kD + 16;                  // bytes per half-tile row (128 fp16)
+  static constexpr int kOtBytes = kTile * kOtStride;         // one warp's residual half-tile
+  static constexpr int kTotal = kQfEnd;                      // without side channels
 };
+
+// Bytes a stage adds for k outliers per row: K and V values (fp16 [16][k], rounded up to 16 bytes)
+// and positions (uint8 [16][k]).
+__host__ __device__ constexpr int side_stage_extra(int k) {
+  return 2 * ((32 * k + 15) / 16 * 16) + 2 * 16 * k;
+}
+
+// Shared memory of the side-channel kernel for k outliers per row.
+template <int BITS>
+__host__ __device__ constexpr int side_smem_bytes(int k) {
+  return kWarps * Lay<BITS, true>::kStages * (Lay<BITS, true>::kBase + side_stage_extra(k)) +
+         kWarps * Lay<BITS, true>::kStages * 16 + 16 * 32 * 8 + kWarps * Lay<BITS, true>::kOtBytes;
+}
 
 constexpr int kMergeBytes = kWarps * 8 * kD * 4 + 2 * kWarps * 8 * 4;
 
@@ -445,65 +459,61 @@ __device__ __forceinline__ int side_col(int d) {
     return 16 * (4 * ((d & 31) >> 3) + (o & 3)) + (d >> 5) + 8 * (o >> 2);
 }
 
-// Write one tile's K or V side terms into the warp's residual tile: the outliers of every live
-// row that is not a sink (lanes 2r and 2r + 1 take row r's entries; positions are bytes, so always
-// < 256), and in the sequence's first tile the sink rows' exact fp16 rows from the sink buffer
-// [seq][n_sink][H][256].  The lane keeps the offsets it wrote in `at` (the stage may be refilled
-// before the tile is cleared).
+// One lane's side entries of a tile, read from the stage before it is handed back: the outliers
+// of row r = lane >> 1 (entries lane & 1, + 2, ...) when the row is live and not a sink, each as
+// bits 0-7 its residual-tile column (side_col), 8-11 the row, 12 valid, 16-31 the fp16 value.
 template <bool KEY>
-__device__ __forceinline__ void side_write(uint16_t* ot, const uint8_t* idx,
-                                               const uint16_t* val, int k, int n_sink,
-                                               const uint16_t* sink, int s, int H, int h, int tb,
-                                               int len, int lane,
-                                               int (&at)[KVQ_MAX_OUTLIERS / 2]) {
-  constexpr int kRowH = (2 * kD + 16) / 2;   // halves per residual-tile row
+__device__ __forceinline__ void side_collect(const uint8_t* idx, const uint16_t* val, int k,
+                                             int n_sink, int tb, int len, int lane,
+                                             uint32_t (&ent)[KVQ_MAX_OUTLIERS / 2]) {
   const int row = lane >> 1;
   const bool live = tb + row < len && tb + row >= n_sink;
 #pragma unroll
   for (int i = 0; i < KVQ_MAX_OUTLIERS / 2; ++i) {
     const int j = (lane & 1) + 2 * i;
-    at[i] = -1;
-    if (live && j < k) {
-      const int col = side_col<KEY>(idx[row * k + j]);
-      at[i] = row * kRowH + col;
-      ot[at[i]] = val[row * k + j];
-    }
+    ent[i] = 0;
+    if (live && j < k)
+      ent[i] = (static_cast<uint32_t>(val[row * k + j]) << 16) | 0x1000u |
+               static_cast<uint32_t>(row << 8) | static_cast<uint32_t>(side_col<KEY>(idx[row * k + j]));
+  }
+}
+
+// Write (or clear) half `hf` of the tile's K or V side terms -- residual-tile columns
+// [128 hf, 128 hf + 128) -- into the warp's half-tile: the lane's entries, and in the sequence's
+// first tile the sink rows' exact fp16 values from the sink buffer [seq][n_sink][H][256].
+template <bool KEY>
+__device__ __forceinline__ void side_half(uint16_t* ot, const uint32_t (&ent)[KVQ_MAX_OUTLIERS / 2],
+                                          int hf, bool clear, int n_sink, const uint16_t* sink,
+                                          int s, int H, int h, int tb, int len, int lane) {
+  constexpr int kRowH = (kD + 16) / 2;   // halves per half-tile row
+#pragma unroll
+  for (int i = 0; i < KVQ_MAX_OUTLIERS / 2; ++i) {
+    const uint32_t e = ent[i];
+    if ((e & 0x1000u) && static_cast<int>((e >> 7) & 1u) == hf)
+      ot[((e >> 8) & 15u) * kRowH + (e & 127u)] = clear ? static_cast<uint16_t>(0)
+                                                        : static_cast<uint16_t>(e >> 16);
   }
   if (tb < n_sink) {   // only the first tile: n_sink <= 16 = kTile
     const int nr = min(min(n_sink - tb, kTile), len - tb);
     for (int e = lane; e < nr * kD; e += 32) {
       const int r = e / kD, d = e - r * kD;
-      ot[r * kRowH + side_col<KEY>(d)] =
-          sink[((static_cast<int64_t>(s) * n_sink + tb + r) * H + h) * kD + d];
+      const int col = side_col<KEY>(d);
+      if ((col >> 7) == hf)
+        ot[r * kRowH + (col & 127)] =
+            clear ? static_cast<uint16_t>(0)
+                  : sink[((static_cast<int64_t>(s) * n_sink + tb + r) * H + h) * kD + d];
     }
   }
 }
 
-// Zero what side_write wrote.
-__device__ __forceinline__ void side_clear(uint16_t* ot, int n_sink, int tb, int len, int lane,
-                                           const int (&at)[KVQ_MAX_OUTLIERS / 2]) {
-  constexpr int kRowH = (2 * kD + 16) / 2;
-#pragma unroll
-  for (int i = 0; i < KVQ_MAX_OUTLIERS / 2; ++i)
-    if (at[i] >= 0) ot[at[i]] = 0;
-  if (tb < n_sink) {
-    const int nr = min(min(n_sink - tb, kTile), len - tb);
-    for (int e = lane; e < nr * kD; e += 32) {
-      const int r = e / kD;
-      ot[r * kRowH + (e - r * kD)] = 0;
-    }
-  }
-}
-
-// Side channels need more shared memory (2 CTAs per SM), so that variant may use more registers.
+// With side channels q6/q4 fit 3 CTAs per SM (168 registers, 74 KB at k = 3); q8 keeps 2.
 template <int BITS, bool APPEND, bool SIDE>
-__global__ void __launch_bounds__(kThreads, SIDE ? 2 : (BITS == 8 ? 3 : 4)) decode_attn_tma_kernel(const AttnArgs a,
+__global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS == 8 ? 3 : 4)) decode_attn_tma_kernel(const AttnArgs a,
                                                                       const AttnSide sd) {
   using W = Wd<BITS>;
   using Ly = Lay<BITS, SIDE>;
   constexpr int S = Ly::kStages;
   constexpr int kPd = W::kPd;
-  constexpr uint32_t kStageBytes = Ly::kStage;
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5;
@@ -524,15 +534,24 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : (BITS == 8 ? 3 : 4)) deco
   const int n_mine = (tile1 - tile0 - warp + kWarps - 1) > 0
                          ? (tile1 - tile0 - warp + kWarps - 1) / kWarps : 0;
 
-  uint8_t* wbase = smem + warp * Ly::kWarpBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kRing) + warp * S;
-  int* flags = reinterpret_cast<int*>(smem + Ly::kRing + kWarps * S * 8) + warp * S;
-  // SIDE: this warp's residual tile (fp16 [16][256], stride Ly::kOtStride), zeroed once; each
-  // tile's side terms are written into it, consumed by tensor-core products and cleared again
+  // stage size: the four page copies, plus the tile's outlier values and positions with side
+  // channels (sized by k; compile-time constants without them)
+  const uint32_t kStageBytes = SIDE ? Ly::kBase + side_stage_extra(sd.k) : Ly::kStage;
+  const uint32_t kvov = Ly::kBase + (SIDE ? (32 * sd.k + 15) / 16 * 16 : 0);   // V values
+  const uint32_t kkoi = kvov + (kvov - Ly::kBase);                              // K positions
+  const uint32_t kvoi = kkoi + 16 * (SIDE ? sd.k : 0);                          // V positions
+  const uint32_t ring = kWarps * S * kStageBytes;
+  uint8_t* wbase = smem + warp * S * kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring) + warp * S;
+  int* flags = reinterpret_cast<int*>(smem + ring + kWarps * S * 8) + warp * S;
+  const uint32_t qf_off = ring + kWarps * S * 16;
+  // SIDE: this warp's residual half-tile (fp16 [16][128], stride Ly::kOtStride), zeroed once;
+  // each tile's side terms are written into it half by half, consumed by tensor-core products
+  // and cleared again
   uint16_t* ot = nullptr;
   if constexpr (SIDE) {
-    ot = reinterpret_cast<uint16_t*>(smem + Ly::kOt + warp * kTile * Ly::kOtStride);
-    for (int i = lane; i < kTile * Ly::kOtStride / 16; i += 32)
+    ot = reinterpret_cast<uint16_t*>(smem + qf_off + 16 * 32 * 8 + warp * Ly::kOtBytes);
+    for (int i = lane; i < Ly::kOtBytes / 16; i += 32)
       reinterpret_cast<uint4*>(ot)[i] = make_uint4(0, 0, 0, 0);
     __syncwarp();
   }
@@ -571,17 +590,17 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : (BITS == 8 ? 3 : 4)) deco
     if (ok) {
       const int64_t row = (static_cast<int64_t>(page) * a.H + h) * a.ps + slot0;
       const int nk = SIDE ? sd.k : 0;
-      mbar_expect_tx(&bars[st], Ly::kBase + 96 * nk);
+      mbar_expect_tx(&bars[st], Ly::kBase + 96 * nk);   // 32k + 32k + 16k + 16k bytes of side data
       bulk_g2s(dst, P.kc + row * kPd, kTile * kPd, &bars[st]);
       bulk_g2s(dst + kTile * kPd, P.vc + row * kPd, kTile * kPd, &bars[st]);
       bulk_g2s(dst + 2 * kTile * kPd, P.ks + row, 2 * kTile, &bars[st]);
       bulk_g2s(dst + 2 * kTile * kPd + 2 * kTile, P.vs + row, 2 * kTile, &bars[st]);
       if constexpr (SIDE) {
         if (nk > 0) {   // the tile's outliers: 16 rows x k values (fp16) and positions (uint8)
-          bulk_g2s(dst + Ly::kOffKov, sd.kov[layer] + row * nk, 32 * nk, &bars[st]);
-          bulk_g2s(dst + Ly::kOffVov, sd.vov[layer] + row * nk, 32 * nk, &bars[st]);
-          bulk_g2s(dst + Ly::kOffKoi, sd.koi[layer] + row * nk, 16 * nk, &bars[st]);
-          bulk_g2s(dst + Ly::kOffVoi, sd.voi[layer] + row * nk, 16 * nk, &bars[st]);
+          bulk_g2s(dst + Ly::kBase, sd.kov[layer] + row * nk, 32 * nk, &bars[st]);
+          bulk_g2s(dst + kvov, sd.vov[layer] + row * nk, 32 * nk, &bars[st]);
+          bulk_g2s(dst + kkoi, sd.koi[layer] + row * nk, 16 * nk, &bars[st]);
+          bulk_g2s(dst + kvoi, sd.voi[layer] + row * nk, 16 * nk, &bars[st]);
         }
       }
     } else {
@@ -600,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : (BITS == 8 ? 3 : 4)) deco
   // in registers.
   constexpr bool kQShared = BITS != 8;
   using QSrc = typename std::conditional<kQShared, QFragSmem, QFragRegs>::type;
-  const uint32_t qaddr = smem_u32(smem + Ly::kQf) + 8 * lane;
+  const uint32_t qaddr = smem_u32(smem + qf_off) + 8 * lane;
   uint32_t qf[kQShared ? 1 : 16][2];
   if constexpr (kQShared) {
     if (warp == 0) {
@@ -668,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : (BITS == 8 ? 3 : 4)) deco
     }
     uint32_t pb0, pb1;
     float sp[4];   // SIDE: the tile's probabilities (unscaled), for the value side terms
-    int side_at[KVQ_MAX_OUTLIERS / 2];   // SIDE: residual-tile offsets this lane wrote
+    uint32_t vent[KVQ_MAX_OUTLIERS / 2];   // SIDE: this lane's value entries (side_collect)
     const bool side_work = SIDE && (sd.k > 0 || (tb == 0 && sd.n_sink > 0));   // warp-uniform
     if constexpr (SIDE) {
       // Key terms the codes do not carry, as a tensor-core product with the query fragments: the
@@ -676,25 +695,32 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : (BITS == 8 ? 3 : 4)) deco
       // is zeroed above).  Columns follow the dense path's MMA k-order.
       float so[4] = {0.f, 0.f, 0.f, 0.f};
       if (side_work) {
-        side_write<true>(ot, sk + Ly::kOffKoi, reinterpret_cast<const uint16_t*>(sk + Ly::kOffKov),
-                         sd.k, sd.n_sink, sd.ksink[layer], s, a.H, h, tb, len, lane, side_at);
-        __syncwarp();
+        uint32_t kent[KVQ_MAX_OUTLIERS / 2];
+        side_collect<true>(sk + kkoi, reinterpret_cast<const uint16_t*>(sk + Ly::kBase), sd.k,
+                           sd.n_sink, tb, len, lane, kent);
+        side_collect<false>(sk + kvoi, reinterpret_cast<const uint16_t*>(sk + kvov), sd.k,
+                            sd.n_sink, tb, len, lane, vent);
         const uint32_t ob = smem_u32(ot) + (lane & 15) * Ly::kOtStride + 16 * (lane >> 4);
         float so4[4][4] = {};   // four independent accumulation chains
 #pragma unroll
-        for (int ks = 0; ks < 16; ++ks) {
-          uint32_t af[4];
-          ldsm_x4(ob + 32 * ks, af);
-          const uint2 qb = Q.pair(ks);
-          mma16816(so4[ks & 3], af[0], af[1], af[2], af[3], qb.x, qb.y);
+        for (int hf = 0; hf < 2; ++hf) {   // k-steps 8 hf .. 8 hf + 7
+          side_half<true>(ot, kent, hf, false, sd.n_sink, sd.ksink[layer], s, a.H, h, tb, len,
+                          lane);
+          __syncwarp();
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            uint32_t af[4];
+            ldsm_x4(ob + 32 * ks, af);
+            const uint2 qb = Q.pair(8 * hf + ks);
+            mma16816(so4[ks & 3], af[0], af[1], af[2], af[3], qb.x, qb.y);
+          }
+          __syncwarp();
+          side_half<true>(ot, kent, hf, true, sd.n_sink, sd.ksink[layer], s, a.H, h, tb, len,
+                          lane);
+          __syncwarp();
         }
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) so[k4] = (so4[0][k4] + so4[1][k4]) + (so4[2][k4] + so4[3][k4]);
-        __syncwarp();
-        side_clear(ot, sd.n_sink, tb, len, lane, side_at);
-        __syncwarp();
-        side_write<false>(ot, sk + Ly::kOffVoi, reinterpret_cast<const uint16_t*>(sk + Ly::kOffVov),
-                          sd.k, sd.n_sink, sd.vsink[layer], s, a.H, h, tb, len, lane, side_at);
       }
       tile_qk_softmax<BITS, true>(K, Q, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1, so, sp);
     } else {
@@ -733,20 +759,26 @@ __global__ void __launch_bounds__(kThreads, SIDE ? 2 : (BITS == 8 ? 3 : 4)) deco
       if (side_work) {
         // value terms: O^T += R_V^T . P^T with the unscaled probabilities (the residual tile holds
         // real fp16 values), into the same accumulators and running-max domain as the codes
-        __syncwarp();
         const uint32_t pv0 = movtrans(pack_h2(sp[0], sp[1]));
         const uint32_t pv1 = movtrans(pack_h2(sp[2], sp[3]));
         const uint32_t ob = smem_u32(ot) + ((lane & 7) + 8 * (lane >> 4)) * Ly::kOtStride +
                             16 * ((lane >> 3) & 1);
 #pragma unroll
-        for (int b = 0; b < 16; ++b) {
-          uint32_t af[4];
-          ldsm_x4_trans(ob + 32 * b, af);
-          mma16816(acc[b], af[0], af[1], af[2], af[3], pv0, pv1);
+        for (int hf = 0; hf < 2; ++hf) {   // blocks 8 hf .. 8 hf + 7
+          side_half<false>(ot, vent, hf, false, sd.n_sink, sd.vsink[layer], s, a.H, h, tb, len,
+                           lane);
+          __syncwarp();
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            uint32_t af[4];
+            ldsm_x4_trans(ob + 32 * b, af);
+            mma16816(acc[8 * hf + b], af[0], af[1], af[2], af[3], pv0, pv1);
+          }
+          __syncwarp();
+          side_half<false>(ot, vent, hf, true, sd.n_sink, sd.vsink[layer], s, a.H, h, tb, len,
+                           lane);
+          __syncwarp();
         }
-        __syncwarp();
-        side_clear(ot, sd.n_sink, tb, len, lane, side_at);
-        __syncwarp();
       }
     }
   }
@@ -899,7 +931,7 @@ template <int BITS, bool APPEND = false, bool SIDE = false>
 cudaError_t launch_attn(const AttnArgs& a, dim3 grid, bool tma, cudaStream_t cs,
                         const AttnSide& sd = AttnSide{}) {
   if (tma) {
-    constexpr int smem = Lay<BITS, SIDE>::kTotal;
+    const int smem = SIDE ? side_smem_bytes<BITS>(sd.k) : Lay<BITS, SIDE>::kTotal;
     static_assert(Lay<BITS, SIDE>::kRing >= kMergeBytes, "merge buffer must fit in the stage ring");
     cudaError_t e = cudaFuncSetAttribute(decode_attn_tma_kernel<BITS, APPEND, SIDE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
