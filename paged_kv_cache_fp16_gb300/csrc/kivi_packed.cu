@@ -42,10 +42,10 @@ struct KPArgs {
   const uint16_t* v[KVQ_MAX_TENSORS];
   int n_layers, lo, hi;
   float eps, levels;
-  int key_blocks;  // blocks [0, key_blocks) pack keys, the rest values
 };
 
 __device__ __forceinline__ __half2 as_h2(uint32_t w) { return *reinterpret_cast<__half2*>(&w); }
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
 // Group parameters as the pack uses them: zero, the stored fp16 scale and RN(1 / scale).
 struct GP {
@@ -202,6 +202,89 @@ __device__ void pack_keys_part(const KPArgs& a, int64_t first, int64_t stride) {
   }
 }
 
+// Keys at head_dim 64: one warp per (layer, batch row, head, token group), every row read once.
+// Lane l takes the 8-channel chunk l & 7 (16 bytes of a row) of the group's token quarter
+// l >> 3 (GS / 4 rows) into registers; the per-channel fp16 min / max reduce over the quarter and
+// then across the four quarters by shuffles, and each lane codes its own rows.  `first` and
+// `stride` count warps, so the lanes of a warp always share an item.
+template <int BITS, int GS>
+__device__ void pack_keys_d64(const KPArgs& a, int64_t first, int64_t stride) {
+  constexpr int kD64 = 64, kQ = GS / 4, kCb = kD64 * BITS / 8;
+  const kivi_packed& c0 = a.c[0];
+  const int B = c0.batch, H = c0.num_heads, S = c0.capacity;
+  const int lane = threadIdx.x & 31, ch = lane & 7, tq = lane >> 3;
+  const int n_groups = (a.hi - a.lo) / GS;
+  const int64_t per_layer = static_cast<int64_t>(B) * H * n_groups;
+  const int64_t items = per_layer * a.n_layers;
+  for (int64_t it = first; it < items; it += stride) {
+    const int layer = static_cast<int>(it / per_layer);
+    const int64_t r = it - layer * per_layer;
+    const int g = static_cast<int>(r % n_groups);
+    const int64_t bh = r / n_groups;
+    const int t0 = a.lo + g * GS;
+    const kivi_packed& C = a.c[layer];
+    const uint4* src =
+        reinterpret_cast<const uint4*>(a.k[layer] + (bh * S + t0 + tq * kQ) * kD64) + ch;
+    uint4 x[kQ];
+#pragma unroll
+    for (int i = 0; i < kQ; ++i) x[i] = src[i * (kD64 / 8)];
+    uint32_t mn[4], mx[4];
+    {
+      const uint32_t w0[4] = {x[0].x, x[0].y, x[0].z, x[0].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mn[k] = mx[k] = w0[k];
+    }
+#pragma unroll
+    for (int i = 1; i < kQ; ++i) {
+      const uint32_t w[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        mn[k] = h2u(__hmin2(as_h2(mn[k]), as_h2(w[k])));
+        mx[k] = h2u(__hmax2(as_h2(mx[k]), as_h2(w[k])));
+      }
+    }
+#pragma unroll
+    for (int o = 8; o <= 16; o <<= 1) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        mn[k] = h2u(__hmin2(as_h2(mn[k]), as_h2(__shfl_xor_sync(kFullMask, mn[k], o))));
+        mx[k] = h2u(__hmax2(as_h2(mx[k]), as_h2(__shfl_xor_sync(kFullMask, mx[k], o))));
+      }
+    }
+    GP gp[8];
+    uint32_t sw[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float z0 = __low2float(as_h2(mn[k])), z1 = __high2float(as_h2(mn[k]));
+      const uint16_t s0 = scale16(z0, __low2float(as_h2(mx[k])), a.levels, a.eps);
+      const uint16_t s1 = scale16(z1, __high2float(as_h2(mx[k])), a.levels, a.eps);
+      gp[2 * k] = make_gp(z0, s0);
+      gp[2 * k + 1] = make_gp(z1, s1);
+      if constexpr (BITS == 2) {
+        set_thresholds3(gp[2 * k]);
+        set_thresholds3(gp[2 * k + 1]);
+      }
+      sw[k] = s0 | (static_cast<uint32_t>(s1) << 16);
+    }
+    if (tq == 0) {
+      const int64_t prow = (bh * (S / GS) + t0 / GS) * kD64 + ch * 8;   // params [B][H][S/gs][D]
+      *reinterpret_cast<uint4*>(C.k_scale + prow) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+      *reinterpret_cast<uint4*>(C.k_zero + prow) = make_uint4(mn[0], mn[1], mn[2], mn[3]);
+    }
+    uint8_t* dst = C.k_codes + (bh * S + t0 + tq * kQ) * kCb + ch * BITS;   // 8 fields = BITS bytes
+#pragma unroll
+    for (int i = 0; i < kQ; ++i) {
+      float xf[8];
+      f8(x[i], xf);
+      uint32_t f[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        f[e] = BITS == 2 ? field3(xf[e], gp[e]) : field(xf[e], gp[e], a.levels);
+      store_fields8<BITS>(dst + static_cast<int64_t>(i) * kCb, f);
+    }
+  }
+}
+
 template <int BITS>
 __device__ void pack_values_part(const KPArgs& a, int64_t first, int64_t stride) {
   const kivi_packed& c0 = a.c[0];
@@ -254,15 +337,22 @@ __device__ void pack_values_part(const KPArgs& a, int64_t first, int64_t stride)
   }
 }
 
-template <int BITS>
-__global__ void __launch_bounds__(kThreads) kivi_pack_kernel(const KPArgs a) {
-  if (static_cast<int>(blockIdx.x) < a.key_blocks)
-    pack_keys_part<BITS>(a, static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x,
-                         static_cast<int64_t>(a.key_blocks) * kThreads);
+// Keys and values in two launches, each with its own register allocation (the head_dim-64 key
+// path holds a token quarter of its group in registers; the value path needs far fewer).
+template <int BITS, int GS>
+__global__ void __launch_bounds__(kThreads) kivi_pack_keys_kernel(const KPArgs a) {
+  if constexpr (GS > 0)   // head_dim 64: a warp per token group
+    pack_keys_d64<BITS, GS>(a, (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5,
+                            static_cast<int64_t>(gridDim.x) * (kThreads / 32));
   else
-    pack_values_part<BITS>(a, static_cast<int64_t>(blockIdx.x - a.key_blocks) * kThreads +
-                                  threadIdx.x,
-                           static_cast<int64_t>(gridDim.x - a.key_blocks) * kThreads);
+    pack_keys_part<BITS>(a, static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x,
+                         static_cast<int64_t>(gridDim.x) * kThreads);
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads) kivi_pack_values_kernel(const KPArgs a) {
+  pack_values_part<BITS>(a, static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x,
+                         static_cast<int64_t>(gridDim.x) * kThreads);
 }
 
 // ================================================================================================
@@ -707,6 +797,22 @@ kvq_status check_caches(const kivi_packed* c, int n, const char* fn) {
 }  // namespace
 }  // namespace kvq
 
+namespace kvq {
+namespace {
+template <int BITS>
+void launch_pack(const KPArgs& a, int gs, int key_blocks, int value_blocks, cudaStream_t cs) {
+  switch (gs) {   // 0: any head_dim (a thread per key chunk); else head_dim 64, group gs
+    case 8: kivi_pack_keys_kernel<BITS, 8><<<key_blocks, kThreads, 0, cs>>>(a); break;
+    case 16: kivi_pack_keys_kernel<BITS, 16><<<key_blocks, kThreads, 0, cs>>>(a); break;
+    case 32: kivi_pack_keys_kernel<BITS, 32><<<key_blocks, kThreads, 0, cs>>>(a); break;
+    case 64: kivi_pack_keys_kernel<BITS, 64><<<key_blocks, kThreads, 0, cs>>>(a); break;
+    default: kivi_pack_keys_kernel<BITS, 0><<<key_blocks, kThreads, 0, cs>>>(a); break;
+  }
+  kivi_pack_values_kernel<BITS><<<value_blocks, kThreads, 0, cs>>>(a);
+}
+}  // namespace
+}  // namespace kvq
+
 extern "C" kvq_status kivi_pack(const kivi_packed* caches, const uint16_t* const* k,
                                 const uint16_t* const* v, int n_layers, int lo, int hi,
                                 float eps, kvq_stream_t stream) {
@@ -738,8 +844,10 @@ extern "C" kvq_status kivi_pack(const kivi_packed* caches, const uint16_t* const
   a.eps = eps;
   a.levels = static_cast<float>((1 << c0.bits) - 1);
   const int sms = sm_count() > 0 ? sm_count() : 152;
+  // keys: a thread per (group, 8-channel chunk), or at head_dim 64 a warp per group
+  const bool d64 = c0.head_dim == 64;
   const int64_t kitems = static_cast<int64_t>(n_layers) * c0.batch * c0.num_heads *
-                         ((hi - lo) / c0.group_size) * (c0.head_dim / 8);
+                         ((hi - lo) / c0.group_size) * (d64 ? 32 : c0.head_dim / 8);
   const int64_t vitems = static_cast<int64_t>(n_layers) * c0.batch * c0.num_heads * (hi - lo) *
                          (c0.head_dim / c0.group_size);
   auto blocks = [&](int64_t items) {
@@ -747,13 +855,13 @@ extern "C" kvq_status kivi_pack(const kivi_packed* caches, const uint16_t* const
     const int64_t cap = static_cast<int64_t>(sms) * 4;
     return static_cast<int>(b > cap ? cap : (b < 1 ? 1 : b));
   };
-  a.key_blocks = blocks(kitems);
-  const int total = a.key_blocks + blocks(vitems);
+  const int key_blocks = blocks(kitems);
+  const int value_blocks = blocks(vitems);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   switch (c0.bits) {
-    case 2: kivi_pack_kernel<2><<<total, kThreads, 0, cs>>>(a); break;
-    case 4: kivi_pack_kernel<4><<<total, kThreads, 0, cs>>>(a); break;
-    default: kivi_pack_kernel<8><<<total, kThreads, 0, cs>>>(a); break;
+    case 2: launch_pack<2>(a, d64 ? c0.group_size : 0, key_blocks, value_blocks, cs); break;
+    case 4: launch_pack<4>(a, d64 ? c0.group_size : 0, key_blocks, value_blocks, cs); break;
+    default: launch_pack<8>(a, d64 ? c0.group_size : 0, key_blocks, value_blocks, cs); break;
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "%s launch: %s", fn, cudaGetErrorString(e));

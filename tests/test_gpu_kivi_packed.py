@@ -22,7 +22,8 @@ def _layer(seed, layer, B, H, S, D):
 
 
 @pytest.mark.parametrize("bits", [2, 4, 8])
-@pytest.mark.parametrize("gs,D", [(32, 64), (16, 64), (8, 32), (64, 128), (32, 256)])
+@pytest.mark.parametrize("gs,D", [(32, 64), (16, 64), (8, 64), (64, 64), (8, 32), (64, 128),
+                                  (32, 256)])
 def test_pack_bit_exact(kvq, cuda_dev, bits, gs, D):
     B, H, S, L = 2, 3, 4 * gs, 2
     lo, hi = gs, 3 * gs
