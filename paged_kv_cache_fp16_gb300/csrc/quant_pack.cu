@@ -238,7 +238,8 @@ int ceil_log2(int v) {
 }
 
 // Persistent grid: blockIdx.y = tensor; per tensor enough blocks for its token blocks, with all
-// tensors together at most what is resident on the SMs at once.
+// tensors together at most what is resident on the SMs at once (rounded down per tensor, so no
+// block waits for a second wave).
 template <typename K>
 dim3 grid_for(K kernel, int& cache, int n_tensors, int total_tokens) {
   if (cache == 0) {
@@ -250,7 +251,7 @@ dim3 grid_for(K kernel, int& cache, int n_tensors, int total_tokens) {
   const int64_t need = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const int sms = sm_count();
   const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * cache;
-  int64_t per = (cap + n_tensors - 1) / n_tensors;
+  int64_t per = cap / n_tensors;
   if (per > need) per = need;
   if (per < 1) per = 1;
   return dim3(static_cast<unsigned>(per), static_cast<unsigned>(n_tensors));
