@@ -766,6 +766,20 @@ def run_e2e(w, kvq, bits, args, stream, world, dev, step_bytes):
     for _ in range(min(args.warmup, 2)):
         step()
     torch.cuda.synchronize()
+    # the host link alone, just before the timed loop: the copies of the first 8 input tensors
+    # (4 GiB) with nothing else running, best of three; the loop cannot beat h2d bytes / this rate
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    probe = host_x[:min(8, len(host_x))]
+    link = 0.0
+    for _ in range(3):
+        p0.record(copy)
+        with torch.cuda.stream(copy):
+            for i, hx in enumerate(probe):
+                w.x[i].copy_(hx, non_blocking=True)
+        p1.record(copy)
+        torch.cuda.synchronize()
+        link = max(link, sum(t_.numel() * t_.element_size() for t_ in probe) /
+                   (p0.elapsed_time(p1) / 1e3))
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
@@ -779,6 +793,8 @@ def run_e2e(w, kvq, bits, args, stream, world, dev, step_bytes):
     return {"value": round(world * step_bytes * n / t / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
             "ms_per_step": round(t / n * 1e3, 3),
+            "host_link_GB_s": round(link / 1e9, 1),
+            "host_link_floor_ms_per_step": round(h2d / link * 1e3, 1),
             "pipeline": "per-layer H2D on a copy stream overlapped with quant-pack"}
 
 
