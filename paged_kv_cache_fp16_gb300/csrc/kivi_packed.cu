@@ -36,12 +36,39 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Division of 32-bit unsigned integers by an invariant divisor d >= 1 with one multiply-high and
+// shifts (T. Granlund and P. L. Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994, the unsigned N-bit method): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, q = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0) for
+// t = mulhi(m, n) is floor(n / d) for every 32-bit n.
+struct DivU32 {
+  uint32_t m, s1, s2;
+};
+
+inline DivU32 make_divu32(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  DivU32 r;
+  r.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+  r.s1 = l < 1 ? l : 1;
+  r.s2 = l > 1 ? l - 1 : 0;
+  return r;
+}
+
+__device__ __forceinline__ uint32_t divu32(uint32_t n, const DivU32& f) {
+  const uint32_t t = __umulhi(n, f.m);
+  return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+
 struct KPArgs {
   kivi_packed c[KVQ_MAX_TENSORS];
   const uint16_t* k[KVQ_MAX_TENSORS];
   const uint16_t* v[KVQ_MAX_TENSORS];
   int n_layers, lo, hi;
   float eps, levels;
+  // item decomposition without 64-bit divisions, when the per-layer item counts are < 2^31
+  bool fast32;
+  DivU32 div_g, div_span, div_ngroups;   // by D / gs, hi - lo, (hi - lo) / gs
 };
 
 __device__ __forceinline__ __half2 as_h2(uint32_t w) { return *reinterpret_cast<__half2*>(&w); }
@@ -216,11 +243,8 @@ __device__ void pack_keys_d64(const KPArgs& a, int64_t first, int64_t stride) {
   const int n_groups = (a.hi - a.lo) / GS;
   const int64_t per_layer = static_cast<int64_t>(B) * H * n_groups;
   const int64_t items = per_layer * a.n_layers;
-  for (int64_t it = first; it < items; it += stride) {
-    const int layer = static_cast<int>(it / per_layer);
-    const int64_t r = it - layer * per_layer;
-    const int g = static_cast<int>(r % n_groups);
-    const int64_t bh = r / n_groups;
+  // one item: (layer, batch row * H + head, token group)
+  auto item = [&](int layer, int64_t bh, int g) {
     const int t0 = a.lo + g * GS;
     const kivi_packed& C = a.c[layer];
     const uint4* src =
@@ -282,6 +306,29 @@ __device__ void pack_keys_d64(const KPArgs& a, int64_t first, int64_t stride) {
         f[e] = BITS == 2 ? field3(xf[e], gp[e]) : field(xf[e], gp[e], a.levels);
       store_fields8<BITS>(dst + static_cast<int64_t>(i) * kCb, f);
     }
+  };
+  if (a.fast32) {   // running (layer, offset); offset / n_groups by multiply-high
+    const uint32_t pl = static_cast<uint32_t>(per_layer);
+    int layer = static_cast<int>(first / per_layer);
+    uint32_t r = static_cast<uint32_t>(first - layer * per_layer);
+    const int dl = static_cast<int>(stride / per_layer);
+    const uint32_t dr = static_cast<uint32_t>(stride - dl * per_layer);
+    for (int64_t it = first; it < items; it += stride) {
+      const uint32_t bh = divu32(r, a.div_ngroups);
+      item(layer, bh, static_cast<int>(r - bh * n_groups));
+      r += dr;
+      layer += dl;
+      if (r >= pl) {
+        r -= pl;
+        ++layer;
+      }
+    }
+  } else {
+    for (int64_t it = first; it < items; it += stride) {
+      const int layer = static_cast<int>(it / per_layer);
+      const int64_t r = it - layer * per_layer;
+      item(layer, r / n_groups, static_cast<int>(r % n_groups));
+    }
   }
 }
 
@@ -294,13 +341,8 @@ __device__ void pack_values_part(const KPArgs& a, int64_t first, int64_t stride)
   const int64_t per_layer = static_cast<int64_t>(B) * H * span * G;
   const int64_t items = per_layer * a.n_layers;
   const int cb = D * BITS / 8;
-  for (int64_t it = first; it < items; it += stride) {
-    const int layer = static_cast<int>(it / per_layer);
-    int64_t r = it - layer * per_layer;
-    const int g = static_cast<int>(r % G);
-    r /= G;
-    const int64_t bh = r / span;
-    const int t = a.lo + static_cast<int>(r - bh * span);
+  // one item: (layer, batch row * H + head, token, channel group)
+  auto item = [&](int layer, int64_t bh, int t, int g) {
     const kivi_packed& C = a.c[layer];
     const uint4* src = reinterpret_cast<const uint4*>(a.v[layer] + (bh * S + t) * D + g * gs);
     uint4 vv[8];
@@ -333,6 +375,33 @@ __device__ void pack_values_part(const KPArgs& a, int64_t first, int64_t stride)
       for (int e = 0; e < 8; ++e)
         f[e] = BITS == 2 ? field3(x[e], gp) : field(x[e], gp, a.levels);
       store_fields8<BITS>(dst + k * BITS, f);
+    }
+  };
+  if (a.fast32) {   // running (layer, offset); offset / G and / span by multiply-high
+    const uint32_t pl = static_cast<uint32_t>(per_layer);
+    int layer = static_cast<int>(first / per_layer);
+    uint32_t r = static_cast<uint32_t>(first - layer * per_layer);
+    const int dl = static_cast<int>(stride / per_layer);
+    const uint32_t dr = static_cast<uint32_t>(stride - dl * per_layer);
+    for (int64_t it = first; it < items; it += stride) {
+      const uint32_t q = divu32(r, a.div_g);          // token row of the layer
+      const uint32_t bh = divu32(q, a.div_span);
+      item(layer, bh, a.lo + static_cast<int>(q - bh * span), static_cast<int>(r - q * G));
+      r += dr;
+      layer += dl;
+      if (r >= pl) {
+        r -= pl;
+        ++layer;
+      }
+    }
+  } else {
+    for (int64_t it = first; it < items; it += stride) {
+      const int layer = static_cast<int>(it / per_layer);
+      int64_t r = it - layer * per_layer;
+      const int g = static_cast<int>(r % G);
+      r /= G;
+      const int64_t bh = r / span;
+      item(layer, bh, a.lo + static_cast<int>(r - bh * span), g);
     }
   }
 }
@@ -843,6 +912,14 @@ extern "C" kvq_status kivi_pack(const kivi_packed* caches, const uint16_t* const
   a.hi = hi;
   a.eps = eps;
   a.levels = static_cast<float>((1 << c0.bits) - 1);
+  {
+    const int64_t span = hi - lo, G = c0.head_dim / c0.group_size;
+    const int64_t bhc = static_cast<int64_t>(c0.batch) * c0.num_heads;
+    a.fast32 = bhc * span * G < (1LL << 31) && bhc * (span / c0.group_size) < (1LL << 31);
+    a.div_g = make_divu32(static_cast<uint32_t>(G));
+    a.div_span = make_divu32(static_cast<uint32_t>(span));
+    a.div_ngroups = make_divu32(static_cast<uint32_t>(span / c0.group_size));
+  }
   const int sms = sm_count() > 0 ? sm_count() : 152;
   // keys: a thread per (group, 8-channel chunk), or at head_dim 64 a warp per group
   const bool d64 = c0.head_dim == 64;
