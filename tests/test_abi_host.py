@@ -298,3 +298,40 @@ def test_kivi_protocol_rejects_bad_arguments_before_launch(kvq):
     assert u(C, xs, xs, 1, 0, 129, None) == 2
     assert u(C, xs, xs, 1, 10, 5, None) == 2
     assert u(C, xs, xs, 1, 7, 7, None) == 0                         # empty: no launch
+
+
+def _side(kvq, k=3, ns=4, max_seqs=1, val=FAKE, idx=FAKE, sink=FAKE):
+    return kvq.kvq_side(k, ns, max_seqs, val, idx, sink)
+
+
+def test_side_rejects_bad_arguments_before_launch(kvq):
+    pools = (kvq.kvq_pool * 1)(_pool(kvq))
+    xs = (ctypes.c_void_p * 1)(FAKE)
+    S = lambda **kw: (kvq.kvq_side * 1)(_side(kvq, **kw))
+    qp = lambda sd, nseq=1: kvq._lib.kvq_quant_pack_paged_side(pools, sd, xs, 1, FAKE, 4, FAKE,
+                                                               FAKE, nseq, 16, None, None)
+    dq = lambda sd: kvq._lib.kvq_dequant_paged_side(pools, sd, xs, 1, FAKE, 4, FAKE, FAKE, 1, 16,
+                                                    None, None)
+    assert qp(None) == 3                            # no side array
+    assert qp(S(k=9)) == 5                          # more than KVQ_MAX_OUTLIERS
+    assert qp(S(k=-1)) == 5
+    assert qp(S(ns=17)) == 5                        # more than KVQ_MAX_SINKS
+    assert qp(S(val=0)) == 3                        # outliers without value / position arrays
+    assert qp(S(idx=0)) == 3
+    assert qp(S(sink=0)) == 3                       # sinks without a buffer
+    assert qp(S(val=FAKE + 2)) == 4
+    assert qp(S(), nseq=2) == 5                     # the sink buffer holds one sequence
+    assert dq(S(k=9)) == 5
+    assert dq(S(idx=FAKE + 8)) == 4
+    two = (kvq.kvq_pool * 2)(_pool(kvq), _pool(kvq))
+    mixed = (kvq.kvq_side * 2)(_side(kvq, k=3), _side(kvq, k=2))
+    assert kvq._lib.kvq_quant_pack_paged_side(two, mixed, (ctypes.c_void_p * 2)(FAKE, FAKE), 2,
+                                              FAKE, 4, FAKE, FAKE, 1, 16, None, None) == 2
+
+    P = lambda **kw: (kvq.kvq_pool * 1)(_pool(kvq, **kw))
+    attn = lambda kp, vp, ks, vs, ws=1 << 30: kvq._lib.kvq_decode_attn_side(
+        kp, vp, ks, vs, 1, FAKE, 24, FAKE, 4, FAKE, 1, 64, 0.0625, FAKE, FAKE, ws, None, None)
+    assert attn(P(ps=8), P(ps=8), S(), S()) == 2    # the staged kernel needs pages of 16k
+    assert attn(P(), P(), S(k=9), S(k=9)) == 5
+    assert attn(P(), P(), S(), S(sink=0)) == 3
+    assert attn(P(), P(), S(), S(), ws=16) == 8
