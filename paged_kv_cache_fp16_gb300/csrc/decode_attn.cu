@@ -397,13 +397,11 @@ __device__ __forceinline__ void cta_merge_write(const AttnArgs& a, float* sm, in
 
 // ------------------------------------------------------------------------------ TMA kernel
 // Fused append: quantize the new K and V rows of (layer, sequence s, KV head h) exactly as
-// kvq_quant_pack_paged does, store them at position `pos` of the pools (physical row `prow`) and
-// over row `slot` of the warp's shared-memory stage, whose copy of that slot predates the write.
-// Lanes 0-15 take the K row, lanes 16-31 the V row, 16 elements (one unit) per lane.
+// kvq_quant_pack_paged does and store them at physical row `prow` of the pools.  Lanes 0-15 take
+// the K row, lanes 16-31 the V row, 16 elements (one unit) per lane.
 template <int BITS>
 __device__ __forceinline__ void append_rows(const AttnArgs& a, const LayerPools& P, int layer,
-                                            int s, int h, int64_t prow, int slot, uint8_t* sk,
-                                            uint8_t* sv, uint16_t* sks, uint16_t* svs, int lane) {
+                                            int s, int h, int64_t prow, int lane) {
   constexpr int kQm = SymQ<BITS>::kQmax;
   constexpr int kB = SymQ<BITS>::kBias;
   constexpr int kM = SymQ<BITS>::kMask;
@@ -438,11 +436,7 @@ __device__ __forceinline__ void append_rows(const AttnArgs& a, const LayerPools&
   uint16_t* gscales = const_cast<uint16_t*>(is_v ? P.vs : P.ks);
   const int off = u * SymQ<BITS>::kUnitBytes;
   store_unit<BITS>(gcodes + prow * kPd + off, pk[0], pk[1], pk[2], pk[3]);
-  store_unit<BITS>((is_v ? sv : sk) + slot * kPd + off, pk[0], pk[1], pk[2], pk[3]);
-  if (u == 0) {
-    gscales[prow] = sbits;
-    (is_v ? svs : sks)[slot] = sbits;
-  }
+  if (u == 0) gscales[prow] = sbits;
 }
 
 // Column of element d in a residual tile.  Keys follow the score product's k-order: the dense
@@ -609,6 +603,25 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
     }
   };
 
+  if constexpr (APPEND) {
+    // The new token (position len - 1) sits in the sequence's last tile, which exactly one warp
+    // of the grid streams.  That warp quantizes the new rows into the pages before it issues any
+    // copy, so its copy of the tile reads them from global memory (each lane orders its stores
+    // before the bulk copies with a proxy fence); the tile loop itself has no append code.
+    const int ta = (len - 1) / kTile;
+    if (len > 0 && ta >= tile0 && ta < tile1 && (ta - tile0) % kWarps == warp) {   // warp-uniform
+      const int pos = len - 1;
+      const int lp = pos / a.ps;
+      const int page = lp < a.max_pages ? __ldg(a.pt + static_cast<int64_t>(s) * a.max_pages + lp)
+                                        : -1;
+      if (page >= 0 && page < P.k_pages && page < P.v_pages)   // else the tile's issue reports it
+        append_rows<BITS>(a, P, layer, s, h,
+                          (static_cast<int64_t>(page) * a.H + h) * a.ps + (pos - lp * a.ps), lane);
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncwarp();
+    }
+  }
+
   for (int j = 0; j < S && j < n_mine; ++j) {
     const int page = page_of(j);
     if (lane == 0) issue(j, page);
@@ -661,15 +674,6 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
     uint16_t* svs = sks + kTile;
     const bool ok = flags[st] != 0;
     const int tb = (tile0 + warp + j * kWarps) * kTile;
-    if constexpr (APPEND) {
-      const int pos = len - 1;   // the new token; exactly one warp of the grid owns its tile
-      if (ok && pos >= tb && pos < tb + kTile) {   // warp-uniform
-        const int page = page_of(j);
-        const int64_t prow = (static_cast<int64_t>(page) * a.H + h) * a.ps + (pos % a.ps);
-        append_rows<BITS>(a, P, layer, s, h, prow, pos - tb, sk, sv, sks, svs, lane);
-        __syncwarp();
-      }
-    }
     KRegs<BITS> K;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
