@@ -638,13 +638,13 @@ __global__ void __launch_bounds__(kAThreads, 4) kivi_attn_kernel(const KAArgs a)
         tm1 = fmaxf(tm1, __shfl_xor_sync(kFullMask, tm1, o));
       }
       const float n0 = fmaxf(m0, tm0), n1 = fmaxf(m1, tm1);
-      const float al0 = (n0 == kNegInfF) ? 1.f : exp2f(m0 - n0);
-      const float al1 = (n1 == kNegInfF) ? 1.f : exp2f(m1 - n1);
+      const float al0 = (n0 == kNegInfF) ? 1.f : ex2_fast(m0 - n0);
+      const float al1 = (n1 == kNegInfF) ? 1.f : ex2_fast(m1 - n1);
       float p[4];
-      p[0] = (n0 == kNegInfF) ? 0.f : exp2f(sc[0] - n0);
-      p[2] = (n0 == kNegInfF) ? 0.f : exp2f(sc[2] - n0);
-      p[1] = (n1 == kNegInfF) ? 0.f : exp2f(sc[1] - n1);
-      p[3] = (n1 == kNegInfF) ? 0.f : exp2f(sc[3] - n1);
+      p[0] = (n0 == kNegInfF) ? 0.f : ex2_fast(sc[0] - n0);
+      p[2] = (n0 == kNegInfF) ? 0.f : ex2_fast(sc[2] - n0);
+      p[1] = (n1 == kNegInfF) ? 0.f : ex2_fast(sc[1] - n1);
+      p[3] = (n1 == kNegInfF) ? 0.f : ex2_fast(sc[3] - n1);
       l0 = l0 * al0 + (p[0] + p[2]);
       l1 = l1 * al1 + (p[1] + p[3]);
       m0 = n0;

@@ -36,6 +36,15 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t r[4]) {
                : "memory");
 }
 
+// 2^x by the hardware's approximate exponential (ex2.approx.ftz: relative error about 2^-22,
+// results below 2^-126 flushed to 0) -- the softmax weights of a tile, far inside the attention
+// tolerance.
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t movtrans(uint32_t x) {
   uint32_t r;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
