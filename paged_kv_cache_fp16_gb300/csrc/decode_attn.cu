@@ -227,6 +227,15 @@ struct QFragSmem {
   }
 };
 
+// The tile softmax's 2^x: the hardware's approximate exponential for q6/q4 (1.305 -> 1.271 ms and
+// 1.145 -> 1.106 ms on the 16-layer decode), the library exp2f for q8, whose kernel measured
+// 2.3 % slower with the approximate one (1.488 vs 1.454 ms).
+template <int BITS>
+__device__ __forceinline__ float softmax_exp2(float x) {
+  if constexpr (BITS == 8) return exp2f(x);
+  else return ex2_fast(x);
+}
+
 // With SIDE, kc[4] (same layout as the scores) is added after the row scale -- the outlier and
 // sink terms of the keys -- and p[4] is returned for the value side terms.
 template <int BITS, bool SIDE = false, typename QF>
@@ -277,13 +286,13 @@ __device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const QF& 
     tm1 = fmaxf(tm1, __shfl_xor_sync(kFullMask, tm1, o));
   }
   const float n0 = fmaxf(m0, tm0), n1 = fmaxf(m1, tm1);
-  const float al0 = (n0 == kNegInf) ? 1.f : ex2_fast(m0 - n0);
-  const float al1 = (n1 == kNegInf) ? 1.f : ex2_fast(m1 - n1);
+  const float al0 = (n0 == kNegInf) ? 1.f : softmax_exp2<BITS>(m0 - n0);
+  const float al1 = (n1 == kNegInf) ? 1.f : softmax_exp2<BITS>(m1 - n1);
   float p[4];
-  p[0] = (n0 == kNegInf) ? 0.f : ex2_fast(sc[0] - n0);
-  p[2] = (n0 == kNegInf) ? 0.f : ex2_fast(sc[2] - n0);
-  p[1] = (n1 == kNegInf) ? 0.f : ex2_fast(sc[1] - n1);
-  p[3] = (n1 == kNegInf) ? 0.f : ex2_fast(sc[3] - n1);
+  p[0] = (n0 == kNegInf) ? 0.f : softmax_exp2<BITS>(sc[0] - n0);
+  p[2] = (n0 == kNegInf) ? 0.f : softmax_exp2<BITS>(sc[2] - n0);
+  p[1] = (n1 == kNegInf) ? 0.f : softmax_exp2<BITS>(sc[1] - n1);
+  p[3] = (n1 == kNegInf) ? 0.f : softmax_exp2<BITS>(sc[3] - n1);
   l0 = l0 * al0 + (p[0] + p[2]);
   l1 = l1 * al1 + (p[1] + p[3]);
   m0 = n0;
