@@ -55,7 +55,7 @@ def _compare_state(pools, sides, opools, osides, n_sink):
 
 @pytest.mark.parametrize("bits", [8, 6, 4])
 @pytest.mark.parametrize("D,k,n_sink", [(256, 3, 4), (256, 8, 16), (128, 2, 0), (64, 0, 4),
-                                        (256, 1, 1), (16, 8, 2)])
+                                        (256, 1, 1), (16, 8, 2), (48, 5, 2), (96, 3, 0)])
 def test_quant_dequant_side_bit_exact(kvq, cuda_dev, bits, D, k, n_sink):
     H, ps = 4, 16
     lens, starts = [1, 5, 40, 100], [0, 0, 0, 0]
