@@ -47,6 +47,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 16;
 constexpr int kRec = kD + 4;   // workspace record per (split, head): O[256], m, l, pad, pad
 #define kNegInf (-__int_as_float(0x7f800000))
+#define kMaxFloor (-1e30f)   // floor of the running max; a max still at it saw no valid token
 
 struct LayerPools {
   const uint8_t* kc;
@@ -245,25 +246,24 @@ __device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const QF& 
                                                 uint32_t& pb0, uint32_t& pb1,
                                                 const float* kc = nullptr,
                                                 float* p_out = nullptr) {
-  // ---------------- S^T = C_K . Q^T on the exact integer codes (four independent accumulation
-  // chains); each token row's fp16 scale multiplies its scores afterwards (the code-times-scale
-  // products are exact instead of rounded to fp16 -- a difference far inside the tolerance)
-  float sacc4[4][4] = {};
+  // ---------------- S^T = C_K . Q^T on the exact integer codes, one accumulation chain (four
+  // independent chains measured 3.3 % slower at q6: their 12 registers cost the 128-register
+  // kernel more than the chain's latency); each token row's fp16 scale multiplies its scores
+  // afterwards (the code-times-scale products are exact instead of rounded to fp16 -- a
+  // difference far inside the tolerance)
+  float sacc[4] = {};
 #define KVQ_QK_GROUP(GI)                                                                \
   {                                                                                     \
     uint32_t p0[4], p1[4];                                                              \
     unpack_group<BITS, GI>(T.kw[0], p0);                                                \
     unpack_group<BITS, GI>(T.kw[1], p1);                                                \
     const uint2 qa = Q.pair(2 * GI), qb = Q.pair(2 * GI + 1);                           \
-    mma16816(sacc4[(2 * GI) & 3], p0[0], p1[0], p0[1], p1[1], qa.x, qa.y);              \
-    mma16816(sacc4[(2 * GI + 1) & 3], p0[2], p1[2], p0[3], p1[3], qb.x, qb.y);          \
+    mma16816(sacc, p0[0], p1[0], p0[1], p1[1], qa.x, qa.y);                             \
+    mma16816(sacc, p0[2], p1[2], p0[3], p1[3], qb.x, qb.y);                             \
   }
   KVQ_QK_GROUP(0) KVQ_QK_GROUP(1) KVQ_QK_GROUP(2) KVQ_QK_GROUP(3)
   KVQ_QK_GROUP(4) KVQ_QK_GROUP(5) KVQ_QK_GROUP(6) KVQ_QK_GROUP(7)
 #undef KVQ_QK_GROUP
-  float sacc[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) sacc[k] = (sacc4[0][k] + sacc4[1][k]) + (sacc4[2][k] + sacc4[3][k]);
 
   // ---------------- online softmax (log2 domain); sacc: [tok g | g+8][head 2c | 2c+1]
   float sc[4];
@@ -285,14 +285,16 @@ __device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const QF& 
     tm0 = fmaxf(tm0, __shfl_xor_sync(kFullMask, tm0, o));
     tm1 = fmaxf(tm1, __shfl_xor_sync(kFullMask, tm1, o));
   }
-  const float n0 = fmaxf(m0, tm0), n1 = fmaxf(m1, tm1);
-  const float al0 = (n0 == kNegInf) ? 1.f : softmax_exp2<BITS>(m0 - n0);
-  const float al1 = (n1 == kNegInf) ? 1.f : softmax_exp2<BITS>(m1 - n1);
+  // the running max never drops below a finite floor (far below any score fp16 inputs can
+  // give), so no exponential below needs a guard against -inf - -inf
+  const float n0 = fmaxf(fmaxf(m0, tm0), kMaxFloor), n1 = fmaxf(fmaxf(m1, tm1), kMaxFloor);
+  const float al0 = softmax_exp2<BITS>(m0 - n0);
+  const float al1 = softmax_exp2<BITS>(m1 - n1);
   float p[4];
-  p[0] = (n0 == kNegInf) ? 0.f : softmax_exp2<BITS>(sc[0] - n0);
-  p[2] = (n0 == kNegInf) ? 0.f : softmax_exp2<BITS>(sc[2] - n0);
-  p[1] = (n1 == kNegInf) ? 0.f : softmax_exp2<BITS>(sc[1] - n1);
-  p[3] = (n1 == kNegInf) ? 0.f : softmax_exp2<BITS>(sc[3] - n1);
+  p[0] = softmax_exp2<BITS>(sc[0] - n0);
+  p[2] = softmax_exp2<BITS>(sc[2] - n0);
+  p[1] = softmax_exp2<BITS>(sc[1] - n1);
+  p[3] = softmax_exp2<BITS>(sc[3] - n1);
   l0 = l0 * al0 + (p[0] + p[2]);
   l1 = l1 * al1 + (p[1] + p[3]);
   m0 = n0;
@@ -361,6 +363,8 @@ __device__ __forceinline__ void cta_merge_write(const AttnArgs& a, float* sm, in
                                                 int split, int warp, int g, int c,
                                                 const float (&acc)[16][4], float m0, float m1,
                                                 float l0, float l1) {
+  if (m0 == kMaxFloor) m0 = kNegInf;   // no valid token: an empty partial for the merges
+  if (m1 == kMaxFloor) m1 = kNegInf;
   float (*sm_o)[8][kD] = reinterpret_cast<float (*)[8][kD]>(sm);
   float (*sm_m)[8] = reinterpret_cast<float (*)[8]>(sm + kWarps * 8 * kD);
   float (*sm_l)[8] = reinterpret_cast<float (*)[8]>(sm + kWarps * 8 * kD + kWarps * 8);
@@ -576,28 +580,32 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
   }
   __syncwarp();
 
-  // Page ids of this warp's tiles, 32 at a time: lane i holds the id of tile 32 * blk + i, so
-  // the per-tile issue needs a shuffle instead of a dependent global load.  All lanes call it.
-  int pg_blk = -1, pg_val = -1;
-  auto page_of = [&](int j) -> int {
+  // Page ids and in-page slots of this warp's tiles, 32 at a time: lane i holds those of tile
+  // 32 * blk + i, so the per-tile issue needs two shuffles instead of a dependent global load and
+  // a division by the page size in one lane (0.85 % of the 16-layer decode).  All lanes call it.
+  int pg_blk = -1, pg_val = -1, sl_val = 0;
+  auto page_of = [&](int j, int& slot) -> int {
     const int blk = j >> 5;
     if (blk != pg_blk) {   // warp-uniform
       pg_blk = blk;
       pg_val = -1;
+      sl_val = 0;
       const int jl = blk * 32 + lane;
       if (jl < n_mine) {
-        const int lp = (tile0 + warp + jl * kWarps) * kTile / a.ps;
+        const int tok = (tile0 + warp + jl * kWarps) * kTile;
+        const int lp = tok / a.ps;
+        sl_val = tok - lp * a.ps;
         if (lp < a.max_pages) pg_val = __ldg(a.pt + static_cast<int64_t>(s) * a.max_pages + lp);
       }
     }
+    slot = __shfl_sync(kFullMask, sl_val, j & 31);
     return __shfl_sync(kFullMask, pg_val, j & 31);
   };
 
-  // Issue the loads of this warp's j-th tile (page id `page`) into stage j % S (lane 0 only).
-  auto issue = [&](int j, int page) {
+  // Issue the loads of this warp's j-th tile (page id `page`, first slot `slot0`) into stage
+  // j % S (lane 0 only).
+  auto issue = [&](int j, int page, int slot0) {
     const int st = j % S;
-    const int tb = (tile0 + warp + j * kWarps) * kTile;
-    const int slot0 = tb % a.ps;
     const bool ok = page >= 0 && page < P.k_pages && page < P.v_pages;
     flags[st] = ok ? 1 : 0;
     uint8_t* dst = wbase + st * kStageBytes;
@@ -643,8 +651,9 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
   }
 
   for (int j = 0; j < S && j < n_mine; ++j) {
-    const int page = page_of(j);
-    if (lane == 0) issue(j, page);
+    int slot;
+    const int page = page_of(j, slot);
+    if (lane == 0) issue(j, page, slot);
   }
 
   // The query fragments: for q6/q4 computed once per CTA (warp 0) into shared memory, which
@@ -773,11 +782,12 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
       }
     }
     // the stage's bytes are in registers: hand it back to the copy engine
-    const int next_page = (j + S < n_mine) ? page_of(j + S) : -1;   // warp-uniform condition
+    int next_slot = 0;
+    const int next_page = (j + S < n_mine) ? page_of(j + S, next_slot) : -1;   // warp-uniform condition
     __syncwarp();
     if (lane == 0 && j + S < n_mine) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(j + S, next_page);
+      issue(j + S, next_page, next_slot);
       ++issued;
     }
     tile_pv<BITS>(V, pb0, pb1, acc);
