@@ -208,6 +208,18 @@ struct KRegs {
   bool kval[2];
 };
 
+// The same tile with the K words left in the stage: the unpack reads each group's words from
+// shared memory as it goes, so no copy of them is held across Q.K^T.  Taken by the side-channel
+// kernel (2.35 -> 2.19 ms at q6: it frees the registers its side passes need) and at q8 (-0.7 %);
+// the plain q6 and q4 kernels measured 0.5 % and 0.3 % slower with it.
+template <int BITS>
+struct KStage {
+  const uint32_t* kw[2];   // the rows' packed K words in the stage
+  float ksc[2];
+  float vsc[2];
+  bool kval[2];
+};
+
 template <int BITS>
 struct VRegs {
   uint32_t vw[4][Wd<BITS>::kVWords];
@@ -239,8 +251,8 @@ __device__ __forceinline__ float softmax_exp2(float x) {
 
 // With SIDE, kc[4] (same layout as the scores) is added after the row scale -- the outlier and
 // sink terms of the keys -- and p[4] is returned for the value side terms.
-template <int BITS, bool SIDE = false, typename QF>
-__device__ __forceinline__ void tile_qk_softmax(const KRegs<BITS>& T, const QF& Q,
+template <int BITS, bool SIDE = false, typename QF, typename KT>
+__device__ __forceinline__ void tile_qk_softmax(const KT& T, const QF& Q,
                                                 float (&acc)[16][4], float& m0, float& m1,
                                                 float& l0, float& l1, float qk_scale,
                                                 uint32_t& pb0, uint32_t& pb1,
@@ -703,7 +715,8 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
     uint16_t* svs = sks + kTile;
     const bool ok = flags[st] != 0;
     const int tb = (tile0 + warp + j * kWarps) * kTile;
-    KRegs<BITS> K;
+    constexpr bool kStageK = SIDE || BITS == 8;
+    typename std::conditional<kStageK, KStage<BITS>, KRegs<BITS>>::type K;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       // fragment row g + 8r holds this token (side channels: in tok_order)
@@ -711,12 +724,17 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
       K.kval[r] = ok && tb + row < len;
       K.ksc[r] = (SIDE && tb + row < sd.n_sink) ? 0.f : h2f(sks[row]);   // sinks: exact below
       K.vsc[r] = (K.kval[r] && !(SIDE && tb + row < sd.n_sink)) ? h2f(svs[row]) : 0.f;
-      const uint4* src = reinterpret_cast<const uint4*>(sk + row * kPd + c * (4 * W::kKWords));
+      const uint8_t* krow = sk + row * kPd + c * (4 * W::kKWords);
+      if constexpr (kStageK) {
+        K.kw[r] = reinterpret_cast<const uint32_t*>(krow);
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(krow);
 #pragma unroll
-      for (int i = 0; i < W::kKWords / 4; ++i) {
-        const uint4 v = src[i];
-        K.kw[r][4 * i] = v.x; K.kw[r][4 * i + 1] = v.y;
-        K.kw[r][4 * i + 2] = v.z; K.kw[r][4 * i + 3] = v.w;
+        for (int i = 0; i < W::kKWords / 4; ++i) {
+          const uint4 v = src[i];
+          K.kw[r][4 * i] = v.x; K.kw[r][4 * i + 1] = v.y;
+          K.kw[r][4 * i + 2] = v.z; K.kw[r][4 * i + 3] = v.w;
+        }
       }
     }
     uint32_t pb0, pb1;
