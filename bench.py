@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 # the CPU baseline is reported for the threads it uses: keep BLAS single-threaded
@@ -115,7 +116,7 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"kvq_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:

@@ -7,7 +7,7 @@ no kernel consumes the packed bytes; plain KV quant dequantizes and then runs SD
 oracle's attention is exactly that: dequantize the cache with the oracle's own quantizer, then
 compute softmax(q . k_hat * scale) . v_hat per query head, here in float64.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 * one decode query per sequence attends to every cached token of that sequence (no mask);
 * grouped-query attention maps query head j to KV head j // (Hq / H);
 * the softmax is the max-subtracted exponential normalised by its sum;

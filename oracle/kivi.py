@@ -15,7 +15,7 @@ repeating its last element); per group gmin, gmax; scale = max((gmax - gmin) / l
 codes = clip(round((x - gmin) / scale), 0, levels); recon = codes * scale + gmin; drop the pad;
 cast back to the input dtype.
 
-Readings where the page is silent (each listed in the design doc):
+Readings where the page is silent:
 * ``round`` is round-half-to-even (numpy/MLX ``round`` semantics);
 * ``codes * scale + gmin`` is two float32 operations with two roundings (no fused multiply-add);
 * ``eps`` is float32(1e-8) and ``levels`` is used as a float32 divisor;

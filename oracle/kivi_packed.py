@@ -8,7 +8,7 @@ fp16 and only estimates what a packed form would cost (module docstring, "Memory
 -- per (token group, channel) for keys, per (token, channel group) for values.  This module is
 that packed form, with the groups, axes, levels and eps of ``_quant_dequant_along``.
 
-Readings (listed in DESIGN.md):
+Readings where the pages leave a step open:
 * zero = gmin, which is an fp16 value already (the minimum of fp16 inputs), so it is stored
   exactly; scale16 = fp16_rne(max(float32(gmax - gmin) / levels, float32(eps)));
 * codes are computed against the stored fp16 scale (as the symmetric quantizer computes its codes

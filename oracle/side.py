@@ -10,7 +10,7 @@ fp16 and kept out of the fit.  The page's non-uniform (Lloyd-Max) levels are not
 are not used: the dense part here is the symmetric per-token-per-head quantizer of MTPLX pull
 request #267 (module ``symmetric``).
 
-Readings (listed in DESIGN.md):
+Readings where the pages leave a step open:
 * a vector is one (token, KV head) row of D elements;
 * a row keeps k = ceil(fraction * D) outliers: its k elements of largest magnitude, ties to the
   lower position (k = 3 at D = 256 and the page's 0.01);

@@ -14,7 +14,7 @@ What the page fixes:
 * packed_dim(D, 6) = 3D/4 and q6 needs D % 4 == 0 (packed_dim sentence); q6 shares q4's uint8
   sub-byte storage branch.
 
-Readings where the page is silent (each listed in the design doc):
+Readings where the page is silent:
 * scale = fp16_rne(float32(amax) / float32(qmax)), an IEEE float32 quotient rounded to fp16;
   codes are computed against that stored fp16 scale:
   c = clamp(rint_half_even(float32(x) / float32(scale)), -qmax, qmax);
