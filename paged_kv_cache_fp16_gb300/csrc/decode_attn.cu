@@ -799,9 +799,9 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
         }
       }
     }
-    // the stage's bytes are in registers: hand it back to the copy engine
+    // every byte of the stage has been read: hand it back to the copy engine
     int next_slot = 0;
-    const int next_page = (j + S < n_mine) ? page_of(j + S, next_slot) : -1;   // warp-uniform condition
+    const int next_page = (j + S < n_mine) ? page_of(j + S, next_slot) : -1;   // warp-uniform
     __syncwarp();
     if (lane == 0 && j + S < n_mine) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
