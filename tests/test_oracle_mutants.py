@@ -12,17 +12,22 @@ the kind a restatement of the pages could make:
 - an off-by-one residual boundary;
 - a dropped softmax scale;
 - a GQA head map taken modulo the KV heads;
-- the outlier tie broken toward the higher position.
+- the outlier tie broken toward the higher position;
+- a paged scatter that ignores the page table;
+- packed KIVI codes by floor;
+- a packed KIVI zero point at the group maximum.
 """
 import numpy as np
 import pytest
 
 import test_oracle_attention as TA
 import test_oracle_kivi as TK
+import test_oracle_kivi_packed as TP
 import test_oracle_side as TS
 import test_oracle_symmetric as TY
 from oracle import attention as A
 from oracle import kivi as K
+from oracle import kivi_packed as P
 from oracle import side as SD
 from oracle import symmetric as S
 
@@ -207,3 +212,51 @@ def test_symmetric_restatement_passes(monkeypatch, bits):
     monkeypatch.setattr(S, "quantize_rows", _quantize_with(_fp16_scale, np.rint))
     assert not _rejected(TY.test_golden_rows,
                          lambda: TY.test_codes_are_nearest_against_stored_scale(bits))
+
+
+# ------------------------------------------------------------------ paged scatter, packed KIVI
+def test_scatter_ignoring_the_page_table_is_rejected(monkeypatch):
+    def locate(page_table, seq, pos, page_size):
+        pos = np.asarray(pos, dtype=np.int64)
+        return seq * page_table.shape[1] + pos // page_size, pos % page_size
+    monkeypatch.setattr(S, "locate", locate)
+    assert _rejected(lambda: TY.test_paged_scatter_places_every_row_through_the_page_table(6))
+
+
+def test_scatter_restatement_passes(monkeypatch):
+    def locate(page_table, seq, pos, page_size):
+        pos = np.asarray(pos, dtype=np.int64)
+        return page_table[seq, pos // page_size].astype(np.int64), pos % page_size
+    monkeypatch.setattr(S, "locate", locate)
+    assert not _rejected(lambda: TY.test_paged_scatter_places_every_row_through_the_page_table(6))
+
+
+def _packed_codes_with(round_fn):
+    def _codes(x32, zero32, scale16, levels):
+        s32 = scale16.astype(np.float32)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            q = (x32 - zero32) / s32
+        c = np.where(s32 == 0, 0, np.clip(round_fn(q), 0, levels))
+        return c.astype(np.int64)
+    return _codes
+
+
+def test_packed_kivi_restatement_passes(monkeypatch):
+    monkeypatch.setattr(P, "_codes", _packed_codes_with(np.rint))
+    assert not _rejected(TP.test_golden_keys, TP.test_golden_values,
+                         lambda: TP.test_codes_nearest_against_stored_scale_and_error_bound(2))
+
+
+def test_packed_kivi_floor_codes_are_rejected(monkeypatch):
+    monkeypatch.setattr(P, "_codes", _packed_codes_with(np.floor))
+    assert _rejected(TP.test_golden_keys, TP.test_golden_values,
+                     lambda: TP.test_codes_nearest_against_stored_scale_and_error_bound(2))
+
+
+def test_packed_kivi_zero_at_the_group_max_is_rejected(monkeypatch):
+    def _params(gmin32, gmax32, levels, eps):
+        scale32 = np.maximum((gmax32 - gmin32) / np.float32(levels), np.float32(eps))
+        return scale32.astype(np.float16), gmax32.astype(np.float16)
+    monkeypatch.setattr(P, "_params", _params)
+    assert _rejected(TP.test_golden_keys, TP.test_golden_values,
+                     lambda: TP.test_codes_nearest_against_stored_scale_and_error_bound(2))
