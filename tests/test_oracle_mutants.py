@@ -15,7 +15,9 @@ the kind a restatement of the pages could make:
 - the outlier tie broken toward the higher position;
 - a paged scatter that ignores the page table;
 - packed KIVI codes by floor;
-- a packed KIVI zero point at the group maximum.
+- a packed KIVI zero point at the group maximum;
+- an attention window missing its last token;
+- a side-channel dense row that keeps its outliers.
 """
 import numpy as np
 import pytest
@@ -260,3 +262,24 @@ def test_packed_kivi_zero_at_the_group_max_is_rejected(monkeypatch):
     monkeypatch.setattr(P, "_params", _params)
     assert _rejected(TP.test_golden_keys, TP.test_golden_values,
                      lambda: TP.test_codes_nearest_against_stored_scale_and_error_bound(2))
+
+
+# ------------------------------------------------------------------ windows and dense rows
+def test_attention_window_missing_its_last_token_is_rejected(monkeypatch):
+    orig = A.gather_dequant
+
+    def gather_dequant(pool, page_table, seq, length, heads=None):
+        out = orig(pool, page_table, seq, length, heads)
+        return out[:-1] if length > 1 else out
+    monkeypatch.setattr(A, "gather_dequant", gather_dequant)
+    assert _rejected(lambda: TA.test_paged_equals_contiguous(6))
+
+
+def test_side_dense_row_keeping_its_outliers_is_rejected(monkeypatch):
+    orig = SD.split_outliers
+
+    def split_outliers(x16, k):
+        _, pos, val = orig(x16, k)
+        return x16.copy(), pos, val      # mistake: the outliers stay in the dense row
+    monkeypatch.setattr(SD, "split_outliers", split_outliers)
+    assert _rejected(lambda: TS.test_dense_scale_exact_outliers_and_round_trip_bound(6, 3))
