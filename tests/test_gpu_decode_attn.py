@@ -10,6 +10,8 @@ import torch
 import kvgen
 from oracle import attention as oa
 from oracle import symmetric as osym
+from _attn_checks import (Planted, assert_attn_close, decode_tiles_per_cta, needle_row,
+                          paged_needle_positions)
 from _gpu_util import cu_of, dev_tensor, i32
 
 pytestmark = pytest.mark.gpu
@@ -43,9 +45,7 @@ def _attend(kvq, dev, kps, vps, q, pt, lens, scale):
 
 
 def _close(got, ref):
-    bad = np.abs(got - ref) > ATOL + RTOL * np.abs(ref)
-    assert not bad.any(), (f"{int(bad.sum())} outside tol; max abs err "
-                           f"{float(np.abs(got - ref).max()):.3e}")
+    assert_attn_close(got, ref)
 
 
 @pytest.mark.parametrize("bits", [8, 6, 4])
@@ -141,7 +141,10 @@ def test_full_context_262144_sampled(kvq, cuda_dev, bits):
     """The full-context workload: a 262,144-token paged cache, 16 layers x 4 KV heads x 256,
     page 16, random table, batch 1, 24 query heads (GQA 6:1), softmax scale 1/16, in one call
     over all layers.  Checked against the oracle for sampled (layer, KV head) pairs; every
-    output must be finite."""
+    output must be finite.  In each sampled pair the keys carry needles for the group's first
+    query head at the first and last tile, both sides of a split boundary, deep in a warp's
+    stream, the middle split and the last token, so one lost or misplaced tile there falls
+    outside the tolerance (which a whole-window average over 262,144 tokens would not show)."""
     w = kvgen.WORKLOADS["decode_attn_262144_16L_4x256_gqa6"]
     L, T, H, D, ps, hq = w["n_layers"], w["n_tok"], w["H"], w["D"], w["page_size"], w["Hq"]
     G = hq // H
@@ -149,12 +152,23 @@ def test_full_context_262144_sampled(kvq, cuda_dev, bits):
     pt = i32(pt_np, cuda_dev)
     cu = i32([0, T], cuda_dev)
     st = i32([0], cuda_dev)
+    samples = [(0, 0), (L - 1, H - 1)] if bits == 6 else [(L // 2, 1)]
+    qn = kvgen.queries_np(w["seed"], L, 1, hq, D)
+    tpc = decode_tiles_per_cta(L, 1, H, T, torch.cuda.get_device_properties(cuda_dev)
+                               .multi_processor_count)
+    pos = paged_needle_positions(T, tpc, stages=3 if bits == 4 else 2)
     kps, vps, specs = [], [], []
     for layer in range(L):
         pair = []
         for is_key in (True, False):
-            s = kvgen.KVSpec(seed=w["seed"], layer=layer, is_key=is_key, n_seq=1, n_tok=T,
-                             num_heads=H, head_dim=D)
+            s = Planted(kvgen.KVSpec(seed=w["seed"], layer=layer, is_key=is_key, n_seq=1,
+                                     n_tok=T, num_heads=H, head_dim=D))
+            if is_key:
+                for sl, h in samples:
+                    if sl == layer:
+                        row = needle_row(qn[layer, 0, h * G], w["softmax_scale"])
+                        for t in pos:
+                            s.rows[t * H + h] = row
             x = s.full_torch(cuda_dev)
             p = kvq.Pool.empty(bits, H, D, ps, pt_np.size, cuda_dev)
             kvq.kvq_quant_pack_paged([p], [x], pt, cu, st)
@@ -163,11 +177,9 @@ def test_full_context_262144_sampled(kvq, cuda_dev, bits):
         specs.append((pair[0][0], pair[1][0]))
         kps.append(pair[0][1])
         vps.append(pair[1][1])
-    q = kvgen.queries_torch(w["seed"], L, 1, hq, D, cuda_dev)
+    q = dev_tensor(qn, cuda_dev)
     got = _attend(kvq, cuda_dev, kps, vps, q, pt, [T], w["softmax_scale"])
     assert np.all(np.isfinite(got))
-    qn = q.cpu().numpy()
-    samples = [(0, 0), (L - 1, H - 1)] if bits == 6 else [(L // 2, 1)]
     rows_all = np.arange(T, dtype=np.int64) * H
     for layer, h in samples:
         ks, vs = specs[layer]

@@ -14,6 +14,8 @@ import torch
 import kvgen
 from oracle import attention as oa
 from oracle import symmetric as osym
+from _attn_checks import (Planted, assert_attn_close, decode_tiles_per_cta, needle_row,
+                          paged_needle_positions, plant_needles)
 from _gpu_util import (check_rows_against_oracle, cu_of, dev_tensor, i32, random_rows, u16)
 
 pytestmark = pytest.mark.gpu
@@ -146,14 +148,32 @@ def test_zero_tokens_is_a_no_op(kvq, cuda_dev):
 
 
 # ------------------------------------------------------------------------ full-size workloads
+# (layer, sequence, KV head) triples whose keys carry needles for the group's first query head,
+# and whose decode outputs are checked against the oracle
+NEEDLE_TRIPLES = [(0, 0, 0), (15, 7, 3), (7, 3, 2)]
+
+
 @pytest.fixture(scope="module")
 def prefill_inputs(cuda_dev):
+    """The paged-prefill inputs, with needles planted in the keys of NEEDLE_TRIPLES at the tiles a
+    decode schedule gets wrong (first/last tile, both sides of a split boundary, deep in a warp's
+    stream, the middle split, the last token)."""
     w = kvgen.WORKLOADS["paged_prefill_16L_8x32768_4x256"]
+    L, nseq, ntok, H, D = w["n_layers"], w["n_seq"], w["n_tok"], w["H"], w["D"]
+    qn = kvgen.queries_np(w["seed"], L, nseq, 24, D)
+    tpc = decode_tiles_per_cta(L, nseq, H, ntok,
+                               torch.cuda.get_device_properties(cuda_dev).multi_processor_count)
+    pos = paged_needle_positions(ntok, tpc, stages=2)
     specs, xs = [], []
-    for layer in range(w["n_layers"]):
+    for layer in range(L):
         for is_key in (True, False):
-            s = kvgen.KVSpec(seed=w["seed"], layer=layer, is_key=is_key, n_seq=w["n_seq"],
-                             n_tok=w["n_tok"], num_heads=w["H"], head_dim=w["D"])
+            s = Planted(kvgen.KVSpec(seed=w["seed"], layer=layer, is_key=is_key, n_seq=nseq,
+                                     n_tok=ntok, num_heads=H, head_dim=D))
+            if is_key:
+                for tl, ts, th in NEEDLE_TRIPLES:
+                    if tl == layer:
+                        plant_needles(s, ts, th, pos, needle_row(qn[layer, ts, th * (24 // H)],
+                                                                 1.0 / 16.0))
             specs.append(s)
             xs.append(s.full_torch(cuda_dev))
     pt_np = kvgen.random_page_table(1, w["n_seq"], w["n_tok"] // w["page_size"])
@@ -181,7 +201,7 @@ def _decode_on_prefill_pools(kvq, dev, w, specs, pools, pt, bits):
     assert np.all(np.isfinite(got))
     qn = q.cpu().numpy()
     rng = np.random.default_rng(100 + bits)
-    triples = [(0, 0, 0), (L - 1, nseq - 1, H - 1)] + [
+    triples = list(NEEDLE_TRIPLES) + [
         (int(rng.integers(L)), int(rng.integers(nseq)), int(rng.integers(H))) for _ in range(2)]
     for layer, s, h in triples:
         rows = (s * ntok + np.arange(ntok, dtype=np.int64)) * H + h
@@ -190,9 +210,7 @@ def _decode_on_prefill_pools(kvq, dev, w, specs, pools, pt, bits):
         v_hat = osym.dequant_rows(*osym.quant_pack_rows(vs.rows_np(rows), bits), bits, D)
         ref = oa.attend(qn[layer, s, h * G:(h + 1) * G], k_hat[:, None, :], v_hat[:, None, :],
                         scale)
-        g = got[layer, s, h * G:(h + 1) * G]
-        bad = np.abs(g - ref) > 2e-3 + 1e-3 * np.abs(ref)
-        assert not bad.any(), (layer, s, h, float(np.abs(g - ref).max()))
+        assert_attn_close(got[layer, s, h * G:(h + 1) * G], ref, f"layer {layer} seq {s} head {h}")
     del out, ws
 
 
