@@ -518,7 +518,8 @@ KVQ_API kvq_status kivi_unpack(const kivi_packed* caches, uint16_t* const* k, ui
  *     other threads) race on it and must be serialized by the caller.  Nothing in it needs to be
  *     cleared between calls: every partial a call reads was written earlier by that same call.
  *   - To fit the array, the number of splits over tokens is capped (each split of each
- *     (layer, sequence, KV head) unit takes 8,320 bytes); a problem with more than 4,032
+ *     (layer, sequence, KV head) unit takes 8,320 bytes), so a split may then cover more than
+ *     the usual 256 tiles (4,096 tokens); a problem with more than 4,032
  *     n_layers * nseq * num_kv_heads units does not fit even with one split each and returns
  *     KVQ_ERR_RANGE with the byte counts in kvq_last_error().
  */

@@ -69,6 +69,7 @@ struct AttnArgs {
   const uint16_t* knew[KVQ_MAX_TENSORS];
   const uint16_t* vnew[KVQ_MAX_TENSORS];
   int n_layers, nseq, H, G, Hq, ps, max_pages, n_splits, tiles_per_cta;
+  int len_add;     // tokens attended beyond lens[s]: 1 with the fused append, else 0
   float qk_scale;  // softmax_scale * log2(e)
 };
 
@@ -560,6 +561,10 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
   const int len = __ldg(a.lens + s) + (APPEND ? 1 : 0);
   const int n_tiles = (len + kTile - 1) / kTile;
   const int tile0 = split * a.tiles_per_cta;
+  // a split that starts past the sequence's end has no work and writes no partial (the merge
+  // reads only the splits that hold tokens): with ragged lengths the grid is sized by the longest
+  // sequence, so this keeps the short ones from costing more than a block launch
+  if (tile0 >= n_tiles) return;
   const int tile1 = min(n_tiles, tile0 + a.tiles_per_cta);
   const int n_mine = (tile1 - tile0 - warp + kWarps - 1) > 0
                          ? (tile1 - tile0 - warp + kWarps - 1) / kWarps : 0;
@@ -704,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
   for (int j = 0; j < n_mine; ++j) {
     const int st = j % S;
     const uint32_t parity = static_cast<uint32_t>((j / S) & 1);
-    const bool arrived = mbar_wait_bounded(&bars[st], parity);
+    const bool arrived = mbar_wait_stage(&bars[st], parity);
     if (__any_sync(kFullMask, !arrived)) {   // warp-uniform exit
       timed_out = true;
       break;
@@ -872,6 +877,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_gather_kernel(const A
   const int len = __ldg(a.lens + s);
   const int n_tiles = (len + kTile - 1) / kTile;
   const int tile0 = split * a.tiles_per_cta;
+  if (tile0 >= n_tiles) return;   // no work and no partial, as in the staged kernel
   const int tile1 = min(n_tiles, tile0 + a.tiles_per_cta);
 
   uint32_t qf[16][2];
@@ -944,19 +950,23 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_gather_kernel(const A
   cta_merge_write(a, sm, ls, h, split, warp, g, c, acc, m0, m1, l0, l1);
 }
 
-// One CTA per (query head, layer * nseq + seq); thread d merges the splits of element d.
+// One CTA per (query head, layer * nseq + seq); thread d merges the splits of element d.  Only
+// the splits that start inside the sequence wrote a partial.
 __global__ void __launch_bounds__(kD) decode_merge_kernel(const AttnArgs a) {
   const int j = blockIdx.x;
   const int ls = blockIdx.y;
   const int h = j / a.G, jj = j - h * a.G;
   const int d = threadIdx.x;
+  const int len = __ldg(a.lens + (ls % a.nseq)) + a.len_add;
+  const int n_tiles = (len + kTile - 1) / kTile;
+  const int n_live = min(a.n_splits, (n_tiles + a.tiles_per_cta - 1) / a.tiles_per_cta);
   const float* base = a.ws + ((static_cast<int64_t>(ls) * a.H + h) * a.n_splits) * 8 * kRec +
                       jj * kRec;
   float M = kNegInf;
-  for (int sp = 0; sp < a.n_splits; ++sp) M = fmaxf(M, base[sp * 8 * kRec + kD]);
+  for (int sp = 0; sp < n_live; ++sp) M = fmaxf(M, base[sp * 8 * kRec + kD]);
   float O = 0.f, L = 0.f;
   if (M != kNegInf) {
-    for (int sp = 0; sp < a.n_splits; ++sp) {
+    for (int sp = 0; sp < n_live; ++sp) {
       const float* r = base + sp * 8 * kRec;
       const float m = r[kD];
       if (m == kNegInf) continue;
@@ -972,7 +982,9 @@ int tiles_per_cta_for(int n_layers, int nseq, int H, int max_seq_len) {
   const int tiles = (max_seq_len + kTile - 1) / kTile;
   const int sms = sm_count() > 0 ? sm_count() : 152;
   const int64_t units = static_cast<int64_t>(n_layers) * nseq * H;
-  // aim for >= 2 resident waves (3 CTAs per SM), at most 256 tiles (4096 tokens) per CTA
+  // aim for >= 2 resident waves (3 CTAs per SM), at most 256 tiles (4096 tokens) per CTA (the
+  // entry point without a workspace may raise a CTA's tiles above 256 to fit its partials in its
+  // static scratch; no kernel sizes storage by the tiles per CTA)
   const int64_t want_splits = (6LL * sms + units - 1) / units;
   int64_t t = (tiles + want_splits - 1) / want_splits;
   if (t > 256) t = 256;
@@ -1015,16 +1027,15 @@ extern "C" size_t kvq_decode_attn_workspace(int n_layers, int nseq, int num_kv_h
 namespace kvq {
 namespace {
 
-// Validation, arguments and launches shared by kvq_decode_attn and kvq_append_decode_attn
-// (knew/vnew non-NULL: the fused append).
-kvq_status decode_attn_entry(const char* fn, const kvq_pool* k_pools, const kvq_pool* v_pools,
-                             int n_layers, const uint16_t* const* knew,
-                             const uint16_t* const* vnew, const kvq_side* k_sides,
-                             const kvq_side* v_sides, const uint16_t* q, int num_q_heads,
-                             const int32_t* page_table, int max_pages, const int32_t* seq_lens,
-                             int nseq, int max_seq_len, float softmax_scale, float* out,
-                             void* workspace, size_t workspace_bytes, int32_t* dev_err,
-                             cudaStream_t cs) {
+// Validation and kernel arguments shared by every decode entry point (knew/vnew non-NULL: the
+// fused append; k_sides/v_sides non-NULL: side channels).  Fills `a` and `sd` except where the
+// split partials go and the split plan (ws, tiles_per_cta, n_splits), which each entry sets.
+kvq_status prepare_attn(const char* fn, const kvq_pool* k_pools, const kvq_pool* v_pools,
+                        int n_layers, const uint16_t* const* knew, const uint16_t* const* vnew,
+                        const kvq_side* k_sides, const kvq_side* v_sides, const uint16_t* q,
+                        int num_q_heads, const int32_t* page_table, int max_pages,
+                        const int32_t* seq_lens, int nseq, int max_seq_len, float softmax_scale,
+                        float* out, int32_t* dev_err, AttnArgs& a, AttnSide& sd) {
   const bool append = knew != nullptr || vnew != nullptr;
   const bool side = k_sides != nullptr || v_sides != nullptr;
   if (n_layers < 1 || n_layers > KVQ_MAX_TENSORS)
@@ -1046,7 +1057,7 @@ kvq_status decode_attn_entry(const char* fn, const kvq_pool* k_pools, const kvq_
                 "head", fn, num_q_heads, H);
   if ((append || side) && k0.page_size % kTile)
     return fail(KVQ_ERR_SHAPE, "%s: page_size %d must be a multiple of 16", fn, k0.page_size);
-  AttnSide sd{};
+  sd = AttnSide{};
   if (side) {
     if (!k_sides || !v_sides) return fail(KVQ_ERR_NULL, "%s: NULL side array", fn);
     const int k = k_sides[0].n_outlier, ns = k_sides[0].n_sink;
@@ -1081,10 +1092,9 @@ kvq_status decode_attn_entry(const char* fn, const kvq_pool* k_pools, const kvq_
     return fail(KVQ_ERR_RANGE, "%s: bad nseq/max_pages/max_seq_len", fn);
   if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages) * k0.page_size)
     return fail(KVQ_ERR_RANGE, "%s: max_seq_len exceeds max_pages * page_size", fn);
-  if (!q || !page_table || !seq_lens || !out || !workspace)
-    return fail(KVQ_ERR_NULL, "%s: NULL pointer", fn);
-  if (!aligned16(q) || !aligned16(out) || !aligned16(workspace))
-    return fail(KVQ_ERR_ALIGN, "%s: q/out/workspace must be 16-byte aligned", fn);
+  if (!q || !page_table || !seq_lens || !out) return fail(KVQ_ERR_NULL, "%s: NULL pointer", fn);
+  if (!aligned16(q) || !aligned16(out))
+    return fail(KVQ_ERR_ALIGN, "%s: q/out must be 16-byte aligned", fn);
   if (append) {
     if (!knew || !vnew) return fail(KVQ_ERR_NULL, "%s: NULL new-token array", fn);
     for (int i = 0; i < n_layers; ++i) {
@@ -1093,14 +1103,9 @@ kvq_status decode_attn_entry(const char* fn, const kvq_pool* k_pools, const kvq_
         return fail(KVQ_ERR_ALIGN, "%s: new K/V rows must be 16-byte aligned", fn);
     }
   }
-  const size_t need = kvq_decode_attn_workspace(n_layers, nseq, H, num_q_heads, kD,
-                                                k0.page_size, max_seq_len);
-  if (workspace_bytes < need)
-    return fail(KVQ_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, workspace_bytes, need);
   if (static_cast<int64_t>(n_layers) * nseq > 65535)
     return fail(KVQ_ERR_RANGE, "%s: n_layers * nseq > 65535", fn);
 
-  AttnArgs a;
   for (int i = 0; i < KVQ_MAX_TENSORS; ++i) {
     if (i < n_layers)
       a.L[i] = LayerPools{k_pools[i].codes, k_pools[i].scales, v_pools[i].codes,
@@ -1112,7 +1117,7 @@ kvq_status decode_attn_entry(const char* fn, const kvq_pool* k_pools, const kvq_
   }
   a.q = q;
   a.out = out;
-  a.ws = static_cast<float*>(workspace);
+  a.ws = nullptr;
   a.pt = page_table;
   a.lens = seq_lens;
   a.err = dev_err;
@@ -1123,15 +1128,21 @@ kvq_status decode_attn_entry(const char* fn, const kvq_pool* k_pools, const kvq_
   a.Hq = num_q_heads;
   a.ps = k0.page_size;
   a.max_pages = max_pages;
-  a.tiles_per_cta = tiles_per_cta_for(n_layers, nseq, H, max_seq_len);
-  const int tiles = (max_seq_len + kTile - 1) / kTile;
-  a.n_splits = tiles > 0 ? (tiles + a.tiles_per_cta - 1) / a.tiles_per_cta : 1;
+  a.n_splits = 0;
+  a.tiles_per_cta = 0;
+  a.len_add = append ? 1 : 0;
   a.qk_scale = softmax_scale * 1.4426950408889634f;
+  return KVQ_OK;
+}
 
-  const dim3 grid(a.n_splits, H, n_layers * nseq);
-  const bool tma = (k0.page_size % kTile) == 0;
+// Launches the attention kernel of the call's width and variant over (split, KV head,
+// layer * nseq + seq), then the split merge.
+kvq_status launch_decode(const char* fn, const AttnArgs& a, int bits, bool append, bool side,
+                         const AttnSide& sd, cudaStream_t cs) {
+  const dim3 grid(a.n_splits, a.H, a.n_layers * a.nseq);
+  const bool tma = (a.ps % kTile) == 0;
   cudaError_t e;
-  switch (k0.bits) {
+  switch (bits) {
     case 8:
       e = side ? launch_attn<8, false, true>(a, grid, tma, cs, sd)
                : append ? launch_attn<8, true>(a, grid, tma, cs) : launch_attn<8>(a, grid, tma, cs);
@@ -1146,11 +1157,41 @@ kvq_status decode_attn_entry(const char* fn, const kvq_pool* k_pools, const kvq_
       break;
   }
   if (e == cudaSuccess) {
-    decode_merge_kernel<<<dim3(num_q_heads, n_layers * nseq), kD, 0, cs>>>(a);
+    decode_merge_kernel<<<dim3(a.Hq, a.n_layers * a.nseq), kD, 0, cs>>>(a);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "%s launch: %s", fn, cudaGetErrorString(e));
   return ok();
+}
+
+// The entry points with a caller-provided workspace for the split partials.
+kvq_status decode_attn_entry(const char* fn, const kvq_pool* k_pools, const kvq_pool* v_pools,
+                             int n_layers, const uint16_t* const* knew,
+                             const uint16_t* const* vnew, const kvq_side* k_sides,
+                             const kvq_side* v_sides, const uint16_t* q, int num_q_heads,
+                             const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                             int nseq, int max_seq_len, float softmax_scale, float* out,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                             cudaStream_t cs) {
+  AttnArgs a;
+  AttnSide sd;
+  const kvq_status st = prepare_attn(fn, k_pools, v_pools, n_layers, knew, vnew, k_sides, v_sides,
+                                     q, num_q_heads, page_table, max_pages, seq_lens, nseq,
+                                     max_seq_len, softmax_scale, out, dev_err, a, sd);
+  if (st != KVQ_OK) return st;
+  if (!workspace) return fail(KVQ_ERR_NULL, "%s: NULL workspace", fn);
+  if (!aligned16(workspace))
+    return fail(KVQ_ERR_ALIGN, "%s: workspace must be 16-byte aligned", fn);
+  const size_t need = kvq_decode_attn_workspace(n_layers, nseq, a.H, num_q_heads, kD, a.ps,
+                                                max_seq_len);
+  if (workspace_bytes < need)
+    return fail(KVQ_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, workspace_bytes, need);
+  a.ws = static_cast<float*>(workspace);
+  a.tiles_per_cta = tiles_per_cta_for(n_layers, nseq, a.H, max_seq_len);
+  const int tiles = (max_seq_len + kTile - 1) / kTile;
+  a.n_splits = tiles > 0 ? (tiles + a.tiles_per_cta - 1) / a.tiles_per_cta : 1;
+  return launch_decode(fn, a, k_pools[0].bits, knew != nullptr || vnew != nullptr,
+                       k_sides != nullptr || v_sides != nullptr, sd, cs);
 }
 
 }  // namespace
@@ -1250,43 +1291,23 @@ extern "C" kvq_status kvq_decode_attn_noalloc(const kvq_pool* k_pools, const kvq
                                               kvq_stream_t stream) {
   using namespace kvq;
   const char* fn = "kvq_decode_attn_noalloc";
-  if (n_layers < 1 || n_layers > KVQ_MAX_TENSORS)
-    return fail(KVQ_ERR_RANGE, "%s: n_layers %d not in [1, %d]", fn, n_layers, KVQ_MAX_TENSORS);
-  kvq_status st = check_pools_uniform(k_pools, n_layers, fn);
+  AttnArgs a;
+  AttnSide sd;
+  kvq_status st = prepare_attn(fn, k_pools, v_pools, n_layers, nullptr, nullptr, nullptr, nullptr,
+                               q, num_q_heads, page_table, max_pages, seq_lens, nseq, max_seq_len,
+                               softmax_scale, out, dev_err, a, sd);
   if (st != KVQ_OK) return st;
-  st = check_pools_uniform(v_pools, n_layers, fn);
-  if (st != KVQ_OK) return st;
-  const kvq_pool& k0 = k_pools[0];
-  const kvq_pool& v0 = v_pools[0];
-  if (v0.bits != k0.bits || v0.num_heads != k0.num_heads || v0.head_dim != k0.head_dim ||
-      v0.page_size != k0.page_size)
-    return fail(KVQ_ERR_SHAPE, "%s: K and V pools differ in shape", fn);
-  if (k0.head_dim != kD)
-    return fail(KVQ_ERR_SHAPE, "%s: head_dim %d unsupported (256 only)", fn, k0.head_dim);
-  const int H = k0.num_heads;
-  if (num_q_heads < H || num_q_heads % H || num_q_heads / H > 8)
-    return fail(KVQ_ERR_SHAPE, "%s: num_q_heads %d must be a multiple of %d, at most 8 per KV "
-                "head", fn, num_q_heads, H);
-  if (nseq < 1 || max_pages < 1 || max_seq_len < 0)
-    return fail(KVQ_ERR_RANGE, "%s: bad nseq/max_pages/max_seq_len", fn);
-  if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages) * k0.page_size)
-    return fail(KVQ_ERR_RANGE, "%s: max_seq_len exceeds max_pages * page_size", fn);
-  if (!q || !page_table || !seq_lens || !out) return fail(KVQ_ERR_NULL, "%s: NULL pointer", fn);
-  if (!aligned16(q) || !aligned16(out))
-    return fail(KVQ_ERR_ALIGN, "%s: q/out must be 16-byte aligned", fn);
-  if (static_cast<int64_t>(n_layers) * nseq > 65535)
-    return fail(KVQ_ERR_RANGE, "%s: n_layers * nseq > 65535", fn);
 
   // One partial record per (layer, sequence, KV head, split); the split count is capped so that
-  // all records fit in the static scratch.
-  const size_t per_split = static_cast<size_t>(n_layers) * nseq * H * 8 * kRec * sizeof(float);
+  // all records fit in the static scratch (the splits then grow past the usual 256 tiles).
+  const size_t per_split = static_cast<size_t>(n_layers) * nseq * a.H * 8 * kRec * sizeof(float);
   if (per_split > kNoAllocScratchBytes)
     return fail(KVQ_ERR_RANGE, "%s: %d layers x %d sequences x %d KV heads need %zu bytes of "
                 "scratch, more than the %zu-byte static scratch; use kvq_decode_attn with a "
-                "workspace", fn, n_layers, nseq, H, per_split, kNoAllocScratchBytes);
+                "workspace", fn, n_layers, nseq, a.H, per_split, kNoAllocScratchBytes);
   const int tiles = (max_seq_len + kTile - 1) / kTile;
   const int max_splits = static_cast<int>(kNoAllocScratchBytes / per_split);
-  int tpc = tiles_per_cta_for(n_layers, nseq, H, max_seq_len);
+  int tpc = tiles_per_cta_for(n_layers, nseq, a.H, max_seq_len);
   int n_splits = tiles > 0 ? (tiles + tpc - 1) / tpc : 1;
   if (n_splits > max_splits) {
     tpc = (tiles + max_splits - 1) / max_splits;
@@ -1296,45 +1317,9 @@ extern "C" kvq_status kvq_decode_attn_noalloc(const kvq_pool* k_pools, const kvq
   void* ws = nullptr;
   st = noalloc_scratch(&ws);
   if (st != KVQ_OK) return st;
-
-  AttnArgs a;
-  for (int i = 0; i < KVQ_MAX_TENSORS; ++i) {
-    if (i < n_layers)
-      a.L[i] = LayerPools{k_pools[i].codes, k_pools[i].scales, v_pools[i].codes,
-                          v_pools[i].scales, k_pools[i].num_pages, v_pools[i].num_pages};
-    else
-      a.L[i] = LayerPools{nullptr, nullptr, nullptr, nullptr, 0, 0};
-  }
-  a.q = q;
-  a.out = out;
   a.ws = static_cast<float*>(ws);
-  a.pt = page_table;
-  a.lens = seq_lens;
-  a.err = dev_err;
-  a.n_layers = n_layers;
-  a.nseq = nseq;
-  a.H = H;
-  a.G = num_q_heads / H;
-  a.Hq = num_q_heads;
-  a.ps = k0.page_size;
-  a.max_pages = max_pages;
   a.tiles_per_cta = tpc;
   a.n_splits = n_splits;
-  a.qk_scale = softmax_scale * 1.4426950408889634f;
-
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const dim3 grid(a.n_splits, H, n_layers * nseq);
-  const bool tma = (k0.page_size % kTile) == 0;
-  cudaError_t e;
-  switch (k0.bits) {
-    case 8: e = launch_attn<8>(a, grid, tma, cs); break;
-    case 6: e = launch_attn<6>(a, grid, tma, cs); break;
-    default: e = launch_attn<4>(a, grid, tma, cs); break;
-  }
-  if (e == cudaSuccess) {
-    decode_merge_kernel<<<dim3(num_q_heads, n_layers * nseq), kD, 0, cs>>>(a);
-    e = cudaGetLastError();
-  }
-  if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "%s launch: %s", fn, cudaGetErrorString(e));
-  return ok();
+  return launch_decode(fn, a, k_pools[0].bits, false, false, sd,
+                       reinterpret_cast<cudaStream_t>(stream));
 }

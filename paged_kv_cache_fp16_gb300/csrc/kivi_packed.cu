@@ -561,7 +561,7 @@ __global__ void __launch_bounds__(kAThreads, 4) kivi_attn_kernel(const KAArgs a)
 
   for (int j = 0; j < n_mine; ++j) {
     const int st = j % kAStages;
-    const bool arrived = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((j / kAStages) & 1));
+    const bool arrived = mbar_wait_stage(&bars[st], static_cast<uint32_t>((j / kAStages) & 1));
     if (__any_sync(kFullMask, !arrived)) {   // warp-uniform exit
       timed_out = true;
       break;

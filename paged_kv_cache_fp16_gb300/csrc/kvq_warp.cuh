@@ -93,6 +93,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// Polls of the decode attention's per-tile stage waits.  The library uses kWaitLimit; a build
+// may define a smaller limit (down to 0: give up at once) to run the timeout path, whose drain of
+// the copies in flight keeps kWaitLimit, so every issued copy completes before the block exits.
+#ifndef KVQ_STAGE_WAIT_LIMIT
+#define KVQ_STAGE_WAIT_LIMIT (1LL << 22)
+#endif
+__device__ __forceinline__ bool mbar_wait_stage(uint64_t* bar, uint32_t parity) {
+  for (long long i = 0; i < static_cast<long long>(KVQ_STAGE_WAIT_LIMIT); ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
                                          uint64_t* bar) {
   asm volatile(
