@@ -7,19 +7,21 @@ any row of a multi-gigabyte device tensor can be regenerated on the host, bit fo
 materialising the rest.  The same integer recipe is written twice, once over numpy arrays (host)
 and once over torch tensors (any device); ``tests/test_kvgen.py`` checks that they agree.
 
-Recipe for one "~N(0,1)" fp16 element at flat index ``i``:
+Recipe for one N(0,1) fp16 element at flat index ``i`` (inverse-CDF sampling):
 
-* two 32-bit words ``w(2i)``, ``w(2i+1)``, where ``w(j) = fmix32(fmix32((j + s0) mod 2^32) ^ s1)``
-  and ``fmix32`` is the 32-bit finaliser of Austin Appleby's MurmurHash3 (public domain);
-  ``(s0, s1)`` are derived from ``(seed, tag)``;
-* the four 16-bit halves of those words are summed (Irwin-Hall with n = 4: mean 131070,
-  variance 4 * (2^32 - 1) / 12), centred, and scaled to unit variance in float32:
-  ``z = float32(S - 131070) * float32(sqrt(3) / 65536)``;
+* one 32-bit word ``u = w(2i)``, where ``w(j) = fmix32(fmix32((j + s0) mod 2^32) ^ s1)`` and
+  ``fmix32`` is the 32-bit finaliser of Austin Appleby's MurmurHash3 (public domain); ``(s0, s1)``
+  are derived from ``(seed, tag)``;
+* ``z`` is the standard normal quantile of ``(u + 1/2) / 2^32``, read from a table: nodes
+  ``T[k]``, k = 0 .. 2^20, are the float64 quantiles at ``u = 4096 k`` (the last one at
+  ``u = 2^32 - 1``) rounded to float32, with float32 slopes ``S[k] = (T[k+1] - T[k]) / 4096``;
+  ``z = float32(T[u >> 12] + float32(float32(u & 4095) * S[u >> 12]))`` -- two IEEE float32
+  operations, so the numpy and torch implementations agree bit for bit on any device.  The
+  tails reach about +-6.3 sigma (the quantile of 2^-33); between nodes the inverse CDF is linear;
 * channels chosen as outliers are multiplied by a float32 factor; the result is rounded to fp16
   (round to nearest even).
 
-The distribution is bounded at about +-3.46 sigma (instead of a Gaussian's unbounded tails); the
-shapes, the outlier channels and the zero rows follow the workloads they stand in for.
+The shapes, the outlier channels and the zero rows follow the workloads they stand in for.
 """
 from __future__ import annotations
 
@@ -32,8 +34,10 @@ MASK32 = 0xFFFFFFFF
 _M1 = 0x85EBCA6B
 _M2 = 0xC2B2AE35
 _GOLDEN = 0x9E3779B1
-_NORM_SCALE = np.float32(math.sqrt(3.0) / 65536.0)
-_NORM_MEAN = 131070
+_QBITS = 20                    # table nodes: 2^20 intervals of 4096 consecutive words
+_QSHIFT = 32 - _QBITS
+_QTABLE = None                  # (T, S) float32 numpy arrays, built on first use
+_QTABLE_T = {}                  # torch copies per device
 
 # tags: distinct generator streams
 TAG_K = 1
@@ -84,14 +88,61 @@ def words_np(seed: int, tag: int, idx: np.ndarray, sub: int = 0) -> np.ndarray:
     return _fmix32_np(_fmix32_np(x) ^ np.uint32(s1))
 
 
+def _normal_quantiles(p: np.ndarray) -> np.ndarray:
+    """Standard normal quantiles in float64: Acklam's rational approximation (relative error
+    below 1.2e-9), then one Halley step on erfc, which takes it to float64 accuracy."""
+    a = (-3.969683028665376e+01, 2.209460984245205e+02, -2.759285104469687e+02,
+         1.383577518672690e+02, -3.066479806614716e+01, 2.506628277459239e+00)
+    b = (-5.447609879822406e+01, 1.615858368580409e+02, -1.556989798598866e+02,
+         6.680131188771972e+01, -1.328068155288572e+01)
+    c = (-7.784894002430293e-03, -3.223964580411365e-01, -2.400758277161838e+00,
+         -2.549732539343734e+00, 4.374664141464968e+00, 2.938163982698783e+00)
+    d = (7.784695709041462e-03, 3.224671290700398e-01, 2.445134137142996e+00,
+         3.754408661907416e+00)
+    p = np.asarray(p, dtype=np.float64)
+    x = np.empty_like(p)
+    lo, hi = p < 0.02425, p > 1 - 0.02425
+    mid = ~(lo | hi)
+    q = np.sqrt(-2 * np.log(p[lo]))
+    x[lo] = ((((((c[0] * q + c[1]) * q + c[2]) * q + c[3]) * q + c[4]) * q + c[5]) /
+             ((((d[0] * q + d[1]) * q + d[2]) * q + d[3]) * q + 1))
+    q = np.sqrt(-2 * np.log1p(-p[hi]))
+    x[hi] = -((((((c[0] * q + c[1]) * q + c[2]) * q + c[3]) * q + c[4]) * q + c[5]) /
+              ((((d[0] * q + d[1]) * q + d[2]) * q + d[3]) * q + 1))
+    q = p[mid] - 0.5
+    r = q * q
+    x[mid] = ((((((a[0] * r + a[1]) * r + a[2]) * r + a[3]) * r + a[4]) * r + a[5]) * q /
+              (((((b[0] * r + b[1]) * r + b[2]) * r + b[3]) * r + b[4]) * r + 1))
+    erfc = np.vectorize(math.erfc)
+    e = 0.5 * erfc(-x / math.sqrt(2.0)) - p
+    u = e * math.sqrt(2.0 * math.pi) * np.exp(x * x / 2.0)
+    return x - u / (1.0 + x * u / 2.0)
+
+
+def quantile_table() -> tuple[np.ndarray, np.ndarray]:
+    """(T, S): float32 nodes and slopes of the inverse-CDF table (see the module docstring)."""
+    global _QTABLE
+    if _QTABLE is None:
+        n = 1 << _QBITS
+        u = np.arange(n + 1, dtype=np.float64) * (1 << _QSHIFT)
+        u[-1] = float(MASK32)
+        t64 = _normal_quantiles((u + 0.5) / 2.0 ** 32)
+        t = t64.astype(np.float32)
+        slope = ((t[1:].astype(np.float64) - t[:-1].astype(np.float64))
+                 / (u[1:] - u[:-1])).astype(np.float32)
+        _QTABLE = (t[:-1].copy(), slope)
+    return _QTABLE
+
+
 def normal_fp16_np(seed: int, tag: int, idx: np.ndarray, sub: int = 0,
                    mult: np.ndarray | None = None) -> np.ndarray:
-    """fp16 ~N(0,1) (Irwin-Hall 4) at flat indices idx; optional float32 multiplier per element."""
+    """fp16 N(0,1) at flat indices idx; optional float32 multiplier per element."""
     idx = np.asarray(idx, dtype=np.int64)
-    w0 = words_np(seed, tag, 2 * idx, sub).astype(np.int64)
-    w1 = words_np(seed, tag, 2 * idx + 1, sub).astype(np.int64)
-    s = (w0 & 0xFFFF) + (w0 >> 16) + (w1 & 0xFFFF) + (w1 >> 16)
-    z = (s - _NORM_MEAN).astype(np.float32) * _NORM_SCALE
+    u = words_np(seed, tag, 2 * idx, sub)
+    t, slope = quantile_table()
+    k = (u >> np.uint32(_QSHIFT)).astype(np.int64)
+    f = (u & np.uint32((1 << _QSHIFT) - 1)).astype(np.float32)
+    z = t[k] + f * slope[k]
     if mult is not None:
         z = z * np.asarray(mult, dtype=np.float32)
     return z.astype(np.float16)
@@ -118,12 +169,22 @@ def words_torch(seed: int, tag: int, idx, sub: int = 0):
     return _fmix32_t(_fmix32_t(x) ^ s1)
 
 
+def _quantile_table_torch(device):
+    import torch
+    key = str(device)
+    if key not in _QTABLE_T:
+        t, slope = quantile_table()
+        _QTABLE_T[key] = (torch.from_numpy(t).to(device), torch.from_numpy(slope).to(device))
+    return _QTABLE_T[key]
+
+
 def normal_fp16_torch(seed: int, tag: int, idx, sub: int = 0, mult=None):
     import torch
-    w0 = words_torch(seed, tag, 2 * idx, sub)
-    w1 = words_torch(seed, tag, 2 * idx + 1, sub)
-    s = (w0 & 0xFFFF) + (w0 >> 16) + (w1 & 0xFFFF) + (w1 >> 16)
-    z = (s - _NORM_MEAN).to(torch.float32) * torch.tensor(float(_NORM_SCALE), dtype=torch.float32)
+    u = words_torch(seed, tag, 2 * idx, sub)
+    t, slope = _quantile_table_torch(u.device)
+    k = u >> _QSHIFT
+    f = (u & ((1 << _QSHIFT) - 1)).to(torch.float32)
+    z = t[k] + f * slope[k]
     if mult is not None:
         z = z * mult
     return z.to(torch.float16)

@@ -204,7 +204,7 @@ __device__ __forceinline__ void cross_group(const uint32_t* wa, const uint32_t* 
 template <int BITS>
 struct KRegs {
   uint32_t kw[2][Wd<BITS>::kKWords];
-  float ksc[2];      // the rows' fp16 scales, applied to the scores
+  uint32_t ks2[2];   // the rows' fp16 scales, twice (half2): k_hat = fp16(code * scale)
   float vsc[2];      // the rows' V scales (0 if masked), folded into P for the P.V product
   bool kval[2];
 };
@@ -216,7 +216,7 @@ struct KRegs {
 template <int BITS>
 struct KStage {
   const uint32_t* kw[2];   // the rows' packed K words in the stage
-  float ksc[2];
+  uint32_t ks2[2];
   float vsc[2];
   bool kval[2];
 };
@@ -250,7 +250,7 @@ __device__ __forceinline__ float softmax_exp2(float x) {
   else return ex2_fast(x);
 }
 
-// With SIDE, kc[4] (same layout as the scores) is added after the row scale -- the outlier and
+// With SIDE, kc[4] (same layout as the scores) is added to the dense scores -- the outlier and
 // sink terms of the keys -- and p[4] is returned for the value side terms.
 template <int BITS, bool SIDE = false, typename QF, typename KT>
 __device__ __forceinline__ void tile_qk_softmax(const KT& T, const QF& Q,
@@ -259,17 +259,22 @@ __device__ __forceinline__ void tile_qk_softmax(const KT& T, const QF& Q,
                                                 uint32_t& pb0, uint32_t& pb1,
                                                 const float* kc = nullptr,
                                                 float* p_out = nullptr) {
-  // ---------------- S^T = C_K . Q^T on the exact integer codes, one accumulation chain (four
-  // independent chains measured 3.3 % slower at q6: their 12 registers cost the 128-register
-  // kernel more than the chain's latency); each token row's fp16 scale multiplies its scores
-  // afterwards (the code-times-scale products are exact instead of rounded to fp16 -- a
-  // difference far inside the tolerance)
+  // ---------------- S^T = K_hat . Q^T, one accumulation chain (four independent chains measured
+  // 3.3 % slower at q6: their 12 registers cost the 128-register kernel more than the chain's
+  // latency).  K_hat is the dequantizer's fp16(code * scale), one half2 multiply of the exact
+  // codes by the row's fp16 scale: keys carry outlier channels, and scaling the scores of the
+  // exact codes instead (one fp32 multiply per score) moves them by the fp16 rounding of those
+  // large elements -- enough to take N(0, 1) caches with x10 channels outside the tolerance
   float sacc[4] = {};
 #define KVQ_QK_GROUP(GI)                                                                \
   {                                                                                     \
     uint32_t p0[4], p1[4];                                                              \
     unpack_group<BITS, GI>(T.kw[0], p0);                                                \
     unpack_group<BITS, GI>(T.kw[1], p1);                                                \
+    _Pragma("unroll") for (int i = 0; i < 4; ++i) {                                     \
+      p0[i] = hmul2u(p0[i], T.ks2[0]);                                                  \
+      p1[i] = hmul2u(p1[i], T.ks2[1]);                                                  \
+    }                                                                                   \
     const uint2 qa = Q.pair(2 * GI), qb = Q.pair(2 * GI + 1);                           \
     mma16816(sacc, p0[0], p1[0], p0[1], p1[1], qa.x, qa.y);                             \
     mma16816(sacc, p0[2], p1[2], p0[3], p1[3], qb.x, qb.y);                             \
@@ -281,16 +286,15 @@ __device__ __forceinline__ void tile_qk_softmax(const KT& T, const QF& Q,
   // ---------------- online softmax (log2 domain); sacc: [tok g | g+8][head 2c | 2c+1]
   float sc[4];
   if constexpr (SIDE) {
-    sc[0] = T.kval[0] ? fmaf(sacc[0], T.ksc[0], kc[0]) * qk_scale : kNegInf;
-    sc[1] = T.kval[0] ? fmaf(sacc[1], T.ksc[0], kc[1]) * qk_scale : kNegInf;
-    sc[2] = T.kval[1] ? fmaf(sacc[2], T.ksc[1], kc[2]) * qk_scale : kNegInf;
-    sc[3] = T.kval[1] ? fmaf(sacc[3], T.ksc[1], kc[3]) * qk_scale : kNegInf;
+    sc[0] = T.kval[0] ? (sacc[0] + kc[0]) * qk_scale : kNegInf;
+    sc[1] = T.kval[0] ? (sacc[1] + kc[1]) * qk_scale : kNegInf;
+    sc[2] = T.kval[1] ? (sacc[2] + kc[2]) * qk_scale : kNegInf;
+    sc[3] = T.kval[1] ? (sacc[3] + kc[3]) * qk_scale : kNegInf;
   } else {
-    const float f0 = T.ksc[0] * qk_scale, f1 = T.ksc[1] * qk_scale;
-    sc[0] = T.kval[0] ? sacc[0] * f0 : kNegInf;
-    sc[1] = T.kval[0] ? sacc[1] * f0 : kNegInf;
-    sc[2] = T.kval[1] ? sacc[2] * f1 : kNegInf;
-    sc[3] = T.kval[1] ? sacc[3] * f1 : kNegInf;
+    sc[0] = T.kval[0] ? sacc[0] * qk_scale : kNegInf;
+    sc[1] = T.kval[0] ? sacc[1] * qk_scale : kNegInf;
+    sc[2] = T.kval[1] ? sacc[2] * qk_scale : kNegInf;
+    sc[3] = T.kval[1] ? sacc[3] * qk_scale : kNegInf;
   }
   float tm0 = fmaxf(sc[0], sc[2]), tm1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
@@ -727,7 +731,8 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
       // fragment row g + 8r holds this token (side channels: in tok_order)
       const int row = SIDE ? tok_order(g + 8 * r) : g + 8 * r;
       K.kval[r] = ok && tb + row < len;
-      K.ksc[r] = (SIDE && tb + row < sd.n_sink) ? 0.f : h2f(sks[row]);   // sinks: exact below
+      K.ks2[r] = (SIDE && tb + row < sd.n_sink) ? 0u                      // sinks: exact below
+                                                : static_cast<uint32_t>(sks[row]) * 0x10001u;
       K.vsc[r] = (K.kval[r] && !(SIDE && tb + row < sd.n_sink)) ? h2f(svs[row]) : 0.f;
       const uint8_t* krow = sk + row * kPd + c * (4 * W::kKWords);
       if constexpr (kStageK) {
@@ -898,7 +903,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_gather_kernel(const A
       int64_t row = -1;
       if (t < len) row = locate_row(a.pt, a.max_pages, a.ps, a.H, P.k_pages, s, t, h, a.err);
       K.kval[r] = row >= 0;
-      K.ksc[r] = 0.f;
+      K.ks2[r] = 0u;
       K.vsc[r] = 0.f;
       if (t < len) {
         const int64_t vrow = locate_row(a.pt, a.max_pages, a.ps, a.H, P.v_pages, s, t, h, a.err);
@@ -914,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_attn_gather_kernel(const A
           K.kw[r][4 * i] = v.x; K.kw[r][4 * i + 1] = v.y;
           K.kw[r][4 * i + 2] = v.z; K.kw[r][4 * i + 3] = v.w;
         }
-        K.ksc[r] = h2f(ld_nc_u16(P.ks + row));
+        K.ks2[r] = static_cast<uint32_t>(ld_nc_u16(P.ks + row)) * 0x10001u;
       }
     }
     uint32_t pb0, pb1;

@@ -53,9 +53,30 @@ def test_kivi_spec_agrees_and_has_outliers():
                           full[1, 1, 10:20].view(np.uint16))
 
 
+def test_quantile_table_against_an_independent_inverse_cdf():
+    """The table's nodes are standard normal quantiles: compared with the standard library's
+    NormalDist (a different algorithm) at nodes across the whole range, tails included."""
+    from statistics import NormalDist
+    t, slope = kvgen.quantile_table()
+    nd = NormalDist()
+    n = t.size
+    for k in list(range(0, 64)) + list(range(n - 64, n)) + list(range(0, n, 4099)):
+        want = nd.inv_cdf((k * 4096 + 0.5) / 2.0 ** 32)
+        assert abs(float(t[k]) - want) <= 2e-7 * max(1.0, abs(want)), k
+    assert np.all(slope > 0)                              # monotone
+    top = float(t[-1]) + 4095.0 * float(slope[-1])        # the node at the largest word, 2^32 - 1
+    assert abs(float(t[0]) + top) < 1e-5                  # symmetric ends
+
+
 def test_moments_and_permutation():
-    x = kvgen.normal_fp16_np(0, 1, np.arange(1 << 20)).astype(np.float64)
-    assert abs(x.mean()) < 5e-3 and abs(x.std() - 1) < 5e-3
+    x = kvgen.normal_fp16_np(0, 1, np.arange(1 << 22)).astype(np.float64)
+    assert abs(x.mean()) < 2e-3 and abs(x.std() - 1) < 2e-3
+    kurt = np.mean((x - x.mean()) ** 4) / x.var() ** 2
+    assert abs(kurt - 3.0) < 0.02                         # Gaussian, not bounded Irwin-Hall (2.7)
+    # Gaussian tails: P(|z| > 4) = 6.3e-5 (about 265 of 4 Mi draws)
+    tail = int(np.count_nonzero(np.abs(x) > 4.0))
+    assert 180 < tail < 360
+    assert np.abs(x).max() > 4.5
     pt = kvgen.random_page_table(1, 8, 100)
     assert sorted(pt.ravel().tolist()) == list(range(800))
     lens = kvgen.decode_append_lengths(2, 64)
