@@ -78,7 +78,8 @@ typedef enum kvq_status {
 typedef struct kvq_pool {
   int32_t bits;       /* 8, 6 or 4 */
   int32_t num_heads;  /* KV heads H */
-  int32_t head_dim;   /* D: a multiple of 16, at most 256 */
+  int32_t head_dim;   /* D <= 256 with kvq_packed_dim(D, bits) > 0: any D at q8, even at q4,
+                         a multiple of 4 at q6 (the decode attention takes D = 256 only) */
   int32_t page_size;  /* tokens per page, >= 1 */
   int64_t num_pages;
   uint8_t* codes;
@@ -186,8 +187,9 @@ KVQ_API kvq_status kvq_table_reserve(kvq_allocator* a, int32_t* page_table, int 
  * dev_err    optional device int32 error word (see the file header).
  * Rows are independent; a row's packed bytes and scale are written whole.  Two rows of one call
  * mapping to the same (page, slot) race (a caller error).
- * Errors: KVQ_ERR_BITS, KVQ_ERR_SHAPE (D % 16, D > 256, mismatched pools), KVQ_ERR_NULL,
- * KVQ_ERR_ALIGN, KVQ_ERR_RANGE (n_tensors not in [1, KVQ_MAX_TENSORS], nseq < 0,
+ * Head dims that are not a multiple of 16 run a one-warp-per-row kernel (same arithmetic).
+ * Errors: KVQ_ERR_BITS, KVQ_ERR_SHAPE (kvq_packed_dim(D, bits) < 1, D > 256, mismatched pools),
+ * KVQ_ERR_NULL, KVQ_ERR_ALIGN, KVQ_ERR_RANGE (n_tensors not in [1, KVQ_MAX_TENSORS], nseq < 0,
  * total_new_tokens < 0, max_pages < 1), KVQ_ERR_CUDA.
  */
 KVQ_API kvq_status kvq_quant_pack_paged(const kvq_pool* pools, const uint16_t* const* x, int n_tensors,
@@ -324,7 +326,7 @@ typedef struct kvq_side {
 
 /*
  * kvq_quant_pack_paged with the side channels: same arguments plus sides[i] for pools[i]
- * (uniform n_outlier and n_sink).  head_dim a multiple of 16, <= 256.  Errors: those of
+ * (uniform n_outlier and n_sink).  Any head_dim a pool accepts.  Errors: those of
  * kvq_quant_pack_paged, KVQ_ERR_RANGE (n_outlier, n_sink, max_seqs < nseq).
  */
 KVQ_API kvq_status kvq_quant_pack_paged_side(const kvq_pool* pools, const kvq_side* sides,

@@ -35,9 +35,9 @@ kvq_status ok() {
 
 kvq_status check_pool(const kvq_pool& p, const char* what) {
   if (qmax_of(p.bits) < 0) return fail(KVQ_ERR_BITS, "%s: bits %d not in {8, 6, 4}", what, p.bits);
-  if (p.head_dim < 16 || p.head_dim > 256 || p.head_dim % 16)
-    return fail(KVQ_ERR_SHAPE, "%s: head_dim %d must be a multiple of 16 in [16, 256]", what,
-                p.head_dim);
+  if (p.head_dim > 256 || kvq_packed_dim(p.head_dim, p.bits) < 1)
+    return fail(KVQ_ERR_SHAPE, "%s: head_dim %d not supported at %d bits (at most 256; q6 needs "
+                "a multiple of 4, q4 of 2)", what, p.head_dim, p.bits);
   if (p.num_heads < 1) return fail(KVQ_ERR_SHAPE, "%s: num_heads %d < 1", what, p.num_heads);
   if (p.page_size < 1) return fail(KVQ_ERR_SHAPE, "%s: page_size %d < 1", what, p.page_size);
   if (p.num_pages < 1 || p.num_pages > INT32_MAX)

@@ -23,6 +23,7 @@
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 #include "kvq_math.cuh"
+#include "kvq_rowwise.cuh"
 
 namespace kvq {
 namespace {
@@ -276,8 +277,25 @@ cudaError_t launch_one(const PackArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// Head dims that are not a multiple of 16: one warp per row (kvq_rowwise.cuh).
+template <int BITS, bool QUANT>
+cudaError_t launch_rowwise(const PackArgs& a, cudaStream_t stream) {
+  const unsigned nb = rowwise_blocks(static_cast<int64_t>(a.n_tensors) * a.total_tokens * a.H,
+                                     sm_count());
+  if (QUANT) rowwise_quant_kernel<BITS, false><<<nb, kRowThreads, 0, stream>>>(a);
+  else rowwise_dequant_kernel<BITS, false><<<nb, kRowThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
 template <bool QUANT>
 cudaError_t launch_bits(const PackArgs& a, int bits, cudaStream_t stream) {
+  if (a.D % 16) {
+    switch (bits) {
+      case 8: return launch_rowwise<8, QUANT>(a, stream);
+      case 6: return launch_rowwise<6, QUANT>(a, stream);
+      default: return launch_rowwise<4, QUANT>(a, stream);
+    }
+  }
   const int upl = (a.units + (1 << a.lpr_log2) - 1) >> a.lpr_log2;  // 1 or 2 for D <= 256
   switch (bits) {
     case 8: return upl == 1 ? launch_one<8, 1, QUANT>(a, stream) : launch_one<8, 2, QUANT>(a, stream);
@@ -308,8 +326,6 @@ kvq_status prepare(PackArgs& a, const kvq_pool* pools, const uint16_t* const* x,
     if (!aligned16(x[i])) return fail(KVQ_ERR_ALIGN, "%s: tensor %d not 16-byte aligned", what, i);
   }
   const kvq_pool& p0 = pools[0];
-  if (p0.head_dim % 16)
-    return fail(KVQ_ERR_SHAPE, "%s: head_dim %d must be a multiple of 16", what, p0.head_dim);
   a.n_tensors = n_tensors;
   a.H = p0.num_heads;
   a.D = p0.head_dim;

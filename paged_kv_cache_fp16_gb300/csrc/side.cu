@@ -37,6 +37,7 @@
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 #include "kvq_math.cuh"
+#include "kvq_rowwise.cuh"
 
 namespace kvq {
 namespace {
@@ -587,9 +588,6 @@ kvq_status side_call(bool quant, const kvq_pool* pools, const kvq_side* sides,
   kvq_status st = check_pools_uniform(pools, n_tensors, fn);
   if (st != KVQ_OK) return st;
   const kvq_pool& p0 = pools[0];
-  if (p0.head_dim % 16 || p0.head_dim > 256)
-    return fail(KVQ_ERR_SHAPE, "%s: head_dim %d must be a multiple of 16, <= 256", fn,
-                p0.head_dim);
   if (nseq < 0 || total < 0 || max_pages < 1)
     return fail(KVQ_ERR_RANGE, "%s: bad nseq/total/max_pages", fn);
   st = check_sides(pools, sides, n_tensors, nseq, fn);
@@ -627,10 +625,28 @@ kvq_status side_call(bool quant, const kvq_pool* pools, const kvq_side* sides,
   a.lpr_log2 = 0;
   while ((1 << a.lpr_log2) < a.units && a.lpr_log2 < 3) ++a.lpr_log2;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  switch (p0.bits) {
-    case 8: launch_side<8>(quant, a, cs); break;
-    case 6: launch_side<6>(quant, a, cs); break;
-    default: launch_side<4>(quant, a, cs); break;
+  if (a.D % 16) {   // head dims that are not a multiple of 16: one warp per row
+    const unsigned nb = rowwise_blocks(static_cast<int64_t>(n_tensors) * total * a.H, sm_count());
+    switch (p0.bits) {
+      case 8:
+        if (quant) rowwise_quant_kernel<8, true><<<nb, kRowThreads, 0, cs>>>(a);
+        else rowwise_dequant_kernel<8, true><<<nb, kRowThreads, 0, cs>>>(a);
+        break;
+      case 6:
+        if (quant) rowwise_quant_kernel<6, true><<<nb, kRowThreads, 0, cs>>>(a);
+        else rowwise_dequant_kernel<6, true><<<nb, kRowThreads, 0, cs>>>(a);
+        break;
+      default:
+        if (quant) rowwise_quant_kernel<4, true><<<nb, kRowThreads, 0, cs>>>(a);
+        else rowwise_dequant_kernel<4, true><<<nb, kRowThreads, 0, cs>>>(a);
+        break;
+    }
+  } else {
+    switch (p0.bits) {
+      case 8: launch_side<8>(quant, a, cs); break;
+      case 6: launch_side<6>(quant, a, cs); break;
+      default: launch_side<4>(quant, a, cs); break;
+    }
   }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "%s launch: %s", fn, cudaGetErrorString(e));

@@ -136,9 +136,12 @@ def _qp(kvq, pool, n=1, x=FAKE, total=16, nseq=1, max_pages=4, pt=FAKE, cu=FAKE,
 def test_quant_pack_rejects_bad_arguments_before_launch(kvq):
     assert _qp(kvq, _pool(kvq, bits=5)) == 1
     assert _qp(kvq, _pool(kvq, bits=16)) == 1
-    assert _qp(kvq, _pool(kvq, D=12)) == 2
-    assert _qp(kvq, _pool(kvq, D=24)) == 2          # multiple of 8 but not of 16
-    assert _qp(kvq, _pool(kvq, D=264)) == 2
+    # head dims: exactly those kvq_packed_dim accepts, up to 256
+    for bits in (8, 6, 4):
+        for D in (0, 1, 2, 3, 4, 6, 10, 12, 20, 100, 252, 255, 256, 257, 264):
+            want_ok = D <= 256 and kvq.kvq_packed_dim(D, bits) > 0
+            got = _qp(kvq, _pool(kvq, bits=bits, D=D), total=0)
+            assert (got == 0) == want_ok and (want_ok or got == 2), (bits, D, got)
     assert _qp(kvq, _pool(kvq, H=0)) == 2
     assert _qp(kvq, _pool(kvq, ps=0)) == 2
     assert _qp(kvq, _pool(kvq, codes=0)) == 3
