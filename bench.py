@@ -199,6 +199,129 @@ def max_over_ranks(x: float, world: int, device) -> float:
 
 
 # ----------------------------------------------------------------------------- GPU arm
+L2_FLUSH_BYTES = 256 << 20   # twice the GB300's 129 MB L2
+
+
+def time_fn_flushed(fn, reps, warmup, stream, dev):
+    """Median device time of one call of fn, the L2 flushed (a 256 MB buffer written) before each
+    repetition; only the call itself is between the events."""
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        flush.fill_(0)
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for i, (a, b) in enumerate(ev):
+        flush.fill_(i & 0xFF)
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    del flush
+    return statistics.median(a.elapsed_time(b) / 1e3 for a, b in ev)
+
+
+def roundtrip_extra(kvq, dev, steps, warmup, stream):
+    """The q6 round trip of one layer: K and V each [1 seq, 1,024 tokens, 4 KV heads, 256] fp16
+    (keys with 4 outlier channels per head x10; two all-zero rows), contiguous (one 1,024-token
+    page per sequence, identity table): kvq_quant_pack_paged of both tensors in one call, then
+    kvq_dequant_paged of both.  The working set (5.78 MB each way) fits in L2, so the L2 is flushed
+    before every repetition and the figures are latency-bound, not HBM roofline figures."""
+    w = kvgen.WORKLOADS["q6_roundtrip_1x1024x4x256"]
+    T, H, D, bits = w["n_tok"], w["H"], w["D"], w["bits"]
+    xs = [kvgen.KVSpec(seed=w["seed"], layer=0, is_key=k, n_seq=1, n_tok=T, num_heads=H,
+                       head_dim=D).full_torch(dev) for k in (True, False)]
+    pools = [kvq.Pool.empty(bits, H, D, T, 1, dev) for _ in xs]
+    outs = [torch.empty_like(x) for x in xs]
+    pt = torch.zeros((1, 1), dtype=torch.int32, device=dev)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def quant():
+        kvq.kvq_quant_pack_paged(pools, xs, pt, cu, st, err)
+
+    def deq():
+        kvq.kvq_dequant_paged(pools, outs, pt, cu, st, err)
+
+    def both():
+        quant()
+        deq()
+
+    reps = max(steps, 20)
+    tq = time_fn_flushed(quant, reps, warmup, stream, dev)
+    td = time_fn_flushed(deq, reps, warmup, stream, dev)
+    tb = time_fn_flushed(both, reps, warmup, stream, dev)
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError("device error word set in the round trip")
+    nb = bytes_quant(2 * T * H, D, bits)
+    return {"rows": 2 * T * H, "bytes_each_way": nb,
+            "quant_pack_us": tq * 1e6, "quant_pack_GB_s": nb / tq / 1e9,
+            "dequant_us": td * 1e6, "dequant_GB_s": nb / td / 1e9,
+            "round_trip_us": tb * 1e6, "round_trip_GB_s": 2 * nb / tb / 1e9,
+            "l2": "L2-resident working set; L2 flushed (256 MB write) before each repetition; "
+                  "median of the repetitions; latency-bound, not an HBM roofline figure"}
+
+
+def append_extra(kvq, dev, steps, warmup, stream, bits=6):
+    """kvq_quant_pack_paged of a decode-step append: 64 sequences with cached lengths uniform in
+    [1,024, 65,536] append 1, 8 or 32 tokens each into their partially filled tail pages (mapped by
+    the host allocator), 16 layers x {K, V} in one call.  Timed back to back (the step's new rows
+    were just produced) and with the L2 flushed before each call."""
+    wl = kvgen.WORKLOADS["decode_append_16L_64seq_4x256"]
+    L, nseq, H, D, ps = wl["n_layers"], wl["n_seq"], wl["H"], wl["D"], wl["page_size"]
+    cur = kvgen.decode_append_lengths(wl["seed"], nseq)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = {}
+    for n_new in wl["appends"]:
+        max_pages = (int(cur.max()) + n_new + ps - 1) // ps
+        table = torch.full((nseq, max_pages), -1, dtype=torch.int32)
+        alloc = kvq.Allocator(nseq * 4)
+        alloc.reserve(table, ps, cur, [n_new] * nseq)
+        pt = table.to(dev)
+        pools = [kvq.Pool.empty(bits, H, D, ps, nseq * 4, dev) for _ in range(2 * L)]
+        xs = [kvgen.KVSpec(seed=wl["seed"], layer=l, is_key=k, n_seq=nseq, n_tok=n_new,
+                           num_heads=H, head_dim=D, zero_rows=False).full_torch(dev)
+              for l in range(L) for k in (True, False)]
+        cu = torch.tensor(np.arange(nseq + 1) * n_new, dtype=torch.int32, device=dev)
+        st = torch.from_numpy(cur.astype(np.int32)).to(dev)
+
+        def fn():
+            kvq.kvq_quant_pack_paged(pools, xs, pt, cu, st, err)
+
+        tw = time_fn(fn, max(steps, 20), warmup, stream)
+        tc = time_fn_flushed(fn, max(steps, 20), warmup, stream, dev)
+        rows = 2 * L * nseq * n_new * H
+        nb = bytes_quant(rows, D, bits)
+        res[f"{n_new}_tok"] = {"rows": rows, "bytes": nb, "us": tw * 1e6, "GB_s": nb / tw / 1e9,
+                               "us_l2_flushed": tc * 1e6, "GB_s_l2_flushed": nb / tc / 1e9,
+                               "ideal_us_at_measured_peak": nb / (measured_peaks()[0] * 1e9) * 1e6}
+        del pools, xs, alloc
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError("device error word set in the append extra")
+    torch.cuda.empty_cache()
+    return res
+
+
+def kivi_flush32_extra(w, steps, warmup, stream, dev):
+    """The KIVI flush of the 32 tokens [3936, 3968) of every layer's K and V (16 layers x
+    [16, 8, 4096, 64]): one group per flush, as decode reaches each group boundary."""
+    lo, hi = KV["flushes"][0]
+
+    def fn():
+        w.kvq.kivi_quant_dequant(w.kivi, w.kivi_flags, lo, hi, KV["group_size"], KV["levels"],
+                                 KV["eps"])
+
+    t = time_fn(fn, max(steps, 20), warmup, stream)
+    tc = time_fn_flushed(fn, max(steps, 20), warmup, stream, dev)
+    nb = bytes_kivi(len(w.kivi), KV["B"], KV["H"], hi - lo, KV["D"])
+    return {"tokens": hi - lo, "bytes": nb, "us": t * 1e6, "GB_s": nb / t / 1e9,
+            "us_l2_flushed": tc * 1e6, "GB_s_l2_flushed": nb / tc / 1e9}
+
+
 def decode_step_extra(kvq, dev, steps, warmup, stream, bits=6):
     """One decode step of 64 sequences with lengths uniform in [1024, 65536] over 16 layers
     (4 KV heads x 256, 24 query heads, page 16): the fused kvq_append_decode_attn against the two
@@ -650,6 +773,15 @@ def run_gpu(args):
     if not args.no_kivi_packed:
         extras["kivi_decode_loop_16L_16x8_2bit"] = kivi_loop_extra(kvq, dev, args.warmup, stream)
 
+    # the small configurations: the q6 round trip of one layer, the decode-step appends and the
+    # 32-token KIVI flush
+    if not args.no_small:
+        extras["q6_roundtrip_1x1024x4x256"] = roundtrip_extra(kvq, dev, args.steps, args.warmup,
+                                                              stream)
+        extras["append_q6_16L_64seq"] = append_extra(kvq, dev, args.steps, args.warmup, stream)
+        extras["kivi_flush_32tok_16L"] = kivi_flush32_extra(w, args.steps, args.warmup, stream,
+                                                            dev)
+
     # one decode step (append + attend) of 64 ragged sequences
     if not args.no_decode_step:
         extras["decode_step_64seq_ragged_16L_q6"] = decode_step_extra(kvq, dev, args.steps,
@@ -676,8 +808,7 @@ def run_gpu(args):
                        "l2": "inputs larger than L2 (no flush)",
                        "bytes_per_step": step_bytes, "parallelism": f"replicas x{world}"},
             "stages": {k: {kk: round(vv, 3) for kk, vv in v.items()} for k, v in stage.items()},
-            "extras": {k: {kk: (round(vv, 3) if isinstance(vv, float) else vv)
-                           for kk, vv in v.items()} for k, v in extras.items()},
+            "extras": _rounded(extras),
             "roofline": roofline,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
@@ -685,6 +816,15 @@ def run_gpu(args):
             "cpu_baseline": cpu,
         }
         print(json.dumps(line))
+
+
+def _rounded(obj):
+    """The extras with floats rounded to 3 decimals, nested dicts included."""
+    if isinstance(obj, dict):
+        return {k: _rounded(v) for k, v in obj.items()}
+    if isinstance(obj, float):
+        return round(obj, 3)
+    return obj
 
 
 def run_only(w, bits, args, stream):
@@ -848,7 +988,64 @@ def cpu_sample_step():
             + bytes_kivi(2, 1, KV["H"], KIVI_HI - KIVI_LO, KV["D"]))
 
 
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+_POOL_BARRIER = None
+
+
+def _cpu_pool_init(barrier):
+    """Pool worker start-up: the shared barrier and this worker's inputs (outside any timing)."""
+    global _POOL_BARRIER
+    _POOL_BARRIER = barrier
+    _cpu_inputs()
+
+
+def _cpu_pool_task(n_iter):
+    """One worker's share: wait until every worker is ready, then n_iter oracle samples.
+    Returns (bytes, start, end) on the host's monotonic clock (common to all processes)."""
+    _POOL_BARRIER.wait()
+    t0 = time.perf_counter()
+    total = 0
+    for _ in range(n_iter):
+        total += cpu_sample_step()
+    return total, t0, time.perf_counter()
+
+
+class OraclePool:
+    """The oracle run on every host core at once: one spawned process per core (a process pool
+    started with `spawn`, so no CUDA state is inherited), each running whole samples of the
+    workload; BLAS stays single-threaded in every process."""
+
+    def __init__(self, n_workers):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self.n = n_workers
+        self.barrier = ctx.Barrier(n_workers)
+        self.pool = ctx.Pool(n_workers, initializer=_cpu_pool_init, initargs=(self.barrier,))
+
+    def run(self, n_iter):
+        """Every worker runs n_iter samples, all starting together; (bytes, wall seconds)."""
+        res = self.pool.map(_cpu_pool_task, [n_iter] * self.n, chunksize=1)
+        return sum(r[0] for r in res), max(r[2] for r in res) - min(r[1] for r in res)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+CPU_SAMPLE = ("1 layer K+V of 4,096 tokens x 4 heads x 256 quant-pack + dequant (q6, page 16), "
+              "decode attn over it (24 q heads), KIVI flush of 128 tokens of 1 layer "
+              "[1, 8, 4096, 64] K+V")
+
+
 def cpu_baseline(seconds):
+    """The oracle on one core for about `seconds`, then on every host core (one process per core,
+    each running the same number of samples) for about as long."""
     _cpu_inputs()
     t0 = time.perf_counter()
     total, n = 0, 0
@@ -858,26 +1055,46 @@ def cpu_baseline(seconds):
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": round(total / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} x (1 layer K+V of 4,096 tokens x 4 heads x 256 quant-pack + dequant "
-                      f"(q6, page 16), decode attn over it (24 q heads), KIVI flush of 128 "
-                      f"tokens of 1 layer [1, 8, 4096, 64] K+V); {dt:.1f} s"}
+    single = total / dt / 1e9
+    cores = host_cores()
+    out = {"value": round(single, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": f"{n} x ({CPU_SAMPLE}); {dt:.1f} s", "single_core_GB_s": round(single, 4)}
+    if cores > 1:
+        pool = OraclePool(cores)
+        try:
+            pool.run(1)                                 # every worker warm
+            per = max(1, int(round(n * 1.0)))           # each core repeats the single-core run
+            tot, wall = pool.run(per)
+        finally:
+            pool.close()
+        out.update({"value": round(tot / wall / 1e9, 4), "cores": cores,
+                    "sample": f"{cores} processes x {per} x ({CPU_SAMPLE}), {wall:.1f} s wall; "
+                              f"single core: {n} x the same, {dt:.1f} s",
+                    "all_cores_GB_s": round(tot / wall / 1e9, 4)})
+    return out
 
 
 def run_reference(args):
+    """The oracle as it stands on the host cores: each step, every core (one spawned process per
+    core) runs one sample of the step's workload, all starting together."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1 and rank != 0:
         return
-    _cpu_inputs()
-    for _ in range(args.warmup):
-        cpu_sample_step()
-    t0 = time.perf_counter()
-    total = 0
-    for _ in range(args.steps):
-        total += cpu_sample_step()
-    dt = time.perf_counter() - t0
+    cores = host_cores()
+    pool = OraclePool(cores)
+    try:
+        for _ in range(max(1, args.warmup)):
+            pool.run(1)
+        total, dt = 0, 0.0
+        for _ in range(args.steps):
+            b, t = pool.run(1)
+            total += b
+            dt += t
+    finally:
+        pool.close()
     value = total / dt / 1e9
+    sample = f"per step: {cores} processes x 1 x ({CPU_SAMPLE})"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -886,10 +1103,8 @@ def run_reference(args):
         "data": "synthetic (seeded counter-based generator)",
         "config": {"workload": "paged_prefill_16L_8x32768_4x256 step, bounded sample per step",
                    "bits": 6},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "per step: 1 layer K+V of 4,096 tokens (quant-pack + dequant "
-                                   "q6), decode attn over it, KIVI flush of 128 tokens of 1 "
-                                   "layer [1, 8, 4096, 64]"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -920,6 +1135,8 @@ def main():
                     help="skip the fused append + decode step extra")
     ap.add_argument("--no-kivi-packed", action="store_true",
                     help="skip the packed KIVI pack/attention extras")
+    ap.add_argument("--no-small", action="store_true",
+                    help="skip the round-trip, append and 32-token flush extras")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the dominant kernel, if captured")
     args = ap.parse_args()
