@@ -222,6 +222,28 @@ def time_fn_flushed(fn, reps, warmup, stream, dev):
     return statistics.median(a.elapsed_time(b) / 1e3 for a, b in ev)
 
 
+def time_fn_graph(fn, reps, warmup, stream):
+    """Device time of one call of fn with the calls back to back: reps calls captured in a CUDA
+    graph and replayed, so the host's launch cost (the Python binding's argument marshalling) is
+    not between them -- for calls of a few microseconds."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return a.elapsed_time(b) / 1e3 / reps
+
+
 def roundtrip_extra(kvq, dev, steps, warmup, stream):
     """The q6 round trip of one layer: K and V each [1 seq, 1,024 tokens, 4 KV heads, 256] fp16
     (keys with 4 outlier channels per head x10; two all-zero rows), contiguous (one 1,024-token
@@ -253,6 +275,7 @@ def roundtrip_extra(kvq, dev, steps, warmup, stream):
     tq = time_fn_flushed(quant, reps, warmup, stream, dev)
     td = time_fn_flushed(deq, reps, warmup, stream, dev)
     tb = time_fn_flushed(both, reps, warmup, stream, dev)
+    tbw = time_fn_graph(both, reps, warmup, stream)
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise RuntimeError("device error word set in the round trip")
@@ -261,6 +284,7 @@ def roundtrip_extra(kvq, dev, steps, warmup, stream):
             "quant_pack_us": tq * 1e6, "quant_pack_GB_s": nb / tq / 1e9,
             "dequant_us": td * 1e6, "dequant_GB_s": nb / td / 1e9,
             "round_trip_us": tb * 1e6, "round_trip_GB_s": 2 * nb / tb / 1e9,
+            "round_trip_us_l2_resident": tbw * 1e6,
             "l2": "L2-resident working set; L2 flushed (256 MB write) before each repetition; "
                   "median of the repetitions; latency-bound, not an HBM roofline figure"}
 
@@ -268,8 +292,9 @@ def roundtrip_extra(kvq, dev, steps, warmup, stream):
 def append_extra(kvq, dev, steps, warmup, stream, bits=6):
     """kvq_quant_pack_paged of a decode-step append: 64 sequences with cached lengths uniform in
     [1,024, 65,536] append 1, 8 or 32 tokens each into their partially filled tail pages (mapped by
-    the host allocator), 16 layers x {K, V} in one call.  Timed back to back (the step's new rows
-    were just produced) and with the L2 flushed before each call."""
+    the host allocator), 16 layers x {K, V} in one call.  Timed back to back from a CUDA graph (the
+    step's new rows were just produced, so they sit in L2) and with the L2 flushed before each
+    call."""
     wl = kvgen.WORKLOADS["decode_append_16L_64seq_4x256"]
     L, nseq, H, D, ps = wl["n_layers"], wl["n_seq"], wl["H"], wl["D"], wl["page_size"]
     cur = kvgen.decode_append_lengths(wl["seed"], nseq)
@@ -291,7 +316,7 @@ def append_extra(kvq, dev, steps, warmup, stream, bits=6):
         def fn():
             kvq.kvq_quant_pack_paged(pools, xs, pt, cu, st, err)
 
-        tw = time_fn(fn, max(steps, 20), warmup, stream)
+        tw = time_fn_graph(fn, max(steps, 20), warmup, stream)
         tc = time_fn_flushed(fn, max(steps, 20), warmup, stream, dev)
         rows = 2 * L * nseq * n_new * H
         nb = bytes_quant(rows, D, bits)
@@ -315,7 +340,7 @@ def kivi_flush32_extra(w, steps, warmup, stream, dev):
         w.kvq.kivi_quant_dequant(w.kivi, w.kivi_flags, lo, hi, KV["group_size"], KV["levels"],
                                  KV["eps"])
 
-    t = time_fn(fn, max(steps, 20), warmup, stream)
+    t = time_fn_graph(fn, max(steps, 20), warmup, stream)
     tc = time_fn_flushed(fn, max(steps, 20), warmup, stream, dev)
     nb = bytes_kivi(len(w.kivi), KV["B"], KV["H"], hi - lo, KV["D"])
     return {"tokens": hi - lo, "bytes": nb, "us": t * 1e6, "GB_s": nb / t / 1e9,

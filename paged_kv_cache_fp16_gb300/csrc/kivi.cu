@@ -25,9 +25,12 @@
 // of RN(d / scale) at 0.5, 1.5, 2.5 go to the even neighbour), and since no scale * m is an
 // fp32 value (the multipliers' odd parts exceed 2^24) each condition is d >= RU(scale * m),
 // one upward-rounded FMA per group from the exact product scale * 2^-k.
+#include <algorithm>
+
 #include <cuda_runtime.h>
 
 #include "kvq_device.cuh"
+#include "kvq_divu32.cuh"
 #include "kvq_internal.h"
 
 namespace kvq {
@@ -238,6 +241,136 @@ __global__ void __launch_bounds__(kThreads) kivi_values_scalar_kernel(const Kivi
   }
 }
 
+// ------------------------------------------------------------------------------ 2 bits
+// levels = 3 with key groups of at most 32 tokens and value groups of 8..64 channels (8 | gs): one
+// thread per item (a key channel pair of one token group, or a value channel group of one row),
+// no grid-stride loop, the flat item index split with multiply-high division.  Key and value
+// blocks are interleaved in proportion to their counts (pattern of period pk + pv), so every wave
+// of the grid streams both.  A group's four reconstructions fp16(RN(RN(c * scale) + gmin)),
+// c = 0..3, are computed once; each element then costs its difference from gmin, the three
+// threshold compares of make_group<true> and three selects of an fp16 value.
+struct L3Plan {
+  DivU32 period;      // pk + pv
+  DivU32 pairs;       // D / 2
+  DivU32 key_groups;  // token groups of the span
+  DivU32 bh;          // B * H
+  DivU32 val_groups;  // channel groups per row
+  DivU32 span;        // hi - lo
+  int pk, pv;
+  uint32_t key_items, val_items;
+};
+
+__device__ __forceinline__ uint32_t recon_bits(const Group& g, float c) {
+  return f2h(__fadd_rn(__fmul_rn(c, g.sc), g.mn));
+}
+
+// fp16 reconstruction of one element given the group's four reconstructions r0..r3.
+__device__ __forceinline__ uint32_t l3_select(float x, const Group& g, uint32_t r0, uint32_t r1,
+                                              uint32_t r2, uint32_t r3) {
+  const float d = __fsub_rn(x, g.mn);
+  return d >= g.t3 ? r3 : (d >= g.t2 ? r2 : (d >= g.t1 ? r1 : r0));
+}
+
+__global__ void __launch_bounds__(kThreads) kivi_l3_kernel(const KiviArgs a, const L3Plan p) {
+  const uint32_t b = blockIdx.x;
+  const uint32_t q = divu32(b, p.period);
+  const int o = static_cast<int>(b - q * static_cast<uint32_t>(p.pk + p.pv));
+  if (o < p.pk) {
+    // ---------------------------------------------------------------- keys
+    const uint32_t it = (q * p.pk + o) * kThreads + threadIdx.x;
+    if (it >= p.key_items) return;
+    const uint32_t r1 = divu32(it, p.pairs);
+    const int pr = static_cast<int>(it - r1 * static_cast<uint32_t>(a.D / 2));
+    const uint32_t r2 = divu32(r1, p.key_groups);
+    const int g = static_cast<int>(r1 - r2 * static_cast<uint32_t>((a.hi - a.lo + a.gs - 1) / a.gs));
+    const uint32_t ki = divu32(r2, p.bh);
+    const int64_t bh = r2 - ki * static_cast<uint32_t>(a.B * a.H);
+    const int t0 = a.lo + g * a.gs;
+    const int n = min(a.gs, a.hi - t0);
+    uint32_t* base = reinterpret_cast<uint32_t*>(a.x[a.key_list[ki]] + (bh * a.S + t0) * a.D) + pr;
+    const int64_t stride_w = a.D / 2;
+    uint32_t keep[kKeepRows];
+    keep[0] = base[0];
+#pragma unroll
+    for (int r = 1; r < kKeepRows; ++r) keep[r] = (r < n) ? base[r * stride_w] : keep[0];
+    __half2 mn[kKeepRows / 2], mx[kKeepRows / 2];
+#pragma unroll
+    for (int r = 0; r < kKeepRows / 2; ++r) {
+      mn[r] = __hmin2(as_h2(keep[2 * r]), as_h2(keep[2 * r + 1]));
+      mx[r] = __hmax2(as_h2(keep[2 * r]), as_h2(keep[2 * r + 1]));
+    }
+#pragma unroll
+    for (int w = kKeepRows / 4; w >= 1; w >>= 1)
+#pragma unroll
+      for (int r = 0; r < w; ++r) {
+        mn[r] = __hmin2(mn[r], mn[r + w]);
+        mx[r] = __hmax2(mx[r], mx[r + w]);
+      }
+    const Group g0 = make_group<true>(__low2float(mn[0]), __low2float(mx[0]), a.levels, a.eps);
+    const Group g1 = make_group<true>(__high2float(mn[0]), __high2float(mx[0]), a.levels, a.eps);
+    // the four reconstructions of both channels, as half2 (low: channel 2 pr, high: 2 pr + 1)
+    const uint32_t rr0 = recon_bits(g0, 0.f) | (recon_bits(g1, 0.f) << 16);
+    const uint32_t rr1 = recon_bits(g0, 1.f) | (recon_bits(g1, 1.f) << 16);
+    const uint32_t rr2 = recon_bits(g0, 2.f) | (recon_bits(g1, 2.f) << 16);
+    const uint32_t rr3 = recon_bits(g0, 3.f) | (recon_bits(g1, 3.f) << 16);
+#pragma unroll
+    for (int r = 0; r < kKeepRows; ++r) {
+      if (r >= n) break;
+      const uint32_t w = keep[r];
+      const uint32_t lo = l3_select(h2f(static_cast<uint16_t>(w & 0xffffu)), g0, rr0 & 0xffffu,
+                                    rr1 & 0xffffu, rr2 & 0xffffu, rr3 & 0xffffu);
+      const uint32_t hi = l3_select(h2f(static_cast<uint16_t>(w >> 16)), g1, rr0 >> 16, rr1 >> 16,
+                                    rr2 >> 16, rr3 >> 16);
+      base[r * stride_w] = lo | (hi << 16);
+    }
+  } else {
+    // ---------------------------------------------------------------- values
+    const uint32_t it = (q * p.pv + (o - p.pk)) * kThreads + threadIdx.x;
+    if (it >= p.val_items) return;
+    const int groups = (a.D + a.gs - 1) / a.gs;
+    const uint32_t row = divu32(it, p.val_groups);
+    const int gi = static_cast<int>(it - row * static_cast<uint32_t>(groups));
+    const uint32_t r2 = divu32(row, p.span);
+    const int t = a.lo + static_cast<int>(row - r2 * static_cast<uint32_t>(a.hi - a.lo));
+    const uint32_t vi = divu32(r2, p.bh);
+    const int64_t bh = r2 - vi * static_cast<uint32_t>(a.B * a.H);
+    const int c0 = gi * a.gs;
+    const int nv = (min(a.D, c0 + a.gs) - c0) / 8;   // 16-byte vectors in this group
+    uint4* pv = reinterpret_cast<uint4*>(a.x[a.val_list[vi]] + (bh * a.S + t) * a.D + c0);
+    uint4 v[kMaxVecs];
+    v[0] = pv[0];
+#pragma unroll
+    for (int k = 1; k < kMaxVecs; ++k) v[k] = (k < nv) ? pv[k] : v[0];   // repeats keep min/max
+    __half2 mn[kMaxVecs], mx[kMaxVecs];
+#pragma unroll
+    for (int k = 0; k < kMaxVecs; ++k) {
+      mn[k] = __hmin2(__hmin2(as_h2(v[k].x), as_h2(v[k].y)), __hmin2(as_h2(v[k].z), as_h2(v[k].w)));
+      mx[k] = __hmax2(__hmax2(as_h2(v[k].x), as_h2(v[k].y)), __hmax2(as_h2(v[k].z), as_h2(v[k].w)));
+    }
+#pragma unroll
+    for (int w = kMaxVecs / 2; w >= 1; w >>= 1)
+#pragma unroll
+      for (int k = 0; k < w; ++k) {
+        mn[k] = __hmin2(mn[k], mn[k + w]);
+        mx[k] = __hmax2(mx[k], mx[k + w]);
+      }
+    const Group gr = make_group<true>(fminf(__low2float(mn[0]), __high2float(mn[0])),
+                                      fmaxf(__low2float(mx[0]), __high2float(mx[0])), a.levels,
+                                      a.eps);
+    const uint32_t r0 = recon_bits(gr, 0.f), r1 = recon_bits(gr, 1.f);
+    const uint32_t r2v = recon_bits(gr, 2.f), r3 = recon_bits(gr, 3.f);
+    auto word = [&](uint32_t w) {
+      return l3_select(h2f(static_cast<uint16_t>(w & 0xffffu)), gr, r0, r1, r2v, r3) |
+             (l3_select(h2f(static_cast<uint16_t>(w >> 16)), gr, r0, r1, r2v, r3) << 16);
+    };
+#pragma unroll
+    for (int k = 0; k < kMaxVecs; ++k) {
+      if (k >= nv) break;
+      pv[k] = make_uint4(word(v[k].x), word(v[k].y), word(v[k].z), word(v[k].w));
+    }
+  }
+}
+
 int blocks_for_threads(int64_t threads, int cap) {
   int64_t b = (threads + kThreads - 1) / kThreads;
   if (b > cap) b = cap;
@@ -298,6 +431,40 @@ extern "C" kvq_status kivi_quant_dequant(uint16_t* const* x, const int32_t* is_k
   const int vb = (a.n_vals > 0 && vec_values) ? blocks_for_threads(val_items, cap) : 0;
   a.key_blocks = kb;
   const bool l3 = levels == 3;   // 2 bits: codes by thresholds
+  const int key_groups = (span + group_size - 1) / group_size;
+  if (l3 && group_size <= kKeepRows && (a.n_vals == 0 || vec_values) &&
+      key_items + val_items > 0 && key_items < (1LL << 31) && val_items < (1LL << 31)) {
+    // one thread per item, key and value blocks interleaved
+    L3Plan p;
+    const int64_t nkb = (key_items + kThreads - 1) / kThreads;
+    const int64_t nvb = (val_items + kThreads - 1) / kThreads;
+    if (nkb == 0) { p.pk = 0; p.pv = 1; }
+    else if (nvb == 0) { p.pk = 1; p.pv = 0; }
+    else if (nvb >= nkb) { p.pk = 1; p.pv = static_cast<int>((nvb + nkb / 2) / nkb); }
+    else { p.pv = 1; p.pk = static_cast<int>((nkb + nvb / 2) / nvb); }
+    if (p.pk + p.pv > 64) {   // very lopsided: plain halves (rare shapes)
+      p.pk = nkb > 0 ? 1 : 0;
+      p.pv = nvb > 0 ? 1 : 0;
+    }
+    int64_t periods = 0;
+    if (p.pk > 0) periods = (nkb + p.pk - 1) / p.pk;
+    if (p.pv > 0) periods = std::max<int64_t>(periods, (nvb + p.pv - 1) / p.pv);
+    p.period = make_divu32(static_cast<uint32_t>(p.pk + p.pv));
+    p.pairs = make_divu32(static_cast<uint32_t>(D / 2));
+    p.key_groups = make_divu32(static_cast<uint32_t>(key_groups));
+    p.bh = make_divu32(static_cast<uint32_t>(B * H));
+    p.val_groups = make_divu32(static_cast<uint32_t>((D + group_size - 1) / group_size));
+    p.span = make_divu32(static_cast<uint32_t>(span));
+    p.key_items = static_cast<uint32_t>(key_items);
+    p.val_items = static_cast<uint32_t>(val_items);
+    const int64_t blocks = periods * (p.pk + p.pv);
+    if (blocks < (1LL << 31)) {
+      kivi_l3_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(a, p);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "kivi launch: %s", cudaGetErrorString(e));
+      return ok();
+    }
+  }
   if (kb + vb > 0) {
     if (l3) kivi_kernel<true><<<kb + vb, kThreads, 0, st>>>(a);
     else kivi_kernel<false><<<kb + vb, kThreads, 0, st>>>(a);
