@@ -426,21 +426,29 @@ __device__ __forceinline__ void cta_merge_write(const AttnArgs& a, float* sm, in
 }
 
 // ------------------------------------------------------------------------------ TMA kernel
-// Fused append: quantize the new K and V rows of (layer, sequence s, KV head h) exactly as
-// kvq_quant_pack_paged does and store them at physical row `prow` of the pools.  Lanes 0-15 take
-// the K row, lanes 16-31 the V row, 16 elements (one unit) per lane.
+// Fused append, first part: this lane's 16 elements of the new K (lanes 0-15) or V (lanes 16-31)
+// row of (layer, sequence s, KV head h), loaded at the start of the kernel so their latency
+// overlaps the block's set-up.
+__device__ __forceinline__ void append_load(const AttnArgs& a, int layer, int s, int h, int lane,
+                                            uint4& x0, uint4& x1) {
+  const uint16_t* src = (lane >= 16 ? a.vnew[layer] : a.knew[layer]) +
+                        (static_cast<int64_t>(s) * a.H + h) * kD + (lane & 15) * 16;
+  x0 = ld_nc_v4(src);
+  x1 = ld_nc_v4(src + 8);
+}
+
+// Fused append, second part: quantize the loaded rows exactly as kvq_quant_pack_paged does and
+// store them at physical row `prow` of the pools (lanes 0-15 the K row, lanes 16-31 the V row, one
+// 16-element unit per lane).
 template <int BITS>
-__device__ __forceinline__ void append_rows(const AttnArgs& a, const LayerPools& P, int layer,
-                                            int s, int h, int64_t prow, int lane) {
+__device__ __forceinline__ void append_rows(const LayerPools& P, int64_t prow, int lane,
+                                            const uint4& x0, const uint4& x1) {
   constexpr int kQm = SymQ<BITS>::kQmax;
   constexpr int kB = SymQ<BITS>::kBias;
   constexpr int kM = SymQ<BITS>::kMask;
   constexpr int kPd = Wd<BITS>::kPd;
   const bool is_v = lane >= 16;
   const int u = lane & 15;
-  const uint16_t* src = (is_v ? a.vnew[layer] : a.knew[layer]) +
-                        (static_cast<int64_t>(s) * a.H + h) * kD + u * 16;
-  const uint4 x0 = ld_nc_v4(src), x1 = ld_nc_v4(src + 8);
   const __half2 m2 = __hmax2(absmax8(x0), absmax8(x1));
   float amax = fmaxf(__low2float(m2), __high2float(m2));
 #pragma unroll
@@ -572,6 +580,21 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
   const int tile1 = min(n_tiles, tile0 + a.tiles_per_cta);
   const int n_mine = (tile1 - tile0 - warp + kWarps - 1) > 0
                          ? (tile1 - tile0 - warp + kWarps - 1) / kWarps : 0;
+  // fused append: the warp whose last tile holds the new token loads its rows and page id now
+  bool append_here = false;
+  int append_page = -1, append_slot = 0;
+  uint4 nx0 = make_uint4(0, 0, 0, 0), nx1 = nx0;
+  if constexpr (APPEND) {
+    const int ta = (len - 1) / kTile;
+    append_here = len > 0 && ta >= tile0 && ta < tile1 && (ta - tile0) % kWarps == warp;
+    if (append_here) {
+      append_load(a, layer, s, h, lane, nx0, nx1);
+      const int pos = len - 1;
+      const int lp = pos / a.ps;
+      append_slot = pos - lp * a.ps;
+      if (lp < a.max_pages) append_page = __ldg(a.pt + static_cast<int64_t>(s) * a.max_pages + lp);
+    }
+  }
 
   // stage size: the four page copies, plus the tile's outlier values and positions with side
   // channels (sized by k; compile-time constants without them)
@@ -656,16 +679,12 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
     // The new token (position len - 1) sits in the sequence's last tile, which exactly one warp
     // of the grid streams.  That warp quantizes the new rows into the pages before it issues any
     // copy, so its copy of the tile reads them from global memory (each lane orders its stores
-    // before the bulk copies with a proxy fence); the tile loop itself has no append code.
-    const int ta = (len - 1) / kTile;
-    if (len > 0 && ta >= tile0 && ta < tile1 && (ta - tile0) % kWarps == warp) {   // warp-uniform
-      const int pos = len - 1;
-      const int lp = pos / a.ps;
-      const int page = lp < a.max_pages ? __ldg(a.pt + static_cast<int64_t>(s) * a.max_pages + lp)
-                                        : -1;
-      if (page >= 0 && page < P.k_pages && page < P.v_pages)   // else the tile's issue reports it
-        append_rows<BITS>(a, P, layer, s, h,
-                          (static_cast<int64_t>(page) * a.H + h) * a.ps + (pos - lp * a.ps), lane);
+    // before the bulk copies with a proxy fence); the tile loop itself has no append code.  The
+    // new rows and the tail's page id were loaded at the start of the kernel.
+    if (append_here) {   // warp-uniform
+      if (append_page >= 0 && append_page < P.k_pages && append_page < P.v_pages)
+        append_rows<BITS>(P, (static_cast<int64_t>(append_page) * a.H + h) * a.ps + append_slot,
+                          lane, nx0, nx1);   // else the tile's issue reports it
       asm volatile("fence.proxy.async.global;" ::: "memory");
       __syncwarp();
     }

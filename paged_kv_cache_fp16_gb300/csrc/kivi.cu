@@ -56,12 +56,12 @@ struct Group {
   float t1, t2, t3;  // levels = 3: thresholds of codes 1, 2, 3 on d = RN(x - gmin)
 };
 
-template <bool L3>
+template <bool L3, bool RCP = true>
 __device__ __forceinline__ Group make_group(float mn, float mx, float levels, float eps) {
   Group g;
   g.mn = mn;
   g.sc = fmaxf(__fdiv_rn(__fsub_rn(mx, mn), levels), eps);
-  g.y = __frcp_rn(g.sc);
+  g.y = RCP ? __frcp_rn(g.sc) : 0.f;
   if constexpr (L3) {
     if (g.sc == 0.f) {   // eps = 0 and a constant group: every code is 0
       g.t1 = g.t2 = g.t3 = __int_as_float(0x7f800000);
@@ -268,7 +268,52 @@ __device__ __forceinline__ uint32_t recon_bits(const Group& g, float c) {
 __device__ __forceinline__ uint32_t l3_select(float x, const Group& g, uint32_t r0, uint32_t r1,
                                               uint32_t r2, uint32_t r3) {
   const float d = __fsub_rn(x, g.mn);
-  return d >= g.t3 ? r3 : (d >= g.t2 ? r2 : (d >= g.t1 ? r1 : r0));
+  uint32_t r = r0;
+  r = d >= g.t1 ? r1 : r;
+  r = d >= g.t2 ? r2 : r;
+  r = d >= g.t3 ? r3 : r;
+  return r;
+}
+
+// The two fp16 elements of a word, each against its own group (lo: g0 / q0.., hi: g1 / q1..).
+__device__ __forceinline__ uint32_t l3_word(uint32_t w, const Group& g0, const Group& g1,
+                                            uint32_t rr0, uint32_t rr1, uint32_t rr2,
+                                            uint32_t rr3) {
+  const uint32_t lo = l3_select(h2f(static_cast<uint16_t>(w & 0xffffu)), g0, rr0 & 0xffffu,
+                                rr1 & 0xffffu, rr2 & 0xffffu, rr3 & 0xffffu);
+  const uint32_t hi = l3_select(h2f(static_cast<uint16_t>(w >> 16)), g1, rr0 >> 16, rr1 >> 16,
+                                rr2 >> 16, rr3 >> 16);
+  return lo | (hi << 16);
+}
+
+// A value group of NV 16-byte vectors (8 * NV channels): load, fp16 min/max tree, the 2-bit
+// round trip, store.
+template <int NV>
+__device__ __forceinline__ void l3_value_group(uint4* pv, float levels, float eps) {
+  uint4 v[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) v[k] = pv[k];
+  __half2 mn = __hmin2(__hmin2(as_h2(v[0].x), as_h2(v[0].y)), __hmin2(as_h2(v[0].z), as_h2(v[0].w)));
+  __half2 mx = __hmax2(__hmax2(as_h2(v[0].x), as_h2(v[0].y)), __hmax2(as_h2(v[0].z), as_h2(v[0].w)));
+#pragma unroll
+  for (int k = 1; k < NV; ++k) {
+    mn = __hmin2(mn, __hmin2(__hmin2(as_h2(v[k].x), as_h2(v[k].y)),
+                             __hmin2(as_h2(v[k].z), as_h2(v[k].w))));
+    mx = __hmax2(mx, __hmax2(__hmax2(as_h2(v[k].x), as_h2(v[k].y)),
+                             __hmax2(as_h2(v[k].z), as_h2(v[k].w))));
+  }
+  const Group gr = make_group<true, false>(fminf(__low2float(mn), __high2float(mn)),
+                                           fmaxf(__low2float(mx), __high2float(mx)), levels, eps);
+  const uint32_t r0 = recon_bits(gr, 0.f), r1 = recon_bits(gr, 1.f);
+  const uint32_t r2 = recon_bits(gr, 2.f), r3 = recon_bits(gr, 3.f);
+  const uint32_t rr0 = r0 | (r0 << 16), rr1 = r1 | (r1 << 16);
+  const uint32_t rr2 = r2 | (r2 << 16), rr3 = r3 | (r3 << 16);
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    pv[k] = make_uint4(l3_word(v[k].x, gr, gr, rr0, rr1, rr2, rr3),
+                       l3_word(v[k].y, gr, gr, rr0, rr1, rr2, rr3),
+                       l3_word(v[k].z, gr, gr, rr0, rr1, rr2, rr3),
+                       l3_word(v[k].w, gr, gr, rr0, rr1, rr2, rr3));
 }
 
 __global__ void __launch_bounds__(kThreads) kivi_l3_kernel(const KiviArgs a, const L3Plan p) {
@@ -306,8 +351,10 @@ __global__ void __launch_bounds__(kThreads) kivi_l3_kernel(const KiviArgs a, con
         mn[r] = __hmin2(mn[r], mn[r + w]);
         mx[r] = __hmax2(mx[r], mx[r + w]);
       }
-    const Group g0 = make_group<true>(__low2float(mn[0]), __low2float(mx[0]), a.levels, a.eps);
-    const Group g1 = make_group<true>(__high2float(mn[0]), __high2float(mx[0]), a.levels, a.eps);
+    const Group g0 = make_group<true, false>(__low2float(mn[0]), __low2float(mx[0]), a.levels,
+                                             a.eps);
+    const Group g1 = make_group<true, false>(__high2float(mn[0]), __high2float(mx[0]), a.levels,
+                                             a.eps);
     // the four reconstructions of both channels, as half2 (low: channel 2 pr, high: 2 pr + 1)
     const uint32_t rr0 = recon_bits(g0, 0.f) | (recon_bits(g1, 0.f) << 16);
     const uint32_t rr1 = recon_bits(g0, 1.f) | (recon_bits(g1, 1.f) << 16);
@@ -337,36 +384,46 @@ __global__ void __launch_bounds__(kThreads) kivi_l3_kernel(const KiviArgs a, con
     const int c0 = gi * a.gs;
     const int nv = (min(a.D, c0 + a.gs) - c0) / 8;   // 16-byte vectors in this group
     uint4* pv = reinterpret_cast<uint4*>(a.x[a.val_list[vi]] + (bh * a.S + t) * a.D + c0);
+    if (nv == 4) {   // groups of 32 channels: no padding, no bounds
+      l3_value_group<4>(pv, a.levels, a.eps);
+      return;
+    }
+    if (nv == 2) {
+      l3_value_group<2>(pv, a.levels, a.eps);
+      return;
+    }
+    if (nv == 1) {
+      l3_value_group<1>(pv, a.levels, a.eps);
+      return;
+    }
+    // other group widths: up to 8 vectors, padded with the first (min / max unchanged)
     uint4 v[kMaxVecs];
     v[0] = pv[0];
 #pragma unroll
-    for (int k = 1; k < kMaxVecs; ++k) v[k] = (k < nv) ? pv[k] : v[0];   // repeats keep min/max
-    __half2 mn[kMaxVecs], mx[kMaxVecs];
+    for (int k = 1; k < kMaxVecs; ++k) v[k] = (k < nv) ? pv[k] : v[0];
+    __half2 mn = __hmin2(__hmin2(as_h2(v[0].x), as_h2(v[0].y)), __hmin2(as_h2(v[0].z), as_h2(v[0].w)));
+    __half2 mx = __hmax2(__hmax2(as_h2(v[0].x), as_h2(v[0].y)), __hmax2(as_h2(v[0].z), as_h2(v[0].w)));
 #pragma unroll
-    for (int k = 0; k < kMaxVecs; ++k) {
-      mn[k] = __hmin2(__hmin2(as_h2(v[k].x), as_h2(v[k].y)), __hmin2(as_h2(v[k].z), as_h2(v[k].w)));
-      mx[k] = __hmax2(__hmax2(as_h2(v[k].x), as_h2(v[k].y)), __hmax2(as_h2(v[k].z), as_h2(v[k].w)));
+    for (int k = 1; k < kMaxVecs; ++k) {
+      mn = __hmin2(mn, __hmin2(__hmin2(as_h2(v[k].x), as_h2(v[k].y)),
+                               __hmin2(as_h2(v[k].z), as_h2(v[k].w))));
+      mx = __hmax2(mx, __hmax2(__hmax2(as_h2(v[k].x), as_h2(v[k].y)),
+                               __hmax2(as_h2(v[k].z), as_h2(v[k].w))));
     }
-#pragma unroll
-    for (int w = kMaxVecs / 2; w >= 1; w >>= 1)
-#pragma unroll
-      for (int k = 0; k < w; ++k) {
-        mn[k] = __hmin2(mn[k], mn[k + w]);
-        mx[k] = __hmax2(mx[k], mx[k + w]);
-      }
-    const Group gr = make_group<true>(fminf(__low2float(mn[0]), __high2float(mn[0])),
-                                      fmaxf(__low2float(mx[0]), __high2float(mx[0])), a.levels,
-                                      a.eps);
-    const uint32_t r0 = recon_bits(gr, 0.f), r1 = recon_bits(gr, 1.f);
-    const uint32_t r2v = recon_bits(gr, 2.f), r3 = recon_bits(gr, 3.f);
-    auto word = [&](uint32_t w) {
-      return l3_select(h2f(static_cast<uint16_t>(w & 0xffffu)), gr, r0, r1, r2v, r3) |
-             (l3_select(h2f(static_cast<uint16_t>(w >> 16)), gr, r0, r1, r2v, r3) << 16);
-    };
+    const Group gr = make_group<true, false>(fminf(__low2float(mn), __high2float(mn)),
+                                             fmaxf(__low2float(mx), __high2float(mx)), a.levels,
+                                             a.eps);
+    const uint32_t c0r = recon_bits(gr, 0.f), c1r = recon_bits(gr, 1.f);
+    const uint32_t c2r = recon_bits(gr, 2.f), c3r = recon_bits(gr, 3.f);
+    const uint32_t rr0 = c0r | (c0r << 16), rr1 = c1r | (c1r << 16);
+    const uint32_t rr2 = c2r | (c2r << 16), rr3 = c3r | (c3r << 16);
 #pragma unroll
     for (int k = 0; k < kMaxVecs; ++k) {
       if (k >= nv) break;
-      pv[k] = make_uint4(word(v[k].x), word(v[k].y), word(v[k].z), word(v[k].w));
+      pv[k] = make_uint4(l3_word(v[k].x, gr, gr, rr0, rr1, rr2, rr3),
+                         l3_word(v[k].y, gr, gr, rr0, rr1, rr2, rr3),
+                         l3_word(v[k].z, gr, gr, rr0, rr1, rr2, rr3),
+                         l3_word(v[k].w, gr, gr, rr0, rr1, rr2, rr3));
     }
   }
 }

@@ -57,9 +57,22 @@ __device__ __forceinline__ uint16_t ld_nc_u16(const void* p) {
 }
 
 // Largest s in [0, nseq) with cu[s] <= i.  For a well-formed cu (non-decreasing, cu[0] = 0,
-// i < cu[nseq]) this is the sequence that owns new-token row i; for any cu it stays in range.
-__device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu, int nseq, int i) {
+// i < cu[nseq] = total) this is the sequence that owns new-token row i; for any cu it stays in
+// range.  The guess g = i * nseq / total is checked first (cu[g] <= i < cu[g + 1], two loads in
+// parallel): it is exact whenever the sequences add equal numbers of tokens (a decode-step
+// append, a uniform prefill), which saves the binary search's chain of dependent loads; otherwise
+// the search runs on the side of g that holds the answer.
+__device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu, int nseq, int total,
+                                        int i) {
   int lo = 0, hi = nseq - 1;
+  if (total > 0 && nseq > 1) {
+    int g = static_cast<int>((static_cast<int64_t>(i) * nseq) / total);
+    g = g < 0 ? 0 : (g > nseq - 1 ? nseq - 1 : g);
+    const int c0 = __ldg(cu + g), c1 = __ldg(cu + g + 1);
+    if (c0 <= i && (g == nseq - 1 || i < c1)) return g;
+    if (c0 > i) hi = g - 1;
+    else lo = g + 1;
+  }
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
     if (__ldg(cu + mid) <= i) lo = mid; else hi = mid - 1;

@@ -43,7 +43,7 @@ __device__ __forceinline__ int64_t row_place(const Args& a, int64_t r, int& t, i
   const int64_t rr = r - t * per_t;
   tok = static_cast<int>(rr / a.H);
   h = static_cast<int>(rr - static_cast<int64_t>(tok) * a.H);
-  s = find_seq(a.cu, a.nseq, tok);
+  s = find_seq(a.cu, a.nseq, a.total_tokens, tok);
   pos = static_cast<int64_t>(__ldg(a.start + s)) + (tok - __ldg(a.cu + s));
   return locate_row(a.page_table, a.max_pages, a.page_size, a.H, a.pool[t].num_pages, s, pos, h,
                     a.err);

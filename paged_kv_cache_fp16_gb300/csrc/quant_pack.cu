@@ -30,7 +30,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarpsPerBlock = kThreads / 32;
-constexpr int kTok = 8;     // tokens per warp work item (all heads of each)
+constexpr int kTok = 8;     // most tokens per warp work item (all heads of each)
 constexpr int kUnroll = 2;  // warp steps with loads in flight (quant-pack)
 // dequant: its loads are smaller than the quantizer's, so more warp steps stay in flight.  The
 // kernel is built for at least 3 blocks per SM (up to 85 registers).  q6 takes 6 steps (80
@@ -50,11 +50,12 @@ struct PackArgs {
   int n_tensors, total_tokens, H, D, page_size, pd, max_pages, nseq;
   int units;     // 16-element units per row: ceil(D / 16)
   int lpr_log2;  // lanes per row = 1 << lpr_log2 = min(next_pow2(units), 8)
+  int tpi;       // tokens per work item, 1..kTok (fewer for calls too small to fill the GPU)
 };
 
 // Physical row of head 0 of new token `tok` ((page * H) * page_size + slot), or -1.
 __device__ __forceinline__ long long token_base(const PackArgs& a, int64_t num_pages, int tok) {
-  const int s = find_seq(a.cu, a.nseq, tok);
+  const int s = find_seq(a.cu, a.nseq, a.total_tokens, tok);
   const int64_t pos = static_cast<int64_t>(__ldg(a.start + s)) + (tok - __ldg(a.cu + s));
   return locate_row(a.page_table, a.max_pages, a.page_size, a.H, num_pages, s, pos, 0, a.err);
 }
@@ -79,13 +80,13 @@ __global__ void __launch_bounds__(kThreads) quant_pack_kernel(const PackArgs a) 
   const int lr = lane & (lpr - 1);       // lane within the row
   const int sub = lane >> a.lpr_log2;    // row within the step
   const int H = a.H, D = a.D;
-  const int n_items = (a.total_tokens + kTok - 1) / kTok;
+  const int n_items = (a.total_tokens + a.tpi - 1) / a.tpi;
   const int n_warps = gridDim.x * kWarpsPerBlock;
 
   for (int item = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); item < n_items;
        item += n_warps) {
-    const int tok0 = item * kTok;
-    const int ntok = min(kTok, a.total_tokens - tok0);
+    const int tok0 = item * a.tpi;
+    const int ntok = min(a.tpi, a.total_tokens - tok0);
     long long base = -1;
     if (lane < ntok) base = token_base(a, pool.num_pages, tok0 + lane);
     const int nrows = ntok * H;
@@ -171,13 +172,13 @@ __global__ void __launch_bounds__(kThreads, 3) dequant_kernel(const PackArgs a) 
   const int lr = lane & (lpr - 1);
   const int sub = lane >> a.lpr_log2;
   const int H = a.H, D = a.D;
-  const int n_items = (a.total_tokens + kTok - 1) / kTok;
+  const int n_items = (a.total_tokens + a.tpi - 1) / a.tpi;
   const int n_warps = gridDim.x * kWarpsPerBlock;
 
   for (int item = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); item < n_items;
        item += n_warps) {
-    const int tok0 = item * kTok;
-    const int ntok = min(kTok, a.total_tokens - tok0);
+    const int tok0 = item * a.tpi;
+    const int ntok = min(a.tpi, a.total_tokens - tok0);
     long long base = -1;
     if (lane < ntok) base = token_base(a, pool.num_pages, tok0 + lane);
     const int nrows = ntok * H;
@@ -246,13 +247,13 @@ int ceil_log2(int v) {
 // tensors together at most what is resident on the SMs at once (rounded down per tensor, so no
 // block waits for a second wave).
 template <typename K>
-dim3 grid_for(K kernel, int& cache, int n_tensors, int total_tokens) {
+dim3 grid_for(K kernel, int& cache, int n_tensors, int total_tokens, int tpi) {
   if (cache == 0) {
     int b = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0);
     cache = (e != cudaSuccess || b < 1) ? 1 : b;
   }
-  const int64_t items = (static_cast<int64_t>(total_tokens) + kTok - 1) / kTok;
+  const int64_t items = (static_cast<int64_t>(total_tokens) + tpi - 1) / tpi;
   const int64_t need = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const int sms = sm_count();
   const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * cache;
@@ -263,16 +264,26 @@ dim3 grid_for(K kernel, int& cache, int n_tensors, int total_tokens) {
 }
 
 template <int BITS, int UPL, bool QUANT>
-cudaError_t launch_one(const PackArgs& a, cudaStream_t stream) {
+cudaError_t launch_one(const PackArgs& a_in, cudaStream_t stream) {
   static int cache = 0;
   if (QUANT) {
+    // A call with few new tokens (a decode-step append) takes fewer tokens per work item, so one
+    // round of the grid's warps covers its items: the warps a tensor gets at most (its share of
+    // the resident blocks) each take one item when tokens / warps <= 8.
+    PackArgs a = a_in;
+    if (cache == 0) grid_for(quant_pack_kernel<BITS, UPL>, cache, a.n_tensors, 1, 1);
+    const int64_t warps = static_cast<int64_t>(sm_count() > 0 ? sm_count() : 152) * cache /
+                          a.n_tensors * kWarpsPerBlock;
+    const int64_t per = warps > 0 ? (a.total_tokens + warps - 1) / warps : kTok;
+    a.tpi = per < 1 ? 1 : (per > kTok ? kTok : static_cast<int>(per));
     quant_pack_kernel<BITS, UPL>
-        <<<grid_for(quant_pack_kernel<BITS, UPL>, cache, a.n_tensors, a.total_tokens), kThreads,
-           0, stream>>>(a);
+        <<<grid_for(quant_pack_kernel<BITS, UPL>, cache, a.n_tensors, a.total_tokens, a.tpi),
+           kThreads, 0, stream>>>(a);
   } else {
     dequant_kernel<BITS, UPL>
-        <<<grid_for(dequant_kernel<BITS, UPL>, cache, a.n_tensors, a.total_tokens), kThreads, 0,
-           stream>>>(a);
+        <<<grid_for(dequant_kernel<BITS, UPL>, cache, a_in.n_tensors, a_in.total_tokens,
+                    a_in.tpi),
+           kThreads, 0, stream>>>(a_in);
   }
   return cudaGetLastError();
 }
@@ -336,6 +347,7 @@ kvq_status prepare(PackArgs& a, const kvq_pool* pools, const uint16_t* const* x,
   a.units = (p0.head_dim + 15) / 16;
   a.lpr_log2 = ceil_log2(a.units) < 3 ? ceil_log2(a.units) : 3;
   a.total_tokens = total_tokens;
+  a.tpi = kTok;
   a.page_table = page_table;
   a.cu = cu;
   a.start = start;

@@ -71,7 +71,7 @@ struct SideArgs {
 // sequence and position (the position clamped to int: it is only compared with n_sink).
 __device__ __forceinline__ long long token_place(const SideArgs& a, int64_t num_pages, int tok,
                                                  int& s, int& pos) {
-  s = find_seq(a.cu, a.nseq, tok);
+  s = find_seq(a.cu, a.nseq, a.total_tokens, tok);
   const int64_t p = static_cast<int64_t>(__ldg(a.start + s)) + (tok - __ldg(a.cu + s));
   pos = p > 0x7fffffffLL ? 0x7fffffff : static_cast<int>(p);
   return locate_row(a.page_table, a.max_pages, a.page_size, a.H, num_pages, s, p, 0, a.err);
