@@ -331,10 +331,10 @@ def append_extra(kvq, dev, steps, warmup, stream, bits=6):
     return res
 
 
-def kivi_flush32_extra(w, steps, warmup, stream, dev):
-    """The KIVI flush of the 32 tokens [3936, 3968) of every layer's K and V (16 layers x
-    [16, 8, 4096, 64]): one group per flush, as decode reaches each group boundary."""
-    lo, hi = KV["flushes"][0]
+def kivi_flush_extra(w, steps, warmup, stream, dev, lo, hi):
+    """A KIVI flush of tokens [lo, hi) of every layer's K and V (16 layers x [16, 8, 4096, 64]):
+    32 tokens is one group, as decode reaches each group boundary; 128 tokens is the step's flush.
+    Timed back to back from a CUDA graph and with the L2 flushed before each call."""
 
     def fn():
         w.kvq.kivi_quant_dequant(w.kivi, w.kivi_flags, lo, hi, KV["group_size"], KV["levels"],
@@ -804,8 +804,9 @@ def run_gpu(args):
         extras["q6_roundtrip_1x1024x4x256"] = roundtrip_extra(kvq, dev, args.steps, args.warmup,
                                                               stream)
         extras["append_q6_16L_64seq"] = append_extra(kvq, dev, args.steps, args.warmup, stream)
-        extras["kivi_flush_32tok_16L"] = kivi_flush32_extra(w, args.steps, args.warmup, stream,
-                                                            dev)
+        for lo, hi in KV["flushes"]:
+            extras[f"kivi_flush_{hi - lo}tok_16L"] = kivi_flush_extra(w, args.steps, args.warmup,
+                                                                      stream, dev, lo, hi)
 
     # one decode step (append + attend) of 64 ragged sequences
     if not args.no_decode_step:
