@@ -61,6 +61,30 @@ __device__ __forceinline__ uint32_t quant_field_c(float x, float se, float y) {
   return rint_biased_bits<BIAS>(q) & static_cast<uint32_t>(MASK);
 }
 
+// Two elements of the quantizer at once without the clamp (rows whose fp16 scale is normal):
+// the quotient and the rounding add of quant_field_c<..., false> with Blackwell's packed float32
+// instructions (mul/fma/add.rn.f32x2), whose two lanes are each the IEEE float32 operation of the
+// scalar path -- four instructions per pair instead of eight.  Returns the two raw sums
+// (rint_biased_bits); tests/cuda/division_check.cu compares them with the scalar path for every
+// finite fp16 x and positive fp16 s.
+__device__ __forceinline__ uint64_t f32x2_of(float lo, float hi) {
+  return static_cast<uint64_t>(__float_as_uint(lo)) |
+         (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+
+template <int BIAS>
+__device__ __forceinline__ uint2 quant_raw2(float xa, float xb, float se, float y) {
+  const uint64_t x = f32x2_of(xa, xb), yy = f32x2_of(y, y), ns = f32x2_of(-se, -se);
+  constexpr float kMagic = 12582912.0f + static_cast<float>(BIAS);
+  const uint64_t mg = f32x2_of(kMagic, kMagic);
+  uint64_t q0, r, q1, t;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x), "l"(yy));        // q0 = RN(x * y)
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(q0), "l"(ns), "l"(x));   // x - q0 * s
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q1) : "l"(r), "l"(yy), "l"(q0));  // q0 + r * y
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(t) : "l"(q1), "l"(mg));           // rint + bias
+  return make_uint2(static_cast<uint32_t>(t), static_cast<uint32_t>(t >> 32));
+}
+
 // ---------------------------------------------------------------------------------------------
 // Packed fields -> exact fp16 codes.  A field u placed in the low mantissa bits of 1024 (fp16
 // 0x6400) reads as 1024 + u (or 1024 + 16u / 1024 + 4u when it sits higher); one half2 FMA then
@@ -180,6 +204,54 @@ __device__ __forceinline__ void store_unit(uint8_t* p, const uint32_t a0, const 
     *reinterpret_cast<uint2*>(p) = make_uint2(a0, a1);
   } else {
     *reinterpret_cast<uint4*>(p) = make_uint4(a0, b0, a1, b1);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Packing fields from the quantizer's raw rounding sums with integer multiply-adds (the FMA pipe)
+// instead of masks and shifts (the integer-logic pipe).
+__device__ __forceinline__ uint32_t mad_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+// The quantizer's raw sum RN(q + 1.5 * 2^23 + B): its pattern is kMagic + B + c for the code c
+// (every term a small integer), so with B + c in [0, 2^BITS) the field is the pattern minus
+// kMagic.  q8 takes B = 128 here (fields c + 128) and flips each byte's top bit after packing.
+constexpr uint32_t kMagic = 0x4B400000u;   // bits of 1.5 * 2^23
+template <int BITS> constexpr int raw_bias() { return BITS == 8 ? 128 : SymQ<BITS>::kBias; }
+
+template <int QMAX, int B, bool CLIP>
+__device__ __forceinline__ uint32_t quant_raw(float x, float se, float y) {
+  float q = div_by_row_scale(x, se, y);
+  if constexpr (CLIP) q = fminf(fmaxf(q, -static_cast<float>(QMAX)), static_cast<float>(QMAX));
+  return rint_biased_bits<B>(q);
+}
+
+// 8 raw sums -> the packed fields (pack8's layout): the fields are the digits of a base-2^BITS
+// number, so one multiply-add per field builds it from the raw patterns and a constant removes
+// the kMagic terms (all arithmetic mod 2^32).
+template <int BITS>
+__device__ __forceinline__ void pack8_raw(const uint32_t r[8], uint32_t& a, uint32_t& b) {
+  if constexpr (BITS == 6) {
+    constexpr uint32_t kOff = kMagic * (1u + 64u + 4096u + 262144u);
+    a = mad_u32(mad_u32(mad_u32(r[3], 64u, r[2]), 64u, r[1]), 64u, r[0]) - kOff;
+    b = mad_u32(mad_u32(mad_u32(r[7], 64u, r[6]), 64u, r[5]), 64u, r[4]) - kOff;
+  } else if constexpr (BITS == 4) {
+    uint32_t t = r[7];
+    uint32_t off = 1u;
+#pragma unroll
+    for (int k = 6; k >= 0; --k) {
+      t = mad_u32(t, 16u, r[k]);
+      off = off * 16u + 1u;
+    }
+    a = t - kMagic * off;
+    b = 0;
+  } else {
+    constexpr uint32_t kOff = kMagic * (1u + 256u + 65536u + 16777216u);
+    a = (mad_u32(mad_u32(mad_u32(r[3], 256u, r[2]), 256u, r[1]), 256u, r[0]) - kOff) ^ 0x80808080u;
+    b = (mad_u32(mad_u32(mad_u32(r[7], 256u, r[6]), 256u, r[5]), 256u, r[4]) - kOff) ^ 0x80808080u;
   }
 }
 

@@ -142,12 +142,39 @@ __global__ void __launch_bounds__(kThreads) quant_pack_kernel(const PackArgs a) 
               const uint4& vv = v[u][j][hh];
               const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
               uint32_t f[8];
+              if constexpr (kClip) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float xe = h2f(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
-                f[e] = quant_field_c<kQm, kB, kM, kClip>(xe, se, y);
+                for (int e = 0; e < 8; ++e) {
+                  const float xe = h2f(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
+                  f[e] = quant_field_c<kQm, kB, kM, true>(xe, se, y);
+                }
+                pack8<BITS>(f, pk[2 * hh], pk[2 * hh + 1]);
+              } else if constexpr (BITS == 4) {
+                // the common path: two elements per packed float32 instruction; at q4 the fields
+                // are packed from the raw rounding sums by integer multiply-adds (measured on one
+                // box: 3.67 -> 3.46 ms for the 16-layer call; masks and shifts: 3.58 ms)
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                  const uint2 r = quant_raw2<raw_bias<BITS>()>(
+                      h2f(static_cast<uint16_t>(w[e >> 1])),
+                      h2f(static_cast<uint16_t>(w[e >> 1] >> 16)), se, y);
+                  f[e] = r.x;
+                  f[e + 1] = r.y;
+                }
+                pack8_raw<BITS>(f, pk[2 * hh], pk[2 * hh + 1]);
+              } else {
+                // q6 / q8: the same packed quotient, fields by masks and shifts (the multiply-add
+                // packing measured 1.9 % slower at q6, 0.4 % at q8; this form 0.6 % faster than the
+                // scalar quotient at q6)
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                  const uint2 r = quant_raw2<kB>(h2f(static_cast<uint16_t>(w[e >> 1])),
+                                                 h2f(static_cast<uint16_t>(w[e >> 1] >> 16)), se, y);
+                  f[e] = r.x & static_cast<uint32_t>(kM);
+                  f[e + 1] = r.y & static_cast<uint32_t>(kM);
+                }
+                pack8<BITS>(f, pk[2 * hh], pk[2 * hh + 1]);
               }
-              pack8<BITS>(f, pk[2 * hh], pk[2 * hh + 1]);
             }
             store_unit<BITS>(crow + unit * SymQ<BITS>::kUnitBytes, pk[0], pk[1], pk[2], pk[3]);
           }

@@ -146,51 +146,6 @@ __device__ __forceinline__ void merge_top(uint32_t* run, const uint32_t* g) {
 }
 
 // ------------------------------------------------------------------------------ quant-pack
-__device__ __forceinline__ uint32_t mad_u32(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t r;
-  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-  return r;
-}
-
-// The quantizer's raw sum RN(q + 1.5 * 2^23 + B): its pattern is kMagic + B + c for the code c
-// (every term a small integer), so with B + c in [0, 2^BITS) the field is the pattern minus
-// kMagic.  q8 takes B = 128 here (fields c + 128) and flips each byte's top bit after packing.
-constexpr uint32_t kMagic = 0x4B400000u;   // bits of 1.5 * 2^23
-template <int BITS> constexpr int raw_bias() { return BITS == 8 ? 128 : SymQ<BITS>::kBias; }
-
-template <int QMAX, int B, bool CLIP>
-__device__ __forceinline__ uint32_t quant_raw(float x, float se, float y) {
-  float q = div_by_row_scale(x, se, y);
-  if constexpr (CLIP) q = fminf(fmaxf(q, -static_cast<float>(QMAX)), static_cast<float>(QMAX));
-  return rint_biased_bits<B>(q);
-}
-
-// 8 raw sums -> the packed fields (pack8's layout): the fields are the digits of a base-2^BITS
-// number, so one multiply-add per field builds it from the raw patterns and a constant removes
-// the kMagic terms (all arithmetic mod 2^32).
-template <int BITS>
-__device__ __forceinline__ void pack8_raw(const uint32_t r[8], uint32_t& a, uint32_t& b) {
-  if constexpr (BITS == 6) {
-    constexpr uint32_t kOff = kMagic * (1u + 64u + 4096u + 262144u);
-    a = mad_u32(mad_u32(mad_u32(r[3], 64u, r[2]), 64u, r[1]), 64u, r[0]) - kOff;
-    b = mad_u32(mad_u32(mad_u32(r[7], 64u, r[6]), 64u, r[5]), 64u, r[4]) - kOff;
-  } else if constexpr (BITS == 4) {
-    uint32_t t = r[7];
-    uint32_t off = 1u;
-#pragma unroll
-    for (int k = 6; k >= 0; --k) {
-      t = mad_u32(t, 16u, r[k]);
-      off = off * 16u + 1u;
-    }
-    a = t - kMagic * off;
-    b = 0;
-  } else {
-    constexpr uint32_t kOff = kMagic * (1u + 256u + 65536u + 16777216u);
-    a = (mad_u32(mad_u32(mad_u32(r[3], 256u, r[2]), 256u, r[1]), 256u, r[0]) - kOff) ^ 0x80808080u;
-    b = (mad_u32(mad_u32(mad_u32(r[7], 256u, r[6]), 256u, r[5]), 256u, r[4]) - kOff) ^ 0x80808080u;
-  }
-}
-
 template <int BITS, int UPL, int DEPTH>
 __global__ void __launch_bounds__(kThreads, 3) quant_pack_side_kernel(const SideArgs a) {
   constexpr int kQm = SymQ<BITS>::kQmax;
@@ -341,10 +296,21 @@ __global__ void __launch_bounds__(kThreads, 3) quant_pack_side_kernel(const Side
                           (g[2 * i + 1] > thr ? 0x0000ffffu : 0xffffffffu);
               }
               uint32_t f[8];
+              if constexpr (kClip) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float xe = h2f(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
-                f[e] = quant_raw<kQm, raw_bias<BITS>(), kClip>(xe, se, y);
+                for (int e = 0; e < 8; ++e) {
+                  const float xe = h2f(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
+                  f[e] = quant_raw<kQm, raw_bias<BITS>(), true>(xe, se, y);
+                }
+              } else {   // two elements per packed float32 instruction
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                  const uint2 r = quant_raw2<raw_bias<BITS>()>(
+                      h2f(static_cast<uint16_t>(w[e >> 1])),
+                      h2f(static_cast<uint16_t>(w[e >> 1] >> 16)), se, y);
+                  f[e] = r.x;
+                  f[e + 1] = r.y;
+                }
               }
               pack8_raw<BITS>(f, pk[2 * hh], pk[2 * hh + 1]);
             }

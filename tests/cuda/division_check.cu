@@ -38,6 +38,16 @@ __global__ void check_kernel(unsigned long long* bad) {
     const float y = __frcp_rn(s);
     const float ref = __fdiv_rn(x, s);
     if (kvq::div_by_row_scale(x, s, y) != ref) ++nq;
+    // the packed two-element path equals the scalar raw sums (biases of q8 / q6 / q4)
+    {
+      const uint2 p0 = kvq::quant_raw2<0>(x, -x, s, y), p32 = kvq::quant_raw2<32>(x, -x, s, y);
+      const uint2 p8 = kvq::quant_raw2<8>(x, -x, s, y);
+      const float qa = kvq::div_by_row_scale(x, s, y), qb = kvq::div_by_row_scale(-x, s, y);
+      if (p0.x != kvq::rint_biased_bits<0>(qa) || p0.y != kvq::rint_biased_bits<0>(qb) ||
+          p32.x != kvq::rint_biased_bits<32>(qa) || p32.y != kvq::rint_biased_bits<32>(qb) ||
+          p8.x != kvq::rint_biased_bits<8>(qa) || p8.y != kvq::rint_biased_bits<8>(qb))
+        ++nq;
+    }
     const bool clip = s < 6.103515625e-05f;
     if (!field_ok<127, 0, 0xff>(x, s, ref, s, y, clip)) ++n8;
     if (!field_ok<31, 32, 0x3f>(x, s, ref, s, y, clip)) ++n6;
