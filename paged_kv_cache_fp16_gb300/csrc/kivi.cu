@@ -247,8 +247,8 @@ __global__ void __launch_bounds__(kThreads) kivi_values_scalar_kernel(const Kivi
 // no grid-stride loop, the flat item index split with multiply-high division.  Key and value
 // blocks are interleaved in proportion to their counts (pattern of period pk + pv), so every wave
 // of the grid streams both.  A group's four reconstructions fp16(RN(RN(c * scale) + gmin)),
-// c = 0..3, are computed once; each element then costs its difference from gmin, the three
-// threshold compares of make_group<true> and three selects of an fp16 value.
+// c = 0..3, are computed once, and so are the group's three code boundaries as fp16 values; each
+// pair of elements then costs three packed fp16 compares and three bit selects.
 struct L3Plan {
   DivU32 period;      // pk + pv
   DivU32 pairs;       // D / 2
@@ -264,26 +264,80 @@ __device__ __forceinline__ uint32_t recon_bits(const Group& g, float c) {
   return f2h(__fadd_rn(__fmul_rn(c, g.sc), g.mn));
 }
 
-// fp16 reconstruction of one element given the group's four reconstructions r0..r3.
-__device__ __forceinline__ uint32_t l3_select(float x, const Group& g, uint32_t r0, uint32_t r1,
-                                              uint32_t r2, uint32_t r3) {
-  const float d = __fsub_rn(x, g.mn);
-  uint32_t r = r0;
-  r = d >= g.t1 ? r1 : r;
-  r = d >= g.t2 ? r2 : r;
-  r = d >= g.t3 ? r3 : r;
-  return r;
+// ---- the same selects as fp16 compares.  d(x) = RN(x - gmin) is nondecreasing in x, so for
+// each code k the elements with d(x) >= t_k are exactly those with x >= X_k, X_k the smallest fp16
+// value that reaches t_k.  Finding X_k costs a few float evaluations per group; each element then
+// costs one packed fp16 compare per code (HSET2 on two elements) and one bit select, in place of
+// two conversions, two subtractions and six float compares and selects per word.
+//
+// Order keys: non-NaN fp16 bit patterns mapped monotonically onto 0x03ff (-inf) .. 0xfc00 (+inf),
+// -0 just below +0.
+constexpr uint32_t kKeyNegInf = 0x03ffu, kKeyPosInf = 0xfc00u;
+constexpr uint32_t kNeverReached = 0x7fffu;   // a NaN: no fp16 compare with it is true
+
+__device__ __forceinline__ uint32_t hkey(uint32_t b) { return b ^ ((b & 0x8000u) ? 0xffffu : 0x8000u); }
+__device__ __forceinline__ uint32_t hbits(uint32_t k) { return k ^ ((k & 0x8000u) ? 0x8000u : 0xffffu); }
+
+__device__ __forceinline__ bool reaches(uint32_t k, float mn, float t) {
+  return __fsub_rn(h2f(static_cast<uint16_t>(hbits(k))), mn) >= t;
 }
 
-// The two fp16 elements of a word, each against its own group (lo: g0 / q0.., hi: g1 / q1..).
-__device__ __forceinline__ uint32_t l3_word(uint32_t w, const Group& g0, const Group& g1,
-                                            uint32_t rr0, uint32_t rr1, uint32_t rr2,
-                                            uint32_t rr3) {
-  const uint32_t lo = l3_select(h2f(static_cast<uint16_t>(w & 0xffffu)), g0, rr0 & 0xffffu,
-                                rr1 & 0xffffu, rr2 & 0xffffu, rr3 & 0xffffu);
-  const uint32_t hi = l3_select(h2f(static_cast<uint16_t>(w >> 16)), g1, rr0 >> 16, rr1 >> 16,
-                                rr2 >> 16, rr3 >> 16);
-  return lo | (hi << 16);
+// fp16 bits of the smallest non-NaN fp16 X with RN(X - mn) >= t, or kNeverReached.  The guess
+// fp16(mn + t) is almost always the answer or its neighbour; otherwise a bisection over the order
+// keys, whose bracket keeps !reaches(lo) and reaches(hi) (-inf never reaches a t > -inf).
+__device__ __forceinline__ uint32_t first_reaching(float mn, float t) {
+  uint32_t k = hkey(f2h(__fadd_rn(mn, t)));
+  k = min(max(k, kKeyNegInf + 1u), kKeyPosInf);
+  uint32_t lo, hi;
+  if (reaches(k, mn, t)) {
+    if (!reaches(k - 1u, mn, t)) return hbits(k);
+    lo = kKeyNegInf;
+    hi = k - 1u;
+  } else {
+    if (k == kKeyPosInf) return kNeverReached;
+    if (reaches(k + 1u, mn, t)) return hbits(k + 1u);
+    if (!reaches(kKeyPosInf, mn, t)) return kNeverReached;
+    lo = k + 1u;
+    hi = kKeyPosInf;
+  }
+  while (hi - lo > 1u) {
+    const uint32_t m = (lo + hi) >> 1;
+    if (reaches(m, mn, t)) hi = m; else lo = m;
+  }
+  return hbits(hi);
+}
+
+// The three code boundaries of two groups as half2 words (low half: group a, high half: group b).
+struct L3Cut {
+  uint32_t x1, x2, x3;
+};
+
+__device__ __forceinline__ L3Cut l3_cut(const Group& a, const Group& b) {
+  L3Cut c;
+  c.x1 = first_reaching(a.mn, a.t1) | (first_reaching(b.mn, b.t1) << 16);
+  c.x2 = first_reaching(a.mn, a.t2) | (first_reaching(b.mn, b.t2) << 16);
+  c.x3 = first_reaching(a.mn, a.t3) | (first_reaching(b.mn, b.t3) << 16);
+  return c;
+}
+
+__device__ __forceinline__ L3Cut l3_cut(const Group& g) {
+  L3Cut c;
+  c.x1 = first_reaching(g.mn, g.t1) * 0x10001u;
+  c.x2 = first_reaching(g.mn, g.t2) * 0x10001u;
+  c.x3 = first_reaching(g.mn, g.t3) * 0x10001u;
+  return c;
+}
+
+// Both elements of a word: the code masks by fp16 compare, then the reconstructions by bit select.
+__device__ __forceinline__ uint32_t l3_cut_word(uint32_t w, const L3Cut& c, uint32_t rr0,
+                                                uint32_t rr1, uint32_t rr2, uint32_t rr3) {
+  const __half2 x = as_h2(w);
+  const uint32_t m1 = __hge2_mask(x, as_h2(c.x1));
+  const uint32_t m2 = __hge2_mask(x, as_h2(c.x2));
+  const uint32_t m3 = __hge2_mask(x, as_h2(c.x3));
+  uint32_t r = (rr0 & ~m1) | (rr1 & m1);
+  r = (r & ~m2) | (rr2 & m2);
+  return (r & ~m3) | (rr3 & m3);
 }
 
 // A value group of NV 16-byte vectors (8 * NV channels): load, fp16 min/max tree, the 2-bit
@@ -308,12 +362,13 @@ __device__ __forceinline__ void l3_value_group(uint4* pv, float levels, float ep
   const uint32_t r2 = recon_bits(gr, 2.f), r3 = recon_bits(gr, 3.f);
   const uint32_t rr0 = r0 | (r0 << 16), rr1 = r1 | (r1 << 16);
   const uint32_t rr2 = r2 | (r2 << 16), rr3 = r3 | (r3 << 16);
+  const L3Cut cut = l3_cut(gr);
 #pragma unroll
   for (int k = 0; k < NV; ++k)
-    pv[k] = make_uint4(l3_word(v[k].x, gr, gr, rr0, rr1, rr2, rr3),
-                       l3_word(v[k].y, gr, gr, rr0, rr1, rr2, rr3),
-                       l3_word(v[k].z, gr, gr, rr0, rr1, rr2, rr3),
-                       l3_word(v[k].w, gr, gr, rr0, rr1, rr2, rr3));
+    pv[k] = make_uint4(l3_cut_word(v[k].x, cut, rr0, rr1, rr2, rr3),
+                       l3_cut_word(v[k].y, cut, rr0, rr1, rr2, rr3),
+                       l3_cut_word(v[k].z, cut, rr0, rr1, rr2, rr3),
+                       l3_cut_word(v[k].w, cut, rr0, rr1, rr2, rr3));
 }
 
 // Built for 4 blocks per SM (64 registers, 8 bytes spilled): 32 warps per SM keep
@@ -363,15 +418,11 @@ __global__ void __launch_bounds__(kThreads, 4) kivi_l3_kernel(const KiviArgs a, 
     const uint32_t rr1 = recon_bits(g0, 1.f) | (recon_bits(g1, 1.f) << 16);
     const uint32_t rr2 = recon_bits(g0, 2.f) | (recon_bits(g1, 2.f) << 16);
     const uint32_t rr3 = recon_bits(g0, 3.f) | (recon_bits(g1, 3.f) << 16);
+    const L3Cut cut = l3_cut(g0, g1);
 #pragma unroll
     for (int r = 0; r < kKeepRows; ++r) {
       if (r >= n) break;
-      const uint32_t w = keep[r];
-      const uint32_t lo = l3_select(h2f(static_cast<uint16_t>(w & 0xffffu)), g0, rr0 & 0xffffu,
-                                    rr1 & 0xffffu, rr2 & 0xffffu, rr3 & 0xffffu);
-      const uint32_t hi = l3_select(h2f(static_cast<uint16_t>(w >> 16)), g1, rr0 >> 16, rr1 >> 16,
-                                    rr2 >> 16, rr3 >> 16);
-      base[r * stride_w] = lo | (hi << 16);
+      base[r * stride_w] = l3_cut_word(keep[r], cut, rr0, rr1, rr2, rr3);
     }
   } else {
     // ---------------------------------------------------------------- values
@@ -420,13 +471,14 @@ __global__ void __launch_bounds__(kThreads, 4) kivi_l3_kernel(const KiviArgs a, 
     const uint32_t c2r = recon_bits(gr, 2.f), c3r = recon_bits(gr, 3.f);
     const uint32_t rr0 = c0r | (c0r << 16), rr1 = c1r | (c1r << 16);
     const uint32_t rr2 = c2r | (c2r << 16), rr3 = c3r | (c3r << 16);
+    const L3Cut cut = l3_cut(gr);
 #pragma unroll
     for (int k = 0; k < kMaxVecs; ++k) {
       if (k >= nv) break;
-      pv[k] = make_uint4(l3_word(v[k].x, gr, gr, rr0, rr1, rr2, rr3),
-                         l3_word(v[k].y, gr, gr, rr0, rr1, rr2, rr3),
-                         l3_word(v[k].z, gr, gr, rr0, rr1, rr2, rr3),
-                         l3_word(v[k].w, gr, gr, rr0, rr1, rr2, rr3));
+      pv[k] = make_uint4(l3_cut_word(v[k].x, cut, rr0, rr1, rr2, rr3),
+                         l3_cut_word(v[k].y, cut, rr0, rr1, rr2, rr3),
+                         l3_cut_word(v[k].z, cut, rr0, rr1, rr2, rr3),
+                         l3_cut_word(v[k].w, cut, rr0, rr1, rr2, rr3));
     }
   }
 }
