@@ -32,6 +32,7 @@
 #include "kvq_device.cuh"
 #include "kvq_divu32.cuh"
 #include "kvq_internal.h"
+#include "kvq_kivi_cut.cuh"
 
 namespace kvq {
 namespace {
@@ -264,81 +265,11 @@ __device__ __forceinline__ uint32_t recon_bits(const Group& g, float c) {
   return f2h(__fadd_rn(__fmul_rn(c, g.sc), g.mn));
 }
 
-// ---- the same selects as fp16 compares.  d(x) = RN(x - gmin) is nondecreasing in x, so for
-// each code k the elements with d(x) >= t_k are exactly those with x >= X_k, X_k the smallest fp16
-// value that reaches t_k.  Finding X_k costs a few float evaluations per group; each element then
-// costs one packed fp16 compare per code (HSET2 on two elements) and one bit select, in place of
-// two conversions, two subtractions and six float compares and selects per word.
-//
-// Order keys: non-NaN fp16 bit patterns mapped monotonically onto 0x03ff (-inf) .. 0xfc00 (+inf),
-// -0 just below +0.
-constexpr uint32_t kKeyNegInf = 0x03ffu, kKeyPosInf = 0xfc00u;
-constexpr uint32_t kNeverReached = 0x7fffu;   // a NaN: no fp16 compare with it is true
-
-__device__ __forceinline__ uint32_t hkey(uint32_t b) { return b ^ ((b & 0x8000u) ? 0xffffu : 0x8000u); }
-__device__ __forceinline__ uint32_t hbits(uint32_t k) { return k ^ ((k & 0x8000u) ? 0x8000u : 0xffffu); }
-
-__device__ __forceinline__ bool reaches(uint32_t k, float mn, float t) {
-  return __fsub_rn(h2f(static_cast<uint16_t>(hbits(k))), mn) >= t;
-}
-
-// fp16 bits of the smallest non-NaN fp16 X with RN(X - mn) >= t, or kNeverReached.  The guess
-// fp16(mn + t) is almost always the answer or its neighbour; otherwise a bisection over the order
-// keys, whose bracket keeps !reaches(lo) and reaches(hi) (-inf never reaches a t > -inf).
-__device__ __forceinline__ uint32_t first_reaching(float mn, float t) {
-  uint32_t k = hkey(f2h(__fadd_rn(mn, t)));
-  k = min(max(k, kKeyNegInf + 1u), kKeyPosInf);
-  uint32_t lo, hi;
-  if (reaches(k, mn, t)) {
-    if (!reaches(k - 1u, mn, t)) return hbits(k);
-    lo = kKeyNegInf;
-    hi = k - 1u;
-  } else {
-    if (k == kKeyPosInf) return kNeverReached;
-    if (reaches(k + 1u, mn, t)) return hbits(k + 1u);
-    if (!reaches(kKeyPosInf, mn, t)) return kNeverReached;
-    lo = k + 1u;
-    hi = kKeyPosInf;
-  }
-  while (hi - lo > 1u) {
-    const uint32_t m = (lo + hi) >> 1;
-    if (reaches(m, mn, t)) hi = m; else lo = m;
-  }
-  return hbits(hi);
-}
-
-// The three code boundaries of two groups as half2 words (low half: group a, high half: group b).
-struct L3Cut {
-  uint32_t x1, x2, x3;
-};
-
 __device__ __forceinline__ L3Cut l3_cut(const Group& a, const Group& b) {
-  L3Cut c;
-  c.x1 = first_reaching(a.mn, a.t1) | (first_reaching(b.mn, b.t1) << 16);
-  c.x2 = first_reaching(a.mn, a.t2) | (first_reaching(b.mn, b.t2) << 16);
-  c.x3 = first_reaching(a.mn, a.t3) | (first_reaching(b.mn, b.t3) << 16);
-  return c;
+  return l3_cut2(a.mn, a.t1, a.t2, a.t3, b.mn, b.t1, b.t2, b.t3);
 }
 
-__device__ __forceinline__ L3Cut l3_cut(const Group& g) {
-  L3Cut c;
-  c.x1 = first_reaching(g.mn, g.t1) * 0x10001u;
-  c.x2 = first_reaching(g.mn, g.t2) * 0x10001u;
-  c.x3 = first_reaching(g.mn, g.t3) * 0x10001u;
-  return c;
-}
-
-// Both elements of a word: the code masks by fp16 compare, then the reconstructions by bit select.
-__device__ __forceinline__ uint32_t l3_cut_word(uint32_t w, const L3Cut& c, uint32_t rr0,
-                                                uint32_t rr1, uint32_t rr2, uint32_t rr3) {
-  const __half2 x = as_h2(w);
-  const uint32_t m1 = __hge2_mask(x, as_h2(c.x1));
-  const uint32_t m2 = __hge2_mask(x, as_h2(c.x2));
-  const uint32_t m3 = __hge2_mask(x, as_h2(c.x3));
-  uint32_t r = (rr0 & ~m1) | (rr1 & m1);
-  r = (r & ~m2) | (rr2 & m2);
-  return (r & ~m3) | (rr3 & m3);
-}
+__device__ __forceinline__ L3Cut l3_cut(const Group& g) { return l3_cut1(g.mn, g.t1, g.t2, g.t3); }
 
 // A value group of NV 16-byte vectors (8 * NV channels): load, fp16 min/max tree, the 2-bit
 // round trip, store.

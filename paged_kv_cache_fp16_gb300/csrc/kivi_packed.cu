@@ -9,10 +9,12 @@
 //   codes LSB-first along the head dimension of each token row.
 // Reconstruction for attention is one fp16 fused multiply-add c * scale + zero per element.
 //
-// kivi_pack: keys -- one thread per (layer, b, h, token group, 8-channel chunk): pass 1 reduces
-// min/max over the group's tokens (fp16, exact), pass 2 re-reads the rows (cache hits), divides
-// by the stored scale and writes one code word per row; values -- one thread per (layer, b, h,
-// token, channel group) holding the group in registers.
+// kivi_pack: keys at head_dim 64 -- one warp per (layer, b, h, token group), each lane holding an
+// 8-channel chunk of a quarter of the group's rows, min/max by shuffles; other head dims -- one
+// thread per (layer, b, h, token group, 8-channel chunk), re-reading the rows (cache hits);
+// values -- one thread per (layer, b, h, token, channel group) holding the group in registers.
+// 2-bit codes come from fp16 compares against each group's code boundaries (kvq_kivi_cut.cuh);
+// wider codes divide by the stored scale.
 //
 // kivi_decode_attn (head_dim 64): one CTA per (split, KV head, layer * batch); 4 warps, 16-token
 // tiles; S^T = K_hat . Q^T and O^T += V_hat^T . P^T on mma.sync m16n8k16 as in the q8/q6/q4
@@ -29,6 +31,7 @@
 #include "kvq_device.cuh"
 #include "kvq_divu32.cuh"
 #include "kvq_internal.h"
+#include "kvq_kivi_cut.cuh"
 #include "kvq_math.cuh"
 #include "kvq_warp.cuh"
 
@@ -99,10 +102,9 @@ __device__ __forceinline__ void set_thresholds3(GP& g) {
   g.t3 = __fmaf_ru(g.s, 2.5f, g.s * 1.1920928955078125e-07f);       // s (2.5 + 2^-23)
 }
 
-__device__ __forceinline__ uint32_t field3(float x, const GP& g) {
-  const float d = __fsub_rn(x, g.z);
-  return static_cast<uint32_t>(d >= g.t1) + static_cast<uint32_t>(d >= g.t2) +
-         static_cast<uint32_t>(d >= g.t3);
+// The code boundaries of two groups' 2-bit fields (fp16 compares replace three float compares).
+__device__ __forceinline__ L3Cut gp_cut(const GP& a, const GP& b) {
+  return l3_cut2(a.z, a.t1, a.t2, a.t3, b.z, b.t1, b.t2, b.t3);
 }
 
 // 8 fields of `bits` bits -> packed LSB-first (2 bits: 16 bits, 4 bits: 32 bits, 8: 64 bits).
@@ -194,14 +196,25 @@ __device__ void pack_keys_part(const KPArgs& a, int64_t first, int64_t stride) {
     *reinterpret_cast<uint4*>(C.k_scale + prow) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
     *reinterpret_cast<uint4*>(C.k_zero + prow) = make_uint4(zw[0], zw[1], zw[2], zw[3]);
     uint8_t* dst = C.k_codes + (bh * S + t0) * cb + ch * BITS;     // 8 fields = BITS bytes
-    for (int t = 0; t < gs; ++t) {
-      float x[8];
-      f8(src[static_cast<int64_t>(t) * row_v], x);
-      uint32_t f[8];
+    if constexpr (BITS == 2) {
+      L3Cut cut[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        f[e] = BITS == 2 ? field3(x[e], gp[e]) : field(x[e], gp[e], a.levels);
-      store_fields8<BITS>(dst + static_cast<int64_t>(t) * cb, f);
+      for (int k = 0; k < 4; ++k) cut[k] = gp_cut(gp[2 * k], gp[2 * k + 1]);
+      for (int t = 0; t < gs; ++t) {
+        const uint4 v = src[static_cast<int64_t>(t) * row_v];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        *reinterpret_cast<uint16_t*>(dst + static_cast<int64_t>(t) * cb) =
+            static_cast<uint16_t>(l3_codes8<4>(w, cut));
+      }
+    } else {
+      for (int t = 0; t < gs; ++t) {
+        float x[8];
+        f8(src[static_cast<int64_t>(t) * row_v], x);
+        uint32_t f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = field(x[e], gp[e], a.levels);
+        store_fields8<BITS>(dst + static_cast<int64_t>(t) * cb, f);
+      }
     }
   }
 }
@@ -252,36 +265,58 @@ __device__ void pack_keys_d64(const KPArgs& a, int64_t first, int64_t stride) {
         mx[k] = h2u(__hmax2(as_h2(mx[k]), as_h2(__shfl_xor_sync(kFullMask, mx[k], o))));
       }
     }
-    GP gp[8];
+    // The four lanes of a chunk share its 8 channels' groups: lane tq derives the scales (and,
+    // for 2 bits, the code boundaries) of channels 2 tq, 2 tq + 1 and the chunk's lanes exchange
+    // them by shuffles.
+    const uint32_t mn_w = tq == 0 ? mn[0] : tq == 1 ? mn[1] : tq == 2 ? mn[2] : mn[3];
+    const uint32_t mx_w = tq == 0 ? mx[0] : tq == 1 ? mx[1] : tq == 2 ? mx[2] : mx[3];
+    const float z0 = __low2float(as_h2(mn_w)), z1 = __high2float(as_h2(mn_w));
+    const uint16_t s0 = scale16(z0, __low2float(as_h2(mx_w)), a.levels, a.eps);
+    const uint16_t s1 = scale16(z1, __high2float(as_h2(mx_w)), a.levels, a.eps);
     uint32_t sw[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float z0 = __low2float(as_h2(mn[k])), z1 = __high2float(as_h2(mn[k]));
-      const uint16_t s0 = scale16(z0, __low2float(as_h2(mx[k])), a.levels, a.eps);
-      const uint16_t s1 = scale16(z1, __high2float(as_h2(mx[k])), a.levels, a.eps);
-      gp[2 * k] = make_gp(z0, s0);
-      gp[2 * k + 1] = make_gp(z1, s1);
-      if constexpr (BITS == 2) {
-        set_thresholds3(gp[2 * k]);
-        set_thresholds3(gp[2 * k + 1]);
-      }
-      sw[k] = s0 | (static_cast<uint32_t>(s1) << 16);
-    }
+    for (int k = 0; k < 4; ++k)
+      sw[k] = __shfl_sync(kFullMask, s0 | (static_cast<uint32_t>(s1) << 16), k * 8 + ch);
     if (tq == 0) {
       const int64_t prow = (bh * (S / GS) + t0 / GS) * kD64 + ch * 8;   // params [B][H][S/gs][D]
       *reinterpret_cast<uint4*>(C.k_scale + prow) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
       *reinterpret_cast<uint4*>(C.k_zero + prow) = make_uint4(mn[0], mn[1], mn[2], mn[3]);
     }
     uint8_t* dst = C.k_codes + (bh * S + t0 + tq * kQ) * kCb + ch * BITS;   // 8 fields = BITS bytes
+    if constexpr (BITS == 2) {
+      GP g0 = make_gp(z0, s0), g1 = make_gp(z1, s1);
+      set_thresholds3(g0);
+      set_thresholds3(g1);
+      const L3Cut mine = gp_cut(g0, g1);
+      L3Cut cut[4];
 #pragma unroll
-    for (int i = 0; i < kQ; ++i) {
-      float xf[8];
-      f8(x[i], xf);
-      uint32_t f[8];
+      for (int k = 0; k < 4; ++k) {
+        cut[k].x1 = __shfl_sync(kFullMask, mine.x1, k * 8 + ch);
+        cut[k].x2 = __shfl_sync(kFullMask, mine.x2, k * 8 + ch);
+        cut[k].x3 = __shfl_sync(kFullMask, mine.x3, k * 8 + ch);
+      }
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        f[e] = BITS == 2 ? field3(xf[e], gp[e]) : field(xf[e], gp[e], a.levels);
-      store_fields8<BITS>(dst + static_cast<int64_t>(i) * kCb, f);
+      for (int i = 0; i < kQ; ++i) {
+        const uint32_t w[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+        *reinterpret_cast<uint16_t*>(dst + static_cast<int64_t>(i) * kCb) =
+            static_cast<uint16_t>(l3_codes8<4>(w, cut));
+      }
+    } else {
+      GP gp[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        gp[2 * k] = make_gp(__low2float(as_h2(mn[k])), static_cast<uint16_t>(sw[k] & 0xffffu));
+        gp[2 * k + 1] = make_gp(__high2float(as_h2(mn[k])), static_cast<uint16_t>(sw[k] >> 16));
+      }
+#pragma unroll
+      for (int i = 0; i < kQ; ++i) {
+        float xf[8];
+        f8(x[i], xf);
+        uint32_t f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = field(xf[e], gp[e], a.levels);
+        store_fields8<BITS>(dst + static_cast<int64_t>(i) * kCb, f);
+      }
     }
   };
   if (a.fast32) {   // running (layer, offset); offset / n_groups by multiply-high
@@ -342,16 +377,25 @@ __device__ void pack_values_part(const KPArgs& a, int64_t first, int64_t stride)
     C.v_scale[pidx] = sb;
     C.v_zero[pidx] = f2h(z);
     uint8_t* dst = C.v_codes + (bh * S + t) * cb + g * gs * BITS / 8;
+    if constexpr (BITS == 2) {
+      const L3Cut cut = l3_cut1(gp.z, gp.t1, gp.t2, gp.t3);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (k >= nv) continue;
-      float x[8];
-      f8(vv[k], x);
-      uint32_t f[8];
+      for (int k = 0; k < 8; ++k) {
+        if (k >= nv) continue;
+        const uint32_t w[4] = {vv[k].x, vv[k].y, vv[k].z, vv[k].w};
+        *reinterpret_cast<uint16_t*>(dst + k * BITS) = static_cast<uint16_t>(l3_codes8<1>(w, &cut));
+      }
+    } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        f[e] = BITS == 2 ? field3(x[e], gp) : field(x[e], gp, a.levels);
-      store_fields8<BITS>(dst + k * BITS, f);
+      for (int k = 0; k < 8; ++k) {
+        if (k >= nv) continue;
+        float x[8];
+        f8(vv[k], x);
+        uint32_t f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = field(x[e], gp, a.levels);
+        store_fields8<BITS>(dst + k * BITS, f);
+      }
     }
   };
   if (a.fast32) {   // running (layer, offset); offset / G and / span by multiply-high
