@@ -344,76 +344,103 @@ __device__ void pack_keys_d64(const KPArgs& a, int64_t first, int64_t stride) {
   }
 }
 
-template <int BITS>
+// One value item -- (layer, batch row * H + head, token, channel group) -- whose NV 16-byte
+// vectors (the group's 8 NV channels) are already in registers: min / max, parameters, codes.
+template <int BITS, int NV>
+__device__ __forceinline__ void value_group(const KPArgs& a, int layer, int64_t bh, int t, int g,
+                                            const uint4 (&vv)[NV]) {
+  const kivi_packed& C = a.c[layer];
+  const int S = C.capacity, D = C.head_dim, G = D / (8 * NV), cb = D * BITS / 8;
+  __half2 mn = as_h2(vv[0].x), mx = mn;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const uint32_t w[4] = {vv[k].x, vv[k].y, vv[k].z, vv[k].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) { mn = __hmin2(mn, as_h2(w[j])); mx = __hmax2(mx, as_h2(w[j])); }
+  }
+  const float z = fminf(__low2float(mn), __high2float(mn));
+  const uint16_t sb = scale16(z, fmaxf(__low2float(mx), __high2float(mx)), a.levels, a.eps);
+  GP gp = make_gp(z, sb);
+  if constexpr (BITS == 2) set_thresholds3(gp);
+  const int64_t pidx = (bh * S + t) * G + g;                      // params [B][H][S][G]
+  C.v_scale[pidx] = sb;
+  C.v_zero[pidx] = f2h(z);
+  uint8_t* dst = C.v_codes + (bh * S + t) * cb + g * NV * BITS;
+  if constexpr (BITS == 2) {
+    const L3Cut cut = l3_cut1(gp.z, gp.t1, gp.t2, gp.t3);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const uint32_t w[4] = {vv[k].x, vv[k].y, vv[k].z, vv[k].w};
+      *reinterpret_cast<uint16_t*>(dst + k * BITS) = static_cast<uint16_t>(l3_codes8<1>(w, &cut));
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      float x[8];
+      f8(vv[k], x);
+      uint32_t f[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = field(x[e], gp, a.levels);
+      store_fields8<BITS>(dst + k * BITS, f);
+    }
+  }
+}
+
+// Values: one thread per item, groups of 8 NV channels.  The running loop loads the next item's
+// vectors before it codes the current one, so every thread keeps a load in flight while it
+// computes.
+template <int BITS, int NV>
 __device__ void pack_values_part(const KPArgs& a, int64_t first, int64_t stride) {
   const kivi_packed& c0 = a.c[0];
-  const int B = c0.batch, H = c0.num_heads, S = c0.capacity, D = c0.head_dim, gs = c0.group_size;
-  const int G = D / gs, nv = gs / 8;
+  const int B = c0.batch, H = c0.num_heads, S = c0.capacity, D = c0.head_dim;
+  const int G = D / (8 * NV);
   const int span = a.hi - a.lo;
   const int64_t per_layer = static_cast<int64_t>(B) * H * span * G;
   const int64_t items = per_layer * a.n_layers;
-  const int cb = D * BITS / 8;
-  // one item: (layer, batch row * H + head, token, channel group)
-  auto item = [&](int layer, int64_t bh, int t, int g) {
-    const kivi_packed& C = a.c[layer];
-    const uint4* src = reinterpret_cast<const uint4*>(a.v[layer] + (bh * S + t) * D + g * gs);
-    uint4 vv[8];
-    __half2 mn = __halves2half2(__ushort_as_half(0x7c00), __ushort_as_half(0x7c00));
-    __half2 mx = __halves2half2(__ushort_as_half(0xfc00), __ushort_as_half(0xfc00));
+  auto load = [&](int layer, int64_t bh, int t, int g, uint4 (&vv)[NV]) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.v[layer] + (bh * S + t) * D) + g * NV;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (k < nv) {
-        vv[k] = src[k];
-        const uint32_t w[4] = {vv[k].x, vv[k].y, vv[k].z, vv[k].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) { mn = __hmin2(mn, as_h2(w[j])); mx = __hmax2(mx, as_h2(w[j])); }
-      }
-    }
-    const float z = fminf(__low2float(mn), __high2float(mn));
-    const uint16_t sb = scale16(z, fmaxf(__low2float(mx), __high2float(mx)), a.levels, a.eps);
-    GP gp = make_gp(z, sb);
-    if constexpr (BITS == 2) set_thresholds3(gp);
-    const int64_t pidx = (bh * S + t) * G + g;                      // params [B][H][S][G]
-    C.v_scale[pidx] = sb;
-    C.v_zero[pidx] = f2h(z);
-    uint8_t* dst = C.v_codes + (bh * S + t) * cb + g * gs * BITS / 8;
-    if constexpr (BITS == 2) {
-      const L3Cut cut = l3_cut1(gp.z, gp.t1, gp.t2, gp.t3);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (k >= nv) continue;
-        const uint32_t w[4] = {vv[k].x, vv[k].y, vv[k].z, vv[k].w};
-        *reinterpret_cast<uint16_t*>(dst + k * BITS) = static_cast<uint16_t>(l3_codes8<1>(w, &cut));
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (k >= nv) continue;
-        float x[8];
-        f8(vv[k], x);
-        uint32_t f[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = field(x[e], gp, a.levels);
-        store_fields8<BITS>(dst + k * BITS, f);
-      }
-    }
+    for (int k = 0; k < NV; ++k) vv[k] = src[k];
   };
   if (a.fast32) {   // running (layer, offset); offset / G and / span by multiply-high
+    if (first >= items) return;
     const uint32_t pl = static_cast<uint32_t>(per_layer);
     int layer = static_cast<int>(first / per_layer);
     uint32_t r = static_cast<uint32_t>(first - layer * per_layer);
     const int dl = static_cast<int>(stride / per_layer);
     const uint32_t dr = static_cast<uint32_t>(stride - dl * per_layer);
-    for (int64_t it = first; it < items; it += stride) {
-      const uint32_t q = divu32(r, a.div_g);          // token row of the layer
-      const uint32_t bh = divu32(q, a.div_span);
-      item(layer, bh, a.lo + static_cast<int>(q - bh * span), static_cast<int>(r - q * G));
+    // position of the running item: (layer, bh, t, g)
+    int cl = layer, ct, cg;
+    uint32_t cbh;
+    auto place = [&](uint32_t rr, uint32_t& bh, int& t, int& g) {
+      const uint32_t q = divu32(rr, a.div_g);          // token row of the layer
+      bh = divu32(q, a.div_span);
+      t = a.lo + static_cast<int>(q - bh * span);
+      g = static_cast<int>(rr - q * G);
+    };
+    place(r, cbh, ct, cg);
+    uint4 cur[NV];
+    load(cl, cbh, ct, cg, cur);
+    for (int64_t it = first;; it += stride) {
       r += dr;
       layer += dl;
       if (r >= pl) {
         r -= pl;
         ++layer;
       }
+      const bool more = it + stride < items;
+      int nl = layer, nt = 0, ng = 0;
+      uint32_t nbh = 0;
+      uint4 nxt[NV];
+      if (more) {
+        place(r, nbh, nt, ng);
+        load(nl, nbh, nt, ng, nxt);
+      }
+      value_group<BITS, NV>(a, cl, cbh, ct, cg, cur);
+      if (!more) break;
+      cl = nl; cbh = nbh; ct = nt; cg = ng;
+#pragma unroll
+      for (int k = 0; k < NV; ++k) cur[k] = nxt[k];
     }
   } else {
     for (int64_t it = first; it < items; it += stride) {
@@ -422,15 +449,21 @@ __device__ void pack_values_part(const KPArgs& a, int64_t first, int64_t stride)
       const int g = static_cast<int>(r % G);
       r /= G;
       const int64_t bh = r / span;
-      item(layer, bh, a.lo + static_cast<int>(r - bh * span), g);
+      const int t = a.lo + static_cast<int>(r - bh * span);
+      uint4 vv[NV];
+      load(layer, bh, t, g, vv);
+      value_group<BITS, NV>(a, layer, bh, t, g, vv);
     }
   }
 }
 
 // Keys and values in two launches, each with its own register allocation (the head_dim-64 key
-// path holds a token quarter of its group in registers; the value path needs far fewer).
+// path holds a token quarter of its group in registers; the value path needs far fewer).  The
+// head_dim-64 key kernel for groups of up to 32 tokens is built for 4 blocks per SM (64
+// registers, 20 bytes spilled): 16-layer 2-bit pack 0.501 -> 0.494 ms against 3 blocks at 72.
 template <int BITS, int GS>
-__global__ void __launch_bounds__(kThreads) kivi_pack_keys_kernel(const KPArgs a) {
+__global__ void __launch_bounds__(kThreads, (GS > 0 && GS <= 32) ? 4 : 1)
+    kivi_pack_keys_kernel(const KPArgs a) {
   if constexpr (GS > 0)   // head_dim 64: a warp per token group
     pack_keys_d64<BITS, GS>(a, (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5,
                             static_cast<int64_t>(gridDim.x) * (kThreads / 32));
@@ -439,10 +472,10 @@ __global__ void __launch_bounds__(kThreads) kivi_pack_keys_kernel(const KPArgs a
                          static_cast<int64_t>(gridDim.x) * kThreads);
 }
 
-template <int BITS>
+template <int BITS, int NV>
 __global__ void __launch_bounds__(kThreads) kivi_pack_values_kernel(const KPArgs a) {
-  pack_values_part<BITS>(a, static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x,
-                         static_cast<int64_t>(gridDim.x) * kThreads);
+  pack_values_part<BITS, NV>(a, static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x,
+                             static_cast<int64_t>(gridDim.x) * kThreads);
 }
 
 // ================================================================================================
@@ -894,16 +927,51 @@ kvq_status check_caches(const kivi_packed* c, int n, const char* fn) {
 
 namespace kvq {
 namespace {
-template <int BITS>
-void launch_pack(const KPArgs& a, int gs, int key_blocks, int value_blocks, cudaStream_t cs) {
-  switch (gs) {   // 0: any head_dim (a thread per key chunk); else head_dim 64, group gs
-    case 8: kivi_pack_keys_kernel<BITS, 8><<<key_blocks, kThreads, 0, cs>>>(a); break;
-    case 16: kivi_pack_keys_kernel<BITS, 16><<<key_blocks, kThreads, 0, cs>>>(a); break;
-    case 32: kivi_pack_keys_kernel<BITS, 32><<<key_blocks, kThreads, 0, cs>>>(a); break;
-    case 64: kivi_pack_keys_kernel<BITS, 64><<<key_blocks, kThreads, 0, cs>>>(a); break;
-    default: kivi_pack_keys_kernel<BITS, 0><<<key_blocks, kThreads, 0, cs>>>(a); break;
+// At most the blocks resident on the SMs at once (the kernels loop over their items), so no block
+// waits for a second wave; `cache` holds the kernel's resident blocks per SM.
+template <typename K>
+int resident_grid(K kernel, int& cache, int64_t threads) {
+  if (cache == 0) {
+    int b = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0);
+    cache = (e != cudaSuccess || b < 1) ? 1 : b;
   }
-  kivi_pack_values_kernel<BITS><<<value_blocks, kThreads, 0, cs>>>(a);
+  const int sms = sm_count() > 0 ? sm_count() : 152;
+  const int64_t need = (threads + kThreads - 1) / kThreads;
+  const int64_t cap = static_cast<int64_t>(sms) * cache;
+  return static_cast<int>(need > cap ? cap : (need < 1 ? 1 : need));
+}
+
+template <int BITS, int GS>
+void launch_keys(const KPArgs& a, int64_t threads, cudaStream_t cs) {
+  static int cache = 0;
+  const int grid = resident_grid(kivi_pack_keys_kernel<BITS, GS>, cache, threads);
+  kivi_pack_keys_kernel<BITS, GS><<<grid, kThreads, 0, cs>>>(a);
+}
+
+template <int BITS, int NV>
+void launch_values(const KPArgs& a, int64_t threads, cudaStream_t cs) {
+  static int cache = 0;
+  const int grid = resident_grid(kivi_pack_values_kernel<BITS, NV>, cache, threads);
+  kivi_pack_values_kernel<BITS, NV><<<grid, kThreads, 0, cs>>>(a);
+}
+
+template <int BITS>
+void launch_pack(const KPArgs& a, int key_gs, int gs, int64_t key_threads, int64_t value_threads,
+                 cudaStream_t cs) {
+  switch (key_gs) {   // 0: any head_dim (a thread per key chunk); else head_dim 64, group gs
+    case 8: launch_keys<BITS, 8>(a, key_threads, cs); break;
+    case 16: launch_keys<BITS, 16>(a, key_threads, cs); break;
+    case 32: launch_keys<BITS, 32>(a, key_threads, cs); break;
+    case 64: launch_keys<BITS, 64>(a, key_threads, cs); break;
+    default: launch_keys<BITS, 0>(a, key_threads, cs); break;
+  }
+  switch (gs) {   // value groups of gs channels: gs / 8 vectors
+    case 8: launch_values<BITS, 1>(a, value_threads, cs); break;
+    case 16: launch_values<BITS, 2>(a, value_threads, cs); break;
+    case 32: launch_values<BITS, 4>(a, value_threads, cs); break;
+    default: launch_values<BITS, 8>(a, value_threads, cs); break;
+  }
 }
 }  // namespace
 }  // namespace kvq
@@ -946,25 +1014,18 @@ extern "C" kvq_status kivi_pack(const kivi_packed* caches, const uint16_t* const
     a.div_span = make_divu32(static_cast<uint32_t>(span));
     a.div_ngroups = make_divu32(static_cast<uint32_t>(span / c0.group_size));
   }
-  const int sms = sm_count() > 0 ? sm_count() : 152;
   // keys: a thread per (group, 8-channel chunk), or at head_dim 64 a warp per group
   const bool d64 = c0.head_dim == 64;
   const int64_t kitems = static_cast<int64_t>(n_layers) * c0.batch * c0.num_heads *
                          ((hi - lo) / c0.group_size) * (d64 ? 32 : c0.head_dim / 8);
   const int64_t vitems = static_cast<int64_t>(n_layers) * c0.batch * c0.num_heads * (hi - lo) *
                          (c0.head_dim / c0.group_size);
-  auto blocks = [&](int64_t items) {
-    int64_t b = (items + kThreads - 1) / kThreads;
-    const int64_t cap = static_cast<int64_t>(sms) * 4;
-    return static_cast<int>(b > cap ? cap : (b < 1 ? 1 : b));
-  };
-  const int key_blocks = blocks(kitems);
-  const int value_blocks = blocks(vitems);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int kgs = d64 ? c0.group_size : 0;
   switch (c0.bits) {
-    case 2: launch_pack<2>(a, d64 ? c0.group_size : 0, key_blocks, value_blocks, cs); break;
-    case 4: launch_pack<4>(a, d64 ? c0.group_size : 0, key_blocks, value_blocks, cs); break;
-    default: launch_pack<8>(a, d64 ? c0.group_size : 0, key_blocks, value_blocks, cs); break;
+    case 2: launch_pack<2>(a, kgs, c0.group_size, kitems, vitems, cs); break;
+    case 4: launch_pack<4>(a, kgs, c0.group_size, kitems, vitems, cs); break;
+    default: launch_pack<8>(a, kgs, c0.group_size, kitems, vitems, cs); break;
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "%s launch: %s", fn, cudaGetErrorString(e));
