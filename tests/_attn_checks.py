@@ -18,6 +18,8 @@ These helpers build inputs and compare outputs; they hold none of the method's a
 """
 from __future__ import annotations
 
+import json
+import os
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -35,8 +37,10 @@ def attn_report(got: np.ndarray, ref: np.ndarray) -> dict:
     bad = err > ATOL + RTOL * np.abs(ref)
     rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
     mx = float(err.max()) if err.size else 0.0
+    tol_frac = float((err / (ATOL + RTOL * np.abs(ref))).max()) if err.size else 0.0
     return {"n_bad": int(bad.sum()), "max_abs_err": mx,
             "max_err_over_rms_ref": (mx / rms) if rms > 0 else float("inf") if mx > 0 else 0.0,
+            "max_err_over_tol": tol_frac,
             "rms_ref": rms, "finite": bool(np.all(np.isfinite(got)))}
 
 
@@ -45,8 +49,19 @@ def attn_close(got, ref) -> bool:
     return r["n_bad"] == 0 and r["finite"]
 
 
+def _log_margin(r: dict, ctx: str) -> None:
+    """With KVQ_ATTN_MARGINS set to a file path, append this check's report to it (one JSON line
+    per check, with the running test's id) -- how close each parity check came to the tolerance."""
+    path = os.environ.get("KVQ_ATTN_MARGINS")
+    if path:
+        rec = dict(r, ctx=ctx, test=os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0])
+        with open(path, "a") as f:
+            f.write(json.dumps(rec) + "\n")
+
+
 def assert_attn_close(got, ref, ctx: str = "") -> dict:
     r = attn_report(got, ref)
+    _log_margin(r, ctx)
     assert r["finite"] and r["n_bad"] == 0, (
         f"{ctx}: {r['n_bad']} outside 2e-3 + 1e-3|ref|; max abs err {r['max_abs_err']:.3e}, "
         f"max err / rms(ref) {r['max_err_over_rms_ref']:.3e} (rms {r['rms_ref']:.3e})")

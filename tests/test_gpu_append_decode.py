@@ -14,7 +14,6 @@ from _gpu_util import cu_of, dev_tensor, i32
 
 pytestmark = pytest.mark.gpu
 
-ATOL, RTOL = 2e-3, 1e-3
 
 
 def _close(got, ref):

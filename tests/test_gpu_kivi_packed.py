@@ -11,7 +11,6 @@ from _attn_checks import PlantedKivi, assert_attn_close, kivi_needle_tokens, nee
 from _gpu_util import dev_tensor, u16
 
 pytestmark = pytest.mark.gpu
-ATOL, RTOL = 2e-3, 1e-3
 
 
 def _layer(seed, layer, B, H, S, D):

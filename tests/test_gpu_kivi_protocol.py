@@ -10,10 +10,10 @@ import torch
 import kvgen
 from oracle import kivi as K
 from oracle import kivi_packed as P
+from _attn_checks import assert_attn_close
 from _gpu_util import dev_tensor, u16
 
 pytestmark = pytest.mark.gpu
-ATOL, RTOL = 2e-3, 1e-3
 
 # (op, n): appends of various sizes (single tokens, chunks straddling group boundaries, a long
 # prefill) and trims that cut inside a group, at a group edge and below the frontier
@@ -118,8 +118,7 @@ def test_packed_protocol_and_attention(kvq, cuda_dev, bits, gs):
                 vp = (r.v_codes[:, :, :nq], r.v_scale[:, :, :nq], r.v_zero[:, :, :nq])
                 want = P.decode_attention(q[l], kp, vp, r.keys[:, :, nq:off], r.values[:, :, nq:off],
                                           2, gs, 0.125)
-                bad = np.abs(got[l] - want) > ATOL + RTOL * np.abs(want)
-                assert not bad.any(), float(np.abs(got[l] - want).max())
+                assert_attn_close(got[l], want, f"layer {l}")
 
 
 def test_unpack_reconstructs_the_oracle_rows(kvq, cuda_dev):

@@ -8,6 +8,7 @@ import torch
 import kvgen
 from oracle import side as osd
 from oracle import symmetric as osym
+from _attn_checks import assert_attn_close
 from _gpu_util import cu_of, dev_tensor, i32, u16
 
 pytestmark = pytest.mark.gpu
@@ -165,13 +166,10 @@ def test_full_size_prefill_sampled(kvq, cuda_dev):
 
 
 # ---------------------------------------------------------------- decode attention
-ATOL, RTOL = 2e-3, 1e-3
 
 
 def _close(got, ref):
-    bad = np.abs(got - ref) > ATOL + RTOL * np.abs(ref)
-    assert not bad.any(), (f"{int(bad.sum())} outside tol; max abs err "
-                           f"{float(np.abs(got - ref).max()):.3e}")
+    assert_attn_close(got, ref, "side-channel decode attention")
 
 
 @pytest.mark.parametrize("bits", [8, 6, 4])
