@@ -33,12 +33,13 @@ constexpr int kWarpsPerBlock = kThreads / 32;
 constexpr int kTok = 8;     // most tokens per warp work item (all heads of each)
 constexpr int kUnroll = 2;  // warp steps with loads in flight (quant-pack)
 // dequant: its loads are smaller than the quantizer's, so more warp steps stay in flight.  The
-// kernel is built for at least 3 blocks per SM (up to 85 registers).  q6 takes 6 steps (80
-// registers, 3 blocks): more bytes in flight per SM than 4 steps at 4 blocks (64 registers,
+// kernel is built for at least 3 blocks per SM (up to 85 registers), q4 for 4.  q6 takes 6 steps
+// (80 registers, 3 blocks): more bytes in flight per SM than 4 steps at 4 blocks (64 registers,
 // which also spilled), 4.09 -> 3.90 ms on the 16-layer workload (5 steps 3.94, 7 steps spill,
-// 4.16).  q4 keeps 4 steps (64 registers, 4 blocks; 6 steps at 3 blocks measured 0.6 % slower)
-// and q8 2 (its 16-byte units at 4 steps cost occupancy).
-template <int BITS> constexpr int dq_unroll() { return BITS == 8 ? 2 : (BITS == 6 ? 6 : 4); }
+// 4.16).  q4 takes 4 steps at 4 blocks (60 registers; 3.770 ms against 3.800 at 3 blocks, 5 and 6
+// steps 3.82 and 3.785), q8 4 steps at 3 blocks (74 registers; 4.44 ms against 4.54 with 2 steps
+// at 4 blocks, 4.50 with 3).
+template <int BITS> constexpr int dq_unroll() { return BITS == 6 ? 6 : 4; }
 
 struct PackArgs {
   const uint16_t* x[KVQ_MAX_TENSORS];  // quant: inputs; dequant: outputs (cast back)
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(kThreads) quant_pack_kernel(const PackArgs a) 
 }
 
 template <int BITS, int UPL>
-__global__ void __launch_bounds__(kThreads, 3) dequant_kernel(const PackArgs a) {
+__global__ void __launch_bounds__(kThreads, BITS == 4 ? 4 : 3) dequant_kernel(const PackArgs a) {
   constexpr int kDqU = dq_unroll<BITS>();
   const int t = blockIdx.y;
   uint16_t* __restrict__ out = const_cast<uint16_t*>(a.x[t]);
