@@ -31,7 +31,10 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarpsPerBlock = kThreads / 32;
 constexpr int kTok = 8;     // most tokens per warp work item (all heads of each)
-constexpr int kUnroll = 2;  // warp steps with loads in flight (quant-pack)
+// quant-pack: warp steps with loads in flight.  q8 takes 3 (80 registers, 3 blocks per SM): 4.30
+// -> 4.21 ms on the 16-layer workload; q6 and q4 keep 2 (64 registers, 4 blocks; 3 steps, or a
+// minimum of 3 or 4 blocks per SM declared in the launch bounds, measured 1-12 % slower there).
+template <int BITS> constexpr int qp_unroll() { return BITS == 8 ? 3 : 2; }
 // dequant: its loads are smaller than the quantizer's, so more warp steps stay in flight.  The
 // kernel is built for at least 3 blocks per SM (up to 85 registers), q4 for 4.  q6 takes 6 steps
 // (80 registers, 3 blocks): more bytes in flight per SM than 4 steps at 4 blocks (64 registers,
@@ -69,6 +72,7 @@ __device__ __forceinline__ long long shfl_ll(long long v, int src) {
 
 template <int BITS, int UPL>
 __global__ void __launch_bounds__(kThreads) quant_pack_kernel(const PackArgs a) {
+  constexpr int kUnroll = qp_unroll<BITS>();
   constexpr int kQm = SymQ<BITS>::kQmax;
   constexpr int kB = SymQ<BITS>::kBias;
   constexpr int kM = SymQ<BITS>::kMask;
