@@ -375,14 +375,22 @@ __device__ __forceinline__ void load_q_frags(const AttnArgs& a, int ls, int h, i
     }
 }
 
-// Merge the CTA's warps in shared memory and write the split's partial record.
+// Merge the CTA's warps in shared memory and write the split's partial record.  The warps' O^T
+// accumulators go to sm_o[warp][head][d] with the low five bits of d XOR-ed by sw(head, d) =
+// (d >> 5) | (head >> 1) << 3, a bijection within each 32-element block: the 32 lanes of a warp
+// store (head 2c or 2c + 1, d = 32 g + ...) for the 32 (g, c) pairs at once, which without the
+// swizzle all fall in one bank (a 32-way conflict per store; the merge had cost 3 % of the decode).
+__device__ __forceinline__ int merge_slot(int j, int d) {
+  return j * kD + (d ^ ((d >> 5) | ((j >> 1) << 3)));
+}
+
 __device__ __forceinline__ void cta_merge_write(const AttnArgs& a, float* sm, int ls, int h,
                                                 int split, int warp, int g, int c,
                                                 const float (&acc)[16][4], float m0, float m1,
                                                 float l0, float l1) {
   if (m0 == kMaxFloor) m0 = kNegInf;   // no valid token: an empty partial for the merges
   if (m1 == kMaxFloor) m1 = kNegInf;
-  float (*sm_o)[8][kD] = reinterpret_cast<float (*)[8][kD]>(sm);
+  float* sm_o = sm;                                              // [warp][8 * kD], swizzled
   float (*sm_m)[8] = reinterpret_cast<float (*)[8]>(sm + kWarps * 8 * kD);
   float (*sm_l)[8] = reinterpret_cast<float (*)[8]>(sm + kWarps * 8 * kD + kWarps * 8);
 #pragma unroll
@@ -394,33 +402,44 @@ __device__ __forceinline__ void cta_merge_write(const AttnArgs& a, float* sm, in
     sm_m[warp][2 * c] = m0; sm_m[warp][2 * c + 1] = m1;
     sm_l[warp][2 * c] = l0; sm_l[warp][2 * c + 1] = l1;
   }
+  float* wo = sm_o + warp * 8 * kD;
 #pragma unroll
   for (int mt = 0; mt < 16; ++mt) {
     const int gi = mt >> 2, k = mt & 3;
     const int d = 32 * g + 8 * gi + k;
-    sm_o[warp][2 * c][d] = acc[mt][0];
-    sm_o[warp][2 * c + 1][d] = acc[mt][1];
-    sm_o[warp][2 * c][d + 4] = acc[mt][2];
-    sm_o[warp][2 * c + 1][d + 4] = acc[mt][3];
+    wo[merge_slot(2 * c, d)] = acc[mt][0];
+    wo[merge_slot(2 * c + 1, d)] = acc[mt][1];
+    wo[merge_slot(2 * c, d + 4)] = acc[mt][2];
+    wo[merge_slot(2 * c + 1, d + 4)] = acc[mt][3];
   }
   __syncthreads();
   float* rec = a.ws + ((static_cast<int64_t>(ls) * a.H + h) * a.n_splits + split) * 8 * kRec;
+  // a thread's elements move through the heads in order: the warps' weights exp2(m_w - M) of
+  // a head are computed once, when its first element comes up
+  int jc = -1;
+  float f[kWarps], M = kNegInf;
   for (int i = threadIdx.x; i < a.G * kD; i += kThreads) {
-    const int j = i / kD, d = i - j * kD;
-    float M = kNegInf;
+    const int jh = i / kD, d = i - jh * kD;
+    if (jh != jc) {
+      jc = jh;
+      M = kNegInf;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][j]);
-    float O = 0.f, Lsum = 0.f;
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][jh]);
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float f = (sm_m[w][j] == kNegInf) ? 0.f : exp2f(sm_m[w][j] - M);
-      O += sm_o[w][j][d] * f;
-      Lsum += sm_l[w][j] * f;
+      for (int w = 0; w < kWarps; ++w)
+        f[w] = (sm_m[w][jh] == kNegInf) ? 0.f : exp2f(sm_m[w][jh] - M);
     }
-    rec[j * kRec + d] = O;
+    const int slot = merge_slot(jh, d);
+    float O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) O += sm_o[w * 8 * kD + slot] * f[w];
+    rec[jh * kRec + d] = O;
     if (d == 0) {
-      rec[j * kRec + kD] = M;
-      rec[j * kRec + kD + 1] = Lsum;
+      float Lsum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) Lsum += sm_l[w][jh] * f[w];
+      rec[jh * kRec + kD] = M;
+      rec[jh * kRec + kD + 1] = Lsum;
     }
   }
 }
