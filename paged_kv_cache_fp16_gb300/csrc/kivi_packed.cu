@@ -816,30 +816,43 @@ __global__ void __launch_bounds__(kAThreads, 4) kivi_attn_kernel(const KAArgs a)
     sm_m[warp][2 * c] = m0; sm_m[warp][2 * c + 1] = m1;
     sm_l[warp][2 * c] = l0; sm_l[warp][2 * c + 1] = l1;
   }
+  // slot of (head j, d) in a warp's [8][64] block: the low three bits of d XOR-ed by
+  // (d >> 5) | (j >> 1) << 1, so the 32 lanes of each store (heads 2c or 2c + 1, d = 8 g + ...)
+  // fall in 32 different banks
+  auto slot = [](int j, int d) { return j * kAD + (d ^ ((d >> 5) | ((j >> 1) << 1))); };
+  float* wo = &sm_o[warp][0][0];
 #pragma unroll
   for (int mt = 0; mt < 4; ++mt) {
     const int d = 8 * g + 2 * mt;
-    sm_o[warp][2 * c][d] = acc[mt][0];
-    sm_o[warp][2 * c + 1][d] = acc[mt][1];
-    sm_o[warp][2 * c][d + 1] = acc[mt][2];
-    sm_o[warp][2 * c + 1][d + 1] = acc[mt][3];
+    wo[slot(2 * c, d)] = acc[mt][0];
+    wo[slot(2 * c + 1, d)] = acc[mt][1];
+    wo[slot(2 * c, d + 1)] = acc[mt][2];
+    wo[slot(2 * c + 1, d + 1)] = acc[mt][3];
   }
   __syncthreads();
   float* rec = a.ws + ((static_cast<int64_t>(lb) * a.H + h) * a.n_splits + split) * 8 * kARec;
+  // the warps' weights exp2(m_w - M) of a head, computed once when its first element comes up
+  int jc = -1;
+  float f[kAWarps], M = kNegInfF;
   for (int i = threadIdx.x; i < a.G * kAD; i += kAThreads) {
     const int jh = i / kAD, d = i - jh * kAD;
-    float M = kNegInfF;
+    if (jh != jc) {
+      jc = jh;
+      M = kNegInfF;
 #pragma unroll
-    for (int w = 0; w < kAWarps; ++w) M = fmaxf(M, sm_m[w][jh]);
-    float O = 0.f, Lsum = 0.f;
+      for (int w = 0; w < kAWarps; ++w) M = fmaxf(M, sm_m[w][jh]);
 #pragma unroll
-    for (int w = 0; w < kAWarps; ++w) {
-      const float f = (sm_m[w][jh] == kNegInfF) ? 0.f : exp2f(sm_m[w][jh] - M);
-      O += sm_o[w][jh][d] * f;
-      Lsum += sm_l[w][jh] * f;
+      for (int w = 0; w < kAWarps; ++w)
+        f[w] = (sm_m[w][jh] == kNegInfF) ? 0.f : exp2f(sm_m[w][jh] - M);
     }
+    float O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kAWarps; ++w) O += (&sm_o[w][0][0])[slot(jh, d)] * f[w];
     rec[jh * kARec + d] = O;
     if (d == 0) {
+      float Lsum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kAWarps; ++w) Lsum += sm_l[w][jh] * f[w];
       rec[jh * kARec + kAD] = M;
       rec[jh * kARec + kAD + 1] = Lsum;
     }
