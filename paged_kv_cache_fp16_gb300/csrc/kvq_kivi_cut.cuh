@@ -58,6 +58,51 @@ __device__ __forceinline__ uint32_t first_reaching(float z, float t) {
   return hbits(hi);
 }
 
+// Two searches at once, one per half (low: a, high: b), on packed operations: the guess is
+// fp16(z + t) rounded up, which is the answer unless fp16(z + t) is exactly representable after a
+// float32 sum that rounded down, or many fp16 values share the difference at the boundary; the
+// guess and its lower neighbour are checked for both halves with one packed float32 subtraction
+// each, and a half that does not settle takes the scalar search.
+__device__ __forceinline__ uint32_t hkey2(uint32_t b) {
+  return b ^ 0x80008000u ^ (((b >> 15) & 0x00010001u) * 0x7fffu);
+}
+__device__ __forceinline__ uint32_t hbits2(uint32_t k) {
+  return k ^ 0xffffffffu ^ (((k >> 15) & 0x00010001u) * 0x7fffu);
+}
+
+// RN32(x - z) >= t for the fp16 values of both halves of `bits`: bit 0 (low half), bit 1 (high).
+__device__ __forceinline__ uint32_t reaches2(uint32_t bits, uint64_t nz, float ta, float tb) {
+  const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&bits));
+  uint64_t xx, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(xx) : "f"(x.x), "f"(x.y));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(xx), "l"(nz));
+  float da, db;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(da), "=f"(db) : "l"(d));
+  return static_cast<uint32_t>(da >= ta) | (static_cast<uint32_t>(db >= tb) << 1);
+}
+
+__device__ __forceinline__ uint32_t first_reaching2(float za, float ta, float zb, float tb) {
+  uint64_t zz, tt, g, nz;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(zz) : "f"(za), "f"(zb));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(tt) : "f"(ta), "f"(tb));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(nz) : "f"(-za), "f"(-zb));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(g) : "l"(zz), "l"(tt));
+  float ga, gb;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(ga), "=f"(gb) : "l"(g));
+  const uint32_t hb = (static_cast<uint32_t>(__half_as_ushort(__float2half_ru(gb))) << 16) |
+                      __half_as_ushort(__float2half_ru(ga));
+  const uint32_t k = __vmaxu2(__vminu2(hkey2(hb), 0xfc00fc00u), 0x04000400u);
+  const uint32_t r0 = reaches2(hbits2(k), nz, ta, tb);
+  const uint32_t rm = reaches2(hbits2(k - 0x00010001u), nz, ta, tb);
+  const uint32_t ok = r0 & ~rm;   // bit i: half i settled at its guess
+  uint32_t out = hbits2(k);
+  if (ok != 3u) {   // rare: the scalar search for the half that did not settle
+    if (!(ok & 1u)) out = (out & 0xffff0000u) | first_reaching(za, ta);
+    if (!(ok & 2u)) out = (out & 0x0000ffffu) | (first_reaching(zb, tb) << 16);
+  }
+  return out;
+}
+
 // The three code boundaries of two groups as half2 words (low half: group a, high half: group b).
 // They nest: x >= X3 implies x >= X2 implies x >= X1.
 struct L3Cut {
@@ -67,16 +112,17 @@ struct L3Cut {
 __device__ __forceinline__ L3Cut l3_cut2(float za, float a1, float a2, float a3, float zb,
                                          float b1, float b2, float b3) {
   L3Cut c;
-  c.x1 = first_reaching(za, a1) | (first_reaching(zb, b1) << 16);
-  c.x2 = first_reaching(za, a2) | (first_reaching(zb, b2) << 16);
-  c.x3 = first_reaching(za, a3) | (first_reaching(zb, b3) << 16);
+  c.x1 = first_reaching2(za, a1, zb, b1);
+  c.x2 = first_reaching2(za, a2, zb, b2);
+  c.x3 = first_reaching2(za, a3, zb, b3);
   return c;
 }
 
 __device__ __forceinline__ L3Cut l3_cut1(float z, float t1, float t2, float t3) {
   L3Cut c;
-  c.x1 = first_reaching(z, t1) * 0x10001u;
-  c.x2 = first_reaching(z, t2) * 0x10001u;
+  const uint32_t x12 = first_reaching2(z, t1, z, t2);
+  c.x1 = (x12 & 0xffffu) * 0x10001u;
+  c.x2 = (x12 >> 16) * 0x10001u;
   c.x3 = first_reaching(z, t3) * 0x10001u;
   return c;
 }
