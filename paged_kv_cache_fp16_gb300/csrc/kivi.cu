@@ -302,6 +302,49 @@ __device__ __forceinline__ void l3_value_group(uint4* pv, float levels, float ep
                        l3_cut_word(v[k].w, cut, rr0, rr1, rr2, rr3));
 }
 
+// One key item: the column pair (channels 2 pr, 2 pr + 1) of one token group in registers, its
+// two groups' fp16 min / max as a tree, parameters, code boundaries and reconstructions, then the
+// round trip of every row.  SW > 0: a full group of kKeepRows rows SW words apart -- the loads
+// and stores take immediate offsets and no row predicate (the workload's head_dim 64, group 32);
+// SW = 0: n rows sw words apart.
+template <int SW>
+__device__ __forceinline__ void l3_key_group(uint32_t* base, int n, int64_t sw,
+                                             const KiviArgs& a) {
+  const int64_t stride = SW > 0 ? SW : sw;
+  uint32_t keep[kKeepRows];
+  keep[0] = base[0];
+#pragma unroll
+  for (int r = 1; r < kKeepRows; ++r) keep[r] = (SW > 0 || r < n) ? base[r * stride] : keep[0];
+  __half2 mn[kKeepRows / 2], mx[kKeepRows / 2];
+#pragma unroll
+  for (int r = 0; r < kKeepRows / 2; ++r) {
+    mn[r] = __hmin2(as_h2(keep[2 * r]), as_h2(keep[2 * r + 1]));
+    mx[r] = __hmax2(as_h2(keep[2 * r]), as_h2(keep[2 * r + 1]));
+  }
+#pragma unroll
+  for (int w = kKeepRows / 4; w >= 1; w >>= 1)
+#pragma unroll
+    for (int r = 0; r < w; ++r) {
+      mn[r] = __hmin2(mn[r], mn[r + w]);
+      mx[r] = __hmax2(mx[r], mx[r + w]);
+    }
+  const Group g0 = make_group<true, false>(__low2float(mn[0]), __low2float(mx[0]), a.levels,
+                                           a.eps);
+  const Group g1 = make_group<true, false>(__high2float(mn[0]), __high2float(mx[0]), a.levels,
+                                           a.eps);
+  // the four reconstructions of both channels, as half2 (low: channel 2 pr, high: 2 pr + 1)
+  const uint32_t rr0 = recon_bits(g0, 0.f) | (recon_bits(g1, 0.f) << 16);
+  const uint32_t rr1 = recon_bits(g0, 1.f) | (recon_bits(g1, 1.f) << 16);
+  const uint32_t rr2 = recon_bits(g0, 2.f) | (recon_bits(g1, 2.f) << 16);
+  const uint32_t rr3 = recon_bits(g0, 3.f) | (recon_bits(g1, 3.f) << 16);
+  const L3Cut cut = l3_cut(g0, g1);
+#pragma unroll
+  for (int r = 0; r < kKeepRows; ++r) {
+    if (SW == 0 && r >= n) break;
+    base[r * stride] = l3_cut_word(keep[r], cut, rr0, rr1, rr2, rr3);
+  }
+}
+
 // Built for 4 blocks per SM (64 registers, 8 bytes spilled): 32 warps per SM keep
 // more loads in flight than 3 blocks at 76 registers (128-token flush of 16 layers, back to back
 // from a CUDA graph: 23.8 against 24.6 us).
@@ -322,39 +365,8 @@ __global__ void __launch_bounds__(kThreads, 4) kivi_l3_kernel(const KiviArgs a, 
     const int t0 = a.lo + g * a.gs;
     const int n = min(a.gs, a.hi - t0);
     uint32_t* base = reinterpret_cast<uint32_t*>(a.x[a.key_list[ki]] + (bh * a.S + t0) * a.D) + pr;
-    const int64_t stride_w = a.D / 2;
-    uint32_t keep[kKeepRows];
-    keep[0] = base[0];
-#pragma unroll
-    for (int r = 1; r < kKeepRows; ++r) keep[r] = (r < n) ? base[r * stride_w] : keep[0];
-    __half2 mn[kKeepRows / 2], mx[kKeepRows / 2];
-#pragma unroll
-    for (int r = 0; r < kKeepRows / 2; ++r) {
-      mn[r] = __hmin2(as_h2(keep[2 * r]), as_h2(keep[2 * r + 1]));
-      mx[r] = __hmax2(as_h2(keep[2 * r]), as_h2(keep[2 * r + 1]));
-    }
-#pragma unroll
-    for (int w = kKeepRows / 4; w >= 1; w >>= 1)
-#pragma unroll
-      for (int r = 0; r < w; ++r) {
-        mn[r] = __hmin2(mn[r], mn[r + w]);
-        mx[r] = __hmax2(mx[r], mx[r + w]);
-      }
-    const Group g0 = make_group<true, false>(__low2float(mn[0]), __low2float(mx[0]), a.levels,
-                                             a.eps);
-    const Group g1 = make_group<true, false>(__high2float(mn[0]), __high2float(mx[0]), a.levels,
-                                             a.eps);
-    // the four reconstructions of both channels, as half2 (low: channel 2 pr, high: 2 pr + 1)
-    const uint32_t rr0 = recon_bits(g0, 0.f) | (recon_bits(g1, 0.f) << 16);
-    const uint32_t rr1 = recon_bits(g0, 1.f) | (recon_bits(g1, 1.f) << 16);
-    const uint32_t rr2 = recon_bits(g0, 2.f) | (recon_bits(g1, 2.f) << 16);
-    const uint32_t rr3 = recon_bits(g0, 3.f) | (recon_bits(g1, 3.f) << 16);
-    const L3Cut cut = l3_cut(g0, g1);
-#pragma unroll
-    for (int r = 0; r < kKeepRows; ++r) {
-      if (r >= n) break;
-      base[r * stride_w] = l3_cut_word(keep[r], cut, rr0, rr1, rr2, rr3);
-    }
+    if (n == kKeepRows && a.D == 64) l3_key_group<32>(base, n, 32, a);
+    else l3_key_group<0>(base, n, a.D / 2, a);
   } else {
     // ---------------------------------------------------------------- values
     const uint32_t it = (q * p.pv + (o - p.pk)) * kThreads + threadIdx.x;
