@@ -5,7 +5,6 @@ whenever the group scale is already an fp16 value the packed round trip equals t
 in-place round trip bit for bit; codes are nearest against the stored scale; attention special
 cases and PyTorch SDPA in float64."""
 import json
-import math
 
 import numpy as np
 import pytest
