@@ -65,6 +65,7 @@ struct SideArgs {
   int n_tensors, total_tokens, H, D, page_size, pd, max_pages, nseq, k, n_sink;
   int units;     // 16-element units per row: D / 16
   int lpr_log2;  // lanes per row = 1 << lpr_log2 = min(next_pow2(units), 8)
+  bool v8;       // every fp16 tensor 32-byte aligned: its 16-element units move in one 256-bit access
 };
 
 // New token `tok` -> physical row of its head 0 ((page * H) * page_size + slot) or -1, with its
@@ -146,7 +147,7 @@ __device__ __forceinline__ void merge_top(uint32_t* run, const uint32_t* g) {
 }
 
 // ------------------------------------------------------------------------------ quant-pack
-template <int BITS, int UPL, int DEPTH>
+template <int BITS, int UPL, int DEPTH, bool V8>
 __global__ void __launch_bounds__(kThreads, 3) quant_pack_side_kernel(const SideArgs a) {
   constexpr int kQm = SymQ<BITS>::kQmax;
   const int lane = threadIdx.x & 31;
@@ -183,8 +184,12 @@ __global__ void __launch_bounds__(kThreads, 3) quant_pack_side_kernel(const Side
           v[u][j][0] = v[u][j][1] = make_uint4(0, 0, 0, 0);
           if (row < nrows && e0 < D) {
             const uint16_t* src = xi + static_cast<int64_t>(row) * D + e0;
-            v[u][j][0] = ld_stream_v4(src);
-            v[u][j][1] = ld_stream_v4(src + 8);
+            if constexpr (V8) {
+              ld_stream_v8(src, v[u][j][0], v[u][j][1]);
+            } else {
+              v[u][j][0] = ld_stream_v4(src);
+              v[u][j][1] = ld_stream_v4(src + 8);
+            }
           }
         }
       }
@@ -355,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 3) quant_pack_side_kernel(const Side
 // The plain dequant kernel's layout and arithmetic (fp16(c * scale), one rounding); then, after a
 // warp barrier that orders the stores, the row's lane j < k writes outlier j over its position.
 // Rows at positions < n_sink are copied from the sink buffer instead.
-template <int BITS, int UPL>
+template <int BITS, int UPL, bool V8>
 __global__ void __launch_bounds__(kThreads) dequant_side_kernel(const SideArgs a) {
   const int lane = threadIdx.x & 31;
   const int lpr = 1 << a.lpr_log2;
@@ -447,8 +452,12 @@ __global__ void __launch_bounds__(kThreads) dequant_side_kernel(const SideArgs a
                                       hmul2u(prmt(q[2], q[3], 0x5410u), s2),
                                       hmul2u(prmt(q[0], q[1], 0x7632u), s2),
                                       hmul2u(prmt(q[2], q[3], 0x7632u), s2));
-          *reinterpret_cast<uint4*>(orow + unit * 16) = o0;
-          *reinterpret_cast<uint4*>(orow + unit * 16 + 8) = o1;
+          if constexpr (V8) {
+            st_v8(orow + unit * 16, o0, o1);
+          } else {
+            *reinterpret_cast<uint4*>(orow + unit * 16) = o0;
+            *reinterpret_cast<uint4*>(orow + unit * 16 + 8) = o1;
+          }
         }
       }
       // the dense stores of every lane come before the outlier stores over them
@@ -493,18 +502,29 @@ unsigned side_grid(K kernel, int& cache, int n_tensors, int total_tokens) {
   return static_cast<unsigned>(need < cap ? (need > 0 ? need : 1) : cap);
 }
 
+template <int BITS, int UPL, int DEPTH, bool V8>
+void launch_quant_w(const SideArgs& a, cudaStream_t cs) {
+  static int cache = 0;
+  auto kern = quant_pack_side_kernel<BITS, UPL, DEPTH, V8>;
+  kern<<<side_grid(kern, cache, a.n_tensors, a.total_tokens), kThreads, 0, cs>>>(a);
+}
+
+template <int BITS, int UPL, bool V8>
+void launch_dequant_w(const SideArgs& a, cudaStream_t cs) {
+  static int cache = 0;
+  auto kern = dequant_side_kernel<BITS, UPL, V8>;
+  kern<<<side_grid(kern, cache, a.n_tensors, a.total_tokens), kThreads, 0, cs>>>(a);
+}
+
+// 256-bit accesses to the fp16 rows when every tensor of the call is 32-byte aligned.
 template <int BITS, int UPL, int DEPTH>
 void launch_quant(const SideArgs& a, cudaStream_t cs) {
-  static int cache = 0;
-  auto kern = quant_pack_side_kernel<BITS, UPL, DEPTH>;
-  kern<<<side_grid(kern, cache, a.n_tensors, a.total_tokens), kThreads, 0, cs>>>(a);
+  a.v8 ? launch_quant_w<BITS, UPL, DEPTH, true>(a, cs) : launch_quant_w<BITS, UPL, DEPTH, false>(a, cs);
 }
 
 template <int BITS, int UPL>
 void launch_dequant(const SideArgs& a, cudaStream_t cs) {
-  static int cache = 0;
-  auto kern = dequant_side_kernel<BITS, UPL>;
-  kern<<<side_grid(kern, cache, a.n_tensors, a.total_tokens), kThreads, 0, cs>>>(a);
+  a.v8 ? launch_dequant_w<BITS, UPL, true>(a, cs) : launch_dequant_w<BITS, UPL, false>(a, cs);
 }
 
 template <int BITS>
@@ -573,6 +593,9 @@ kvq_status side_call(bool quant, const kvq_pool* pools, const kvq_side* sides,
     a.pool[i] = PoolRef{pools[j].codes, pools[j].scales, pools[j].num_pages};
     a.side[i] = SideRef{sides[j].out_val, sides[j].out_idx, sides[j].sink};
   }
+  a.v8 = true;
+  for (int i = 0; i < n_tensors; ++i)
+    if (reinterpret_cast<uintptr_t>(x[i]) % 32) a.v8 = false;
   a.page_table = page_table;
   a.cu = cu;
   a.start = start;

@@ -294,3 +294,42 @@ def test_decode_append_full_size(kvq, cuda_dev, n_new):
         osym.quant_pack_paged(p, x, pt_np, cu_of([n_new] * nseq), cur)
         assert np.array_equal(pool.codes.cpu().numpy(), p.codes)
         assert np.array_equal(u16(pool.scales), p.scales.view(np.uint16))
+
+
+@pytest.mark.parametrize("bits", [8, 6, 4])
+@pytest.mark.parametrize("D", [64, 256])
+def test_tensors_aligned_to_16_but_not_32_bytes(kvq, cuda_dev, bits, D):
+    """fp16 rows move in 256-bit accesses only when every tensor of a call is 32-byte aligned;
+    tensors that are 16-byte aligned (what the API requires) take the 128-bit path.  Both must
+    give the oracle's bytes and values: here K is 32-byte aligned and V is offset by 16 bytes in
+    one call (the narrow path for both), then each alone."""
+    H, ps = 3, 16
+    lens, start = [5, 33, 17], [0, 3, 16]
+    pps = (max(s + n for s, n in zip(start, lens)) + ps - 1) // ps
+    pt = kvgen.random_page_table(90 + D, len(lens), pps)
+    tot = int(sum(lens))
+    x = [random_rows(tot * H, D, 91 + i).reshape(tot, H, D) for i in range(2)]
+
+    def offset_view(a, elems):
+        flat = torch.empty(a.size + 64, dtype=torch.float16, device=cuda_dev)
+        v = flat[elems:elems + a.size].view(a.shape)
+        v.copy_(torch.from_numpy(np.ascontiguousarray(a)).to(cuda_dev))
+        return v
+
+    ref = _oracle(x, bits, H, D, ps, lens, start, pt, pt.size)
+    args = (i32(pt, cuda_dev), i32(cu_of(lens), cuda_dev), i32(start, cuda_dev))
+    for offs in ((16, 8), (8, 8), (16, 16)):   # fp16 elements: 32 and 16 bytes
+        xs = [offset_view(a, o) for a, o in zip(x, offs)]
+        assert [t.data_ptr() % 32 for t in xs] == [2 * o % 32 for o in offs]
+        pools = [kvq.Pool.empty(bits, H, D, ps, pt.size, cuda_dev) for _ in x]
+        for p in pools:
+            p.codes.fill_(0xAB)
+            p.scales.fill_(7.0)
+        kvq.kvq_quant_pack_paged(pools, xs, *args)
+        outs = [offset_view(np.full(a.shape, np.float16(12345)), o) for a, o in zip(x, offs)]
+        kvq.kvq_dequant_paged(pools, outs, *args)
+        torch.cuda.synchronize()
+        for (op, od), p, o in zip(ref, pools, outs):
+            assert np.array_equal(p.codes.cpu().numpy(), op.codes)
+            assert np.array_equal(u16(p.scales), op.scales.view(np.uint16))
+            assert np.array_equal(u16(o), od.view(np.uint16))

@@ -165,6 +165,41 @@ def test_full_size_prefill_sampled(kvq, cuda_dev):
         torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("bits", [8, 6, 4])
+def test_side_tensors_aligned_to_16_but_not_32_bytes(kvq, cuda_dev, bits):
+    """The fp16 rows take 256-bit accesses only when every tensor is 32-byte aligned; a call
+    with a tensor offset by 16 bytes takes the 128-bit path, with the same results."""
+    H, D, ps, k, n_sink = 4, 256, 16, 3, 4
+    lens, starts = [1, 5, 40, 21], [0, 0, 0, 3]
+    tot = int(sum(lens))
+    xs = [_rows(5, True, tot, H, D), _rows(5, False, tot, H, D)]
+    cu = cu_of(lens)
+
+    def offset_view(a, elems):
+        flat = torch.empty(a.size + 64, dtype=torch.float16, device=cuda_dev)
+        v = flat[elems:elems + a.size].view(a.shape)
+        v.copy_(torch.from_numpy(np.ascontiguousarray(a)).to(cuda_dev))
+        return v
+
+    for offs in ((16, 16), (16, 8)):   # fp16 elements: 32-byte aligned, then V off by 16 bytes
+        pt_np, pools, sides, opools, osides = _setup(kvq, cuda_dev, bits, H, D, ps, k, n_sink,
+                                                     lens, starts, seed=7)
+        err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+        args = (i32(pt_np, cuda_dev), i32(cu, cuda_dev), i32(starts, cuda_dev), err)
+        kvq.kvq_quant_pack_paged_side(pools, sides, [offset_view(x, o) for x, o in zip(xs, offs)],
+                                      *args)
+        outs = [offset_view(np.full((tot, H, D), np.float16(12345)), o) for o in offs]
+        kvq.kvq_dequant_paged_side(pools, sides, outs, *args)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        for x, osp in zip(xs, osides):
+            osd.quant_pack_paged_side(osp, x, pt_np, cu, np.asarray(starts))
+        _compare_state(pools, sides, opools, osides, n_sink)
+        for o, osp in zip(outs, osides):
+            ref = osd.dequant_paged_side(osp, pt_np, cu, np.asarray(starts))
+            assert np.array_equal(u16(o), ref.view(np.uint16))
+
+
 # ---------------------------------------------------------------- decode attention
 
 
