@@ -272,12 +272,17 @@ __device__ __forceinline__ L3Cut l3_cut(const Group& a, const Group& b) {
 __device__ __forceinline__ L3Cut l3_cut(const Group& g) { return l3_cut1(g.mn, g.t1, g.t2, g.t3); }
 
 // A value group of NV 16-byte vectors (8 * NV channels): load, fp16 min/max tree, the 2-bit
-// round trip, store.
-template <int NV>
+// round trip, store.  V8: the group is 32-byte aligned and moves in 256-bit accesses.
+template <int NV, bool V8>
 __device__ __forceinline__ void l3_value_group(uint4* pv, float levels, float eps) {
   uint4 v[NV];
+  if constexpr (V8 && NV % 2 == 0) {
 #pragma unroll
-  for (int k = 0; k < NV; ++k) v[k] = pv[k];
+    for (int k = 0; k < NV; k += 2) ld_v8(pv + k, v[k], v[k + 1]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) v[k] = pv[k];
+  }
   __half2 mn = __hmin2(__hmin2(as_h2(v[0].x), as_h2(v[0].y)), __hmin2(as_h2(v[0].z), as_h2(v[0].w)));
   __half2 mx = __hmax2(__hmax2(as_h2(v[0].x), as_h2(v[0].y)), __hmax2(as_h2(v[0].z), as_h2(v[0].w)));
 #pragma unroll
@@ -294,12 +299,20 @@ __device__ __forceinline__ void l3_value_group(uint4* pv, float levels, float ep
   const uint32_t rr0 = r0 | (r0 << 16), rr1 = r1 | (r1 << 16);
   const uint32_t rr2 = r2 | (r2 << 16), rr3 = r3 | (r3 << 16);
   const L3Cut cut = l3_cut(gr);
+  uint4 o[NV];
 #pragma unroll
   for (int k = 0; k < NV; ++k)
-    pv[k] = make_uint4(l3_cut_word(v[k].x, cut, rr0, rr1, rr2, rr3),
-                       l3_cut_word(v[k].y, cut, rr0, rr1, rr2, rr3),
-                       l3_cut_word(v[k].z, cut, rr0, rr1, rr2, rr3),
-                       l3_cut_word(v[k].w, cut, rr0, rr1, rr2, rr3));
+    o[k] = make_uint4(l3_cut_word(v[k].x, cut, rr0, rr1, rr2, rr3),
+                      l3_cut_word(v[k].y, cut, rr0, rr1, rr2, rr3),
+                      l3_cut_word(v[k].z, cut, rr0, rr1, rr2, rr3),
+                      l3_cut_word(v[k].w, cut, rr0, rr1, rr2, rr3));
+  if constexpr (V8 && NV % 2 == 0) {
+#pragma unroll
+    for (int k = 0; k < NV; k += 2) st_v8(pv + k, o[k], o[k + 1]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) pv[k] = o[k];
+  }
 }
 
 // One key item: the column pair (channels 2 pr, 2 pr + 1) of one token group in registers, its
@@ -348,6 +361,7 @@ __device__ __forceinline__ void l3_key_group(uint32_t* base, int n, int64_t sw,
 // Built for 4 blocks per SM (64 registers, 8 bytes spilled): 32 warps per SM keep
 // more loads in flight than 3 blocks at 76 registers (128-token flush of 16 layers, back to back
 // from a CUDA graph: 23.8 against 24.6 us).
+template <bool V8>
 __global__ void __launch_bounds__(kThreads, 4) kivi_l3_kernel(const KiviArgs a, const L3Plan p) {
   const uint32_t b = blockIdx.x;
   const uint32_t q = divu32(b, p.period);
@@ -382,15 +396,15 @@ __global__ void __launch_bounds__(kThreads, 4) kivi_l3_kernel(const KiviArgs a, 
     const int nv = (min(a.D, c0 + a.gs) - c0) / 8;   // 16-byte vectors in this group
     uint4* pv = reinterpret_cast<uint4*>(a.x[a.val_list[vi]] + (bh * a.S + t) * a.D + c0);
     if (nv == 4) {   // groups of 32 channels: no padding, no bounds
-      l3_value_group<4>(pv, a.levels, a.eps);
+      l3_value_group<4, V8>(pv, a.levels, a.eps);
       return;
     }
     if (nv == 2) {
-      l3_value_group<2>(pv, a.levels, a.eps);
+      l3_value_group<2, V8>(pv, a.levels, a.eps);
       return;
     }
     if (nv == 1) {
-      l3_value_group<1>(pv, a.levels, a.eps);
+      l3_value_group<1, V8>(pv, a.levels, a.eps);
       return;
     }
     // other group widths: up to 8 vectors, padded with the first (min / max unchanged)
@@ -514,7 +528,13 @@ extern "C" kvq_status kivi_quant_dequant(uint16_t* const* x, const int32_t* is_k
     p.val_items = static_cast<uint32_t>(val_items);
     const int64_t blocks = periods * (p.pk + p.pv);
     if (blocks < (1LL << 31)) {
-      kivi_l3_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(a, p);
+      // 256-bit value accesses when every tensor is 32-byte aligned (value groups are 16 or 32
+      // channels at 16-channel offsets: D and group_size are multiples of 8 here, so check both)
+      bool v8 = D % 16 == 0 && group_size % 16 == 0;
+      for (int i = 0; i < n_tensors; ++i)
+        if (reinterpret_cast<uintptr_t>(x[i]) % 32) v8 = false;
+      if (v8) kivi_l3_kernel<true><<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(a, p);
+      else kivi_l3_kernel<false><<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(a, p);
       const cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "kivi launch: %s", cudaGetErrorString(e));
       return ok();

@@ -38,6 +38,15 @@ __device__ __forceinline__ void ld_stream_v8(const void* p, uint4& lo, uint4& hi
                : "l"(p));
 }
 
+// 32-byte coherent load in one 256-bit access (data the same launch also writes).
+__device__ __forceinline__ void ld_v8(const void* p, uint4& lo, uint4& hi) {
+  asm volatile("ld.global.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y),
+                 "=r"(hi.z), "=r"(hi.w)
+               : "l"(p)
+               : "memory");
+}
+
 // 32-byte store in one 256-bit access (the address must be 32-byte aligned).
 __device__ __forceinline__ void st_v8(void* p, const uint4& lo, const uint4& hi) {
   asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(lo.x),
