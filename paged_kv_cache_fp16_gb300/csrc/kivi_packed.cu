@@ -48,6 +48,7 @@ struct KPArgs {
   float eps, levels;
   // item decomposition without 64-bit divisions, when the per-layer item counts are < 2^31
   bool fast32;
+  bool v8;                               // value tensors 32-byte aligned, head dim % 16 == 0
   DivU32 div_g, div_span, div_ngroups;   // by D / gs, hi - lo, (hi - lo) / gs
 };
 
@@ -389,7 +390,7 @@ __device__ __forceinline__ void value_group(const KPArgs& a, int layer, int64_t 
 // Values: one thread per item, groups of 8 NV channels.  The running loop loads the next item's
 // vectors before it codes the current one, so every thread keeps a load in flight while it
 // computes.
-template <int BITS, int NV>
+template <int BITS, int NV, bool V8>
 __device__ void pack_values_part(const KPArgs& a, int64_t first, int64_t stride) {
   const kivi_packed& c0 = a.c[0];
   const int B = c0.batch, H = c0.num_heads, S = c0.capacity, D = c0.head_dim;
@@ -399,8 +400,13 @@ __device__ void pack_values_part(const KPArgs& a, int64_t first, int64_t stride)
   const int64_t items = per_layer * a.n_layers;
   auto load = [&](int layer, int64_t bh, int t, int g, uint4 (&vv)[NV]) {
     const uint4* src = reinterpret_cast<const uint4*>(a.v[layer] + (bh * S + t) * D) + g * NV;
+    if constexpr (V8 && NV % 2 == 0) {   // 32-byte aligned: pairs of vectors in 256-bit loads
 #pragma unroll
-    for (int k = 0; k < NV; ++k) vv[k] = src[k];
+      for (int k = 0; k < NV; k += 2) ld_stream_v8(src + k, vv[k], vv[k + 1]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < NV; ++k) vv[k] = src[k];
+    }
   };
   if (a.fast32) {   // running (layer, offset); offset / G and / span by multiply-high
     if (first >= items) return;
@@ -472,10 +478,10 @@ __global__ void __launch_bounds__(kThreads, (GS > 0 && GS <= 32) ? 4 : 1)
                          static_cast<int64_t>(gridDim.x) * kThreads);
 }
 
-template <int BITS, int NV>
+template <int BITS, int NV, bool V8>
 __global__ void __launch_bounds__(kThreads) kivi_pack_values_kernel(const KPArgs a) {
-  pack_values_part<BITS, NV>(a, static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x,
-                             static_cast<int64_t>(gridDim.x) * kThreads);
+  pack_values_part<BITS, NV, V8>(a, static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x,
+                                 static_cast<int64_t>(gridDim.x) * kThreads);
 }
 
 // ================================================================================================
@@ -962,11 +968,19 @@ void launch_keys(const KPArgs& a, int64_t threads, cudaStream_t cs) {
   kivi_pack_keys_kernel<BITS, GS><<<grid, kThreads, 0, cs>>>(a);
 }
 
+template <int BITS, int NV, bool V8>
+void launch_values_w(const KPArgs& a, int64_t threads, cudaStream_t cs) {
+  static int cache = 0;
+  const int grid = resident_grid(kivi_pack_values_kernel<BITS, NV, V8>, cache, threads);
+  kivi_pack_values_kernel<BITS, NV, V8><<<grid, kThreads, 0, cs>>>(a);
+}
+
+// Value groups of 16 or more channels load their fp16 vectors in pairs (256-bit accesses) when
+// every value tensor is 32-byte aligned and the head dim a multiple of 16.
 template <int BITS, int NV>
 void launch_values(const KPArgs& a, int64_t threads, cudaStream_t cs) {
-  static int cache = 0;
-  const int grid = resident_grid(kivi_pack_values_kernel<BITS, NV>, cache, threads);
-  kivi_pack_values_kernel<BITS, NV><<<grid, kThreads, 0, cs>>>(a);
+  if (NV % 2 == 0 && a.v8) launch_values_w<BITS, NV, true>(a, threads, cs);
+  else launch_values_w<BITS, NV, false>(a, threads, cs);
 }
 
 template <int BITS>
@@ -1019,6 +1033,9 @@ extern "C" kvq_status kivi_pack(const kivi_packed* caches, const uint16_t* const
   a.hi = hi;
   a.eps = eps;
   a.levels = static_cast<float>((1 << c0.bits) - 1);
+  a.v8 = c0.head_dim % 16 == 0;
+  for (int i = 0; i < n_layers; ++i)
+    if (reinterpret_cast<uintptr_t>(v[i]) % 32) a.v8 = false;
   {
     const int64_t span = hi - lo, G = c0.head_dim / c0.group_size;
     const int64_t bhc = static_cast<int64_t>(c0.batch) * c0.num_heads;
