@@ -358,9 +358,9 @@ __device__ __forceinline__ void l3_key_group(uint32_t* base, int n, int64_t sw,
   }
 }
 
-// Built for 4 blocks per SM (64 registers, 8 bytes spilled): 32 warps per SM keep
-// more loads in flight than 3 blocks at 76 registers (128-token flush of 16 layers, back to back
-// from a CUDA graph: 23.8 against 24.6 us).
+// Built for 4 blocks per SM (64 registers, no spills): 32 warps per SM keep more loads in flight
+// than 3 blocks at 76 registers did (128-token flush of 16 layers, back to back from a CUDA graph:
+// 23.8 against 24.6 us when that choice was made).
 template <bool V8>
 __global__ void __launch_bounds__(kThreads, 4) kivi_l3_kernel(const KiviArgs a, const L3Plan p) {
   const uint32_t b = blockIdx.x;
