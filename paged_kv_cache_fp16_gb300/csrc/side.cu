@@ -15,20 +15,24 @@
 // 16-element units, 8 lanes share a row (fewer for short rows) and lane j of a row holds units j
 // and j + 8, so one warp instruction serves 4 rows.
 //
-// Selection.  Element x at position p of a row has the key (|x| bits << 8) | (255 - p): unique
-// within the row, larger for a larger magnitude and, among equal magnitudes, for the lower
-// position (one byte permute per element builds it).  Each lane sorts the keys of its elements
-// with small sorting networks into a descending list of its DEPTH largest (DEPTH >= k + 1, or
-// the lane's own remaining maximum is recomputed for the last round); k + 1 rounds of a max over
-// the row's lanes pick the k outlier keys and then the (k+1)-th largest key, whose magnitude T
-// is the dense row's amax, the lane that held each winner popping it from its list.  An element
-// is an outlier iff its key exceeds that last key; unless the k-th outlier's magnitude equals T
-// (a tie at the threshold), that is simply |x| > T, one half2 compare per pair of elements,
-// else the keys are rebuilt and compared.  Outliers are zeroed in the dense row, whose scale and
-// codes are the quant-pack kernel's arithmetic (the fields packed by integer multiply-adds from
-// the rounding sums, which keeps them off the integer-logic pipe); the row's lane j < k stores
-// the outlier whose key is the j-th largest at its rank among the k positions (ascending order
-// without a sort), its fp16 value (with its sign) read back from the input row.
+// Selection.  For k <= 3 by magnitude first: each lane sorts its elements' magnitudes two at a
+// time (fp16 pairs through min/max networks) into its 4 largest, tags each (magnitude << 3) |
+// lane so equal magnitudes of different lanes differ, and k + 1 rounds of a max over the row's
+// lanes give the k-th largest magnitude M and the (k+1)-th, T, the dense row's amax (counted
+// with multiplicity).  When M > T the outliers are exactly the elements with |x| > T, one half2
+// compare per pair of elements.  When M == T (a tie at the threshold) positions decide: if any
+// row of the warp step has one, the step selects again by keys.  Element x at position p has
+// the key (|x| bits << 8) | (255 - p) (one byte permute per element): unique in the row, larger
+// for a larger magnitude and, among equal magnitudes, for the lower position.  Each lane keeps
+// its DEPTH largest keys (sorting networks, bitonic merges; DEPTH >= k + 1, or the lane's own
+// remaining maximum is recomputed for the last round) and k + 1 rounds of a max over the row's
+// lanes give the (k+1)-th largest key; an element is an outlier iff its key exceeds it.  k > 3
+// always selects by keys.  Outliers are zeroed in the dense row, whose scale and codes are the
+// quant-pack kernel's arithmetic (the fields packed by integer multiply-adds from the rounding
+// sums, which keeps them off the integer-logic pipe).  Each lane notes its outliers in a bit
+// mask; an outlier's place among the row's k (ascending by position) is the count of outliers
+// before it, from the lanes' counts scanned over the row; the lane stores its own outliers, the
+// fp16 values (with their signs) read back from the input row.
 #include <type_traits>
 
 #include <cuda_runtime.h>
@@ -85,25 +89,54 @@ __device__ __forceinline__ long long shfl_ll(long long v, int src) {
 }
 
 // ---------------------------------------------------------------------------- selection keys
-// Compare-exchange: a >= b afterwards.
-__device__ __forceinline__ void cx(uint32_t& a, uint32_t& b) {
-  const uint32_t hi = max(a, b);
-  b = min(a, b);
-  a = hi;
+// Compare-exchange: a >= b afterwards; P: in each half of a pair of non-negative fp16 values
+// (for those, the fp16 order is the order of their bit patterns).
+// |x| of both halves of an fp16 pair, as an fp16 operation (the compares can take it as an
+// operand modifier).
+__device__ __forceinline__ uint32_t habs_u(uint32_t x) {
+  __half2 h = __habs2(*reinterpret_cast<const __half2*>(&x));
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+template <bool P = false>
+__device__ __forceinline__ void cx(uint32_t& a, uint32_t& b) {
+  if constexpr (P) {
+    uint32_t hi, lo;
+    asm("max.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(a), "r"(b));
+    asm("min.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(b));
+    a = hi;
+    b = lo;
+  } else {
+    const uint32_t hi = max(a, b);
+    b = min(a, b);
+    a = hi;
+  }
+}
+
+template <bool P = false>
+__device__ __forceinline__ uint32_t max_of(uint32_t a, uint32_t b) {
+  if constexpr (P) {
+    uint32_t d;
+    asm("max.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  } else {
+    return max(a, b);
+  }
+}
+
+template <bool P = false>
 __device__ __forceinline__ void sort4(uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
-  cx(a, b); cx(c, d); cx(a, c); cx(b, d); cx(b, c);
+  cx<P>(a, b); cx<P>(c, d); cx<P>(a, c); cx<P>(b, d); cx<P>(b, c);
 }
 
 // A bitonic sequence t[0..N) -> descending (half-cleaners of Batcher's bitonic sorter).
-template <int N>
+template <int N, bool P = false>
 __device__ __forceinline__ void bitonic_desc(uint32_t* t) {
 #pragma unroll
   for (int len = N / 2; len >= 1; len /= 2) {
 #pragma unroll
     for (int i = 0; i < N; ++i)
-      if ((i & len) == 0) cx(t[i], t[i + len]);
+      if ((i & len) == 0) cx<P>(t[i], t[i + len]);
   }
 }
 
@@ -139,11 +172,130 @@ __device__ __forceinline__ void top_of8(uint32_t k[8]) {
 }
 
 // run = the DEPTH largest of two descending lists run, g.
-template <int DEPTH>
+template <int DEPTH, bool P = false>
 __device__ __forceinline__ void merge_top(uint32_t* run, const uint32_t* g) {
 #pragma unroll
-  for (int i = 0; i < DEPTH; ++i) run[i] = max(run[i], g[DEPTH - 1 - i]);
-  bitonic_desc<DEPTH>(run);
+  for (int i = 0; i < DEPTH; ++i) run[i] = max_of<P>(run[i], g[DEPTH - 1 - i]);
+  bitonic_desc<DEPTH, P>(run);
+}
+
+// Exact selection by keys: thr = the row's (k+1)-th largest key, last = its k-th (0 if k = 0).
+// Each lane keeps its DEPTH largest keys; k + 1 rounds of a max over the row's lanes take the
+// winners, the lane that held each popping it from its list (all lanes take part).
+template <int UPL, int DEPTH>
+__device__ __forceinline__ void key_select(const uint4 (&v)[UPL][2], int lr, int lpr, int D,
+                                           int k, uint32_t& thr, uint32_t& last) {
+  uint32_t top[DEPTH];
+#pragma unroll
+  for (int i = 0; i < DEPTH; ++i) top[i] = 0u;
+#pragma unroll
+  for (int j = 0; j < UPL; ++j) {
+    const int unit = lr + j * lpr;
+    if (unit * 16 >= D) continue;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t g[8];
+      keys8(v[j][hh], 255u - static_cast<uint32_t>(16 * unit + 8 * hh), g);
+      top_of8<DEPTH>(g);
+      if (j == 0 && hh == 0) {
+#pragma unroll
+        for (int i = 0; i < DEPTH; ++i) top[i] = g[i];
+      } else {
+        merge_top<DEPTH>(top, g);
+      }
+    }
+  }
+  thr = 0u;
+  last = 0u;
+#pragma unroll
+  for (int j = 0; j <= KVQ_MAX_OUTLIERS; ++j) {
+    if (j > k) break;
+    uint32_t m = top[0];
+    if (j >= DEPTH && j == k) {
+      // this lane may have given all DEPTH listed keys: its largest key below the last
+      // outlier's, rebuilt from the elements
+      m = 0u;
+#pragma unroll
+      for (int jj = 0; jj < UPL; ++jj) {
+        const int unit = lr + jj * lpr;
+        if (unit * 16 >= D) continue;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t g[8];
+          keys8(v[jj][hh], 255u - static_cast<uint32_t>(16 * unit + 8 * hh), g);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m = max(m, g[e] < last ? g[e] : 0u);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 4; o >= 1; o >>= 1)
+      if (o < lpr) m = max(m, __shfl_xor_sync(kFullMask, m, o));
+    if (j == k) {
+      thr = m;
+      break;
+    }
+    last = m;
+    const bool pop = top[0] == m;
+#pragma unroll
+    for (int i = 0; i + 1 < DEPTH; ++i) top[i] = pop ? top[i + 1] : top[i];
+    top[DEPTH - 1] = pop ? 0u : top[DEPTH - 1];
+  }
+}
+
+// Selection by magnitude alone (k <= 3): T = the row's (k+1)-th largest magnitude and M = its
+// k-th (fp16 bits, counted with multiplicity; M = 0 if k = 0).  Each lane sorts its magnitudes
+// two at a time (fp16 pairs) into the 4 largest of its lower and of its upper halves, merges the two lists, tags each entry (magnitude << 3) | lane so that equal
+// magnitudes of different lanes differ, and k + 1 rounds of a max over the row's lanes take the
+// winners.  When M > T the outliers are exactly the elements with |x| > T; when M == T (a tie
+// at the threshold) positions decide, and the keys are needed.
+template <int UPL>
+__device__ __forceinline__ void magnitude_select(const uint4 (&v)[UPL][2], int lr, int lpr,
+                                                 int D, int k, uint32_t& T, uint32_t& M) {
+  uint32_t run[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int j = 0; j < UPL; ++j) {
+    if ((lr + j * lpr) * 16 >= D) continue;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t g[4] = {habs_u(v[j][hh].x), habs_u(v[j][hh].y), habs_u(v[j][hh].z),
+                       habs_u(v[j][hh].w)};
+      sort4<true>(g[0], g[1], g[2], g[3]);
+      if (j == 0 && hh == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) run[i] = g[i];
+      } else {
+        merge_top<4, true>(run, g);
+      }
+    }
+  }
+  // the lower-half list against the upper-half list reversed: a bitonic sequence per half
+  uint32_t top[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) top[i] = max_of<true>(run[i], prmt(run[3 - i], 0u, 0x1032u));
+  bitonic_desc<4, true>(top);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) top[i] = ((top[i] & 0x7fffu) << 3) | static_cast<uint32_t>(lr);
+  uint32_t thr = 0u, last = 0u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (j > k) break;
+    uint32_t m = top[0];
+#pragma unroll
+    for (int o = 4; o >= 1; o >>= 1)
+      if (o < lpr) m = max(m, __shfl_xor_sync(kFullMask, m, o));
+    if (j == k) {
+      thr = m;
+      break;
+    }
+    last = m;
+    const bool pop = top[0] == m;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) top[i] = pop ? top[i + 1] : top[i];
+    top[3] = pop ? 0u : top[3];
+  }
+  T = thr >> 3;
+  M = last >> 3;
 }
 
 // ------------------------------------------------------------------------------ quant-pack
@@ -201,70 +353,28 @@ __global__ void __launch_bounds__(kThreads, 3) quant_pack_side_kernel(const Side
         const long long b = shfl_ll(base, src);
         const int s = __shfl_sync(kFullMask, my_s, src);
         const int pos = __shfl_sync(kFullMask, my_pos, src);
-        // the lane's DEPTH largest keys
-        uint32_t top[DEPTH];
-#pragma unroll
-        for (int i = 0; i < DEPTH; ++i) top[i] = 0u;
-#pragma unroll
-        for (int j = 0; j < UPL; ++j) {
-          const int unit = lr + j * lpr;
-          if (unit * 16 >= D) continue;
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t g[8];
-            keys8(v[u][j][hh], 255u - static_cast<uint32_t>(16 * unit + 8 * hh), g);
-            top_of8<DEPTH>(g);
-            if (j == 0 && hh == 0) {
-#pragma unroll
-              for (int i = 0; i < DEPTH; ++i) top[i] = g[i];
-            } else {
-              merge_top<DEPTH>(top, g);
-            }
+        // T = the dense row's amax (fp16 bits); by_key: outliers decided by key, not |x| > T
+        uint32_t T, thr = 0u;
+        bool by_key;
+        if constexpr (DEPTH == 4) {
+          uint32_t M;
+          magnitude_select<UPL>(v[u], lr, lpr, D, k, T, M);
+          by_key = false;
+          if (__any_sync(kFullMask, k > 0 && M == T && row < nrows)) {
+            uint32_t last;
+            key_select<UPL, 4>(v[u], lr, lpr, D, k, thr, last);
+            T = thr >> 8;
+            by_key = k > 0 && (last >> 8) == T;
           }
+        } else {
+          uint32_t last;
+          key_select<UPL, DEPTH>(v[u], lr, lpr, D, k, thr, last);
+          T = thr >> 8;
+          by_key = k > 0 && (last >> 8) == T;
         }
-        // k + 1 rounds of a max over the row's lanes (all lanes take part in the shuffles)
-        uint32_t okey[KVQ_MAX_OUTLIERS];
-        uint32_t thr = 0u, last = 0u;
-#pragma unroll
-        for (int j = 0; j <= KVQ_MAX_OUTLIERS; ++j) {
-          if (j > k) break;
-          uint32_t m = top[0];
-          if (j >= DEPTH && j == k) {
-            // this lane may have given all DEPTH listed keys: its largest key below the last
-            // outlier's, rebuilt from the elements
-            m = 0u;
-#pragma unroll
-            for (int jj = 0; jj < UPL; ++jj) {
-              const int unit = lr + jj * lpr;
-              if (unit * 16 >= D) continue;
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                uint32_t g[8];
-                keys8(v[u][jj][hh], 255u - static_cast<uint32_t>(16 * unit + 8 * hh), g);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) m = max(m, g[e] < last ? g[e] : 0u);
-              }
-            }
-          }
-#pragma unroll
-          for (int o = 4; o >= 1; o >>= 1)
-            if (o < lpr) m = max(m, __shfl_xor_sync(kFullMask, m, o));
-          if (j == k) {
-            thr = m;
-            break;
-          }
-          if (j < KVQ_MAX_OUTLIERS) okey[j] = m;
-          last = m;
-          const bool pop = top[0] == m;
-#pragma unroll
-          for (int i = 0; i + 1 < DEPTH; ++i) top[i] = pop ? top[i + 1] : top[i];
-          top[DEPTH - 1] = pop ? 0u : top[DEPTH - 1];
-        }
-        if (row >= nrows || b < 0) continue;
+        const bool valid = row < nrows && b >= 0;
         const int h = row - kt * H;
         const int64_t prow = b + static_cast<int64_t>(h) * a.page_size;
-        const uint32_t T = thr >> 8;   // the dense row's amax, fp16 bits
-        const bool tie = k > 0 && (last >> 8) == T;
         const uint16_t sbits = f2h(row_scale_f32<kQm>(h2f(static_cast<uint16_t>(T))));
         const float sc = h2f(sbits);
         const float y = (sc == 0.f) ? 0.f : __frcp_rn(sc);
@@ -272,6 +382,8 @@ __global__ void __launch_bounds__(kThreads, 3) quant_pack_side_kernel(const Side
         const bool clip = sc < 6.103515625e-05f;   // 2^-14, smallest normal fp16
         const uint32_t T2 = T | (T << 16);
         uint8_t* crow = pool.codes + prow * a.pd;
+        // the lane's outliers: bit 16 j + 8 hh + e for element e of half hh of its unit j
+        uint32_t omask = 0u;
         auto units = [&](auto clip_tag) {
           constexpr bool kClip = decltype(clip_tag)::value;
 #pragma unroll
@@ -283,23 +395,29 @@ __global__ void __launch_bounds__(kThreads, 3) quant_pack_side_kernel(const Side
             for (int hh = 0; hh < 2; ++hh) {
               const uint4& vv = v[u][j][hh];
               uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
-              // zero the outliers: |x| > T, or (tie at T) key > thr
-              if (!tie) {
+              // outliers (|x| > T, or at a tie key > thr) as 0xffff per half, zeroed
+              uint32_t gt[4];
+              if (!by_key) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                  const uint32_t m = w[i] & 0x7fff7fffu;
-                  const uint32_t gt = __hgt2_mask(*reinterpret_cast<const __half2*>(&m),
-                                                  *reinterpret_cast<const __half2*>(&T2));
-                  w[i] &= ~gt;
+                  gt[i] = __hgt2_mask(__habs2(*reinterpret_cast<const __half2*>(&w[i])),
+                                      *reinterpret_cast<const __half2*>(&T2));
                 }
               } else {
                 uint32_t g[8];
                 keys8(vv, 255u - static_cast<uint32_t>(16 * unit + 8 * hh), g);
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                  w[i] &= (g[2 * i] > thr ? 0xffff0000u : 0xffffffffu) &
-                          (g[2 * i + 1] > thr ? 0x0000ffffu : 0xffffffffu);
+                  gt[i] = (g[2 * i] > thr ? 0x0000ffffu : 0u) |
+                          (g[2 * i + 1] > thr ? 0xffff0000u : 0u);
               }
+#pragma unroll
+              for (int i = 0; i < 4; ++i) w[i] &= ~gt[i];
+              // one flag byte per element, then one bit per element in the product's top byte
+              const uint32_t fx = prmt(gt[0], gt[1], 0x7531u), fy = prmt(gt[2], gt[3], 0x7531u);
+              const uint32_t fb = ((fx & 0x08040201u) | (fy & 0x80402010u)) * 0x01010101u;
+              const int gi = 2 * j + hh;
+              omask = prmt(omask, fb, (0x3210u & ~(0xfu << (4 * gi))) | (7u << (4 * gi)));
               uint32_t f[8];
               if constexpr (kClip) {
 #pragma unroll
@@ -319,29 +437,43 @@ __global__ void __launch_bounds__(kThreads, 3) quant_pack_side_kernel(const Side
               }
               pack8_raw<BITS>(f, pk[2 * hh], pk[2 * hh + 1]);
             }
-            store_unit<BITS>(crow + unit * SymQ<BITS>::kUnitBytes, pk[0], pk[1], pk[2], pk[3]);
+            if (valid)
+              store_unit<BITS>(crow + unit * SymQ<BITS>::kUnitBytes, pk[0], pk[1], pk[2], pk[3]);
           }
         };
         if (clip) units(std::true_type{});
         else units(std::false_type{});
-        if (lr == 0) pool.scales[prow] = sbits;
-        // outliers, ascending by position: lane j of the row stores the j-th largest key at its
-        // rank among the k positions (a larger low byte = a lower position)
-        for (int j = lr; j < k; j += lpr) {
-          uint32_t kj = 0u;
+        if (valid && lr == 0) pool.scales[prow] = sbits;
+        // outliers, ascending by position: an outlier's rank is the count of the row's outliers
+        // in earlier units (the units j * lpr + i, i < lpr, precede those of j + 1) plus those
+        // before it in its own unit; the counts per j scanned over the row's lanes
+        const uint32_t cnt = static_cast<uint32_t>(__popc(omask & 0xffffu)) |
+                             (static_cast<uint32_t>(__popc(omask >> 16)) << 16);
+        uint32_t incl = cnt;
 #pragma unroll
-          for (int i = 0; i < KVQ_MAX_OUTLIERS; ++i)
-            if (i == j) kj = okey[i];
-          uint32_t rank = 0;
-#pragma unroll
-          for (int i = 0; i < KVQ_MAX_OUTLIERS; ++i)
-            if (i < k) rank += (okey[i] & 0xffu) > (kj & 0xffu) ? 1u : 0u;
-          const uint32_t p = 255u - (kj & 0xffu);
-          const uint16_t val = __ldg(xi + static_cast<int64_t>(row) * D + p);
-          sd.out_idx[prow * k + rank] = static_cast<uint8_t>(p);
-          sd.out_val[prow * k + rank] = val;
+        for (int o = 1; o < 8; o <<= 1) {
+          if (o >= lpr) break;
+          const uint32_t n = __shfl_up_sync(kFullMask, incl, o, lpr);
+          if (lr >= o) incl += n;
         }
-        if (pos < a.n_sink) {
+        const uint32_t tot = __shfl_sync(kFullMask, incl, lpr - 1, lpr);
+        const uint32_t ex = incl - cnt;
+        if (valid) {
+          for (uint32_t mk = omask; mk != 0u; mk &= mk - 1u) {
+            const int n = __ffs(static_cast<int>(mk)) - 1;
+            const bool hi = n >= 16;
+            const uint32_t before = omask & ((1u << n) - 1u) & (hi ? 0xffff0000u : 0x0000ffffu);
+            const uint32_t rank = (hi ? (tot & 0xffffu) + (ex >> 16) : (ex & 0xffffu)) +
+                                  static_cast<uint32_t>(__popc(before));
+            const int p = 16 * (lr + (hi ? lpr : 0)) + (n & 15);
+            if (rank < static_cast<uint32_t>(k)) {
+              const uint16_t val = __ldg(xi + static_cast<int64_t>(row) * D + p);
+              sd.out_idx[prow * k + rank] = static_cast<uint8_t>(p);
+              sd.out_val[prow * k + rank] = val;
+            }
+          }
+        }
+        if (valid && pos < a.n_sink) {
           uint16_t* dst = sd.sink + ((static_cast<int64_t>(s) * a.n_sink + pos) * H + h) * D;
 #pragma unroll
           for (int j = 0; j < UPL; ++j) {

@@ -83,6 +83,88 @@ def test_quant_dequant_side_bit_exact(kvq, cuda_dev, bits, D, k, n_sink):
         assert np.array_equal(u16(o), want.view(np.uint16))
 
 
+def _distinct(cands, D, n):
+    """The first n distinct positions of cands taken modulo D."""
+    out = []
+    for c in cands:
+        if c % D not in out:
+            out.append(c % D)
+        if len(out) == n:
+            return out
+    return out + [p for p in range(D) if p not in out][:n - len(out)]
+
+
+def _selection_rows(D, k, rng):
+    """Rows that stress the choice of outliers: the k + 1 largest magnitudes in one lane's
+    elements (lanes hold units i and i + 8 of a row), equal outliers above the threshold, ties at
+    the threshold (the k-th and (k+1)-th magnitudes equal, the lower position wins) and just
+    below it, runs of equal maxima across lanes, subnormal rows, rows with exactly k and k - 1
+    nonzeros, signed zeros, outliers at the row's ends; each crafted row sits between plain rows
+    so a warp step sees rows with and without ties."""
+    def base():
+        return np.clip(rng.standard_normal(D) * 0.5, -2, 2).astype(np.float16)
+
+    def put(r, pos, mags, signs=None):
+        for i, (p, m) in enumerate(zip(pos, mags)):
+            sg = -1.0 if signs is not None and i < len(signs) and signs[i] else 1.0
+            r[p] = np.float16(sg * m)
+        return r
+
+    lane0 = [3, 130, 7, 140, 12, 135, 1, 129, 9, 14] if D > 128 else [3, 7, 12, 1, 9, 14, 0, 5]
+    spread = [37 * i + 11 for i in range(2 * k + 4)]
+    crafted = [
+        put(base(), _distinct(lane0, D, k + 1), [9.0 - i for i in range(k + 1)]),
+        put(base(), _distinct(spread, D, k), [10.0] * k, [i % 2 for i in range(k)]),
+        # tie at the threshold, the later position first in the list
+        put(base(), _distinct([D - 1, D // 2] + spread, D, k + 1),
+            [6.0, 6.0] + [10.0 + i for i in range(k - 1)]),
+        # tie just below the threshold
+        put(base(), _distinct(spread, D, k + 2), [10.0 + i for i in range(k)] + [5.0, 5.0]),
+        # three equal at the threshold
+        put(base(), _distinct([D - 2, 5, D // 3] + spread, D, k + 2),
+            [7.0, 7.0, 7.0] + [12.0 + i for i in range(k - 1)], [1, 0, 1]),
+        # 2k + 1 equal maxima across the lanes
+        put(base(), _distinct(spread[::-1], D, 2 * k + 1), [8.0] * (2 * k + 1)),
+        (rng.standard_normal(D) * 2.0 ** -20).astype(np.float16),
+        put(np.zeros(D, np.float16), _distinct(spread, D, k), rng.uniform(1, 5, k).tolist()),
+        put(np.zeros(D, np.float16), _distinct(spread, D, max(k - 1, 0)),
+            rng.uniform(1, 5, max(k - 1, 0)).tolist()),
+        np.where(np.arange(D) % 5 == 0, np.float16(-0.0), np.float16(0.0)).astype(np.float16),
+        put(base(), _distinct([0, D - 1, D - 2, 1, D - 3, 2], D, k + 1), [4.0, 3.5, 9.0, 3.5]
+            + [3.0] * max(0, k - 3), [1, 0, 1, 0]),
+    ]
+    rows = []
+    for r in crafted:
+        rows.extend([base(), r, base()])
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("D,k", [(256, 3), (256, 1), (256, 2), (256, 0), (256, 5), (256, 8),
+                                 (128, 3), (96, 3), (64, 2), (16, 3), (16, 8)])
+def test_outlier_selection_cases(kvq, cuda_dev, D, k):
+    bits, H, ps = 6, 4, 16
+    rng = np.random.default_rng(1000 + 10 * D + k)
+    rows = _selection_rows(D, k, rng)
+    tot = -(-rows.shape[0] // H)
+    pad = tot * H - rows.shape[0]
+    rows = np.concatenate([rows, np.zeros((pad, D), np.float16)]).reshape(tot, H, D)
+    rows_v = rows[::-1].copy()
+    lens, starts = [tot], [0]
+    pt_np, pools, sides, opools, osides = _setup(kvq, cuda_dev, bits, H, D, ps, k, 0, lens,
+                                                 starts)
+    cu = cu_of(lens)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    kvq.kvq_quant_pack_paged_side(pools, sides, [dev_tensor(rows, cuda_dev),
+                                                 dev_tensor(rows_v, cuda_dev)],
+                                  i32(pt_np, cuda_dev), i32(cu, cuda_dev), i32(starts, cuda_dev),
+                                  err)
+    for x, osp in zip((rows, rows_v), osides):
+        osd.quant_pack_paged_side(osp, x, pt_np, cu, np.asarray(starts))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    _compare_state(pools, sides, opools, osides, 0)
+
+
 def test_append_across_the_sink_boundary(kvq, cuda_dev):
     """Appending to sequences at positions below and above n_sink: the sink buffer takes exactly
     the positions < n_sink, in place, and the rest of the state is untouched."""
