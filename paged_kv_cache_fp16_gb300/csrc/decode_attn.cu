@@ -523,14 +523,14 @@ __device__ __forceinline__ int side_col(int d) {
 // of token row r = lane >> 1 (entries lane & 1, + 2, ...) when the row is live and not a sink,
 // each as bits 0-7 its residual-tile column (side_col), 8-11 its residual-tile row
 // (tok_order(r)), 12 valid, 16-31 the fp16 value.
-template <bool KEY>
+template <bool KEY, int NE>
 __device__ __forceinline__ void side_collect(const uint8_t* idx, const uint16_t* val, int k,
                                              int n_sink, int tb, int len, int lane,
-                                             uint32_t (&ent)[KVQ_MAX_OUTLIERS / 2]) {
+                                             uint32_t (&ent)[NE]) {
   const int row = lane >> 1;
   const bool live = tb + row < len && tb + row >= n_sink;
 #pragma unroll
-  for (int i = 0; i < KVQ_MAX_OUTLIERS / 2; ++i) {
+  for (int i = 0; i < NE; ++i) {
     const int j = (lane & 1) + 2 * i;
     ent[i] = 0;
     if (live && j < k)
@@ -543,13 +543,13 @@ __device__ __forceinline__ void side_collect(const uint8_t* idx, const uint16_t*
 // Write (or clear) half `hf` of the tile's K or V side terms -- residual-tile columns
 // [128 hf, 128 hf + 128) -- into the warp's half-tile: the lane's entries, and in the sequence's
 // first tile the sink rows' exact fp16 values from the sink buffer [seq][n_sink][H][256].
-template <bool KEY>
-__device__ __forceinline__ void side_half(uint16_t* ot, const uint32_t (&ent)[KVQ_MAX_OUTLIERS / 2],
+template <bool KEY, int NE>
+__device__ __forceinline__ void side_half(uint16_t* ot, const uint32_t (&ent)[NE],
                                           int hf, bool clear, int n_sink, const uint16_t* sink,
                                           int s, int H, int h, int tb, int len, int lane) {
   constexpr int kRowH = (kD + 16) / 2;   // halves per half-tile row
 #pragma unroll
-  for (int i = 0; i < KVQ_MAX_OUTLIERS / 2; ++i) {
+  for (int i = 0; i < NE; ++i) {
     const uint32_t e = ent[i];
     if ((e & 0x1000u) && static_cast<int>((e >> 7) & 1u) == hf)
       ot[((e >> 8) & 15u) * kRowH + (e & 127u)] = clear ? static_cast<uint16_t>(0)
@@ -569,7 +569,7 @@ __device__ __forceinline__ void side_half(uint16_t* ot, const uint32_t (&ent)[KV
 }
 
 // With side channels q6/q4 fit 3 CTAs per SM (168 registers, 74 KB at k = 3); q8 keeps 2.
-template <int BITS, bool APPEND, bool SIDE>
+template <int BITS, bool APPEND, bool SIDE, int NE = KVQ_MAX_OUTLIERS / 2>
 __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS == 8 ? 3 : 4)) decode_attn_tma_kernel(const AttnArgs a,
                                                                       const AttnSide sd) {
   using W = Wd<BITS>;
@@ -787,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
     }
     uint32_t pb0, pb1;
     float sp[4];   // SIDE: the tile's probabilities (unscaled), for the value side terms
-    uint32_t vent[KVQ_MAX_OUTLIERS / 2];   // SIDE: this lane's value entries (side_collect)
+    uint32_t vent[NE];   // SIDE: this lane's value entries (side_collect)
     const bool side_work = SIDE && (sd.k > 0 || (tb == 0 && sd.n_sink > 0));   // warp-uniform
     if constexpr (SIDE) {
       // Key terms the codes do not carry, as a tensor-core product with the query fragments: the
@@ -795,16 +795,16 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
       // is zeroed above).  Columns follow the dense path's MMA k-order.
       float so[4] = {0.f, 0.f, 0.f, 0.f};
       if (side_work) {
-        uint32_t kent[KVQ_MAX_OUTLIERS / 2];
-        side_collect<true>(sk + kkoi, reinterpret_cast<const uint16_t*>(sk + Ly::kBase), sd.k,
+        uint32_t kent[NE];
+        side_collect<true, NE>(sk + kkoi, reinterpret_cast<const uint16_t*>(sk + Ly::kBase), sd.k,
                            sd.n_sink, tb, len, lane, kent);
-        side_collect<false>(sk + kvoi, reinterpret_cast<const uint16_t*>(sk + kvov), sd.k,
+        side_collect<false, NE>(sk + kvoi, reinterpret_cast<const uint16_t*>(sk + kvov), sd.k,
                             sd.n_sink, tb, len, lane, vent);
         const uint32_t ob = smem_u32(ot) + (lane & 15) * Ly::kOtStride + 16 * (lane >> 4);
         float so4[4][4] = {};   // four independent accumulation chains
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {   // k-steps 8 hf .. 8 hf + 7
-          side_half<true>(ot, kent, hf, false, sd.n_sink, sd.ksink[layer], s, a.H, h, tb, len,
+          side_half<true, NE>(ot, kent, hf, false, sd.n_sink, sd.ksink[layer], s, a.H, h, tb, len,
                           lane);
           __syncwarp();
 #pragma unroll
@@ -815,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
             mma16816(so4[ks & 3], af[0], af[1], af[2], af[3], qb.x, qb.y);
           }
           __syncwarp();
-          side_half<true>(ot, kent, hf, true, sd.n_sink, sd.ksink[layer], s, a.H, h, tb, len,
+          side_half<true, NE>(ot, kent, hf, true, sd.n_sink, sd.ksink[layer], s, a.H, h, tb, len,
                           lane);
           __syncwarp();
         }
@@ -867,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
                             16 * ((lane >> 3) & 1);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {   // blocks 8 hf .. 8 hf + 7
-          side_half<false>(ot, vent, hf, false, sd.n_sink, sd.vsink[layer], s, a.H, h, tb, len,
+          side_half<false, NE>(ot, vent, hf, false, sd.n_sink, sd.vsink[layer], s, a.H, h, tb, len,
                            lane);
           __syncwarp();
 #pragma unroll
@@ -877,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
             mma16816(acc[8 * hf + b], af[0], af[1], af[2], af[3], pv0, pv1);
           }
           __syncwarp();
-          side_half<false>(ot, vent, hf, true, sd.n_sink, sd.vsink[layer], s, a.H, h, tb, len,
+          side_half<false, NE>(ot, vent, hf, true, sd.n_sink, sd.vsink[layer], s, a.H, h, tb, len,
                            lane);
           __syncwarp();
         }
@@ -1036,16 +1036,31 @@ int tiles_per_cta_for(int n_layers, int nseq, int H, int max_seq_len) {
   return static_cast<int>(t);
 }
 
+template <int BITS, bool APPEND, bool SIDE, int NE>
+cudaError_t launch_tma(const AttnArgs& a, dim3 grid, cudaStream_t cs, const AttnSide& sd) {
+  const int smem = SIDE ? side_smem_bytes<BITS>(sd.k) : Lay<BITS, SIDE>::kTotal;
+  static_assert(Lay<BITS, SIDE>::kRing >= kMergeBytes, "merge buffer must fit in the stage ring");
+  cudaError_t e = cudaFuncSetAttribute(decode_attn_tma_kernel<BITS, APPEND, SIDE, NE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  decode_attn_tma_kernel<BITS, APPEND, SIDE, NE><<<grid, kThreads, smem, cs>>>(a, sd);
+  return cudaSuccess;
+}
+
+// With side channels each lane holds the outlier entries j = (lane & 1) + 2i, i < NE, of its
+// token row: NE = 2 serves up to 4 outliers per row (the pages' 0.01 gives 3 at D = 256) with
+// half the entry loops of NE = 4 (up to 8).
 template <int BITS, bool APPEND = false, bool SIDE = false>
 cudaError_t launch_attn(const AttnArgs& a, dim3 grid, bool tma, cudaStream_t cs,
                         const AttnSide& sd = AttnSide{}) {
   if (tma) {
-    const int smem = SIDE ? side_smem_bytes<BITS>(sd.k) : Lay<BITS, SIDE>::kTotal;
-    static_assert(Lay<BITS, SIDE>::kRing >= kMergeBytes, "merge buffer must fit in the stage ring");
-    cudaError_t e = cudaFuncSetAttribute(decode_attn_tma_kernel<BITS, APPEND, SIDE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e;
+    if constexpr (SIDE)
+      e = sd.k <= 4 ? launch_tma<BITS, APPEND, SIDE, 2>(a, grid, cs, sd)
+                    : launch_tma<BITS, APPEND, SIDE, 4>(a, grid, cs, sd);
+    else
+      e = launch_tma<BITS, APPEND, SIDE, 4>(a, grid, cs, sd);
     if (e != cudaSuccess) return e;
-    decode_attn_tma_kernel<BITS, APPEND, SIDE><<<grid, kThreads, smem, cs>>>(a, sd);
   } else {
     decode_attn_gather_kernel<BITS><<<grid, kThreads, 0, cs>>>(a);
   }
