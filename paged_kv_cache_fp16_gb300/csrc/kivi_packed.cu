@@ -565,6 +565,7 @@ __global__ void __launch_bounds__(kAThreads, 4) kivi_attn_kernel(const KAArgs a)
   const int layer = lb / a.B, b = lb - layer * a.B;
   const kivi_packed& C = a.c[layer];
   const int S = a.S, gs = C.group_size, G = kAD / gs;
+  const int gsh = __ffs(gs) - 1;   // group sizes are powers of two: divisions by gs are shifts
   const int64_t bh = static_cast<int64_t>(b) * a.H + h;
   const int n_tiles = (a.offset + kATile - 1) / kATile;
   const int tile0 = split * a.tiles_per_cta;
@@ -596,12 +597,12 @@ __global__ void __launch_bounds__(kAThreads, 4) kivi_attn_kernel(const KAArgs a)
     const int cnt = min(kChunk, max(0, a.n_packed - t0));   // a multiple of gs (and of 16)
     uint8_t* dst = wbase + st * kStageBytes;
     if (cnt > 0) {
-      const uint32_t code = cnt * 16, kpar = (cnt / gs) * kAD * 2, vpar = cnt * G * 2;
+      const uint32_t code = cnt * 16, kpar = (cnt >> gsh) * kAD * 2, vpar = cnt * G * 2;
       mbar_expect_tx(&bars[st], 2 * code + 2 * kpar + 2 * vpar);
       bulk_g2s(dst, kc + static_cast<int64_t>(t0) * 16, code, &bars[st]);
       bulk_g2s(dst + kOffVC, vc + static_cast<int64_t>(t0) * 16, code, &bars[st]);
-      bulk_g2s(dst + kOffKS, ksc + (t0 / gs) * kAD, kpar, &bars[st]);
-      bulk_g2s(dst + kOffKZ, kze + (t0 / gs) * kAD, kpar, &bars[st]);
+      bulk_g2s(dst + kOffKS, ksc + (t0 >> gsh) * kAD, kpar, &bars[st]);
+      bulk_g2s(dst + kOffKZ, kze + (t0 >> gsh) * kAD, kpar, &bars[st]);
       bulk_g2s(dst + kOffVS, vsc + static_cast<int64_t>(t0) * G, vpar, &bars[st]);
       bulk_g2s(dst + kOffVZ, vze + static_cast<int64_t>(t0) * G, vpar, &bars[st]);
     } else {
@@ -663,10 +664,10 @@ __global__ void __launch_bounds__(kAThreads, 4) kivi_attn_kernel(const KAArgs a)
 #pragma unroll
       for (int r = 0; r < 2; ++r) kval[r] = tb + g + 8 * r < a.offset;
       if (packed) {
-        const int grp = tb / gs;
+        const int grp = tb >> gsh;
         if (grp != kgroup) {   // group parameters of the thread's 16 channels (warp-uniform)
           kgroup = grp;
-          const uint32_t sp = sb + kOffKS + ((tb - t0) / gs) * (kAD * 2) + 32 * c;
+          const uint32_t sp = sb + kOffKS + ((tb - t0) >> gsh) * (kAD * 2) + 32 * c;
           const uint4 s0 = lds_v4(sp);
           const uint4 s1 = lds_v4(sp + 16);
           const uint4 z0 = lds_v4(sp + (kOffKZ - kOffKS));
@@ -746,7 +747,7 @@ __global__ void __launch_bounds__(kAThreads, 4) kivi_attn_kernel(const KAArgs a)
       // ---------------- V^T fragments: tokens (2c, 2c+1) and (2c+8, 2c+9), elements 8g + j
       uint32_t vf[2][8];   // [token pair][element j]: {A.e_j, B.e_j}
       if (packed) {
-        const int gi = (8 * g) / gs;
+        const int gi = (8 * g) >> gsh;
 #pragma unroll
         for (int pr = 0; pr < 2; ++pr) {
           const int ta = lt + 2 * c + 8 * pr;   // local token of A; B = A + 1 (all packed)
