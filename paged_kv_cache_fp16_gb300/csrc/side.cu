@@ -41,6 +41,7 @@
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 #include "kvq_math.cuh"
+#include "kvq_divu32.cuh"
 #include "kvq_rowwise.cuh"
 
 namespace kvq {
@@ -70,7 +71,15 @@ struct SideArgs {
   int units;     // 16-element units per row: D / 16
   int lpr_log2;  // lanes per row = 1 << lpr_log2 = min(next_pow2(units), 8)
   bool v8;       // every fp16 tensor 32-byte aligned: its 16-element units move in one 256-bit access
+  bool items32;  // work items (tensor, token block) index in 32 bits: split by div_items
+  DivU32 div_h, div_items;   // by the head count and the token blocks per tensor
 };
+
+// Work item g -> its tensor (the item within the tensor is g - tensor * n_items).
+__device__ __forceinline__ int item_tensor(const SideArgs& a, int64_t g, int n_items) {
+  return a.items32 ? static_cast<int>(divu32(static_cast<uint32_t>(g), a.div_items))
+                   : static_cast<int>(g / n_items);
+}
 
 // New token `tok` -> physical row of its head 0 ((page * H) * page_size + slot) or -1, with its
 // sequence and position (the position clamped to int: it is only compared with n_sink).
@@ -313,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 3) quant_pack_side_kernel(const Side
   const int n_warps = gridDim.x * kWarps;
 
   for (int64_t g = blockIdx.x * kWarps + (threadIdx.x >> 5); g < n_work; g += n_warps) {
-    const int t = static_cast<int>(g / n_items);
+    const int t = item_tensor(a, g, n_items);
     const int item = static_cast<int>(g - static_cast<int64_t>(t) * n_items);
     const uint16_t* __restrict__ x = a.x[t];
     const PoolRef pool = a.pool[t];
@@ -348,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 3) quant_pack_side_kernel(const Side
 #pragma unroll
       for (int u = 0; u < kQU; ++u) {
         const int row = r0 + u * rps + sub;
-        const int kt = row / H;
+        const int kt = static_cast<int>(divu32(static_cast<uint32_t>(row), a.div_h));
         const int src = kt < kTok ? kt : 0;
         const long long b = shfl_ll(base, src);
         const int s = __shfl_sync(kFullMask, my_s, src);
@@ -505,7 +514,7 @@ __global__ void __launch_bounds__(kThreads) dequant_side_kernel(const SideArgs a
   const int n_warps = gridDim.x * kWarps;
 
   for (int64_t g = blockIdx.x * kWarps + (threadIdx.x >> 5); g < n_work; g += n_warps) {
-    const int t = static_cast<int>(g / n_items);
+    const int t = item_tensor(a, g, n_items);
     const int item = static_cast<int>(g - static_cast<int64_t>(t) * n_items);
     uint16_t* __restrict__ out = const_cast<uint16_t*>(a.x[t]);
     const PoolRef pool = a.pool[t];
@@ -527,7 +536,7 @@ __global__ void __launch_bounds__(kThreads) dequant_side_kernel(const SideArgs a
 #pragma unroll
       for (int u = 0; u < kDU; ++u) {
         const int row = r0 + u * rps + sub;
-        const int kt = row / H;
+        const int kt = static_cast<int>(divu32(static_cast<uint32_t>(row), a.div_h));
         const int src = kt < kTok ? kt : 0;
         const long long b = shfl_ll(base, src);
         const bool snk = __shfl_sync(kFullMask, static_cast<int>(sink_row >= 0), src) != 0;
@@ -553,7 +562,7 @@ __global__ void __launch_bounds__(kThreads) dequant_side_kernel(const SideArgs a
 #pragma unroll
       for (int u = 0; u < kDU; ++u) {
         const int row = r0 + u * rps + sub;
-        const int kt = row / H;
+        const int kt = static_cast<int>(divu32(static_cast<uint32_t>(row), a.div_h));
         const long long srow = shfl_ll(sink_row, kt < kTok ? kt : 0);
         if (!act[u]) continue;
         uint16_t* orow = oi + static_cast<int64_t>(row) * D;
@@ -603,7 +612,7 @@ __global__ void __launch_bounds__(kThreads) dequant_side_kernel(const SideArgs a
           if (d < static_cast<uint32_t>(D)) orow[d] = static_cast<uint16_t>(ov[u] >> 16);
         }
         if (k > lpr) {   // more outliers than lanes per row (short rows): lane lr also takes lr + lpr, ...
-          const int kt = row / H;
+          const int kt = static_cast<int>(divu32(static_cast<uint32_t>(row), a.div_h));
           const long long b = shfl_ll(base, kt < kTok ? kt : 0);
           if (dense[u]) {
             const int64_t prow = b + static_cast<int64_t>(row - kt * H) * a.page_size;
@@ -743,6 +752,12 @@ kvq_status side_call(bool quant, const kvq_pool* pools, const kvq_side* sides,
   a.k = sides[0].n_outlier;
   a.n_sink = sides[0].n_sink;
   a.units = p0.head_dim / 16;
+  a.div_h = make_divu32(static_cast<uint32_t>(a.H));
+  {
+    const int64_t n_items = (static_cast<int64_t>(total) + kTok - 1) / kTok;
+    a.items32 = n_items * n_tensors <= 0xffffffffLL;
+    a.div_items = make_divu32(static_cast<uint32_t>(n_items));
+  }
   a.lpr_log2 = 0;
   while ((1 << a.lpr_log2) < a.units && a.lpr_log2 < 3) ++a.lpr_log2;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
