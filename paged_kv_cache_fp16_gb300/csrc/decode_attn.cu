@@ -805,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {   // k-steps 8 hf .. 8 hf + 7
           side_half<true, NE>(ot, kent, hf, false, sd.n_sink, sd.ksink[layer], s, a.H, h, tb, len,
-                          lane);
+                              lane);
           __syncwarp();
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
@@ -816,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
           }
           __syncwarp();
           side_half<true, NE>(ot, kent, hf, true, sd.n_sink, sd.ksink[layer], s, a.H, h, tb, len,
-                          lane);
+                              lane);
           __syncwarp();
         }
 #pragma unroll
@@ -868,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {   // blocks 8 hf .. 8 hf + 7
           side_half<false, NE>(ot, vent, hf, false, sd.n_sink, sd.vsink[layer], s, a.H, h, tb, len,
-                           lane);
+                               lane);
           __syncwarp();
 #pragma unroll
           for (int b = 0; b < 8; ++b) {
@@ -878,7 +878,7 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
           }
           __syncwarp();
           side_half<false, NE>(ot, vent, hf, true, sd.n_sink, sd.vsink[layer], s, a.H, h, tb, len,
-                           lane);
+                               lane);
           __syncwarp();
         }
       }

@@ -22,6 +22,7 @@
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
+#include "kvq_divu32.cuh"
 #include "kvq_math.cuh"
 #include "kvq_rowwise.cuh"
 
@@ -56,6 +57,7 @@ struct PackArgs {
   int lpr_log2;  // lanes per row = 1 << lpr_log2 = min(next_pow2(units), 8)
   int tpi;       // tokens per work item, 1..kTok (fewer for calls too small to fill the GPU)
   bool v8;       // every fp16 tensor 32-byte aligned: its 16-element units move in one 256-bit access
+  DivU32 div_h;  // by the head count: a row's token
 };
 
 // Physical row of head 0 of new token `tok` ((page * H) * page_size + slot), or -1.
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(kThreads) quant_pack_kernel(const PackArgs a) 
         float amax = fmaxf(__low2float(m2), __high2float(m2));
         for (int o = lpr >> 1; o >= 1; o >>= 1)
           amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, o));
-        const int k = row / H;
+        const int k = static_cast<int>(divu32(static_cast<uint32_t>(row), a.div_h));
         const long long b = shfl_ll(base, k < kTok ? k : 0);
         if (row >= nrows || b < 0) continue;
         const int64_t prow = b + static_cast<int64_t>(row - k * H) * a.page_size;
@@ -227,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, BITS == 4 ? 4 : 3) dequant_kernel(co
 #pragma unroll
       for (int u = 0; u < kDqU; ++u) {
         const int row = r0 + u * rps + sub;
-        const int k = row / H;
+        const int k = static_cast<int>(divu32(static_cast<uint32_t>(row), a.div_h));
         const long long b = shfl_ll(base, k < kTok ? k : 0);
         act[u] = row < nrows && b >= 0;
         sc[u] = 0;
@@ -396,6 +398,7 @@ kvq_status prepare(PackArgs& a, const kvq_pool* pools, const uint16_t* const* x,
   a.max_pages = max_pages;
   a.nseq = nseq;
   a.units = (p0.head_dim + 15) / 16;
+  a.div_h = make_divu32(static_cast<uint32_t>(a.H));
   a.lpr_log2 = ceil_log2(a.units) < 3 ? ceil_log2(a.units) : 3;
   a.total_tokens = total_tokens;
   a.tpi = kTok;
