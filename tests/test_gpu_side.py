@@ -291,7 +291,7 @@ def _close(got, ref):
 
 @pytest.mark.parametrize("bits", [8, 6, 4])
 @pytest.mark.parametrize("k,n_sink,ps", [(3, 4, 16), (0, 4, 16), (3, 0, 16), (8, 16, 32),
-                                         (1, 1, 16)])
+                                         (1, 1, 16), (4, 2, 16), (5, 2, 16)])
 def test_decode_attn_side(kvq, cuda_dev, bits, k, n_sink, ps):
     H, G, D, L = 4, 6, 256, 2
     lens = [1, 3, 16, 17, 100, 1000, 0]
