@@ -790,37 +790,72 @@ __global__ void __launch_bounds__(kThreads, SIDE ? (BITS == 8 ? 2 : 3) : (BITS =
     uint32_t vent[NE];   // SIDE: this lane's value entries (side_collect)
     const bool side_work = SIDE && (sd.k > 0 || (tb == 0 && sd.n_sink > 0));   // warp-uniform
     if constexpr (SIDE) {
-      // Key terms the codes do not carry, as a tensor-core product with the query fragments: the
-      // outliers (q[pos] * value) and, for sink rows, the whole exact fp16 row (their dense scale
-      // is zeroed above).  Columns follow the dense path's MMA k-order.
+      // Key terms the codes do not carry: the outliers (q[pos] * value) and, for sink rows, the
+      // whole exact fp16 row (their dense scale is zeroed above).  With the query fragments in
+      // shared memory (q6, q4) each thread adds its two tokens' outliers to its four scores
+      // directly, reading q[head][pos] from the fragments; sink rows (a sequence's first tile)
+      // and q8 go through a tensor-core product of the residual half-tile with the fragments,
+      // columns in the dense path's MMA k-order.
       float so[4] = {0.f, 0.f, 0.f, 0.f};
       if (side_work) {
-        uint32_t kent[NE];
-        side_collect<true, NE>(sk + kkoi, reinterpret_cast<const uint16_t*>(sk + Ly::kBase), sd.k,
-                           sd.n_sink, tb, len, lane, kent);
         side_collect<false, NE>(sk + kvoi, reinterpret_cast<const uint16_t*>(sk + kvov), sd.k,
-                            sd.n_sink, tb, len, lane, vent);
-        const uint32_t ob = smem_u32(ot) + (lane & 15) * Ly::kOtStride + 16 * (lane >> 4);
-        float so4[4][4] = {};   // four independent accumulation chains
+                                sd.n_sink, tb, len, lane, vent);
+        uint32_t kent[NE];
+        bool mma_pass = true;
+        if constexpr (kQShared) {
+          // q[n][d] sits in k-step ks = 2 ((d >> 3) & 7) + ((d >> 1) & 1) of lane 4n + (d >> 6),
+          // word d & 1, half (d >> 2) & 1; this thread's heads are n = 2c and 2c + 1
+          const uint8_t* koi = sk + kkoi;
+          const uint16_t* kov = reinterpret_cast<const uint16_t*>(sk + Ly::kBase);
+          const uint8_t* qh = smem + qf_off + 64 * c;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {   // k-steps 8 hf .. 8 hf + 7
-          side_half<true, NE>(ot, kent, hf, false, sd.n_sink, sd.ksink[layer], s, a.H, h, tb, len,
-                              lane);
-          __syncwarp();
+          for (int r = 0; r < 2; ++r) {
+            const int row = tok_order(g + 8 * r);
+            if (tb + row < len && tb + row >= sd.n_sink) {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            uint32_t af[4];
-            ldsm_x4(ob + 32 * ks, af);
-            const uint2 qb = Q.pair(8 * hf + ks);
-            mma16816(so4[ks & 3], af[0], af[1], af[2], af[3], qb.x, qb.y);
+              for (int j = 0; j < 2 * NE; ++j) {
+                if (j >= sd.k) break;
+                const int d = koi[row * sd.k + j];
+                const float v = h2f(kov[row * sd.k + j]);
+                const uint8_t* qa = qh + 256 * (2 * ((d >> 3) & 7) + ((d >> 1) & 1)) +
+                                    8 * (d >> 6) + 4 * (d & 1) + 2 * ((d >> 2) & 1);
+                so[2 * r] = fmaf(h2f(*reinterpret_cast<const uint16_t*>(qa)), v, so[2 * r]);
+                so[2 * r + 1] =
+                    fmaf(h2f(*reinterpret_cast<const uint16_t*>(qa + 32)), v, so[2 * r + 1]);
+              }
+            }
           }
-          __syncwarp();
-          side_half<true, NE>(ot, kent, hf, true, sd.n_sink, sd.ksink[layer], s, a.H, h, tb, len,
-                              lane);
-          __syncwarp();
-        }
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) so[k4] = (so4[0][k4] + so4[1][k4]) + (so4[2][k4] + so4[3][k4]);
+          for (int i = 0; i < NE; ++i) kent[i] = 0u;   // the pass below carries sink rows only
+          mma_pass = tb < sd.n_sink;                    // warp-uniform
+        } else {
+          side_collect<true, NE>(sk + kkoi, reinterpret_cast<const uint16_t*>(sk + Ly::kBase),
+                                 sd.k, sd.n_sink, tb, len, lane, kent);
+        }
+        if (mma_pass) {
+          const uint32_t ob = smem_u32(ot) + (lane & 15) * Ly::kOtStride + 16 * (lane >> 4);
+          float so4[4][4] = {};   // four independent accumulation chains
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {   // k-steps 8 hf .. 8 hf + 7
+            side_half<true, NE>(ot, kent, hf, false, sd.n_sink, sd.ksink[layer], s, a.H, h, tb,
+                                len, lane);
+            __syncwarp();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              uint32_t af[4];
+              ldsm_x4(ob + 32 * ks, af);
+              const uint2 qb = Q.pair(8 * hf + ks);
+              mma16816(so4[ks & 3], af[0], af[1], af[2], af[3], qb.x, qb.y);
+            }
+            __syncwarp();
+            side_half<true, NE>(ot, kent, hf, true, sd.n_sink, sd.ksink[layer], s, a.H, h, tb,
+                                len, lane);
+            __syncwarp();
+          }
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4)
+            so[k4] += (so4[0][k4] + so4[1][k4]) + (so4[2][k4] + so4[3][k4]);
+        }
       }
       tile_qk_softmax<BITS, true>(K, Q, acc, m0, m1, l0, l1, a.qk_scale, pb0, pb1, so, sp);
     } else {
