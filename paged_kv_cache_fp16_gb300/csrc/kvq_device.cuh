@@ -5,6 +5,7 @@
 #include <cuda_fp16.h>
 
 #include "kvq.h"
+#include "kvq_divu32.cuh"
 
 namespace kvq {
 
@@ -86,12 +87,11 @@ __device__ __forceinline__ uint16_t ld_nc_u16(const void* p) {
 // parallel): it is exact whenever the sequences add equal numbers of tokens (a decode-step
 // append, a uniform prefill), which saves the binary search's chain of dependent loads; otherwise
 // the search runs on the side of g that holds the answer.
-__device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu, int nseq, int total,
-                                        int i) {
+// The search from a guess g in [0, nseq).
+__device__ __forceinline__ int find_seq_from(const int32_t* __restrict__ cu, int nseq, int i,
+                                             int g) {
   int lo = 0, hi = nseq - 1;
-  if (total > 0 && nseq > 1) {
-    int g = static_cast<int>((static_cast<int64_t>(i) * nseq) / total);
-    g = g < 0 ? 0 : (g > nseq - 1 ? nseq - 1 : g);
+  if (nseq > 1) {
     const int c0 = __ldg(cu + g), c1 = __ldg(cu + g + 1);
     if (c0 <= i && (g == nseq - 1 || i < c1)) return g;
     if (c0 > i) hi = g - 1;
@@ -104,6 +104,38 @@ __device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu, int nseq
   return lo;
 }
 
+__device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu, int nseq, int total,
+                                        int i) {
+  int g = 0;
+  if (total > 0 && nseq > 1) {
+    g = static_cast<int>((static_cast<int64_t>(i) * nseq) / total);
+    g = g < 0 ? 0 : (g > nseq - 1 ? nseq - 1 : g);
+  }
+  return find_seq_from(cu, nseq, i, g);
+}
+
+// The same with the guess's division by a divider made on the host (`div_total` divides by
+// total; valid when nseq * total < 2^32, 0 <= i < total).
+__device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu, int nseq, int i,
+                                        const DivU32& div_total) {
+  int g = static_cast<int>(divu32(static_cast<uint32_t>(i) * static_cast<uint32_t>(nseq),
+                                  div_total));
+  g = g > nseq - 1 ? nseq - 1 : g;
+  return find_seq_from(cu, nseq, i, g);
+}
+
+// Physical row index ((page * H + h) * page_size + slot) of slot `slot` of logical page `lp` of
+// sequence `s`, or -1 (and the error bit) if the logical or physical page is out of range.
+__device__ __forceinline__ int64_t locate_row_at(const int32_t* __restrict__ page_table,
+                                                 int max_pages, int page_size, int num_heads,
+                                                 int64_t num_pages, int s, int64_t lp, int slot,
+                                                 int h, int32_t* err) {
+  if (lp >= max_pages) { report(err, KVQ_DEVERR_PAGE_RANGE); return -1; }
+  int page = __ldg(page_table + static_cast<int64_t>(s) * max_pages + lp);
+  if (page < 0 || page >= num_pages) { report(err, KVQ_DEVERR_PAGE_RANGE); return -1; }
+  return (static_cast<int64_t>(page) * num_heads + h) * page_size + slot;
+}
+
 // Physical row index ((page * H + h) * page_size + slot) of token `pos` of sequence `s`,
 // or -1 (and the error bit) if the logical or physical page is out of range.
 __device__ __forceinline__ int64_t locate_row(const int32_t* __restrict__ page_table,
@@ -111,12 +143,20 @@ __device__ __forceinline__ int64_t locate_row(const int32_t* __restrict__ page_t
                                               int64_t num_pages, int s, int64_t pos, int h,
                                               int32_t* err) {
   if (pos < 0) { report(err, KVQ_DEVERR_PAGE_RANGE); return -1; }
-  int64_t lp = pos / page_size;
-  if (lp >= max_pages) { report(err, KVQ_DEVERR_PAGE_RANGE); return -1; }
-  int slot = static_cast<int>(pos - lp * page_size);
-  int page = __ldg(page_table + static_cast<int64_t>(s) * max_pages + lp);
-  if (page < 0 || page >= num_pages) { report(err, KVQ_DEVERR_PAGE_RANGE); return -1; }
-  return (static_cast<int64_t>(page) * num_heads + h) * page_size + slot;
+  const int64_t lp = pos / page_size;
+  return locate_row_at(page_table, max_pages, page_size, num_heads, num_pages, s, lp,
+                       static_cast<int>(pos - lp * page_size), h, err);
+}
+
+// The same with the division by the page size made by a divider (`div_ps`; 0 <= pos < 2^32).
+__device__ __forceinline__ int64_t locate_row(const int32_t* __restrict__ page_table,
+                                              int max_pages, int page_size, int num_heads,
+                                              int64_t num_pages, int s, int64_t pos, int h,
+                                              int32_t* err, const DivU32& div_ps) {
+  if (pos < 0 || pos > 0xffffffffLL) { report(err, KVQ_DEVERR_PAGE_RANGE); return -1; }
+  const uint32_t lp = divu32(static_cast<uint32_t>(pos), div_ps);
+  return locate_row_at(page_table, max_pages, page_size, num_heads, num_pages, s, lp,
+                       static_cast<int>(static_cast<uint32_t>(pos) - lp * page_size), h, err);
 }
 
 // Load one 16-element unit of packed codes (12 / 8 / 16 bytes for q6 / q4 / q8) into the words

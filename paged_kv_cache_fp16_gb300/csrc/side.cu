@@ -72,7 +72,9 @@ struct SideArgs {
   int lpr_log2;  // lanes per row = 1 << lpr_log2 = min(next_pow2(units), 8)
   bool v8;       // every fp16 tensor 32-byte aligned: its 16-element units move in one 256-bit access
   bool items32;  // work items (tensor, token block) index in 32 bits: split by div_items
+  bool seq32;    // nseq * total_tokens < 2^32: the sequence guess takes div_total
   DivU32 div_h, div_items;   // by the head count and the token blocks per tensor
+  DivU32 div_ps, div_total;  // by the page size, by the token count (sequence guesses)
 };
 
 // Work item g -> its tensor (the item within the tensor is g - tensor * n_items).
@@ -85,10 +87,12 @@ __device__ __forceinline__ int item_tensor(const SideArgs& a, int64_t g, int n_i
 // sequence and position (the position clamped to int: it is only compared with n_sink).
 __device__ __forceinline__ long long token_place(const SideArgs& a, int64_t num_pages, int tok,
                                                  int& s, int& pos) {
-  s = find_seq(a.cu, a.nseq, a.total_tokens, tok);
+  s = a.seq32 ? find_seq(a.cu, a.nseq, tok, a.div_total)
+              : find_seq(a.cu, a.nseq, a.total_tokens, tok);
   const int64_t p = static_cast<int64_t>(__ldg(a.start + s)) + (tok - __ldg(a.cu + s));
   pos = p > 0x7fffffffLL ? 0x7fffffff : static_cast<int>(p);
-  return locate_row(a.page_table, a.max_pages, a.page_size, a.H, num_pages, s, p, 0, a.err);
+  return locate_row(a.page_table, a.max_pages, a.page_size, a.H, num_pages, s, p, 0, a.err,
+                    a.div_ps);
 }
 
 __device__ __forceinline__ long long shfl_ll(long long v, int src) {
@@ -753,6 +757,9 @@ kvq_status side_call(bool quant, const kvq_pool* pools, const kvq_side* sides,
   a.n_sink = sides[0].n_sink;
   a.units = p0.head_dim / 16;
   a.div_h = make_divu32(static_cast<uint32_t>(a.H));
+  a.div_ps = make_divu32(static_cast<uint32_t>(a.page_size));
+  a.seq32 = static_cast<int64_t>(total) * nseq < (1LL << 32);
+  a.div_total = make_divu32(static_cast<uint32_t>(total));
   {
     const int64_t n_items = (static_cast<int64_t>(total) + kTok - 1) / kTok;
     a.items32 = n_items * n_tensors <= 0xffffffffLL;
