@@ -303,9 +303,9 @@ __device__ __forceinline__ void magnitude_select(const uint4 (&v)[UPL][2], int l
     }
     last = m;
     const bool pop = top[0] == m;
+    // at most k <= 3 pops: the last entry never needs clearing (after three pops it is the head)
 #pragma unroll
     for (int i = 0; i < 3; ++i) top[i] = pop ? top[i + 1] : top[i];
-    top[3] = pop ? 0u : top[3];
   }
   T = thr >> 3;
   M = last >> 3;
@@ -313,7 +313,7 @@ __device__ __forceinline__ void magnitude_select(const uint4 (&v)[UPL][2], int l
 
 // ------------------------------------------------------------------------------ quant-pack
 template <int BITS, int UPL, int DEPTH, bool V8>
-__global__ void __launch_bounds__(kThreads, 3) quant_pack_side_kernel(const SideArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) quant_pack_side_kernel(const SideArgs a) {
   constexpr int kQm = SymQ<BITS>::kQmax;
   const int lane = threadIdx.x & 31;
   const int lpr = 1 << a.lpr_log2;
